@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Benchmark of one token-choice MoE layer, forward + backward, on GB300.
+
+One step = the whole layer over one micro-batch of synthetic inputs: router,
+top-k, dispatch, grouped SwiGLU experts (+ shared expert), combine, aux loss,
+and their backward, all through libmoe's C ABI on one stream. Default
+workload: the Mixtral-style layer (T=4096, d=4096, 8 experts, top-2 softmax,
+FFN width 14336, bf16 with an fp32 router).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle, bounded sample
+
+Prints one JSON line (rank 0). Multi-GPU: the layer does not shard inside one
+GPU's step; N ranks run N independent replicas (weak scaling, no collective on
+the data path; a barrier and a max-reduce of the step time only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer fwd+bwd tokens/s at 1 GB300; grouped-GEMM % bf16 peak; permute GB/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral_style")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time the forward only (the workload's own pass if it has no backward)")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_desc(wl, backward):
+    s = (f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} top-{wl.k} {wl.score} F={wl.F}"
+         f"{' shared F=' + str(wl.F_shared) if wl.F_shared else ''} {wl.act_dtype} "
+         f"(fp32 router){' +sel-bias' if wl.sel_bias_range else ''}"
+         f"{' +zipf-skew' if wl.zipf_s else ''} {'fwd+bwd' if backward else 'fwd'}")
+    return s
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "routing_grouped_expert_gate_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel_key)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ our arm
+def stage_work(wl, cfg_backward):
+    """Algorithmic FLOPs / bytes of each ABI call of one step."""
+    es = 2 if wl.act_dtype == "bf16" else 4
+    T, d, E, k, F, Fs = wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared
+    A = T * k
+    w = {
+        "route": {"flops": 2.0 * T * d * E,
+                  "bytes": T * d * es + E * d * 4 + T * E * 4 * 2 + T * k * 8},
+        "permute": {"bytes": T * d * es + A * d * es + T * k * 12},
+        "grouped_fwd": {"flops": 6.0 * A * d * F,
+                        "bytes": (A * d * 2 + A * F * 3 + A * 2 * F) * es + E * 3 * d * F * es},
+        "combine": {"bytes": A * d * es + T * d * es * (2 if Fs else 1) + T * k * 8},
+        "aux": {"bytes": T * E * 4},
+    }
+    if Fs:
+        w["shared_fwd"] = {"flops": 6.0 * T * d * Fs}
+    if cfg_backward:
+        w["combine_bwd"] = {"bytes": T * d * es + 2 * A * d * es + T * k * 12}
+        w["grouped_bwd"] = {"flops": 12.0 * A * d * F}
+        if Fs:
+            w["shared_bwd"] = {"flops": 12.0 * T * d * Fs}
+        w["aux_bwd"] = {"bytes": T * E * 8}
+        w["route_bwd"] = {"flops": 4.0 * T * d * E,
+                          "bytes": T * d * (es + 4) + T * E * 4 * 3 + E * d * 8}
+        w["permute_bwd"] = {"bytes": A * d * es + T * d * 4 + T * d * es * (2 if Fs else 1)}
+    return w
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import moe_inputs as mi
+    from routing_grouped_expert_gate_gb300 import build as B
+    B.build()
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    from routing_grouped_expert_gate_gb300 import layer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = mi.WORKLOADS[args.workload]
+    backward = wl.backward and not args.fwd_only
+    cfg = moe.cfg_from_workload(wl)
+    inp = mi.make_inputs(wl, seed=0, device=dev, with_dy=backward)
+    p = layer.params_from_inputs(inp)
+    x, dy = inp["x"], inp["dy"]
+    b = layer.alloc_buffers(cfg, dev, backward=backward)
+    stream = torch.cuda.current_stream()
+    T, k, E, F, Fs = cfg.T, cfg.k, cfg.E, cfg.F, cfg.F_shared
+
+    # the step, as a list of (stage, call) so that events can bracket each call
+    def calls():
+        c = [("route", lambda: L.route_topk(cfg, x, p["w_router"], p.get("logit_bias"),
+                                             p.get("sel_bias"), b["logits"], b["idx"], b["w"])),
+             ("permute", lambda: L.permute(cfg, x, b["idx"], b["counts"], b["offsets"], b["row_of"],
+                                           b["src_tok"], b["x_perm"], b["ws"])),
+             ("grouped_fwd", lambda: L.grouped_swiglu(cfg, E, T * k, F, b["offsets"], b["x_perm"],
+                                                      p["w1"], p["w2"], b["pre_gu"], b["h"],
+                                                      b["out_perm"], b["ws"]))]
+        if Fs:
+            c.append(("shared_fwd", lambda: L.grouped_swiglu(cfg, 1, T, Fs, None, x, p["w1_s"],
+                                                             p["w2_s"], b["pre_gu_s"], b["h_s"],
+                                                             b["y_s"], b["ws"])))
+        c += [("combine", lambda: L.unpermute_combine(cfg, b["out_perm"], b["row_of"], b["w"],
+                                                      b["y_s"] if Fs else None, b["y"])),
+              ("aux", lambda: L.aux_loss(cfg, b["logits"], b["counts"], b["aux"], b["ws"]))]
+        if backward:
+            c += [("combine_bwd", lambda: L.unpermute_combine_bwd(cfg, dy, b["out_perm"], b["row_of"],
+                                                                  b["w"], b["d_out_perm"], b["dw"])),
+                  ("grouped_bwd", lambda: L.grouped_swiglu_bwd(
+                      cfg, E, T * k, F, b["offsets"], b["x_perm"], p["w1"], p["w2"], b["pre_gu"],
+                      b["h"], b["d_out_perm"], b["d_pre"], b["dx_perm"], b["dw1"], b["dw2"],
+                      b["ws"]))]
+            if Fs:
+                c.append(("shared_bwd", lambda: L.grouped_swiglu_bwd(
+                    cfg, 1, T, Fs, None, x, p["w1_s"], p["w2_s"], b["pre_gu_s"], b["h_s"], dy,
+                    b["d_pre_s"], b["dx_s"], b["dw1_s"], b["dw2_s"], b["ws"])))
+            c += [("aux_bwd", lambda: L.aux_loss_bwd(cfg, b["logits"], b["counts"], 1.0,
+                                                     b["d_logits"], 0)),
+                  ("route_bwd", lambda: L.route_topk_bwd(cfg, x, p["w_router"], b["logits"],
+                                                         b["idx"], b["dw"], b["d_logits"], 1,
+                                                         b["dx_router"], b["dw_router"], b["ws"])),
+                  ("permute_bwd", lambda: L.permute_bwd(cfg, b["dx_perm"], b["row_of"],
+                                                        b["dx_router"], b["dx_s"] if Fs else None,
+                                                        b["dx"]))]
+        return c
+
+    step_calls = calls()
+
+    def step():
+        for _, fn in step_calls:
+            fn()
+
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    rc, detail = L.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {rc} ({L.status_string(rc)}) {detail}")
+
+    # ---- timed region: K steps, events around every call
+    K = args.steps
+    names = [n for n, _ in step_calls]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step_calls) + 1)]
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = L.launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(step_calls):
+            fn()
+            ev[i][j + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = L.launch_count() - launches0
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    stage_ms = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
+                for j, n in enumerate(names)}
+    rc, detail = L.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {rc} ({L.status_string(rc)}) {detail}")
+
+    peaks = measured_peaks()
+    work = stage_work(wl, backward)
+    stages = {}
+    for n, ms in stage_ms.items():
+        e = {"ms": round(ms, 4)}
+        wk = work.get(n, {})
+        if "flops" in wk:
+            e["tflops"] = round(wk["flops"] / (ms * 1e-3) / 1e12, 2)
+        if "bytes" in wk:
+            e["gbs"] = round(wk["bytes"] / (ms * 1e-3) / 1e9, 1)
+        stages[n] = e
+    grouped = [n for n in stage_ms if n in ("grouped_fwd", "grouped_bwd", "shared_fwd",
+                                            "shared_bwd")]
+    g_flops = sum(work[n]["flops"] for n in grouped)
+    g_ms = sum(stage_ms[n] for n in grouped)
+    g_tflops = g_flops / (g_ms * 1e-3) / 1e12
+    dom = max(grouped, key=lambda n: stage_ms[n])
+    dom_tflops = work[dom]["flops"] / (stage_ms[dom] * 1e-3) / 1e12
+    peak_sust = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(dom_tflops, 2),
+                "peak": peak_sust, "unit": "TFLOP/s",
+                "frac": round(dom_tflops / peak_sust, 4),
+                "traffic": recorded_traffic(dom),
+                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
+                "per_launch_flops": work[dom]["flops"]}
+
+    out = {
+        "metric": METRIC, "value": None, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.act_dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; no dataset)",
+        "config": {"workload": workload_desc(wl, backward), "tokens_per_step_per_gpu": T,
+                   "l2": "no flush: each step streams %.1f GB of expert weights (> 129 MB L2)"
+                         % (E * 3 * cfg.d * F * (2 if wl.act_dtype == "bf16" else 4) / 1e9),
+                   "parallelism": f"replicas x{ws}"},
+        "grouped_gemm_pct_bf16_peak": round(100 * g_tflops / peak_sust, 2),
+        "grouped_gemm_tflops": round(g_tflops, 2),
+        "permute_gbs": stages["permute"].get("gbs"),
+        "roofline": roofline,
+        "stages": stages,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "peaks": peaks,
+    }
+    out["value"] = round(ws * T / (ms_per_step * 1e-3), 1)
+
+    # ---- end to end: host inputs in, result out, through the same calls
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        dyh = dy.cpu().pin_memory() if backward else None
+        yh = torch.empty_like(b["y"], device="cpu").pin_memory()
+        auxh = torch.empty(1, dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(x)
+        dyd = torch.empty_like(dy) if backward else None
+        # the e2e step reads its inputs from xd / dyd
+        x_saved, dy_saved = x, dy
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            if backward:
+                dyd.copy_(dyh, non_blocking=True)
+            for _, fn in step_calls:
+                fn()
+            yh.copy_(b["y"], non_blocking=True)
+            auxh.copy_(b["aux"], non_blocking=True)
+
+        # rebind the calls to the copied inputs
+        x, dy = xd, dyd
+        step_calls = calls()
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        bi = xh.numel() * xh.element_size() + (dyh.numel() * dyh.element_size() if backward else 0)
+        bo = yh.numel() * yh.element_size() + 4
+        out["e2e"] = {"value": round(ws * T / (e_ms / K * 1e-3), 1), "unit": UNIT,
+                      "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+                      "ms_per_step": round(e_ms / K, 4)}
+        x, dy = x_saved, dy_saved
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 at N = 1
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_sample_tokens, backward)
+    return out
+
+
+def oracle_sample(wl, inp, n_tok, backward):
+    """float64 inputs of the first n_tok tokens with the full weights."""
+    import dataclasses
+    from oracle import moe_oracle as O
+    sub = dataclasses.replace(wl, T=n_tok)
+    ref = {}
+    for key, v in inp.items():
+        if v is None:
+            ref[key] = None
+        elif key in ("x", "dy"):
+            ref[key] = O.as_f64(v[:n_tok])
+        else:
+            ref[key] = O.as_f64(v)
+    return sub, ref
+
+
+def run_oracle_step(sub, ref, backward):
+    from oracle import moe_oracle as O
+    f = O.layer_forward(sub, ref)
+    if backward:
+        O.layer_backward(sub, ref, f, ref["dy"])
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(wl, inp, n_tok, backward):
+    sub, ref = oracle_sample(wl, inp, n_tok, backward)
+    t0 = time.perf_counter()
+    run_oracle_step(sub, ref, backward)
+    dt = time.perf_counter() - t0
+    return {"value": round(n_tok / dt, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {n_tok} tokens of the workload with all {wl.E} experts' full weights, "
+                      f"{'fwd+bwd' if backward else 'fwd'} in float64 numpy (BLAS threads = cores); "
+                      f"{dt:.2f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, ws, rank):
+    """The float64 CPU oracle on the same workload, a bounded sample per step."""
+    if rank != 0:
+        return None
+    import torch
+    import moe_inputs as mi
+    wl = mi.WORKLOADS[args.workload]
+    backward = wl.backward and not args.fwd_only
+    inp = mi.make_inputs(wl, seed=0, device="cpu", with_dy=backward)
+    n_tok = max(1, args.cpu_sample_tokens // 3)
+    sub, ref = oracle_sample(wl, inp, n_tok, backward)
+    del inp
+    for _ in range(max(args.warmup, 0) and 1):
+        run_oracle_step(sub, ref, backward)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_oracle_step(sub, ref, backward)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
+    value = round(n_tok / dt, 3)
+    sample = (f"first {n_tok} tokens per step with all {wl.E} experts' full weights, "
+              f"{'fwd+bwd' if backward else 'fwd'} in float64 numpy")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(wl, backward), "tokens_per_step": n_tok},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, ws, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = run_ours(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

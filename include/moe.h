@@ -1,0 +1,274 @@
+/*
+ * moe.h — C ABI of libmoe: forward and backward of one token-choice
+ * mixture-of-experts layer on one GB300 (sm_103a).
+ *
+ * The layer, as the source pages state it:
+ *   router     logits = x · W_rᵀ (fp32), scores, top-k, mixing weights
+ *              (The Ultimate MoE Training Handbook, §3.1 "Router scoring")
+ *   dispatch   per-expert histogram, exclusive scan, stable permutation of
+ *              token rows into expert-contiguous order (MoE training cluster:
+ *              routing, load balancing — "Read the timeline before blaming the
+ *              network")
+ *   experts    bias-free SwiGLU FFNs run as one grouped GEMM over the expert
+ *              segments, plus an optional shared expert (Handbook §3.4)
+ *   combine    y[t] = Σ_j w[t,j]·out[row(t,j)] + y_shared[t] (LeCompute,
+ *              "An expert transforms numbers inside the model")
+ *   aux loss   Switch load-balancing loss (Handbook §3.3, "Aux loss")
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named x, w_router, logits, ... are DEVICE pointers unless stated.
+ *    The caller owns every buffer. Apart from a few bytes of device status
+ *    kept for the process, the library allocates nothing: calls that need
+ *    scratch take (ws, ws_bytes), sized by moe_workspace_bytes().
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronises the host. Work whose size depends
+ *    on the routing (the per-expert segments) is scheduled on the device from
+ *    the offsets array, with no copy back to the host.
+ *  - Layouts are row-major and dense. act dtype (cfg->act_dtype) is bf16 or
+ *    fp32 for x, expert weights and every activation; the router (W_r,
+ *    logits, weights w, their gradients) is always fp32; indices are int32.
+ *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code for errors the host
+ *    can see (bad arguments, alignment, a failed launch). Errors only the
+ *    device can see (an expert index out of range, offsets that do not add
+ *    up, a wait that ran out of time) are recorded in a device status word;
+ *    read it with moe_last_device_status(). Kernels never trap: on such an
+ *    error they skip the offending access and record it.
+ *  - Results are deterministic: no floating-point atomics, fixed reduction
+ *    orders, so two runs on the same inputs give identical bytes.
+ *  - Rows must start on 16-byte boundaries: d and every FFN width must be
+ *    multiples of 8 (MOE_ERR_ALIGN otherwise), and every pointer 16-byte
+ *    aligned.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+/* ---- status codes ---- */
+#define MOE_OK                0
+#define MOE_ERR_INVALID_ARG  -1  /* null pointer, bad size, refused configuration  */
+#define MOE_ERR_UNSUPPORTED  -2  /* valid but not built (e.g. k > 8, E > 256)      */
+#define MOE_ERR_ALIGN        -3  /* a row or pointer not 16-byte aligned           */
+#define MOE_ERR_CUDA         -4  /* a CUDA runtime call or launch failed           */
+#define MOE_ERR_TIMEOUT      -5  /* (device) a bounded wait ran out of time        */
+#define MOE_ERR_DEVICE_INDEX -6  /* (device) index / offsets out of range          */
+#define MOE_ERR_WORKSPACE    -7  /* ws_bytes smaller than moe_workspace_bytes()    */
+#define MOE_ERR_NO_DEVICE    -8  /* no usable sm_103 device                        */
+
+/* ---- enumerations ---- */
+#define MOE_SCORE_SOFTMAX 0 /* top-k on logits, softmax over the k chosen     */
+#define MOE_SCORE_SIGMOID 1 /* top-k on sigmoid(l)+bias, renormalised (+1e-20) */
+#define MOE_F32  0
+#define MOE_BF16 1
+
+/* which workspace moe_workspace_bytes() sizes */
+#define MOE_WS_PERMUTE      0
+#define MOE_WS_GROUPED      1
+#define MOE_WS_GROUPED_BWD  2
+#define MOE_WS_AUX          3
+#define MOE_WS_ROUTE_BWD    4
+
+/* Layer configuration. Names follow the flags the Handbook uses for the layer
+ * (§2.5 and §3.4: --num-experts, --moe-ffn-hidden-size, --moe-router-topk,
+ * --moe-shared-expert-intermediate-size, --moe-router-score-function,
+ * --moe-aux-loss-coeff; §3.1 "Output scale": the routed scaling factor). */
+typedef struct {
+  int64_t T;         /* tokens in the micro-batch, >= 0                       */
+  int32_t d;         /* hidden size, multiple of 8                            */
+  int32_t E;         /* routed experts, 1..256                                */
+  int32_t k;         /* experts per token, 1..min(8, E)                       */
+  int32_t F;         /* routed expert FFN width, multiple of 8                */
+  int32_t F_shared;  /* shared expert FFN width (multiple of 8), 0 = none     */
+  int32_t score_fn;  /* MOE_SCORE_SOFTMAX | MOE_SCORE_SIGMOID                 */
+  int32_t act_dtype; /* MOE_BF16 | MOE_F32                                    */
+  float scaling;     /* routed scaling factor (1.0 = none)                    */
+  float aux_coeff;   /* Switch aux-loss coefficient                           */
+} moe_cfg;
+
+/* Validates cfg the way the Handbook says Megatron does: softmax with top-1
+ * and renormalisation is refused (§3.1 "Output scale": the router would get
+ * no gradient); k <= E. Returns MOE_OK or an error code. */
+int moe_check_cfg(const moe_cfg* cfg);
+
+/* ------------------------------------------------------------------------ *
+ * S1 + S2. Router: gate GEMM, scores, sorted top-k, mixing weights.
+ * Handbook §3.1 "Router scoring" ("Precision": logits = x·W_rᵀ in fp32 from
+ * the [E, d] fp32 router weight; "Gating function": softmax selects on the
+ * logits and takes the softmax over the k chosen; sigmoid selects on
+ * sigmoid(l) + sel_bias and divides the chosen scores by their sum + 1e-20;
+ * "Output scale": times the routed scaling factor) and §3.2 "Who selects"
+ * (top-k sorted while training).
+ *   x          [T, d] act dtype
+ *   w_router   [E, d] fp32
+ *   logit_bias [E] fp32 or NULL: added to the logits (moves selection AND
+ *              weights; used for a fixed per-expert skew of the logits)
+ *   sel_bias   [E] fp32 or NULL: the aux-loss-free expert bias, added to the
+ *              sigmoid scores for selection only (Handbook §3.3 "Loss-free
+ *              bias"); refused with softmax (MOE_ERR_INVALID_ARG)
+ *   logits     [T, E] fp32 out (kept for the backward and the aux loss)
+ *   idx        [T, k] int32 out, by descending key; equal keys: lower index
+ *   w          [T, k] fp32 out
+ * The logits are accumulated with compensated fp32 sums, so their error is
+ * far below the 1e-6 gap that separates a decided top-k from a near tie.   */
+int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
+                   const float* logit_bias, const float* sel_bias, float* logits,
+                   int32_t* idx, float* w, moe_stream_t stream);
+
+/* S3. Dispatch: counts[e] = #{(t,j): idx[t,j] = e}; offsets = exclusive scan
+ * (offsets[E] = T·k); stable permutation row(t,j) = offsets[e] +
+ * #{t' < t : t' chose e}; x_perm[row(t,j)] = x[t]. LeCompute, "Four GPUs, with
+ * one holding up the group" (counts over the T·k assignments) and "Read the
+ * timeline before blaming the network" (grouping rows by expert).
+ *   idx      [T, k] int32 (each entry in [0, E); an entry out of range is
+ *            skipped and recorded as MOE_ERR_DEVICE_INDEX)
+ *   counts   [E] int32 out;  offsets [E+1] int32 out
+ *   row_of   [T, k] int32 out;  src_tok [T·k] int32 out
+ *   x_perm   [T·k, d] act dtype out
+ *   ws       >= moe_workspace_bytes(cfg, MOE_WS_PERMUTE) bytes of scratch  */
+int moe_permute(const moe_cfg* cfg, const void* x, const int32_t* idx, int32_t* counts,
+                int32_t* offsets, int32_t* row_of, int32_t* src_tok, void* x_perm,
+                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* S4 + S5. Grouped SwiGLU experts: for group g and its rows r in
+ * [offsets[g], offsets[g+1]):  [gate | up] = x_rows[r]·W1_gᵀ,
+ * h[r] = silu(gate)·up,  out[r] = h[r]·W2_gᵀ. Handbook §3.4 "Count and size"
+ * (fc1 is 2F wide, fc2 maps F back to d) and "Activation" (the first half of
+ * fc1's output is the gate). One launch covers all groups; the tile schedule
+ * is built on the device from `offsets`. Used for the routed experts
+ * (n_groups = E, offsets from moe_permute) and the shared expert (n_groups = 1,
+ * offsets = NULL meaning one group of n_rows rows).
+ *   n_groups  groups (experts), n_rows total rows (= offsets[n_groups])
+ *   F         FFN width of these experts (cfg->F or cfg->F_shared)
+ *   offsets   [n_groups+1] int32 device, or NULL when n_groups == 1
+ *   x_rows    [n_rows, d] act dtype
+ *   w1        [n_groups, 2F, d] act dtype (rows [0,F) gate, [F,2F) up)
+ *   w2        [n_groups, d, F] act dtype
+ *   pre_gu    [n_rows, 2F] act dtype out (gate | up, kept for the backward),
+ *             or NULL (forward only)
+ *   h         [n_rows, F] act dtype out
+ *   out       [n_rows, d] act dtype out
+ * Rows are computed with fp32 accumulation (bf16: tcgen05 tensor cores; fp32:
+ * CUDA cores). */
+int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int32_t F,
+                       const int32_t* offsets, const void* x_rows, const void* w1,
+                       const void* w2, void* pre_gu, void* h, void* out, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* S6. Weighted unpermute-combine: y[t] = Σ_{j<k} w[t,j]·out_perm[row_of[t,j]]
+ * (+ shared_out[t]), accumulated in fp32 in j order, then rounded once.
+ * LeCompute, "An expert transforms numbers inside the model"; Handbook §3.4
+ * "Shared experts" (shared output added at weight 1).
+ *   out_perm [T·k, d], shared_out [T, d] or NULL, y [T, d] out: act dtype  */
+int moe_unpermute_combine(const moe_cfg* cfg, const void* out_perm, const int32_t* row_of,
+                          const float* w, const void* shared_out, void* y,
+                          moe_stream_t stream);
+
+/* S7. Switch load-balancing loss (Handbook §3.3 "Aux loss"):
+ * aux = coeff · E / (k · T²) · Σ_e counts[e] · Σ_t P[t,e], with P the softmax
+ * of each token's logits over all E experts (sigmoid scores: s / Σ_e s).
+ *   logits [T, E] fp32, counts [E] int32, aux: one fp32 on the device, out.
+ *   ws >= moe_workspace_bytes(cfg, MOE_WS_AUX) bytes of scratch            */
+int moe_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* counts,
+                 float* aux, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------- backward ---------------------------------- */
+
+/* B6. Backward of the combine: d_out_perm[row_of[t,j]] = w[t,j]·dy[t];
+ * dw[t,j] = <dy[t], out_perm[row_of[t,j]]> (fp32). The shared expert's
+ * upstream gradient is dy itself.
+ *   dy [T, d], out_perm [T·k, d], d_out_perm [T·k, d] out: act dtype;
+ *   dw [T, k] fp32 out                                                      */
+int moe_unpermute_combine_bwd(const moe_cfg* cfg, const void* dy, const void* out_perm,
+                              const int32_t* row_of, const float* w, void* d_out_perm,
+                              float* dw, moe_stream_t stream);
+
+/* B5 + B4. Backward of moe_grouped_swiglu for the same groups:
+ *   dh = d_out·W2_g;  d_pre = [dh·up·σ(g)(1+g(1-σ(g))) | dh·silu(g)];
+ *   dx_rows = d_pre·W1_g;  dW2_g = d_outᵀ·h;  dW1_g = d_preᵀ·x_rows.
+ * A group with no rows gets dW1_g = dW2_g = 0.
+ *   pre_gu [n_rows, 2F] and h [n_rows, F] from the forward; d_out [n_rows, d]
+ *   d_pre [n_rows, 2F] act dtype out; dx_rows [n_rows, d] act dtype out;
+ *   dw1 [n_groups, 2F, d], dw2 [n_groups, d, F] act dtype out (fp32 sums).
+ *   ws >= moe_workspace_bytes(cfg, MOE_WS_GROUPED_BWD)                     */
+int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows,
+                           int32_t F, const int32_t* offsets, const void* x_rows,
+                           const void* w1, const void* w2, const void* pre_gu,
+                           const void* h, const void* d_out, void* d_pre, void* dx_rows,
+                           void* dw1, void* dw2, void* ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/* B7. Gradient of the aux loss w.r.t. the logits, counts held constant:
+ * dP[e] = g_aux·coeff·E·counts[e]/(k·T²); softmax: d_l = P ⊙ (dP − <P,dP>);
+ * sigmoid (P = s/S): d_l = (dP − <P,dP>)/S ⊙ s(1−s).
+ *   d_logits [T, E] fp32: written (accumulate = 0) or added to (= 1).      */
+int moe_aux_loss_bwd(const moe_cfg* cfg, const float* logits, const int32_t* counts,
+                     float g_aux, float* d_logits, int32_t accumulate, moe_stream_t stream);
+
+/* B2 + B1/B3. Router backward. From dw (gradient of the mixing weights):
+ *   softmax: p = softmax(chosen logits), d_l_chosen = p ⊙ (c·dw − <p, c·dw>);
+ *   sigmoid: d_s = c·(dw − <dw,s>/S)/S (k > 1; c·dw for k = 1), d_l = d_s·s(1−s);
+ * zero for experts not chosen; the selection bias gets no gradient (c = the
+ * routed scaling factor, S = Σ chosen s + 1e-20). Then, with the full
+ * d_logits (this part plus whatever d_logits already holds when
+ * accumulate = 1, e.g. the aux-loss part):
+ *   dx_router = d_logits · W_r   ([T, d] fp32 out)
+ *   dw_router = d_logitsᵀ · x    ([E, d] fp32 out)
+ *   ws >= moe_workspace_bytes(cfg, MOE_WS_ROUTE_BWD)                       */
+int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
+                       const float* logits, const int32_t* idx, const float* dw,
+                       float* d_logits, int32_t accumulate, float* dx_router,
+                       float* dw_router, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* B1. Backward of the permutation, fused with the other input gradients:
+ * dx[t] = Σ_j dx_perm[row_of[t,j]] (+ dx_router[t]) (+ dx_shared[t]), summed
+ * in fp32 and rounded once to the act dtype.
+ *   dx_perm [T·k, d] act dtype; dx_router [T, d] fp32 or NULL;
+ *   dx_shared [T, d] act dtype or NULL; dx [T, d] act dtype out            */
+int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_of,
+                    const float* dx_router, const void* dx_shared, void* dx,
+                    moe_stream_t stream);
+
+/* ---------------------------- utilities --------------------------------- */
+
+/* Bytes of scratch the call `which` (MOE_WS_*) needs for cfg. For
+ * MOE_WS_GROUPED / MOE_WS_GROUPED_BWD the size covers the routed experts
+ * (T·k rows, F) and the shared expert (T rows, F_shared). 0 on bad input. */
+size_t moe_workspace_bytes(const moe_cfg* cfg, int which);
+
+/* Static English text for a status code. */
+const char* moe_status_string(int status);
+
+/* Synchronises `stream`, returns the first device-detected error recorded
+ * on the current device since the previous call (MOE_OK if none) and clears
+ * it. `detail` (may be NULL) receives the offending index or a site code. */
+int moe_last_device_status(moe_stream_t stream, int32_t* detail);
+
+/* Upper bound, in nanoseconds, of every spin-wait inside the kernels
+ * (default 2e9). A wait that runs out records MOE_ERR_TIMEOUT and its kernel
+ * returns after releasing what it holds. Returns the previous value. */
+uint64_t moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Launches one kernel that waits for a device flag nothing ever sets, with
+ * the current timeout; used to test that bounded waits end and report
+ * MOE_ERR_TIMEOUT (read it with moe_last_device_status). */
+int moe_selftest_wait_timeout(moe_stream_t stream);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * devices, all streams), counted on the host at launch time. */
+uint64_t moe_launch_count(void);
+
+/* Library build identification: "libmoe <version> sm_103a". */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,238 @@
+"""ctypes binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function here has the name of the C entry point without the ``moe_``
+prefix, takes torch tensors (device memory from PyTorch) or None, checks that
+they are contiguous and on the current device, and calls the C function on the
+current torch stream. All arithmetic runs in the library's CUDA kernels; there
+is no Python or CPU fallback: if libmoe.so is missing or fails to load, the
+import raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_ALIGN = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+MOE_ERR_DEVICE_INDEX = -6
+MOE_ERR_WORKSPACE = -7
+MOE_ERR_NO_DEVICE = -8
+
+MOE_SCORE_SOFTMAX = 0
+MOE_SCORE_SIGMOID = 1
+MOE_F32 = 0
+MOE_BF16 = 1
+
+MOE_WS_PERMUTE = 0
+MOE_WS_GROUPED = 1
+MOE_WS_GROUPED_BWD = 2
+MOE_WS_AUX = 3
+MOE_WS_ROUTE_BWD = 4
+
+
+class MoeCfg(ctypes.Structure):
+    _fields_ = [("T", c_int64), ("d", c_int32), ("E", c_int32), ("k", c_int32),
+                ("F", c_int32), ("F_shared", c_int32), ("score_fn", c_int32),
+                ("act_dtype", c_int32), ("scaling", c_float), ("aux_coeff", c_float)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {code} ({status_string(code)})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libmoe.so is not built ({LIB_PATH}); run __graft_entry__.build() or "
+            "python -m routing_grouped_expert_gate_gb300.build")
+    return ctypes.CDLL(LIB_PATH)
+
+
+lib = _load()
+
+_VP = c_void_p
+_SIGS = {
+    "moe_check_cfg": (c_int, [POINTER(MoeCfg)]),
+    "moe_route_topk": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_permute": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
+    "moe_grouped_swiglu": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP, _VP,
+                                   _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
+    "moe_unpermute_combine": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_aux_loss": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, c_size_t, _VP]),
+    "moe_unpermute_combine_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_grouped_swiglu_bwd": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP,
+                                       _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                       c_size_t, _VP]),
+    "moe_aux_loss_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, c_float, _VP, c_int32, _VP]),
+    "moe_route_topk_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, c_int32, _VP,
+                                   _VP, _VP, c_size_t, _VP]),
+    "moe_permute_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_workspace_bytes": (c_size_t, [POINTER(MoeCfg), c_int]),
+    "moe_status_string": (c_char_p, [c_int]),
+    "moe_last_device_status": (c_int, [_VP, POINTER(c_int32)]),
+    "moe_set_wait_timeout_ns": (c_uint64, [c_uint64]),
+    "moe_selftest_wait_timeout": (c_int, [_VP]),
+    "moe_version": (c_char_p, []),
+    "moe_launch_count": (c_uint64, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+# ------------------------------------------------------------------ helpers
+
+def status_string(code: int) -> str:
+    return lib.moe_status_string(code).decode()
+
+
+def launch_count() -> int:
+    return int(lib.moe_launch_count())
+
+
+def version() -> str:
+    return lib.moe_version().decode()
+
+
+def make_cfg(T, d, E, k, F, F_shared=0, score="softmax", act_dtype="bf16", scaling=1.0,
+             aux_coeff=1e-3) -> MoeCfg:
+    return MoeCfg(T=T, d=d, E=E, k=k, F=F, F_shared=F_shared,
+                  score_fn=MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID,
+                  act_dtype=MOE_BF16 if act_dtype == "bf16" else MOE_F32,
+                  scaling=scaling, aux_coeff=aux_coeff)
+
+
+def cfg_from_workload(wl, T: Optional[int] = None) -> MoeCfg:
+    return make_cfg(wl.T if T is None else T, wl.d, wl.E, wl.k, wl.F, wl.F_shared, wl.score,
+                    wl.act_dtype, wl.scaling, wl.aux_coeff)
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    if t.device.type != "cuda":
+        raise ValueError("libmoe takes device tensors")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def check_cfg(cfg: MoeCfg) -> int:
+    return lib.moe_check_cfg(ctypes.byref(cfg))
+
+
+def workspace_bytes(cfg: MoeCfg, which: int) -> int:
+    return int(lib.moe_workspace_bytes(ctypes.byref(cfg), which))
+
+
+def last_device_status(stream=None):
+    detail = c_int32(0)
+    rc = lib.moe_last_device_status(_stream(stream), ctypes.byref(detail))
+    return rc, detail.value
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    return int(lib.moe_set_wait_timeout_ns(ns))
+
+
+def selftest_wait_timeout(stream=None):
+    _check(lib.moe_selftest_wait_timeout(_stream(stream)), "moe_selftest_wait_timeout")
+
+
+# ------------------------------------------------------------------ entry points
+
+def route_topk(cfg, x, w_router, logit_bias, sel_bias, logits, idx, w, stream=None):
+    _check(lib.moe_route_topk(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias),
+                              _p(sel_bias), _p(logits), _p(idx), _p(w), _stream(stream)),
+           "moe_route_topk")
+
+
+def permute(cfg, x, idx, counts, offsets, row_of, src_tok, x_perm, ws, stream=None):
+    _check(lib.moe_permute(ctypes.byref(cfg), _p(x), _p(idx), _p(counts), _p(offsets),
+                           _p(row_of), _p(src_tok), _p(x_perm), _p(ws),
+                           0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_permute")
+
+
+def grouped_swiglu(cfg, n_groups, n_rows, F, offsets, x_rows, w1, w2, pre_gu, h, out, ws,
+                   stream=None):
+    _check(lib.moe_grouped_swiglu(ctypes.byref(cfg), n_groups, n_rows, F, _p(offsets),
+                                  _p(x_rows), _p(w1), _p(w2), _p(pre_gu), _p(h), _p(out), _p(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(),
+                                  _stream(stream)),
+           "moe_grouped_swiglu")
+
+
+def unpermute_combine(cfg, out_perm, row_of, w, shared_out, y, stream=None):
+    _check(lib.moe_unpermute_combine(ctypes.byref(cfg), _p(out_perm), _p(row_of), _p(w),
+                                     _p(shared_out), _p(y), _stream(stream)),
+           "moe_unpermute_combine")
+
+
+def aux_loss(cfg, logits, counts, aux, ws, stream=None):
+    _check(lib.moe_aux_loss(ctypes.byref(cfg), _p(logits), _p(counts), _p(aux), _p(ws),
+                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_aux_loss")
+
+
+def unpermute_combine_bwd(cfg, dy, out_perm, row_of, w, d_out_perm, dw, stream=None):
+    _check(lib.moe_unpermute_combine_bwd(ctypes.byref(cfg), _p(dy), _p(out_perm), _p(row_of),
+                                         _p(w), _p(d_out_perm), _p(dw), _stream(stream)),
+           "moe_unpermute_combine_bwd")
+
+
+def grouped_swiglu_bwd(cfg, n_groups, n_rows, F, offsets, x_rows, w1, w2, pre_gu, h, d_out,
+                       d_pre, dx_rows, dw1, dw2, ws, stream=None):
+    _check(lib.moe_grouped_swiglu_bwd(ctypes.byref(cfg), n_groups, n_rows, F, _p(offsets),
+                                      _p(x_rows), _p(w1), _p(w2), _p(pre_gu), _p(h), _p(d_out),
+                                      _p(d_pre), _p(dx_rows), _p(dw1), _p(dw2), _p(ws),
+                                      0 if ws is None else ws.numel() * ws.element_size(),
+                                      _stream(stream)),
+           "moe_grouped_swiglu_bwd")
+
+
+def aux_loss_bwd(cfg, logits, counts, g_aux, d_logits, accumulate, stream=None):
+    _check(lib.moe_aux_loss_bwd(ctypes.byref(cfg), _p(logits), _p(counts), float(g_aux),
+                                _p(d_logits), int(accumulate), _stream(stream)),
+           "moe_aux_loss_bwd")
+
+
+def route_topk_bwd(cfg, x, w_router, logits, idx, dw, d_logits, accumulate, dx_router,
+                   dw_router, ws, stream=None):
+    _check(lib.moe_route_topk_bwd(ctypes.byref(cfg), _p(x), _p(w_router), _p(logits), _p(idx),
+                                  _p(dw), _p(d_logits), int(accumulate), _p(dx_router),
+                                  _p(dw_router), _p(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(),
+                                  _stream(stream)),
+           "moe_route_topk_bwd")
+
+
+def permute_bwd(cfg, dx_perm, row_of, dx_router, dx_shared, dx, stream=None):
+    _check(lib.moe_permute_bwd(ctypes.byref(cfg), _p(dx_perm), _p(row_of), _p(dx_router),
+                               _p(dx_shared), _p(dx), _stream(stream)),
+           "moe_permute_bwd")

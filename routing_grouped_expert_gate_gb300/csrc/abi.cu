@@ -1,0 +1,463 @@
+// The extern "C" entry points declared in include/moe.h: argument checks,
+// the device status word, workspace sizing, and the order in which each call
+// launches its kernels on the caller's stream.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// status[0] = first error code, status[1] = detail, status[2] = a flag nothing sets
+__device__ int g_status[4];
+
+static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+static std::atomic<uint64_t> g_launches{0};
+
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_dev_mu;
+static int* g_status_ptr[kMaxDevices];
+static int g_sm_count[kMaxDevices];
+
+static int make_ctx(cudaStream_t stream, Ctx* c) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return MOE_ERR_NO_DEVICE;  // built for sm_103a only
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    g_sm_count[dev] = sms;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  c->stream = stream;
+  c->status = g_status_ptr[dev];
+  c->timeout_ns = g_timeout_ns.load();
+  c->sm_count = g_sm_count[dev];
+  return MOE_OK;
+}
+
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_cfg(const moe_cfg* cfg) {
+  if (cfg == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->T < 0 || cfg->d <= 0 || cfg->E <= 0 || cfg->k <= 0 || cfg->F <= 0 ||
+      cfg->F_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->act_dtype != MOE_F32 && cfg->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (cfg->k > cfg->E) return MOE_ERR_INVALID_ARG;
+  // The Ultimate MoE Training Handbook, §3.1 "Output scale": softmax over a
+  // single chosen logit is always 1, so top-1 softmax with renormalisation
+  // gives the router no gradient and is refused.
+  if (cfg->score_fn == MOE_SCORE_SOFTMAX && cfg->k == 1) return MOE_ERR_INVALID_ARG;
+  if (cfg->E > kMaxE || cfg->k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if ((cfg->d & 7) || (cfg->F & 7) || (cfg->F_shared & 7)) return MOE_ERR_ALIGN;
+  if (cfg->T * (int64_t)cfg->k >= (int64_t)0x7fffffff) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static int act_size(const moe_cfg& cfg) { return cfg.act_dtype == MOE_BF16 ? 2 : 4; }
+
+#define MOE_REQUIRE(cond, code) \
+  do {                           \
+    if (!(cond)) return (code);  \
+  } while (0)
+#define MOE_PTR(p) MOE_REQUIRE((p) != nullptr, MOE_ERR_INVALID_ARG); MOE_REQUIRE(aligned16(p), MOE_ERR_ALIGN)
+#define MOE_OPT_PTR(p) MOE_REQUIRE((p) == nullptr || aligned16(p), MOE_ERR_ALIGN)
+#define MOE_CHECK_CFG(cfg)               \
+  do {                                   \
+    const int _rc = check_cfg(cfg);      \
+    if (_rc != MOE_OK) return _rc;       \
+  } while (0)
+#define MOE_CTX(stream, ctx)                                   \
+  Ctx ctx;                                                     \
+  do {                                                         \
+    const int _rc = make_ctx((cudaStream_t)(stream), &ctx);    \
+    if (_rc != MOE_OK) return _rc;                             \
+  } while (0)
+#define MOE_LAUNCH(expr)                          \
+  do {                                            \
+    const cudaError_t _e = (expr);                \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;   \
+  } while (0)
+
+static int route_bwd_splits(const moe_cfg& cfg) {
+  int64_t s = (cfg.T + 511) / 512;
+  if (s < 1) s = 1;
+  if (s > 32) s = 32;
+  return (int)s;
+}
+
+static size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+static size_t grouped_fwd_ws(const moe_cfg& cfg) {
+  const size_t es = (size_t)act_size(cfg);
+  size_t rows_r = (size_t)cfg.T * cfg.k, rows_s = (size_t)cfg.T;
+  size_t need = round256(rows_r * 2 * cfg.F * es);  // gate|up when the caller passes none
+  if (cfg.F_shared > 0) {
+    const size_t s = round256(rows_s * 2 * cfg.F_shared * es);
+    if (s > need) need = s;
+  }
+  return need + round256(tc_grouped_ws_bytes(cfg.E));
+}
+
+static size_t grouped_bwd_ws(const moe_cfg& cfg) {
+  size_t rows_r = (size_t)cfg.T * cfg.k, rows_s = (size_t)cfg.T;
+  size_t need = round256(rows_r * cfg.F * sizeof(float));  // dh in fp32
+  if (cfg.F_shared > 0) {
+    const size_t s = round256(rows_s * cfg.F_shared * sizeof(float));
+    if (s > need) need = s;
+  }
+  return need + round256(tc_grouped_ws_bytes(cfg.E));
+}
+
+static size_t route_bwd_ws(const moe_cfg& cfg) {
+  return round256((size_t)route_bwd_splits(cfg) * cfg.E * cfg.d * sizeof(float));
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_check_cfg(const moe_cfg* cfg) { return check_cfg(cfg); }
+
+const char* moe_version(void) { return "libmoe 0.1 sm_103a"; }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument or refused configuration";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size (E <= 256, k <= 8, T*k < 2^31)";
+    case MOE_ERR_ALIGN: return "row or pointer not 16-byte aligned (d, F must be multiples of 8)";
+    case MOE_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait ran out of time";
+    case MOE_ERR_DEVICE_INDEX: return "device saw an index or offset out of range";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
+
+uint64_t moe_launch_count(void) { return launches_so_far(); }
+
+int moe_last_device_status(moe_stream_t stream, int32_t* detail) {
+  MOE_CTX(stream, c);
+  if (cudaStreamSynchronize(c.stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, c.status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(c.status, 0, 2 * sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return h[0];
+}
+
+size_t moe_workspace_bytes(const moe_cfg* cfg, int which) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  switch (which) {
+    case MOE_WS_PERMUTE: return permute_ws_bytes(*cfg);
+    case MOE_WS_GROUPED: return grouped_fwd_ws(*cfg);
+    case MOE_WS_GROUPED_BWD: return grouped_bwd_ws(*cfg);
+    case MOE_WS_AUX: return aux_ws_bytes(*cfg);
+    case MOE_WS_ROUTE_BWD: return route_bwd_ws(*cfg);
+    default: return 0;
+  }
+}
+
+int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
+                   const float* logit_bias, const float* sel_bias, float* logits, int32_t* idx,
+                   float* w, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (sel_bias != nullptr && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(x); MOE_PTR(w_router); MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(w);
+  MOE_REQUIRE(logit_bias == nullptr || (reinterpret_cast<uintptr_t>(logit_bias) & 3u) == 0, MOE_ERR_ALIGN);
+  MOE_REQUIRE(sel_bias == nullptr || (reinterpret_cast<uintptr_t>(sel_bias) & 3u) == 0, MOE_ERR_ALIGN);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_router_logits(c, *cfg, x, w_router, logit_bias, logits));
+  MOE_LAUNCH(launch_router_topk(c, *cfg, logits, sel_bias, idx, w));
+  return MOE_OK;
+}
+
+int moe_permute(const moe_cfg* cfg, const void* x, const int32_t* idx, int32_t* counts,
+                int32_t* offsets, int32_t* row_of, int32_t* src_tok, void* x_perm, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(counts); MOE_PTR(offsets);
+  if (cfg->T > 0) {
+    MOE_PTR(x); MOE_PTR(idx); MOE_PTR(row_of); MOE_PTR(src_tok); MOE_PTR(x_perm); MOE_PTR(ws);
+  }
+  MOE_REQUIRE(ws_bytes >= permute_ws_bytes(*cfg), MOE_ERR_WORKSPACE);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_permute(c, *cfg, x, idx, counts, offsets, row_of, src_tok, x_perm, ws));
+  return MOE_OK;
+}
+
+int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int32_t F,
+                       const int32_t* offsets, const void* x_rows, const void* w1,
+                       const void* w2, void* pre_gu, void* h, void* out, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(n_groups >= 1 && n_groups <= kMaxE && n_rows >= 0 && F > 0, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE((F & 7) == 0, MOE_ERR_ALIGN);
+  MOE_REQUIRE(offsets != nullptr || n_groups == 1, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE(n_rows < (int64_t)0x7fffffff, MOE_ERR_UNSUPPORTED);
+  MOE_PTR(w1); MOE_PTR(w2); MOE_OPT_PTR(pre_gu); MOE_OPT_PTR(offsets);
+  if (n_rows > 0) { MOE_PTR(x_rows); MOE_PTR(h); MOE_PTR(out); }
+  MOE_CTX(stream, c);
+  if (n_rows == 0) return MOE_OK;
+  const int dt = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
+  const int d = cfg->d;
+  if (dt == kBF16 && tc_available()) {
+    MOE_REQUIRE(ws_bytes >= round256(tc_grouped_ws_bytes(n_groups)), MOE_ERR_WORKSPACE);
+    MOE_REQUIRE(ws != nullptr || tc_grouped_ws_bytes(n_groups) == 0, MOE_ERR_INVALID_ARG);
+    int err = MOE_OK;
+    MOE_LAUNCH(launch_tc_grouped_swiglu_fwd(c, n_groups, n_rows, F, d, offsets, x_rows, w1, w2,
+                                            pre_gu, h, out, ws, &err));
+    return err;
+  }
+  void* pre = pre_gu;
+  if (pre == nullptr) {
+    MOE_PTR(ws);
+    MOE_REQUIRE(ws_bytes >= round256((size_t)n_rows * 2 * F * act_size(*cfg)), MOE_ERR_WORKSPACE);
+    pre = ws;
+  }
+  SimtGemm g1{};
+  g1.mode = kGroupM; g1.M = (int)n_rows; g1.N = 2 * F; g1.K = d;
+  g1.dtA = g1.dtB = g1.dtC = dt;
+  g1.A = x_rows; g1.a_sm = d; g1.a_sk = 1; g1.a_sg = 0;
+  g1.B = w1; g1.b_sn = d; g1.b_sk = 1; g1.b_sg = (int64_t)2 * F * d;
+  g1.C = pre; g1.c_sm = 2 * F; g1.c_sg = 0;
+  g1.offsets = offsets; g1.n_groups = n_groups; g1.alpha = 1.f;
+  MOE_LAUNCH(launch_simt_gemm(c, g1));
+  MOE_LAUNCH(launch_swiglu_fwd_elem(c, dt, pre, h, n_rows, F));
+  SimtGemm g2{};
+  g2.mode = kGroupM; g2.M = (int)n_rows; g2.N = d; g2.K = F;
+  g2.dtA = g2.dtB = g2.dtC = dt;
+  g2.A = h; g2.a_sm = F; g2.a_sk = 1;
+  g2.B = w2; g2.b_sn = F; g2.b_sk = 1; g2.b_sg = (int64_t)d * F;
+  g2.C = out; g2.c_sm = d;
+  g2.offsets = offsets; g2.n_groups = n_groups; g2.alpha = 1.f;
+  MOE_LAUNCH(launch_simt_gemm(c, g2));
+  return MOE_OK;
+}
+
+int moe_unpermute_combine(const moe_cfg* cfg, const void* out_perm, const int32_t* row_of,
+                          const float* w, const void* shared_out, void* y, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(out_perm); MOE_PTR(row_of); MOE_PTR(w); MOE_PTR(y); MOE_OPT_PTR(shared_out);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_combine(c, *cfg, out_perm, row_of, w, shared_out, y));
+  return MOE_OK;
+}
+
+int moe_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* counts, float* aux,
+                 void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(counts); MOE_PTR(ws);
+  MOE_REQUIRE(aux != nullptr && (reinterpret_cast<uintptr_t>(aux) & 3u) == 0, MOE_ERR_INVALID_ARG);
+  if (cfg->T > 0) MOE_PTR(logits);
+  MOE_REQUIRE(ws_bytes >= aux_ws_bytes(*cfg), MOE_ERR_WORKSPACE);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_aux_loss(c, *cfg, logits, counts, aux, ws));
+  return MOE_OK;
+}
+
+int moe_unpermute_combine_bwd(const moe_cfg* cfg, const void* dy, const void* out_perm,
+                              const int32_t* row_of, const float* w, void* d_out_perm, float* dw,
+                              moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(dy); MOE_PTR(out_perm); MOE_PTR(row_of); MOE_PTR(w); MOE_PTR(d_out_perm); MOE_PTR(dw);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_combine_bwd(c, *cfg, dy, out_perm, row_of, w, d_out_perm, dw));
+  return MOE_OK;
+}
+
+int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int32_t F,
+                           const int32_t* offsets, const void* x_rows, const void* w1,
+                           const void* w2, const void* pre_gu, const void* h, const void* d_out,
+                           void* d_pre, void* dx_rows, void* dw1, void* dw2, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(n_groups >= 1 && n_groups <= kMaxE && n_rows >= 0 && F > 0, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE((F & 7) == 0, MOE_ERR_ALIGN);
+  MOE_REQUIRE(offsets != nullptr || n_groups == 1, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE(n_rows < (int64_t)0x7fffffff, MOE_ERR_UNSUPPORTED);
+  MOE_PTR(w1); MOE_PTR(w2); MOE_PTR(dw1); MOE_PTR(dw2); MOE_OPT_PTR(offsets);
+  if (n_rows > 0) {
+    MOE_PTR(x_rows); MOE_PTR(pre_gu); MOE_PTR(h); MOE_PTR(d_out); MOE_PTR(d_pre); MOE_PTR(dx_rows);
+    MOE_PTR(ws);
+  }
+  const size_t need_dh = round256((size_t)n_rows * F * sizeof(float));
+  MOE_CTX(stream, c);
+  const int dt = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
+  const int d = cfg->d;
+  if (dt == kBF16 && tc_available()) {
+    MOE_REQUIRE(ws_bytes >= round256(tc_grouped_ws_bytes(n_groups)), MOE_ERR_WORKSPACE);
+    int err = MOE_OK;
+    MOE_LAUNCH(launch_tc_grouped_swiglu_bwd(c, n_groups, n_rows, F, d, offsets, x_rows, w1, w2,
+                                            pre_gu, h, d_out, d_pre, dx_rows, dw1, dw2, ws,
+                                            &err));
+    return err;
+  }
+  MOE_REQUIRE(ws_bytes >= need_dh, MOE_ERR_WORKSPACE);
+  float* dh = static_cast<float*>(ws);
+  if (n_rows > 0) {
+    SimtGemm a{};  // dh = d_out · W2_g      [rows, F]
+    a.mode = kGroupM; a.M = (int)n_rows; a.N = F; a.K = d;
+    a.dtA = dt; a.dtB = dt; a.dtC = kF32;
+    a.A = d_out; a.a_sm = d; a.a_sk = 1;
+    a.B = w2; a.b_sn = 1; a.b_sk = F; a.b_sg = (int64_t)d * F;
+    a.C = dh; a.c_sm = F;
+    a.offsets = offsets; a.n_groups = n_groups; a.alpha = 1.f;
+    MOE_LAUNCH(launch_simt_gemm(c, a));
+    MOE_LAUNCH(launch_swiglu_bwd_elem(c, dt, dh, pre_gu, d_pre, n_rows, F));
+    SimtGemm b{};  // dx_rows = d_pre · W1_g [rows, d]
+    b.mode = kGroupM; b.M = (int)n_rows; b.N = d; b.K = 2 * F;
+    b.dtA = b.dtB = b.dtC = dt;
+    b.A = d_pre; b.a_sm = 2 * F; b.a_sk = 1;
+    b.B = w1; b.b_sn = 1; b.b_sk = d; b.b_sg = (int64_t)2 * F * d;
+    b.C = dx_rows; b.c_sm = d;
+    b.offsets = offsets; b.n_groups = n_groups; b.alpha = 1.f;
+    MOE_LAUNCH(launch_simt_gemm(c, b));
+  }
+  SimtGemm w2g{};  // dW2_g = d_outᵀ · h   [d, F] per group, K = the group's rows
+  w2g.mode = kGroupK; w2g.M = d; w2g.N = F; w2g.K = (int)n_rows;
+  w2g.dtA = w2g.dtB = w2g.dtC = dt;
+  w2g.A = d_out; w2g.a_sm = 1; w2g.a_sk = d;
+  w2g.B = h; w2g.b_sn = 1; w2g.b_sk = F;
+  w2g.C = dw2; w2g.c_sm = F; w2g.c_sg = (int64_t)d * F;
+  w2g.offsets = offsets; w2g.n_groups = n_groups; w2g.alpha = 1.f;
+  MOE_LAUNCH(launch_simt_gemm(c, w2g));
+  SimtGemm w1g{};  // dW1_g = d_preᵀ · x_rows [2F, d] per group
+  w1g.mode = kGroupK; w1g.M = 2 * F; w1g.N = d; w1g.K = (int)n_rows;
+  w1g.dtA = w1g.dtB = w1g.dtC = dt;
+  w1g.A = d_pre; w1g.a_sm = 1; w1g.a_sk = 2 * F;
+  w1g.B = x_rows; w1g.b_sn = 1; w1g.b_sk = d;
+  w1g.C = dw1; w1g.c_sm = d; w1g.c_sg = (int64_t)2 * F * d;
+  w1g.offsets = offsets; w1g.n_groups = n_groups; w1g.alpha = 1.f;
+  MOE_LAUNCH(launch_simt_gemm(c, w1g));
+  return MOE_OK;
+}
+
+int moe_aux_loss_bwd(const moe_cfg* cfg, const float* logits, const int32_t* counts, float g_aux,
+                     float* d_logits, int32_t accumulate, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(counts);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(logits); MOE_PTR(d_logits);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_aux_loss_bwd(c, *cfg, logits, counts, g_aux, d_logits, accumulate));
+  return MOE_OK;
+}
+
+int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
+                       const float* logits, const int32_t* idx, const float* dw, float* d_logits,
+                       int32_t accumulate, float* dx_router, float* dw_router, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(w_router); MOE_PTR(dw_router); MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= route_bwd_ws(*cfg), MOE_ERR_WORKSPACE);
+  if (cfg->T > 0) {
+    MOE_PTR(x); MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(dw); MOE_PTR(d_logits); MOE_PTR(dx_router);
+  }
+  MOE_CTX(stream, c);
+  const int dtx = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
+  const int T = (int)cfg->T, E = cfg->E, d = cfg->d;
+  MOE_LAUNCH(launch_router_scores_bwd(c, *cfg, logits, idx, dw, d_logits, accumulate));
+  if (T > 0) {
+    SimtGemm a{};  // dx_router = d_logits · W_r   [T, d], K = E
+    a.mode = kGroupNone; a.M = T; a.N = d; a.K = E;
+    a.dtA = kF32; a.dtB = kF32; a.dtC = kF32;
+    a.A = d_logits; a.a_sm = E; a.a_sk = 1;
+    a.B = w_router; a.b_sn = 1; a.b_sk = d;
+    a.C = dx_router; a.c_sm = d;
+    a.n_groups = 1; a.alpha = 1.f; a.split_k = 1;
+    MOE_LAUNCH(launch_simt_gemm(c, a));
+  }
+  const int S = route_bwd_splits(*cfg);
+  float* part = static_cast<float*>(ws);
+  SimtGemm b{};  // dW_r = d_logitsᵀ · x  [E, d], K = T split S ways
+  b.mode = kGroupNone; b.M = E; b.N = d; b.K = T;
+  b.dtA = kF32; b.dtB = dtx; b.dtC = kF32;
+  b.A = d_logits; b.a_sm = 1; b.a_sk = E;
+  b.B = x; b.b_sn = 1; b.b_sk = d;
+  b.C = part; b.c_sm = d; b.c_sg = (int64_t)E * d;
+  b.n_groups = 1; b.alpha = 1.f; b.split_k = S;
+  if (T > 0) {
+    MOE_LAUNCH(launch_simt_gemm(c, b));
+    MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)E * d, S, (int64_t)E * d, dw_router, kF32, 0));
+  } else {
+    MOE_LAUNCH(cudaMemsetAsync(dw_router, 0, (size_t)E * d * sizeof(float), c.stream));
+  }
+  return MOE_OK;
+}
+
+int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_of,
+                    const float* dx_router, const void* dx_shared, void* dx,
+                    moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(dx_perm); MOE_PTR(row_of); MOE_PTR(dx); MOE_OPT_PTR(dx_router); MOE_OPT_PTR(dx_shared);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_permute_bwd(c, *cfg, dx_perm, row_of, dx_router, dx_shared, dx));
+  return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(moe_stream_t stream) {
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_wait_selftest(c));
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace moe {
+
+// Waits for status[2], which nothing sets, until the timeout; records
+// MOE_ERR_TIMEOUT (detail 1) and returns.
+__global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+  if (threadIdx.x != 0) return;
+  volatile int* flag = status + 2;
+  const uint64_t t0 = global_timer_ns();
+  while (*flag == 0) {
+    if (global_timer_ns() - t0 > timeout_ns) {
+      record_error(status, MOE_ERR_TIMEOUT, 1);
+      return;
+    }
+    __nanosleep(1000);
+  }
+}
+
+cudaError_t launch_wait_selftest(const Ctx& c) {
+  wait_selftest_kernel<<<1, 32, 0, c.stream>>>(c.status, c.timeout_ns);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,104 @@
+// Launchers shared between the kernel files and the C-ABI file (C++ linkage).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+struct Ctx {
+  cudaStream_t stream;
+  int* status;          // device status word of the current device
+  uint64_t timeout_ns;  // bound of every spin-wait
+  int sm_count;
+};
+
+// ---- router (router.cu)
+cudaError_t launch_router_logits(const Ctx& c, const moe_cfg& cfg, const void* x,
+                                 const float* w_router, const float* logit_bias,
+                                 float* logits);
+cudaError_t launch_router_topk(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                               const float* sel_bias, int32_t* idx, float* w);
+cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                     const int32_t* idx, const float* dw, float* d_logits,
+                                     int accumulate);
+
+// ---- dispatch (dispatch.cu)
+size_t permute_ws_bytes(const moe_cfg& cfg);
+cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, const int32_t* idx,
+                           int32_t* counts, int32_t* offsets, int32_t* row_of,
+                           int32_t* src_tok, void* x_perm, void* ws);
+cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_perm,
+                               const int32_t* row_of, const float* dx_router,
+                               const void* dx_shared, void* dx);
+
+// ---- combine (combine.cu)
+cudaError_t launch_combine(const Ctx& c, const moe_cfg& cfg, const void* out_perm,
+                           const int32_t* row_of, const float* w, const void* shared_out,
+                           void* y);
+cudaError_t launch_combine_bwd(const Ctx& c, const moe_cfg& cfg, const void* dy,
+                               const void* out_perm, const int32_t* row_of, const float* w,
+                               void* d_out_perm, float* dw);
+
+// ---- aux loss (aux_loss.cu)
+size_t aux_ws_bytes(const moe_cfg& cfg);
+cudaError_t launch_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                            const int32_t* counts, float* aux, void* ws);
+cudaError_t launch_aux_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                const int32_t* counts, float g_aux, float* d_logits,
+                                int accumulate);
+
+// ---- generic fp32-accumulating SIMT GEMM (simt_gemm.cu)
+// C(m, n) = alpha * sum_k A(m, k) * B(n, k)  (+ C(m, n) when accumulate)
+// A(m, k) = A[m*a_sm + k*a_sk], B(n, k) = B[n*b_sn + k*b_sk], C(m, n) = C[m*c_sm + n].
+enum SimtGrouping { kGroupNone = 0, kGroupM = 1, kGroupK = 2 };
+enum SimtDtype { kF32 = 0, kBF16 = 1 };
+struct SimtGemm {
+  int mode;                // SimtGrouping
+  int M, N, K;             // kGroupM: M = total rows; kGroupK: K = total rows
+  int dtA, dtB, dtC;       // SimtDtype
+  const void* A; int64_t a_sm, a_sk, a_sg;
+  const void* B; int64_t b_sn, b_sk, b_sg;
+  void* C; int64_t c_sm, c_sg;
+  const int32_t* offsets;  // [n_groups + 1] device (grouped modes), NULL = one group
+  int n_groups;
+  float alpha;
+  int accumulate;
+  int split_k;             // kGroupNone only: >1 writes partials C + z*c_sg, then reduce
+};
+cudaError_t launch_simt_gemm(const Ctx& c, const SimtGemm& g);
+// out[i] = sum_z part[z*stride + i] (fixed order), i < n; dtype of out: dt_out
+cudaError_t launch_reduce_partials(const Ctx& c, const float* part, int64_t stride, int nz,
+                                   int64_t n, void* out, int dt_out, int accumulate);
+
+// ---- SwiGLU elementwise (simt_gemm.cu)
+cudaError_t launch_swiglu_fwd_elem(const Ctx& c, int dt, const void* pre_gu, void* h,
+                                   int64_t rows, int F);
+cudaError_t launch_swiglu_bwd_elem(const Ctx& c, int dt, const float* dh, const void* pre_gu,
+                                   void* d_pre, int64_t rows, int F);
+
+// ---- tcgen05 grouped GEMM (grouped_gemm_tc.cu)
+struct TcGroupedArgs;
+bool tc_available();
+cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int n_groups, int64_t n_rows, int F,
+                                         int d, const int32_t* offsets, const void* x_rows,
+                                         const void* w1, const void* w2, void* pre_gu,
+                                         void* h, void* out, void* ws, int* err);
+cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int n_groups, int64_t n_rows, int F,
+                                         int d, const int32_t* offsets, const void* x_rows,
+                                         const void* w1, const void* w2, const void* pre_gu,
+                                         const void* h, const void* d_out, void* d_pre,
+                                         void* dx_rows, void* dw1, void* dw2, void* ws,
+                                         int* err);
+size_t tc_grouped_ws_bytes(int n_groups);
+
+// ---- misc
+cudaError_t launch_wait_selftest(const Ctx& c);
+// host-side count of kernels this library has launched (for the bench's claim)
+void note_launches(int n);
+uint64_t launches_so_far();
+
+}  // namespace moe

@@ -1,0 +1,494 @@
+// Router: gate GEMM (S1), scores + sorted top-k + mixing weights (S2), and the
+// score backward (B2).
+//
+// The Ultimate MoE Training Handbook, §3.1 "Router scoring": logits come from
+// an fp32 GEMM of the token with the [E, d] fp32 router weight ("Precision");
+// softmax routing picks the top-k logits and takes the softmax over them,
+// sigmoid routing picks on sigmoid(l) + expert bias and divides the chosen
+// scores by their sum + 1e-20 ("Gating function", "Output scale"), then the
+// routed scaling factor multiplies the weights. §3.2 "Who selects": the top-k
+// is sorted.
+//
+// Accuracy: each logit is a sum of d products. The kernels add the products of
+// one 32-element chunk in plain fp32 FMAs and fold the chunk sums into a
+// (hi, lo) pair with an error-free TwoSum, so the only rounding that grows with
+// d is confined to 32-term partial sums. The logits end within a few fp32 ulps
+// of the exact value, far inside the 1e-6 band that marks a near tie.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ S1, E <= 16
+// One warp per TPW tokens; lane l reads the 8-element groups l, l+32, ... of
+// the hidden dimension, so a token row is read once, 16 B per lane at a time.
+// The 32 lane partials are combined by a butterfly of compensated sums.
+template <typename Tx, int EMAX, int TPW>
+__global__ void __launch_bounds__(256)
+router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
+                    const float* __restrict__ logit_bias, float* __restrict__ logits,
+                    int64_t T, int d, int E) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t t0 = warp * TPW;
+  if (t0 >= T) return;
+
+  float hi[TPW][EMAX], lo[TPW][EMAX], acc[TPW][EMAX];
+#pragma unroll
+  for (int a = 0; a < TPW; ++a)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = acc[a][e] = 0.f;
+
+  const int ngroups = d >> 3;
+  int cnt = 0;
+  for (int g = lane; g < ngroups; g += 32) {
+    float xv[TPW][8];
+#pragma unroll
+    for (int a = 0; a < TPW; ++a) {
+      if (t0 + a < T) {
+        load8(x + (t0 + a) * (int64_t)d + 8 * g, xv[a]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xv[a][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (e < E) {
+        float wv[8];
+        load8(W + (int64_t)e * d + 8 * g, wv);
+#pragma unroll
+        for (int a = 0; a < TPW; ++a)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[a][e] = fmaf(xv[a][i], wv[i], acc[a][e]);
+      }
+    }
+    if (++cnt == 4) {  // 32 elements per lane
+#pragma unroll
+      for (int a = 0; a < TPW; ++a)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          comp_add(hi[a][e], lo[a][e], acc[a][e]);
+          acc[a][e] = 0.f;
+        }
+      cnt = 0;
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < TPW; ++a)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) comp_add(hi[a][e], lo[a][e], acc[a][e]);
+
+  // Butterfly over lanes. Both partners compute the same (hi, lo): TwoSum's
+  // error term is exact, hence symmetric in its operands.
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int a = 0; a < TPW; ++a)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        float oh = __shfl_xor_sync(0xffffffffu, hi[a][e], off);
+        float ol = __shfl_xor_sync(0xffffffffu, lo[a][e], off);
+        float s, er;
+        two_sum(hi[a][e], oh, s, er);
+        hi[a][e] = s;
+        lo[a][e] = __fadd_rn(__fadd_rn(lo[a][e], ol), er);
+      }
+  }
+#pragma unroll
+  for (int a = 0; a < TPW; ++a) {
+    if (t0 + a >= T) break;
+    float v = 0.f;
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (lane == e) {
+        float h = hi[a][e], l = lo[a][e];
+        if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
+        v = __fadd_rn(h, l);
+      }
+    }
+    if (lane < E) logits[(t0 + a) * (int64_t)E + lane] = v;
+  }
+}
+
+// ------------------------------------------------------------------ S1, E > 16
+// Register-tiled fp32 SIMT GEMM: a CTA computes 128 tokens x 64 experts; a
+// thread computes 4 tokens x 8 experts ({4tx..4tx+3} and {32+4tx..32+4tx+3},
+// so that the eight threads of one shared-memory phase read 128 consecutive
+// bytes). K advances in chunks of 32; the next chunk is prefetched into
+// registers while the current one is multiplied.
+constexpr int RT_BT = 128, RT_BE = 64, RT_KC = 32;
+
+template <typename Tx>
+__global__ void __launch_bounds__(256)
+router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
+                    const float* __restrict__ logit_bias, float* __restrict__ logits,
+                    int64_t T, int d, int E) {
+  __shared__ __align__(16) float xs[RT_KC][RT_BT + 4];
+  __shared__ __align__(16) float ws[RT_KC][RT_BE + 4];
+
+  const int tid = threadIdx.x;
+  const int ty = tid >> 3;  // token group: tokens 4ty..4ty+3
+  const int tx = tid & 7;   // expert group
+  const int64_t t_base = (int64_t)blockIdx.x * RT_BT;
+  const int e_base = blockIdx.y * RT_BE;
+
+  float acc[4][8], hi[4][8], lo[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = hi[i][j] = lo[i][j] = 0.f;
+
+  // loader roles: x: 2 x (token = v & 127, group kg = v >> 7); W: expert tid & 63, kg tid >> 6
+  float xr[2][8], wr[8];
+  auto load_chunk = [&](int k0) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int v = tid + 256 * r;
+      const int tok = v & 127, kg = v >> 7;
+      const int64_t t = t_base + tok;
+      const int kk = k0 + 8 * kg;
+      if (t < T && kk < d) {
+        load8(x + t * d + kk, xr[r]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xr[r][i] = 0.f;
+      }
+    }
+    {
+      const int e = tid & 63, kg = tid >> 6;
+      const int kk = k0 + 8 * kg;
+      if (e_base + e < E && kk < d) {
+        load8(W + (int64_t)(e_base + e) * d + kk, wr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wr[i] = 0.f;
+      }
+    }
+  };
+  auto store_chunk = [&]() {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int v = tid + 256 * r;
+      const int tok = v & 127, kg = v >> 7;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[kg * 8 + i][tok] = xr[r][i];
+    }
+    const int e = tid & 63, kg = tid >> 6;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ws[kg * 8 + i][e] = wr[i];
+  };
+
+  load_chunk(0);
+  for (int k0 = 0; k0 < d; k0 += RT_KC) {
+    __syncthreads();
+    store_chunk();
+    __syncthreads();
+    if (k0 + RT_KC < d) load_chunk(k0 + RT_KC);
+#pragma unroll
+    for (int kk = 0; kk < RT_KC; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&ws[kk][32 + 4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        comp_add(hi[i][j], lo[i][j], acc[i][j]);
+        acc[i][j] = 0.f;
+      }
+  }
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t t = t_base + 4 * ty + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int e0 = e_base + 32 * half + 4 * tx;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float h = hi[i][4 * half + j], l = lo[i][4 * half + j];
+        if (logit_bias != nullptr && e0 + j < E) comp_add(h, l, logit_bias[e0 + j]);
+        v[j] = __fadd_rn(h, l);
+      }
+      if (e0 + 3 < E && (E & 3) == 0) {
+        *reinterpret_cast<float4*>(logits + t * E + e0) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j < E) logits[t * E + e0 + j] = v[j];
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ S2
+// One warp per token. Lane l holds experts l, l+32, ... The k winners are found
+// by k rounds of a warp arg-max over (key descending, index ascending); a
+// non-finite key counts as -inf so a valid expert always wins.
+__device__ __forceinline__ bool outranks(float ka, int ea, float kb, int eb) {
+  return ka > kb || (ka == kb && ea < eb);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256)
+router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias,
+            int32_t* __restrict__ idx, float* __restrict__ w, int64_t T, int E, int k,
+            int score_fn, float scaling) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    float key[EPL], lg[EPL];
+    bool taken[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        const float l = logits[t * E + e];
+        float kv;
+        if (score_fn == MOE_SCORE_SOFTMAX) {
+          kv = l;
+        } else {
+          kv = sigmoidf_acc(l);
+          if (sel_bias != nullptr) kv = __fadd_rn(kv, sel_bias[e]);
+        }
+        key[i] = (kv == kv) ? kv : -INFINITY;
+        lg[i] = l;
+        taken[i] = false;
+      } else {
+        key[i] = -INFINITY;
+        lg[i] = 0.f;
+        taken[i] = true;
+      }
+    }
+    int sel_e[kMaxK];
+    float sel_l[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      sel_e[j] = 0;
+      sel_l[j] = 0.f;
+      if (j < k) {
+        float bk = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (!taken[i] && outranks(key[i], lane + 32 * i, bk, be)) {
+            bk = key[i];
+            be = lane + 32 * i;
+          }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (outranks(ok, oe, bk, be)) {
+            bk = ok;
+            be = oe;
+          }
+        }
+        const int owner = be & 31, slot = be >> 5;
+        float l_own = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (i == slot) {
+            if (lane == owner) taken[i] = true;
+            l_own = lg[i];
+          }
+        sel_e[j] = be;
+        sel_l[j] = __shfl_sync(0xffffffffu, l_own, owner);
+      }
+    }
+    // mixing weights of the chosen experts
+    float wv[kMaxK];
+    if (score_fn == MOE_SCORE_SOFTMAX) {
+      float m = sel_l[0];
+#pragma unroll
+      for (int j = 1; j < kMaxK; ++j)
+        if (j < k) m = fmaxf(m, sel_l[j]);
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        wv[j] = (j < k) ? expf(sel_l[j] - m) : 0.f;
+        s += wv[j];
+      }
+      const float inv = scaling / s;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) wv[j] *= inv;
+    } else {
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        wv[j] = (j < k) ? sigmoidf_acc(sel_l[j]) : 0.f;
+        s += wv[j];
+      }
+      const float inv = (k > 1) ? scaling / (s + 1e-20f) : scaling;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) wv[j] *= inv;
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k && lane == j) {
+        idx[t * k + j] = sel_e[j];
+        w[t * k + j] = wv[j];
+      }
+  }
+}
+
+// ------------------------------------------------------------------ B2
+// One warp per token: zero the row (unless accumulating), then each of the
+// first k lanes adds the gradient of its chosen logit.
+__global__ void __launch_bounds__(256)
+router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ idx,
+                  const float* __restrict__ dw, float* __restrict__ d_logits, int64_t T,
+                  int E, int k, int score_fn, float scaling, int accumulate, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    if (!accumulate)
+      for (int e = lane; e < E; e += 32) d_logits[t * E + e] = 0.f;
+    int ej[kMaxK];
+    float lj[kMaxK], gj[kMaxK];
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      ej[j] = 0;
+      lj[j] = 0.f;
+      gj[j] = 0.f;
+      if (j < k) {
+        int e = idx[t * k + j];
+        if (e < 0 || e >= E) {
+          ok = false;
+          e = 0;
+        }
+        ej[j] = e;
+        lj[j] = logits[t * E + e];
+        gj[j] = dw[t * k + j];
+      }
+    }
+    if (!ok) {
+      if (lane == 0) record_error(status, MOE_ERR_DEVICE_INDEX, (int)t);
+      continue;
+    }
+    float dl[kMaxK];
+    if (score_fn == MOE_SCORE_SOFTMAX) {
+      float m = lj[0];
+#pragma unroll
+      for (int j = 1; j < kMaxK; ++j)
+        if (j < k) m = fmaxf(m, lj[j]);
+      float p[kMaxK], s = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        p[j] = (j < k) ? expf(lj[j] - m) : 0.f;
+        s += p[j];
+      }
+      float dot = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        p[j] /= s;
+        dot += p[j] * (scaling * gj[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) dl[j] = p[j] * (scaling * gj[j] - dot);
+    } else {
+      float sj[kMaxK], S = 0.f, dsd = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        sj[j] = (j < k) ? sigmoidf_acc(lj[j]) : 0.f;
+        S += sj[j];
+        dsd += gj[j] * sj[j];
+      }
+      S += 1e-20f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        const float ds = (k > 1) ? scaling * (gj[j] - dsd / S) / S : scaling * gj[j];
+        dl[j] = ds * sj[j] * (1.f - sj[j]);
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k && lane == j) d_logits[t * E + ej[j]] += dl[j];
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+template <typename Tx>
+static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, const Tx* x,
+                                          const float* w_router, const float* logit_bias,
+                                          float* logits) {
+  const int64_t T = cfg.T;
+  if (T == 0) return cudaSuccess;
+  if (cfg.E <= 8) {
+    constexpr int TPW = 2;
+    const int64_t warps = (T + TPW - 1) / TPW;
+    router_logits_small<Tx, 8, TPW><<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
+        x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+  } else if (cfg.E <= 16) {
+    constexpr int TPW = 1;
+    const int64_t warps = T;
+    router_logits_small<Tx, 16, TPW><<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
+        x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+  } else {
+    dim3 grid((unsigned)((T + RT_BT - 1) / RT_BT), (unsigned)((cfg.E + RT_BE - 1) / RT_BE));
+    router_logits_tiled<Tx><<<grid, 256, 0, c.stream>>>(x, w_router, logit_bias, logits, T,
+                                                         cfg.d, cfg.E);
+  }
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_logits(const Ctx& c, const moe_cfg& cfg, const void* x,
+                                 const float* w_router, const float* logit_bias,
+                                 float* logits) {
+  if (cfg.act_dtype == MOE_BF16)
+    return router_logits_dispatch(c, cfg, static_cast<const bf16*>(x), w_router, logit_bias,
+                                  logits);
+  return router_logits_dispatch(c, cfg, static_cast<const float*>(x), w_router, logit_bias,
+                                logits);
+}
+
+static unsigned warp_grid(const Ctx& c, int64_t items) {
+  const int64_t blocks = (items + 7) / 8;
+  const int64_t cap = (int64_t)c.sm_count * 16;
+  return (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+cudaError_t launch_router_topk(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                               const float* sel_bias, int32_t* idx, float* w) {
+  if (cfg.T == 0) return cudaSuccess;
+  const unsigned grid = warp_grid(c, cfg.T);
+  const int epl = (cfg.E + 31) / 32;
+#define MOE_TOPK(N)                                                                        \
+  router_topk<N><<<grid, 256, 0, c.stream>>>(logits, sel_bias, idx, w, cfg.T, cfg.E, cfg.k, \
+                                             cfg.score_fn, cfg.scaling)
+  switch (epl) {
+    case 1: MOE_TOPK(1); break;
+    case 2: MOE_TOPK(2); break;
+    case 3: case 4: MOE_TOPK(4); break;
+    default: MOE_TOPK(8); break;
+  }
+#undef MOE_TOPK
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                     const int32_t* idx, const float* dw, float* d_logits,
+                                     int accumulate) {
+  if (cfg.T == 0) return cudaSuccess;
+  router_scores_bwd<<<warp_grid(c, cfg.T), 256, 0, c.stream>>>(
+      logits, idx, dw, d_logits, cfg.T, cfg.E, cfg.k, cfg.score_fn, cfg.scaling, accumulate,
+      c.status);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI: no GPU needed, no kernel launched.
+
+The library must build, load, export every entry point include/moe.h declares,
+and refuse bad configurations on the host, the way the Handbook says Megatron
+validates them (§3.1 "Gating function": the expert bias is refused with
+softmax; §3.1 "Output scale": top-1 softmax with renormalisation is refused).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from routing_grouped_expert_gate_gb300 import build
+    build.build()
+    from routing_grouped_expert_gate_gb300 import _lib
+    return _lib
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_symbols()
+    assert len(names) >= 17
+    lib = ctypes.CDLL(L.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert L.version().startswith("libmoe")
+
+
+def _cfg(L, **kw):
+    base = dict(T=64, d=64, E=8, k=2, F=64, F_shared=0, score="softmax", act_dtype="bf16")
+    base.update(kw)
+    return L.make_cfg(**base)
+
+
+def test_workloads_validate(L):
+    import moe_inputs as mi
+    for wl in mi.WORKLOADS.values():
+        cfg = L.cfg_from_workload(wl)
+        assert L.check_cfg(cfg) == L.MOE_OK, wl.name
+        for which in (L.MOE_WS_PERMUTE, L.MOE_WS_GROUPED, L.MOE_WS_GROUPED_BWD, L.MOE_WS_AUX,
+                      L.MOE_WS_ROUTE_BWD):
+            assert L.workspace_bytes(cfg, which) > 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=1), "MOE_ERR_INVALID_ARG"),                     # top-1 softmax renormalised
+    (dict(k=9, E=16), "MOE_ERR_UNSUPPORTED"),
+    (dict(k=4, E=3), "MOE_ERR_INVALID_ARG"),                # k > E
+    (dict(E=257, k=2), "MOE_ERR_UNSUPPORTED"),
+    (dict(d=12), "MOE_ERR_ALIGN"),
+    (dict(F=100), "MOE_ERR_ALIGN"),
+    (dict(F_shared=20), "MOE_ERR_ALIGN"),
+    (dict(T=-1), "MOE_ERR_INVALID_ARG"),
+    (dict(d=0), "MOE_ERR_INVALID_ARG"),
+])
+def test_bad_configs_refused(L, kw, code):
+    cfg = _cfg(L, **kw)
+    assert L.check_cfg(cfg) == getattr(L, code)
+    assert L.workspace_bytes(cfg, L.MOE_WS_PERMUTE) == 0
+
+
+def test_top1_sigmoid_is_allowed(L):
+    assert L.check_cfg(_cfg(L, k=1, score="sigmoid")) == L.MOE_OK
+
+
+def test_selection_bias_with_softmax_refused_before_any_device_work(L):
+    cfg = _cfg(L)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: the call returns first
+    rc = L.lib.moe_route_topk(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake, None)
+    assert rc == L.MOE_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_refused(L):
+    cfg = _cfg(L)
+    good = ctypes.c_void_p(0x10000)
+    bad = ctypes.c_void_p(0x10008)
+    rc = L.lib.moe_unpermute_combine(ctypes.byref(cfg), None, good, good, None, good, None)
+    assert rc == L.MOE_ERR_INVALID_ARG
+    rc = L.lib.moe_unpermute_combine(ctypes.byref(cfg), bad, good, good, None, good, None)
+    assert rc == L.MOE_ERR_ALIGN
+    rc = L.lib.moe_permute(ctypes.byref(cfg), good, good, good, good, good, good, good, good, 0,
+                           None)
+    assert rc == L.MOE_ERR_WORKSPACE
+
+
+def test_status_strings_and_timeout_setter(L):
+    for code in range(0, -9, -1):
+        s = L.status_string(code)
+        assert s and s != "unknown status"
+    old = L.set_wait_timeout_ns(12345)
+    assert L.set_wait_timeout_ns(old) == 12345
+
+
+def test_cfg_struct_layout(L):
+    # int64 T, seven int32, two floats: 44 bytes, padded to 48 like the C struct
+    assert ctypes.sizeof(L.MoeCfg) == 48
+    assert L.MoeCfg.scaling.offset == 36 and L.MoeCfg.aux_coeff.offset == 40

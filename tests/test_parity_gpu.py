@@ -1,0 +1,230 @@
+"""GPU parity: every stage of the layer, through the C ABI, against the oracle.
+
+Sizes are small enough for the float64 oracle to finish in seconds yet span
+several GEMM tiles with ragged tails (T, F and d not multiples of the tiles),
+empty experts (E = 128/256 with few tokens, a Zipf-skewed router) and both
+router types. Each bf16 workload also runs as fp32, where every float output
+must agree to 1e-4.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from oracle import moe_oracle as O
+from tests.parity import (TOL_AUX, TOL_BF16, TOL_F32, act_tol, assert_close, matched_rows,
+                          rel_err, routing_checks, to_np)
+
+pytestmark = pytest.mark.gpu
+
+W = mi.WORKLOADS
+SMALL = {
+    "tiny_fp32": dataclasses.replace(W["tiny_fp32"], backward=True),
+    "mixtral_small": mi.shrink(W["mixtral_style"], name="mixtral_small", T=300, d=256, F=320),
+    "fine_grained_small": mi.shrink(W["fine_grained_64e"], name="fine_grained_small", T=517,
+                                    d=320, F=192, F_shared=128),
+    "deepseek_small": mi.shrink(W["deepseek_v3_shaped"], name="deepseek_small", T=256, d=512,
+                                F=128, F_shared=192, backward=True),
+    "zipf_small": mi.shrink(W["zipf_imbalance"], name="zipf_small", T=1024, d=192, F=136),
+}
+CASES = [(n, "native") for n in SMALL] + [(n, "f32") for n in SMALL if n != "tiny_fp32"]
+
+
+def _wl(name, dt):
+    wl = SMALL[name]
+    if dt == "f32":
+        wl = dataclasses.replace(wl, act_dtype="f32", name=wl.name + "_f32")
+    return wl
+
+
+def run_gpu(wl, seed=0, backward=True):
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import layer
+    inp = mi.make_inputs(wl, seed=seed, device="cuda", with_dy=backward)
+    cfg = moe.cfg_from_workload(wl)
+    p = layer.params_from_inputs(inp)
+    b = layer.alloc_buffers(cfg, "cuda", backward=backward)
+    layer.forward(cfg, p, inp["x"], b)
+    if backward:
+        layer.backward(cfg, p, inp["x"], inp["dy"], b)
+    torch.cuda.synchronize()
+    rc, detail = moe._lib.last_device_status()
+    assert rc == 0, f"device status {rc} ({moe.status_string(rc)}) detail {detail}"
+    return inp, b
+
+
+@pytest.fixture(scope="module")
+def built():
+    from routing_grouped_expert_gate_gb300 import build
+    build.build()
+    import routing_grouped_expert_gate_gb300  # noqa: F401
+
+
+@pytest.mark.parametrize("name,dt", CASES)
+def test_layer_parity(built, name, dt):
+    wl = _wl(name, dt)
+    inp, b = run_gpu(wl, backward=True)
+    ref = {k: O.as_f64(v) for k, v in inp.items()}
+    f = O.layer_forward(wl, ref)
+    g = O.layer_backward(wl, ref, f, ref["dy"])
+    report = {}
+    tol = act_tol(wl)
+
+    # S1/S2: logits and weights are fp32 results of exact inputs
+    assert_close("logits", b["logits"], f["logits"], TOL_F32)
+    assert float(np.max(np.abs(to_np(b["logits"]) - f["logits"]))) < 1e-6, \
+        "logit error must stay far below the near-tie band"
+    ok = routing_checks(wl, b, f, report)
+    assert_close("w", to_np(b["w"])[ok], f["w"][ok], TOL_F32)
+
+    # S3: the row copy is exact
+    gr, orow = matched_rows(b, f, ok)
+    xp = to_np(b["x_perm"])
+    assert np.array_equal(xp[gr], f["x_perm"][orow])
+    src = b["src_tok"].cpu().numpy().astype(np.int64)
+    assert np.array_equal(xp, to_np(inp["x"])[src])
+
+    # S4/S5
+    F = wl.F
+    pre = to_np(b["pre_gu"])
+    assert_close("gate", pre[gr, :F], f["g"][orow], tol)
+    assert_close("up", pre[gr, F:], f["u"][orow], tol)
+    assert_close("h", to_np(b["h"])[gr], f["h"][orow], tol)
+    assert_close("out_perm", to_np(b["out_perm"])[gr], f["out_perm"][orow], tol)
+    if wl.F_shared:
+        assert_close("y_shared", b["y_s"], f["y_s"], tol)
+    # S6, S7
+    assert_close("y", to_np(b["y"])[ok], f["y"][ok], tol)
+    aux = float(b["aux"].item())
+    assert abs(aux - f["aux"]) <= TOL_AUX * abs(f["aux"]), (aux, f["aux"])
+
+    # backward (bf16 workloads: everything here is downstream of bf16 activations)
+    assert_close("d_out_perm", to_np(b["d_out_perm"])[gr], g["d_out_perm"][orow], tol)
+    assert_close("dw", to_np(b["dw"])[ok], g["dw"][ok], tol)
+    assert_close("d_pre", to_np(b["d_pre"])[gr], g["d_pre"][orow], tol)
+    assert_close("dx_perm", to_np(b["dx_perm"])[gr], g["dx_perm"][orow], tol)
+    if report["near_tie_tokens"] == 0:
+        assert_close("dW1", b["dw1"], g["dW1"], tol)
+        assert_close("dW2", b["dw2"], g["dW2"], tol)
+        assert_close("d_logits", b["d_logits"], g["d_logits"], tol)
+        assert_close("dW_r", b["dw_router"], g["dW_r"], tol)
+        assert_close("dx", b["dx"], g["dx"], tol)
+        if wl.F_shared:
+            assert_close("dW1_s", b["dw1_s"][0], g["dW1_s"], tol)
+            assert_close("dW2_s", b["dw2_s"][0], g["dW2_s"], tol)
+    # experts that received no rows get an exactly zero weight gradient
+    empty = np.nonzero(f["counts"] == 0)[0]
+    for e in empty:
+        assert float(b["dw1"][e].abs().max()) == 0.0 and float(b["dw2"][e].abs().max()) == 0.0
+
+
+def test_zero_load_experts_exist_in_skewed_case(built):
+    wl = SMALL["zipf_small"]
+    inp = mi.make_inputs(wl, seed=0)
+    ref = {k: O.as_f64(v) for k, v in inp.items()}
+    r = O.route(ref["x"], ref["w_router"], wl.k, wl.score, 1.0, ref["logit_bias"], None)
+    counts = O.dispatch(r["idx"], wl.E)["counts"]
+    assert (counts == 0).sum() >= 1 and counts.max() > 3 * counts.mean()
+
+
+def test_deterministic_bytes(built):
+    wl = SMALL["fine_grained_small"]
+    _, b1 = run_gpu(wl, backward=True)
+    _, b2 = run_gpu(wl, backward=True)
+    for key in ("logits", "idx", "w", "row_of", "x_perm", "pre_gu", "out_perm", "y", "aux",
+                "d_pre", "dw1", "dw2", "dw_router", "dx"):
+        assert torch.equal(b1[key], b2[key]), key
+
+
+def test_mixture_example_through_gpu(built):
+    """The 0.75/0.25 mixture (LeCompute, 'An expert transforms numbers inside
+    the model') embedded in d = F = 8 and run through the fp32 path."""
+    import json
+    import os
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import layer
+    with open(os.path.join(os.path.dirname(__file__), "golden", "mixture_075_025.json")) as fh:
+        gold = json.load(fh)
+    c = gold["construction"]
+    d = F = 8
+    dev = "cuda"
+    x = torch.zeros(1, d, device=dev)
+    x[0, :2] = torch.tensor(c["x"])
+    wr = torch.zeros(2, d, device=dev)
+    wr[:, :2] = torch.tensor(c["w_router"])
+    w1 = torch.zeros(2, 2 * F, d, device=dev)
+    w2 = torch.zeros(2, d, F, device=dev)
+    for e in range(2):
+        w1[e, 0, :2] = torch.tensor(c["w1"][e][0])      # gate row 0
+        w1[e, F, :2] = torch.tensor(c["w1"][e][1])      # up row 0
+        w2[e, :2, 0] = torch.tensor([r[0] for r in c["w2"][e]])
+    cfg = moe.make_cfg(T=1, d=d, E=2, k=2, F=F, act_dtype="f32", aux_coeff=0.0)
+    b = layer.alloc_buffers(cfg, dev, backward=False)
+    layer.forward(cfg, {"w_router": wr, "w1": w1, "w2": w2}, x, b)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(b["w"].cpu().numpy()[0],
+                               [gold["page_values"]["weight_A"], gold["page_values"]["weight_B"]],
+                               atol=1e-7)
+    np.testing.assert_allclose(b["y"].cpu().numpy()[0, :2], gold["expected_y"], atol=1e-6)
+
+
+def test_zero_tokens(built):
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import layer
+    wl = mi.shrink(SMALL["mixtral_small"], T=0)
+    inp = mi.make_inputs(wl, device="cuda", with_dy=True)
+    cfg = moe.cfg_from_workload(wl)
+    p = layer.params_from_inputs(inp)
+    b = layer.alloc_buffers(cfg, "cuda", backward=True)
+    layer.forward(cfg, p, inp["x"], b)
+    layer.backward(cfg, p, inp["x"], inp["dy"], b)
+    torch.cuda.synchronize()
+    assert int(b["offsets"].abs().sum()) == 0 and int(b["counts"].abs().sum()) == 0
+    assert float(b["aux"].item()) == 0.0
+    assert float(b["dw1"].abs().max()) == 0.0 and float(b["dw_router"].abs().max()) == 0.0
+
+
+def test_out_of_range_index_is_reported_not_faulted(built):
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    T, d, E, k = 64, 64, 8, 2
+    cfg = moe.make_cfg(T=T, d=d, E=E, k=k, F=64)
+    dev = "cuda"
+    x = torch.randn(T, d, device=dev).to(torch.bfloat16)
+    idx = torch.stack([torch.arange(T) % E, (torch.arange(T) + 1) % E], 1).to(torch.int32).to(dev)
+    idx[5, 1] = E  # one bad entry
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T, k, dtype=torch.int32, device=dev)
+    src = torch.zeros(T * k, dtype=torch.int32, device=dev)
+    xp = torch.zeros(T * k, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.workspace_bytes(cfg, L.MOE_WS_PERMUTE), dtype=torch.uint8, device=dev)
+    L.last_device_status()
+    L.permute(cfg, x, idx, counts, offsets, row_of, src, xp, ws)
+    rc, detail = L.last_device_status()
+    assert rc == L.MOE_ERR_DEVICE_INDEX and detail == 5
+    assert int(offsets[-1]) == T * k - 1  # the bad assignment was skipped
+    assert int(row_of[5, 1]) == -1
+    # the combine refuses the bad row instead of reading out of bounds
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    w = torch.ones(T, k, device=dev)
+    L.unpermute_combine(cfg, xp, row_of, w, None, y)
+    rc, detail = L.last_device_status()
+    assert rc == L.MOE_ERR_DEVICE_INDEX and detail == 5
+    assert L.last_device_status()[0] == 0  # reading clears it
+
+
+def test_bounded_wait_reports_timeout(built):
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    old = L.set_wait_timeout_ns(2_000_000)  # 2 ms
+    try:
+        L.last_device_status()
+        L.selftest_wait_timeout()
+        rc, detail = L.last_device_status()
+        assert rc == L.MOE_ERR_TIMEOUT and detail == 1
+        # the context is still usable afterwards
+        assert float(torch.ones(4, device="cuda").sum()) == 4.0
+    finally:
+        L.set_wait_timeout_ns(old)
