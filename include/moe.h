@@ -261,6 +261,15 @@ uint64_t moe_set_wait_timeout_ns(uint64_t ns);
  * MOE_ERR_TIMEOUT (read it with moe_last_device_status). */
 int moe_selftest_wait_timeout(moe_stream_t stream);
 
+/* Which kernels run the grouped expert GEMMs (moe_grouped_swiglu and its
+ * backward). MOE_GEMM_AUTO (default): bf16 on the tcgen05 tensor cores, fp32
+ * on CUDA cores. MOE_GEMM_CUDA_CORES: every dtype on the CUDA-core kernels
+ * (fp32 accumulation; for cross-checking). Process-wide; returns the previous
+ * setting, or MOE_ERR_INVALID_ARG for an unknown value. */
+#define MOE_GEMM_AUTO       0
+#define MOE_GEMM_CUDA_CORES 1
+int moe_set_grouped_gemm_impl(int impl);
+
 /* Number of CUDA kernels this library has launched in this process (all
  * devices, all streams), counted on the host at launch time. */
 uint64_t moe_launch_count(void);

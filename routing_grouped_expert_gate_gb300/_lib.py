@@ -35,6 +35,9 @@ MOE_SCORE_SIGMOID = 1
 MOE_F32 = 0
 MOE_BF16 = 1
 
+MOE_GEMM_AUTO = 0
+MOE_GEMM_CUDA_CORES = 1
+
 MOE_WS_PERMUTE = 0
 MOE_WS_GROUPED = 1
 MOE_WS_GROUPED_BWD = 2
@@ -55,10 +58,13 @@ class MoeError(RuntimeError):
 
 
 def _load():
+    if not _build.up_to_date():
+        try:
+            _build.build()
+        except Exception as e:  # no toolkit, compile error: no library, no fallback
+            raise ImportError(f"libmoe.so could not be built ({LIB_PATH}): {e}") from e
     if not os.path.exists(LIB_PATH):
-        raise ImportError(
-            f"libmoe.so is not built ({LIB_PATH}); run __graft_entry__.build() or "
-            "python -m routing_grouped_expert_gate_gb300.build")
+        raise ImportError(f"libmoe.so is missing ({LIB_PATH})")
     return ctypes.CDLL(LIB_PATH)
 
 
@@ -88,6 +94,7 @@ _SIGS = {
     "moe_selftest_wait_timeout": (c_int, [_VP]),
     "moe_version": (c_char_p, []),
     "moe_launch_count": (c_uint64, []),
+    "moe_set_grouped_gemm_impl": (c_int, [c_int]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -103,6 +110,14 @@ def status_string(code: int) -> str:
 
 def launch_count() -> int:
     return int(lib.moe_launch_count())
+
+
+def set_grouped_gemm_impl(impl: int) -> int:
+    """MOE_GEMM_AUTO (bf16 on tcgen05) or MOE_GEMM_CUDA_CORES; returns the previous one."""
+    rc = int(lib.moe_set_grouped_gemm_impl(impl))
+    if rc < 0:
+        raise MoeError(rc, "moe_set_grouped_gemm_impl")
+    return rc
 
 
 def version() -> str:

@@ -14,6 +14,11 @@ __device__ int g_status[4];
 
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<int> g_gemm_impl{MOE_GEMM_AUTO};
+
+static bool use_tc(int dt) {
+  return dt == kBF16 && g_gemm_impl.load() == MOE_GEMM_AUTO && tc_available();
+}
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
@@ -164,6 +169,11 @@ uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns)
 
 uint64_t moe_launch_count(void) { return launches_so_far(); }
 
+int moe_set_grouped_gemm_impl(int impl) {
+  if (impl != MOE_GEMM_AUTO && impl != MOE_GEMM_CUDA_CORES) return MOE_ERR_INVALID_ARG;
+  return g_gemm_impl.exchange(impl);
+}
+
 int moe_last_device_status(moe_stream_t stream, int32_t* detail) {
   MOE_CTX(stream, c);
   if (cudaStreamSynchronize(c.stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -231,7 +241,7 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
   if (n_rows == 0) return MOE_OK;
   const int dt = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
   const int d = cfg->d;
-  if (dt == kBF16 && tc_available()) {
+  if (use_tc(dt)) {
     MOE_REQUIRE(ws_bytes >= round256(tc_grouped_ws_bytes(n_groups)), MOE_ERR_WORKSPACE);
     MOE_REQUIRE(ws != nullptr || tc_grouped_ws_bytes(n_groups) == 0, MOE_ERR_INVALID_ARG);
     int err = MOE_OK;
@@ -317,7 +327,7 @@ int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows,
   MOE_CTX(stream, c);
   const int dt = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
   const int d = cfg->d;
-  if (dt == kBF16 && tc_available()) {
+  if (use_tc(dt)) {
     MOE_REQUIRE(ws_bytes >= round256(tc_grouped_ws_bytes(n_groups)), MOE_ERR_WORKSPACE);
     int err = MOE_OK;
     MOE_LAUNCH(launch_tc_grouped_swiglu_bwd(c, n_groups, n_rows, F, d, offsets, x_rows, w1, w2,

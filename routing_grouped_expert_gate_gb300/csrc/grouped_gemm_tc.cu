@@ -1,14 +1,779 @@
-// placeholder until the tcgen05 grouped GEMM lands
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// The Ultimate MoE Training Handbook, §3.4 "Experts": each expert is a bias-free
+// SwiGLU FFN whose fc1 is 2F wide (gate half first, "Activation") and whose fc2
+// maps F back to d ("Count and size"); the local experts' GEMMs run as one
+// grouped GEMM. MoE training cluster: routing, load balancing (LeCompute),
+// "Read the timeline before blaming the network": grouping lets a GPU stay busy
+// even when single experts receive few tokens.
+//
+// One persistent, warp-specialised kernel template serves every contraction of
+// the layer's expert FFNs (bf16 operands, fp32 accumulation in TMEM):
+//
+//   fc1 forward    h = silu(x W1gᵀ) * (x W1uᵀ)   M-grouped, SwiGLU epilogue
+//   fc2 forward    out = h W2ᵀ                    M-grouped
+//   fc2 dgrad      d_pre = SwiGLU'(d_out W2)      M-grouped, SwiGLU-backward epilogue
+//   fc1 dgrad      dx = d_pre W1                  M-grouped
+//   fc2 wgrad      dW2_e = d_outᵀ h               K-grouped (K = the expert's rows)
+//   fc1 wgrad      dW1_e = d_preᵀ x               K-grouped
+//
+// Tiles are 128 x 256 (M x N) with K stepping 64 bf16 (one 128-byte swizzle row)
+// per pipeline stage. Warp 0 issues TMA loads into a 4-stage shared-memory ring;
+// warp 1 allocates 512 TMEM columns (two 256-column fp32 accumulators) and one
+// of its threads issues tcgen05.mma (M=128, N=256, K=16); warps 2..5 drain an
+// accumulator through tcgen05.ld while the next tile accumulates in the other.
+// The tile list is built on the device from the segment offsets: no host sync.
+// M-grouped tiles of one expert run m-fastest so that concurrently running CTAs
+// share the expert's weight tile through L2. K-grouped tiles take the experts
+// longest-first.
+//
+// Safety: every mbarrier wait is bounded by the caller's timeout (globaltimer);
+// on expiry the kernel records MOE_ERR_TIMEOUT, raises an abort flag that every
+// role polls, waits (bounded) for its own TMA copies, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
+
 namespace moe {
-bool tc_available() { return false; }
-size_t tc_grouped_ws_bytes(int) { return 0; }
-cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx&, int, int64_t, int, int, const int32_t*,
-                                         const void*, const void*, const void*, void*, void*,
-                                         void*, void*, int*) { return cudaErrorNotSupported; }
-cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx&, int, int64_t, int, int, const int32_t*,
-                                         const void*, const void*, const void*, const void*,
-                                         const void*, const void*, void*, void*, void*, void*,
-                                         void*, int*) { return cudaErrorNotSupported; }
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;      // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int NUM_THREADS = 192;                // 6 warps
+constexpr int TMEM_COLS = 512;
+constexpr int MAXG = 256;
+
+enum Epi { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_WGRAD = 3 };
+
+struct Params {
+  int G;              // groups (experts)
+  int n_rows;         // rows of the grouped operand (sum of the segments)
+  int K;              // M-grouped: reduction length
+  int N_out;          // output columns (M-grouped) / per-group N (K-grouped)
+  int M_out;          // K-grouped: per-group M
+  int NT, MT;         // tiles along N (and M for K-grouped)
+  int b_group_rows;   // M-grouped: rows of the B tensor map per group
+  int F;              // SwiGLU width
+  const int32_t* offsets;  // [G+1], NULL = one group of n_rows
+  bf16* out0;
+  int64_t ld0;
+  bf16* out1;         // fc1 forward: gate|up output (may be NULL)
+  const bf16* aux_in; // fc2 dgrad: gate|up input
+  int* status;
+  uint64_t timeout_ns;
+};
+
+struct __align__(8) Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int off[MAXG + 1];
+  int prefix[MAXG + 1];
+  int order[MAXG];
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the timeout ran out or another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Shared& sh,
+                                          const Params& P, int site) {
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((++n & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
+      if (global_timer_ns() - t0 > P.timeout_ns) {
+        record_error(P.status, MOE_ERR_TIMEOUT, site);
+        *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns: thread i gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout:
+// start>>4 [0,14), LBO>>4 [16,30), SBO>>4 [32,46), version 1 at [46,48),
+// layout type SWIZZLE_128B = 2 at [61,64)).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
+// A/B major-ness (0 = K-major, 1 = MN-major), N>>3 at [17,23), M>>4 at [24,29).
+__host__ __device__ constexpr uint32_t make_idesc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
+
+__device__ __forceinline__ void store_bf16x8(bf16* p, const float* v) {
+  uint4 r;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = r;
+}
+__device__ __forceinline__ void load_bf16x8(const bf16* p, float* v) {
+  uint4 r = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// ---------------------------------------------------------------- tile schedule
+struct Tile {
+  int grp;
+  int m0;       // M-grouped: first row (absolute); K-grouped: first output row
+  int m_end;    // row limit for stores
+  int n0;       // first output column (SwiGLU fwd: first gate column)
+  int k_begin;  // K-grouped: first row of the segment
+  int k_end;
+  int nk;       // k-blocks
+};
+
+template <bool KGROUPED, int EPI>
+__device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, int t) {
+  Tile ti;
+  if (!KGROUPED) {
+    int lo = 0, hi = P.G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sh.prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    const int rows = sh.off[g + 1] - sh.off[g];
+    const int mt = (rows + BM - 1) / BM;
+    const int local = t - sh.prefix[g];
+    const int ni = local / mt, mi = local - ni * mt;
+    ti.grp = g;
+    ti.m0 = sh.off[g] + mi * BM;
+    ti.m_end = sh.off[g + 1];
+    ti.n0 = ni * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
+    ti.k_begin = 0;
+    ti.k_end = P.K;
+    ti.nk = (P.K + BK - 1) / BK;
+  } else {
+    const int per = P.MT * P.NT;
+    const int gi = t / per;
+    const int local = t - gi * per;
+    const int g = sh.order[gi];
+    const int mi = local / P.NT, ni = local - mi * P.NT;
+    ti.grp = g;
+    ti.m0 = mi * BM;
+    ti.m_end = P.M_out;
+    ti.n0 = ni * BN;
+    ti.k_begin = sh.off[g];
+    ti.k_end = sh.off[g + 1];
+    ti.nk = (ti.k_end - ti.k_begin + BK - 1) / BK;
+  }
+  return ti;
+}
+
+// ---------------------------------------------------------------- the kernel
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Params P) {
+  constexpr bool KGROUPED = (EPI == EPI_WGRAD);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled stages
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stage_base = smem;
+  Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- set-up: segment offsets, tile prefix, barriers, TMEM
+  if (tid == 0) {
+    sh.abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh.tmem_full[a], 1);
+      mbar_init(&sh.tmem_empty[a], 4 * 32);
+    }
+    fence_barrier_init();
+  }
+  for (int g = tid; g <= P.G; g += NUM_THREADS) {
+    int v = P.offsets ? P.offsets[g] : (g == 0 ? 0 : P.n_rows);
+    sh.off[g] = v;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // validate: monotone, within [0, n_rows]; a bad segment becomes empty
+    int prev = 0;
+    bool bad = false;
+    for (int g = 0; g <= P.G; ++g) {
+      int v = sh.off[g];
+      if (v < prev || v > P.n_rows || (g == 0 && v != 0)) {
+        bad = true;
+        v = prev;
+      }
+      sh.off[g] = v;
+      prev = v;
+    }
+    if (bad) record_error(P.status, MOE_ERR_DEVICE_INDEX, -1);
+    if (!KGROUPED) {
+      int acc = 0;
+      for (int g = 0; g < P.G; ++g) {
+        sh.prefix[g] = acc;
+        acc += ((sh.off[g + 1] - sh.off[g] + BM - 1) / BM) * P.NT;
+      }
+      sh.prefix[P.G] = acc;
+      sh.total_tiles = acc;
+    } else {
+      sh.total_tiles = P.G * P.MT * P.NT;
+    }
+  }
+  if (KGROUPED) {
+    __syncthreads();
+    // longest segment first; ties by group index
+    for (int g = tid; g < P.G; g += NUM_THREADS) {
+      const int ng = sh.off[g + 1] - sh.off[g];
+      int rank = 0;
+      for (int h = 0; h < P.G; ++h) {
+        const int nh = sh.off[h + 1] - sh.off[h];
+        rank += (nh > ng) || (nh == ng && h < g);
+      }
+      sh.order[rank] = g;
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = sh.total_tiles;
+  const uint32_t tmem_base = sh.tmem_base;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;  // loads issued whose stage the MMA warp has not been seen to free
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh, P, 1)) { ok = false; break; }
+          uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
+          uint8_t* b_dst = a_dst + A_STAGE_BYTES;
+          uint64_t* bar = &sh.full[stage];
+          mbar_expect_tx(bar, STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (!A_MN) {
+            tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
+          } else {
+            tma_load_2d(a_dst, &tmA, bar, ti.m0, ti.k_begin + k0);
+            tma_load_2d(a_dst + 8192, &tmA, bar, ti.m0 + 64, ti.k_begin + k0);
+          }
+          if (!B_MN) {
+            if (EPI == EPI_SWIGLU_FWD) {
+              const int r0 = ti.grp * 2 * P.F;
+              tma_load_2d(b_dst, &tmB, bar, k0, r0 + ti.n0);
+              tma_load_2d(b_dst + 16384, &tmB, bar, k0, r0 + P.F + ti.n0);
+            } else {
+              tma_load_2d(b_dst, &tmB, bar, k0, ti.grp * P.b_group_rows + ti.n0);
+            }
+          } else {
+            const int y = KGROUPED ? ti.k_begin + k0 : ti.grp * P.b_group_rows + k0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + j * 8192, &tmB, bar, ti.n0 + 64 * j, y);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s) mbar_try_wait(&sh.full[s], 0);
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 2000000ull) { }
+      }
+      (void)issued;
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer (whole warp walks; lane 0 issues) =================
+    constexpr uint32_t IDESC = make_idesc(A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+      if (ti.nk == 0) continue;  // empty segment: the epilogue writes zeros itself
+      if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh, P, 2)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < ti.nk; ++kb) {
+        if (!mbar_wait(&sh.full[stage], phase, sh, P, 3)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* a_s = stage_base + stage * STAGE_BYTES;
+        uint8_t* b_s = a_s + A_STAGE_BYTES;
+        if (KGROUPED && kb == ti.nk - 1) {
+          // rows past the segment end belong to the next expert: zero them in A
+          const int valid = ti.k_end - (ti.k_begin + kb * BK);
+          if (valid < BK) {
+            for (int half = 0; half < 2; ++half) {
+              uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
+              const int n16 = (BK - valid) * 8;
+              for (int i = lane; i < n16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+            }
+            fence_async_shared();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const uint32_t a_addr = su32(a_s), b_addr = su32(b_s);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            uint64_t ad, bd;
+            if (!A_MN) ad = sw128_desc(a_addr + kk * 32, 16, 1024);
+            else ad = sw128_desc(a_addr + kk * 2048, 8192, 1024);
+            if (!B_MN) bd = sw128_desc(b_addr + kk * 32, 16, 1024);
+            else bd = sw128_desc(b_addr + kk * 2048, 8192, 1024);
+            mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&sh.empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&sh.tmem_full[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  } else {
+    // ================= epilogue: warps 2..5 =================
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+      if (EPI == EPI_WGRAD) {
+        const int m = ti.m0 + row_in_tile;
+        bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
+        if (ti.nk == 0) {
+          if (m < P.M_out) {
+            const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int c = 0; c < BN; c += 8)
+              if (ti.n0 + c < P.N_out) store_bf16x8(dst_row + ti.n0 + c, z);
+          }
+          continue;
+        }
+      }
+      if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh, P, 4)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+
+      if (EPI == EPI_SWIGLU_FWD) {
+        const int r = ti.m0 + row_in_tile;
+        const bool rv = r < ti.m_end;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          float g[32], u[32], h[32];
+          tmem_ld32(t_row + c, g);
+          tmem_ld32(t_row + BN / 2 + c, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
+          if (rv) {
+            const int f0 = ti.n0 + c;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (f0 + 8 * j < P.F) {
+                store_bf16x8(P.out0 + (int64_t)r * P.ld0 + f0 + 8 * j, h + 8 * j);
+                if (P.out1) {
+                  bf16* pr = P.out1 + (int64_t)r * 2 * P.F;
+                  store_bf16x8(pr + f0 + 8 * j, g + 8 * j);
+                  store_bf16x8(pr + P.F + f0 + 8 * j, u + 8 * j);
+                }
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_STORE) {
+        const int r = ti.m0 + row_in_tile;
+        const bool rv = r < ti.m_end;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(t_row + c, v);
+          if (rv) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (ti.n0 + c + 8 * j < P.N_out)
+                store_bf16x8(P.out0 + (int64_t)r * P.ld0 + ti.n0 + c + 8 * j, v + 8 * j);
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        const int r = ti.m0 + row_in_tile;
+        const bool rv = r < ti.m_end;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float dh[32];
+          tmem_ld32(t_row + c, dh);
+          if (rv) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int f = ti.n0 + c + 8 * j;
+              if (f < P.F) {
+                const bf16* pr = P.aux_in + (int64_t)r * 2 * P.F;
+                float gv[8], uv[8], dg[8], du[8];
+                load_bf16x8(pr + f, gv);
+                load_bf16x8(pr + P.F + f, uv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float s = 1.f / (1.f + __expf(-gv[i]));
+                  const float d = dh[8 * j + i];
+                  dg[i] = d * uv[i] * s * (1.f + gv[i] * (1.f - s));
+                  du[i] = d * gv[i] * s;
+                }
+                bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
+                store_bf16x8(dp + f, dg);
+                store_bf16x8(dp + P.F + f, du);
+              }
+            }
+          }
+        }
+      } else {  // EPI_WGRAD
+        const int m = ti.m0 + row_in_tile;
+        const bool rv = m < P.M_out;
+        bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(t_row + c, v);
+          if (rv) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (ti.n0 + c + 8 * j < P.N_out) store_bf16x8(dst_row + ti.n0 + c + 8 * j, v + 8 * j);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.tmem_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::mutex g_mu;
+
+static bool get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    cudaGetLastError();
+    return false;
+  }
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// bf16 row-major [rows, cols]; box = 64 columns (128 B, the swizzle span) x box_rows
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  if (!get_encoder()) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim,
+                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+
+template <bool A_MN, bool B_MN, int EPI>
+static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
+                              const Params& P) {
+  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
+  static std::atomic<uint64_t> attr_set_mask{0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set_mask.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set_mask.fetch_or(bit);
+  }
+  kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, P);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* offsets) {
+  Params P{};
+  P.G = G;
+  P.n_rows = (int)n_rows;
+  P.offsets = offsets;
+  P.status = c.status;
+  P.timeout_ns = c.timeout_ns;
+  return P;
+}
+
+}  // namespace tc
+
+bool tc_available() { return tc::get_encoder(); }
+
+size_t tc_grouped_ws_bytes(int) { return 0; }
+
+cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
+                                         const int32_t* offsets, const void* x_rows,
+                                         const void* w1, const void* w2, void* pre_gu, void* h,
+                                         void* out, void*, int* err) {
+  using namespace tc;
+  *err = MOE_OK;
+  if (n_rows == 0) return cudaSuccess;
+  CUtensorMap mA, mB;
+  // fc1: A = x_rows [n_rows, d] (K-major), B = W1 [G*2F, d] (K-major, 128-row boxes)
+  if (!make_map(&mA, x_rows, n_rows, d, 128) || !make_map(&mB, w1, (int64_t)G * 2 * F, d, 128)) {
+    *err = MOE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  Params P = base_params(c, G, n_rows, offsets);
+  P.K = d;
+  P.F = F;
+  P.NT = (F + BN / 2 - 1) / (BN / 2);
+  P.out0 = static_cast<bf16*>(h);
+  P.ld0 = F;
+  P.out1 = static_cast<bf16*>(pre_gu);
+  cudaError_t e = launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P);
+  if (e != cudaSuccess) return e;
+  // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
+  if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, 256)) {
+    *err = MOE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  Params Q = base_params(c, G, n_rows, offsets);
+  Q.K = F;
+  Q.N_out = d;
+  Q.NT = (d + BN - 1) / BN;
+  Q.b_group_rows = d;
+  Q.out0 = static_cast<bf16*>(out);
+  Q.ld0 = d;
+  return launch_one<false, false, EPI_STORE>(c, mA, mB, Q);
+}
+
+cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
+                                         const int32_t* offsets, const void* x_rows,
+                                         const void* w1, const void* w2, const void* pre_gu,
+                                         const void* h, const void* d_out, void* d_pre,
+                                         void* dx_rows, void* dw1, void* dw2, void*, int* err) {
+  using namespace tc;
+  *err = MOE_OK;
+  CUtensorMap mA, mB;
+  cudaError_t e;
+  if (n_rows > 0) {
+    // fc2 dgrad + SwiGLU backward: A = d_out [n_rows, d] K-major; B = W2 [G*d, F] MN-major
+    if (!make_map(&mA, d_out, n_rows, d, 128) || !make_map(&mB, w2, (int64_t)G * d, F, 64)) {
+      *err = MOE_ERR_CUDA;
+      return cudaSuccess;
+    }
+    Params P = base_params(c, G, n_rows, offsets);
+    P.K = d;
+    P.F = F;
+    P.N_out = F;
+    P.NT = (F + BN - 1) / BN;
+    P.b_group_rows = d;
+    P.out0 = static_cast<bf16*>(d_pre);
+    P.aux_in = static_cast<const bf16*>(pre_gu);
+    e = launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P);
+    if (e != cudaSuccess) return e;
+    // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
+    if (!make_map(&mA, d_pre, n_rows, 2 * F, 128) || !make_map(&mB, w1, (int64_t)G * 2 * F, d, 64)) {
+      *err = MOE_ERR_CUDA;
+      return cudaSuccess;
+    }
+    Params Q = base_params(c, G, n_rows, offsets);
+    Q.K = 2 * F;
+    Q.N_out = d;
+    Q.NT = (d + BN - 1) / BN;
+    Q.b_group_rows = 2 * F;
+    Q.out0 = static_cast<bf16*>(dx_rows);
+    Q.ld0 = d;
+    e = launch_one<false, true, EPI_STORE>(c, mA, mB, Q);
+    if (e != cudaSuccess) return e;
+  }
+  // fc2 wgrad: dW2_g [d, F] = d_outᵀ h : A = d_out [n_rows, d] MN-major, B = h [n_rows, F] MN-major
+  // (with no rows at all, 1-row maps are never read: every group is empty)
+  const int64_t mr = n_rows > 0 ? n_rows : 1;
+  if (!make_map(&mA, n_rows > 0 ? d_out : w2, mr, d, 64) ||
+      !make_map(&mB, n_rows > 0 ? h : w2, mr, F, 64)) {
+    *err = MOE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  Params R = base_params(c, G, n_rows, offsets);
+  R.M_out = d;
+  R.N_out = F;
+  R.MT = (d + BM - 1) / BM;
+  R.NT = (F + BN - 1) / BN;
+  R.out0 = static_cast<bf16*>(dw2);
+  e = launch_one<true, true, EPI_WGRAD>(c, mA, mB, R);
+  if (e != cudaSuccess) return e;
+  // fc1 wgrad: dW1_g [2F, d] = d_preᵀ x : A = d_pre [n_rows, 2F] MN-major, B = x_rows MN-major
+  if (!make_map(&mA, n_rows > 0 ? d_pre : w1, mr, 2 * F, 64) ||
+      !make_map(&mB, n_rows > 0 ? x_rows : w1, mr, d, 64)) {
+    *err = MOE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  Params S = base_params(c, G, n_rows, offsets);
+  S.M_out = 2 * F;
+  S.N_out = d;
+  S.MT = (2 * F + BM - 1) / BM;
+  S.NT = (d + BN - 1) / BN;
+  S.out0 = static_cast<bf16*>(dw1);
+  return launch_one<true, true, EPI_WGRAD>(c, mA, mB, S);
+}
+
+}  // namespace moe

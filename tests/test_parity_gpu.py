@@ -29,7 +29,11 @@ SMALL = {
                                 F=128, F_shared=192, backward=True),
     "zipf_small": mi.shrink(W["zipf_imbalance"], name="zipf_small", T=1024, d=192, F=136),
 }
-CASES = [(n, "native") for n in SMALL] + [(n, "f32") for n in SMALL if n != "tiny_fp32"]
+# bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
+# on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
+CASES = ([(n, "native", "tcgen05") for n in SMALL if n != "tiny_fp32"]
+         + [(n, "native", "cudacores") for n in SMALL]
+         + [(n, "f32", "cudacores") for n in SMALL if n != "tiny_fp32"])
 
 
 def _wl(name, dt):
@@ -39,17 +43,22 @@ def _wl(name, dt):
     return wl
 
 
-def run_gpu(wl, seed=0, backward=True):
+def run_gpu(wl, seed=0, backward=True, impl="tcgen05"):
     import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
     from routing_grouped_expert_gate_gb300 import layer
     inp = mi.make_inputs(wl, seed=seed, device="cuda", with_dy=backward)
     cfg = moe.cfg_from_workload(wl)
     p = layer.params_from_inputs(inp)
     b = layer.alloc_buffers(cfg, "cuda", backward=backward)
-    layer.forward(cfg, p, inp["x"], b)
-    if backward:
-        layer.backward(cfg, p, inp["x"], inp["dy"], b)
-    torch.cuda.synchronize()
+    old = L.set_grouped_gemm_impl(L.MOE_GEMM_AUTO if impl == "tcgen05" else L.MOE_GEMM_CUDA_CORES)
+    try:
+        layer.forward(cfg, p, inp["x"], b)
+        if backward:
+            layer.backward(cfg, p, inp["x"], inp["dy"], b)
+        torch.cuda.synchronize()
+    finally:
+        L.set_grouped_gemm_impl(old)
     rc, detail = moe._lib.last_device_status()
     assert rc == 0, f"device status {rc} ({moe.status_string(rc)}) detail {detail}"
     return inp, b
@@ -62,10 +71,10 @@ def built():
     import routing_grouped_expert_gate_gb300  # noqa: F401
 
 
-@pytest.mark.parametrize("name,dt", CASES)
-def test_layer_parity(built, name, dt):
+@pytest.mark.parametrize("name,dt,impl", CASES)
+def test_layer_parity(built, name, dt, impl):
     wl = _wl(name, dt)
-    inp, b = run_gpu(wl, backward=True)
+    inp, b = run_gpu(wl, backward=True, impl=impl)
     ref = {k: O.as_f64(v) for k, v in inp.items()}
     f = O.layer_forward(wl, ref)
     g = O.layer_backward(wl, ref, f, ref["dy"])
@@ -129,10 +138,11 @@ def test_zero_load_experts_exist_in_skewed_case(built):
     assert (counts == 0).sum() >= 1 and counts.max() > 3 * counts.mean()
 
 
-def test_deterministic_bytes(built):
+@pytest.mark.parametrize("impl", ["tcgen05", "cudacores"])
+def test_deterministic_bytes(built, impl):
     wl = SMALL["fine_grained_small"]
-    _, b1 = run_gpu(wl, backward=True)
-    _, b2 = run_gpu(wl, backward=True)
+    _, b1 = run_gpu(wl, backward=True, impl=impl)
+    _, b2 = run_gpu(wl, backward=True, impl=impl)
     for key in ("logits", "idx", "w", "row_of", "x_perm", "pre_gu", "out_perm", "y", "aux",
                 "d_pre", "dw1", "dw2", "dw_router", "dx"):
         assert torch.equal(b1[key], b2[key]), key
