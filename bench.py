@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (smaller cases for profiling)")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the forward only (the workload's own pass if it has no backward)")
     return ap.parse_args()
@@ -194,6 +196,8 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = mi.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        wl = mi.shrink(wl, name=f"{wl.name}_T{args.tokens}", T=args.tokens)
     backward = wl.backward and not args.fwd_only
     cfg = moe.cfg_from_workload(wl)
     inp = mi.make_inputs(wl, seed=0, device=dev, with_dy=backward)
@@ -443,6 +447,8 @@ def run_reference(args, ws, rank):
     import torch
     import moe_inputs as mi
     wl = mi.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        wl = mi.shrink(wl, name=f"{wl.name}_T{args.tokens}", T=args.tokens)
     backward = wl.backward and not args.fwd_only
     inp = mi.make_inputs(wl, seed=0, device="cpu", with_dy=backward)
     n_tok = max(1, args.cpu_sample_tokens // 3)
