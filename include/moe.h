@@ -179,6 +179,31 @@ int moe_unpermute_combine(const moe_cfg* cfg, const void* out_perm, const int32_
 int moe_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* counts,
                  float* aux, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Dispatch for callers that cannot allocate device memory. The source pages
+ * have no counterpart: this entry point exists for users of the library, not
+ * for the method. Some callers own no device allocator of their own: their
+ * device memory belongs to a host framework's pool that the library may not
+ * draw from, or they run where a cudaMalloc (with the synchronisation it can
+ * imply) is not allowed. Such callers cannot pass moe_permute a workspace.
+ * moe_permute_noalloc computes exactly what moe_permute computes (same
+ * kernels, same outputs, bit for bit) but keeps its scratch in a fixed device
+ * array inside the library (MOE_PERMUTE_NOALLOC_SCRATCH_BYTES = 1 MiB), which
+ * every GPU that loads the library holds until the process exits. It calls no
+ * allocation routine. The caller still passes every input and output.
+ *   Limit: ceil(T / 128) * E * 4 bytes of scratch, i.e. ceil(T/128) * E <=
+ *   262144 (T <= 131072 at E = 256); larger sizes return MOE_ERR_UNSUPPORTED
+ *   before any device work.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array and leaves its contents behind; nothing in
+ *   it needs to start at zero. Calls that overlap on the GPU (other streams,
+ *   other host threads) race on the array: serialise them.               */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
+int moe_permute_noalloc(const moe_cfg* cfg, const void* x, const int32_t* idx,
+                        int32_t* counts, int32_t* offsets, int32_t* row_of,
+                        int32_t* src_tok, void* x_perm, moe_stream_t stream);
+
 /* ---------------------------- backward ---------------------------------- */
 
 /* B6. Backward of the combine: d_out_perm[row_of[t,j]] = w[t,j]·dy[t];

@@ -95,6 +95,7 @@ _SIGS = {
     "moe_version": (c_char_p, []),
     "moe_launch_count": (c_uint64, []),
     "moe_set_grouped_gemm_impl": (c_int, [c_int]),
+    "moe_permute_noalloc": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -192,6 +193,13 @@ def permute(cfg, x, idx, counts, offsets, row_of, src_tok, x_perm, ws, stream=No
                            _p(row_of), _p(src_tok), _p(x_perm), _p(ws),
                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
            "moe_permute")
+
+
+def permute_noalloc(cfg, x, idx, counts, offsets, row_of, src_tok, x_perm, stream=None):
+    """moe_permute without a workspace: scratch lives in a fixed device array."""
+    _check(lib.moe_permute_noalloc(ctypes.byref(cfg), _p(x), _p(idx), _p(counts), _p(offsets),
+                                   _p(row_of), _p(src_tok), _p(x_perm), _stream(stream)),
+           "moe_permute_noalloc")
 
 
 def grouped_swiglu(cfg, n_groups, n_rows, F, offsets, x_rows, w1, w2, pre_gu, h, out, ws,

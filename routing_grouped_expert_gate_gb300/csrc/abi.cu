@@ -439,6 +439,52 @@ int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_
   return MOE_OK;
 }
 
+// ---- dispatch with a fixed device scratch array (no allocation by anyone)
+}  // extern "C"
+
+namespace moe {
+// The scratch of moe_permute_noalloc: per-block expert counts, then bases.
+// In host code this name is only a stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) int32_t g_noalloc_scratch[MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / 4];
+static std::mutex g_noalloc_mu;
+static int32_t* g_noalloc_ptr[kMaxDevices];
+}  // namespace moe
+
+extern "C" {
+
+int moe_permute_noalloc(const moe_cfg* cfg, const void* x, const int32_t* idx, int32_t* counts,
+                        int32_t* offsets, int32_t* row_of, int32_t* src_tok, void* x_perm,
+                        moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(counts); MOE_PTR(offsets);
+  if (cfg->T > 0) {
+    MOE_PTR(x); MOE_PTR(idx); MOE_PTR(row_of); MOE_PTR(src_tok); MOE_PTR(x_perm);
+  }
+  if (permute_ws_bytes(*cfg) > sizeof(g_noalloc_scratch)) return MOE_ERR_UNSUPPORTED;
+  MOE_CTX(stream, c);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  MOE_LAUNCH(launch_permute(c, *cfg, x, idx, counts, offsets, row_of, src_tok, x_perm, scratch));
+  return MOE_OK;
+}
+
 int moe_selftest_wait_timeout(moe_stream_t stream) {
   MOE_CTX(stream, c);
   MOE_LAUNCH(launch_wait_selftest(c));
