@@ -184,6 +184,16 @@ def stage_work(wl, cfg_backward):
     return w
 
 
+def kernel_flops(wl, backward):
+    """Algorithmic FLOPs per step of each grouped-GEMM kernel kind (routed + shared)."""
+    A, T, d, F, Fs = wl.T * wl.k, wl.T, wl.d, wl.F, wl.F_shared
+    one = 2.0 * (A * d * F + T * d * Fs)  # one d x F contraction over every row
+    k = {"fc1_fwd": 2 * one, "fc2_fwd": one}
+    if backward:
+        k.update({"fc2_dgrad": one, "fc1_dgrad": 2 * one, "fc2_wgrad": one, "fc1_wgrad": 2 * one})
+    return k
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import moe_inputs as mi
@@ -273,6 +283,7 @@ def run_ours(args, ws, rank, local):
     clocks.start()
     time.sleep(0.3)
     launches0 = L.launch_count()
+    L.kernel_timing(True)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -284,6 +295,8 @@ def run_ours(args, ws, rank, local):
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = L.launch_count() - launches0
+    L.kernel_timing(False)
+    ktimes = L.kernel_times()
     clk = clocks.stop()
     if dist:
         dist.barrier()
@@ -315,15 +328,36 @@ def run_ours(args, ws, rank, local):
     g_flops = sum(work[n]["flops"] for n in grouped)
     g_ms = sum(stage_ms[n] for n in grouped)
     g_tflops = g_flops / (g_ms * 1e-3) / 1e12
-    dom = max(grouped, key=lambda n: stage_ms[n])
-    dom_tflops = work[dom]["flops"] / (stage_ms[dom] * 1e-3) / 1e12
-    peak_sust = peaks["bf16_tflops_sustained"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(dom_tflops, 2),
-                "peak": peak_sust, "unit": "TFLOP/s",
-                "frac": round(dom_tflops / peak_sust, 4),
-                "traffic": recorded_traffic(dom),
-                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
-                "per_launch_flops": work[dom]["flops"]}
+    # Which peak: the clocks record decides. SM clock at its maximum through the
+    # timed region = burst conditions (the kernel ran like one timed alone);
+    # clock pulled down (power cap) = sustained conditions.
+    burst = (clk.get("sm_mhz") is not None and clk.get("sm_max_mhz")
+             and clk["sm_mhz"] >= 0.95 * clk["sm_max_mhz"])
+    peak = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    peak_src = (f"{peaks['source']} bf16 " + ("burst (SM clock stayed at its maximum)" if burst
+                else "sustained (SM clock below its maximum)"))
+    # per-kernel table from the library's own events on the launching stream
+    kflops = kernel_flops(wl, backward)
+    kernels = {}
+    for kind, (tot_ms, n) in ktimes.items():
+        if n == 0:
+            continue
+        per_step_ms = tot_ms / K
+        kernels[kind] = {"launches_per_step": n // K, "ms_per_step": round(per_step_ms, 4),
+                         "tflops": round(kflops[kind] / (per_step_ms * 1e-3) / 1e12, 2)}
+    if kernels:
+        dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+        n_per_step = kernels[dom]["launches_per_step"]
+        per_launch_flops = kflops[dom] / n_per_step
+        per_launch_ms = kernels[dom]["ms_per_step"] / n_per_step
+        achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": f"tc_grouped_gemm {dom}",
+                    "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom),
+                    "peak_source": peak_src, "flops_per_launch": per_launch_flops,
+                    "ms_per_launch": round(per_launch_ms, 4)}
+    else:
+        roofline = None
 
     out = {
         "metric": METRIC, "value": None, "unit": UNIT, "n_gpus": ws, "steps": K,
@@ -334,10 +368,11 @@ def run_ours(args, ws, rank, local):
                    "l2": "no flush: each step streams %.1f GB of expert weights (> 129 MB L2)"
                          % (E * 3 * cfg.d * F * (2 if wl.act_dtype == "bf16" else 4) / 1e9),
                    "parallelism": f"replicas x{ws}"},
-        "grouped_gemm_pct_bf16_peak": round(100 * g_tflops / peak_sust, 2),
+        "grouped_gemm_pct_bf16_peak": round(100 * g_tflops / peak, 2),
         "grouped_gemm_tflops": round(g_tflops, 2),
         "permute_gbs": stages["permute"].get("gbs"),
         "roofline": roofline,
+        "kernels": kernels,
         "stages": stages,
         "gpu_launches": int(launches),
         "clocks": clk,

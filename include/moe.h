@@ -295,6 +295,22 @@ int moe_selftest_wait_timeout(moe_stream_t stream);
 #define MOE_GEMM_CUDA_CORES 1
 int moe_set_grouped_gemm_impl(int impl);
 
+/* Per-kernel timing of the tcgen05 grouped GEMM kernels, for measurement.
+ * moe_kernel_timing(1) starts recording a CUDA event pair around every such
+ * launch on the current device (on the launching stream) and discards earlier
+ * records; moe_kernel_timing(0) stops recording. moe_kernel_times() waits for
+ * the recorded events and returns, per kernel kind (MOE_KERNEL_*), the summed
+ * milliseconds and the number of launches. Arrays hold MOE_KERNEL_KINDS entries. */
+#define MOE_KERNEL_FC1_FWD   0  /* fc1 + SwiGLU forward           */
+#define MOE_KERNEL_FC2_FWD   1  /* fc2 forward                    */
+#define MOE_KERNEL_FC2_DGRAD 2  /* fc2 dgrad + SwiGLU backward    */
+#define MOE_KERNEL_FC1_DGRAD 3  /* fc1 dgrad                      */
+#define MOE_KERNEL_FC2_WGRAD 4  /* fc2 weight gradient            */
+#define MOE_KERNEL_FC1_WGRAD 5  /* fc1 weight gradient            */
+#define MOE_KERNEL_KINDS     6
+int moe_kernel_timing(int enable);
+int moe_kernel_times(float* ms_total, int32_t* launches);
+
 /* Number of CUDA kernels this library has launched in this process (all
  * devices, all streams), counted on the host at launch time. */
 uint64_t moe_launch_count(void);

@@ -95,6 +95,8 @@ _SIGS = {
     "moe_version": (c_char_p, []),
     "moe_launch_count": (c_uint64, []),
     "moe_set_grouped_gemm_impl": (c_int, [c_int]),
+    "moe_kernel_timing": (c_int, [c_int]),
+    "moe_kernel_times": (c_int, [POINTER(c_float), POINTER(c_int32)]),
     "moe_permute_noalloc": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -119,6 +121,21 @@ def set_grouped_gemm_impl(impl: int) -> int:
     if rc < 0:
         raise MoeError(rc, "moe_set_grouped_gemm_impl")
     return rc
+
+
+KERNEL_KINDS = ["fc1_fwd", "fc2_fwd", "fc2_dgrad", "fc1_dgrad", "fc2_wgrad", "fc1_wgrad"]
+
+
+def kernel_timing(enable: bool):
+    _check(lib.moe_kernel_timing(1 if enable else 0), "moe_kernel_timing")
+
+
+def kernel_times():
+    """{kind: (total ms, launches)} of the tcgen05 grouped GEMM kernels recorded."""
+    ms = (c_float * len(KERNEL_KINDS))()
+    n = (c_int32 * len(KERNEL_KINDS))()
+    _check(lib.moe_kernel_times(ms, n), "moe_kernel_times")
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
 
 
 def version() -> str:

@@ -169,6 +169,12 @@ uint64_t moe_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns)
 
 uint64_t moe_launch_count(void) { return launches_so_far(); }
 
+int moe_kernel_timing(int enable) { return tc_timing_enable(enable); }
+
+int moe_kernel_times(float* ms_total, int32_t* launches) {
+  return tc_timing_read(ms_total, launches);
+}
+
 int moe_set_grouped_gemm_impl(int impl) {
   if (impl != MOE_GEMM_AUTO && impl != MOE_GEMM_CUDA_CORES) return MOE_ERR_INVALID_ARG;
   return g_gemm_impl.exchange(impl);

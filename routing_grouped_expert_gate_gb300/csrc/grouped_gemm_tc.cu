@@ -35,6 +35,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -539,10 +540,31 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
       } else if (EPI == EPI_SWIGLU_BWD) {
+        // gate/up of the row are read from global memory; the loads of the next
+        // 32-column chunk are issued before the current chunk is computed, so
+        // their latency hides behind the TMEM read and the math.
         const int r = ti.m0 + row_in_tile;
         const bool rv = r < ti.m_end;
+        const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
+        bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
+        uint4 gq[4], uq[4], gn[4], un[4];
+        auto fetch = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int f = ti.n0 + c + 8 * j;
+            if (rv && f < P.F) {
+              g[j] = __ldg(reinterpret_cast<const uint4*>(pr + f));
+              u[j] = __ldg(reinterpret_cast<const uint4*>(pr + P.F + f));
+            } else {
+              g[j] = make_uint4(0, 0, 0, 0);
+              u[j] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        };
+        fetch(0, gq, uq);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
+          if (c + 32 < BN) fetch(c + 32, gn, un);
           float dh[32];
           tmem_ld32(t_row + c, dh);
           if (rv) {
@@ -550,22 +572,32 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int j = 0; j < 4; ++j) {
               const int f = ti.n0 + c + 8 * j;
               if (f < P.F) {
-                const bf16* pr = P.aux_in + (int64_t)r * 2 * P.F;
                 float gv[8], uv[8], dg[8], du[8];
-                load_bf16x8(pr + f, gv);
-                load_bf16x8(pr + P.F + f, uv);
+                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gq[j]);
+                const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 a = __bfloat1622float2(g2[i]);
+                  const float2 b2 = __bfloat1622float2(u2[i]);
+                  gv[2 * i] = a.x; gv[2 * i + 1] = a.y;
+                  uv[2 * i] = b2.x; uv[2 * i + 1] = b2.y;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  const float s = 1.f / (1.f + __expf(-gv[i]));
+                  const float sg = 1.f / (1.f + __expf(-gv[i]));
                   const float d = dh[8 * j + i];
-                  dg[i] = d * uv[i] * s * (1.f + gv[i] * (1.f - s));
-                  du[i] = d * gv[i] * s;
+                  dg[i] = d * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
+                  du[i] = d * gv[i] * sg;
                 }
-                bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
                 store_bf16x8(dp + f, dg);
                 store_bf16x8(dp + P.F + f, du);
               }
             }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            gq[j] = gn[j];
+            uq[j] = un[j];
           }
         }
       } else {  // EPI_WGRAD
@@ -633,9 +665,38 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
 
+// ---- optional per-kernel timing (CUDA events on the launching stream)
+struct KernelTiming {
+  std::mutex mu;
+  bool on = false;
+  int device = -1;
+  std::vector<cudaEvent_t> ev[kTcKinds];  // start/end pairs, in launch order
+};
+static KernelTiming g_timing;
+
+static void timing_mark(int kind, cudaStream_t s, bool start) {
+  if (!g_timing.on) return;
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (!g_timing.on || dev != g_timing.device) return;
+  cudaEvent_t e;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  cudaEventRecord(e, s);
+  auto& v = g_timing.ev[kind];
+  if (!start && (v.size() & 1) == 0) {  // an end without its start: drop it
+    cudaEventDestroy(e);
+    return;
+  }
+  v.push_back(e);
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
-                              const Params& P) {
+                              const Params& P, int kind) {
   auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   int dev = 0;
@@ -647,9 +708,12 @@ static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtenso
     if (e != cudaSuccess) return e;
     attr_set_mask.fetch_or(bit);
   }
+  timing_mark(kind, c.stream, true);
   kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, P);
   note_launches(1);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  timing_mark(kind, c.stream, false);
+  return e;
 }
 
 static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* offsets) {
@@ -667,6 +731,44 @@ static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* of
 bool tc_available() { return tc::get_encoder(); }
 
 size_t tc_grouped_ws_bytes(int) { return 0; }
+
+int tc_timing_enable(int on) {
+  using namespace tc;
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  for (int k = 0; k < kTcKinds; ++k) {
+    for (cudaEvent_t e : g_timing.ev[k]) cudaEventDestroy(e);
+    g_timing.ev[k].clear();
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    g_timing.on = false;
+    return MOE_ERR_NO_DEVICE;
+  }
+  g_timing.device = dev;
+  g_timing.on = on != 0;
+  return MOE_OK;
+}
+
+int tc_timing_read(float* ms_total, int32_t* launches) {
+  using namespace tc;
+  std::lock_guard<std::mutex> lk(g_timing.mu);
+  for (int k = 0; k < kTcKinds; ++k) {
+    float tot = 0.f;
+    int n = 0;
+    auto& v = g_timing.ev[k];
+    for (size_t i = 0; i + 1 < v.size(); i += 2) {
+      if (cudaEventSynchronize(v[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, v[i], v[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+      tot += ms;
+      ++n;
+    }
+    if (ms_total) ms_total[k] = tot;
+    if (launches) launches[k] = n;
+  }
+  return MOE_OK;
+}
 
 cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
                                          const int32_t* offsets, const void* x_rows,
@@ -688,7 +790,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   P.out0 = static_cast<bf16*>(h);
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
-  cudaError_t e = launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P);
+  cudaError_t e = launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
   // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
   if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, 256)) {
@@ -702,7 +804,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   Q.b_group_rows = d;
   Q.out0 = static_cast<bf16*>(out);
   Q.ld0 = d;
-  return launch_one<false, false, EPI_STORE>(c, mA, mB, Q);
+  return launch_one<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd);
 }
 
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
@@ -728,7 +830,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     P.b_group_rows = d;
     P.out0 = static_cast<bf16*>(d_pre);
     P.aux_in = static_cast<const bf16*>(pre_gu);
-    e = launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P);
+    e = launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
     if (!make_map(&mA, d_pre, n_rows, 2 * F, 128) || !make_map(&mB, w1, (int64_t)G * 2 * F, d, 64)) {
@@ -742,7 +844,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     Q.b_group_rows = 2 * F;
     Q.out0 = static_cast<bf16*>(dx_rows);
     Q.ld0 = d;
-    e = launch_one<false, true, EPI_STORE>(c, mA, mB, Q);
+    e = launch_one<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad);
     if (e != cudaSuccess) return e;
   }
   // fc2 wgrad: dW2_g [d, F] = d_outᵀ h : A = d_out [n_rows, d] MN-major, B = h [n_rows, F] MN-major
@@ -759,7 +861,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   R.MT = (d + BM - 1) / BM;
   R.NT = (F + BN - 1) / BN;
   R.out0 = static_cast<bf16*>(dw2);
-  e = launch_one<true, true, EPI_WGRAD>(c, mA, mB, R);
+  e = launch_one<true, true, EPI_WGRAD>(c, mA, mB, R, kFc2Wgrad);
   if (e != cudaSuccess) return e;
   // fc1 wgrad: dW1_g [2F, d] = d_preᵀ x : A = d_pre [n_rows, 2F] MN-major, B = x_rows MN-major
   if (!make_map(&mA, n_rows > 0 ? d_pre : w1, mr, 2 * F, 64) ||
@@ -773,7 +875,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   S.MT = (2 * F + BM - 1) / BM;
   S.NT = (d + BN - 1) / BN;
   S.out0 = static_cast<bf16*>(dw1);
-  return launch_one<true, true, EPI_WGRAD>(c, mA, mB, S);
+  return launch_one<true, true, EPI_WGRAD>(c, mA, mB, S, kFc1Wgrad);
 }
 
 }  // namespace moe
