@@ -735,6 +735,10 @@ size_t tc_grouped_ws_bytes(int) { return 0; }
 int tc_timing_enable(int on) {
   using namespace tc;
   std::lock_guard<std::mutex> lk(g_timing.mu);
+  if (!on) {  // stop recording; keep what was recorded for tc_timing_read
+    g_timing.on = false;
+    return MOE_OK;
+  }
   for (int k = 0; k < kTcKinds; ++k) {
     for (cudaEvent_t e : g_timing.ev[k]) cudaEventDestroy(e);
     g_timing.ev[k].clear();
@@ -746,7 +750,7 @@ int tc_timing_enable(int on) {
     return MOE_ERR_NO_DEVICE;
   }
   g_timing.device = dev;
-  g_timing.on = on != 0;
+  g_timing.on = true;
   return MOE_OK;
 }
 
