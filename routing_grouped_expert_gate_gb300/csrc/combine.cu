@@ -45,41 +45,35 @@ combine_kernel(const T* __restrict__ out_perm, const int32_t* __restrict__ row_o
       }
       rows[j] = r;
     }
-    for (int g0 = 0; g0 < ng; g0 += 64) {
-      // two 8-element groups per lane in flight
-      float acc[2][8];
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+    // one 8-element group per lane per step; the k rows (and the shared row)
+    // are all loaded before any is used
+    for (int g = lane; g < ng; g += 32) {
+      Raw8<T> raw[kMaxK];
+      Raw8<T> sraw;
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        if (j < k && rows[j] >= 0) {
+        if (j < k && rows[j] >= 0) raw[j].load(out_perm + rows[j] * d + 8 * g);
+        else raw[j].zero();
+      }
+      if (shared_out != nullptr) sraw.load(shared_out + t * d + 8 * g);
+      else sraw.zero();
+      float acc[8];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int g = g0 + 32 * u + lane;
-            if (g < ng) {
-              float v[8];
-              load8(out_perm + rows[j] * d + 8 * g, v);
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wj[j], v[i], acc[u][i]);
-            }
-          }
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          float v[8];
+          raw[j].to_float(v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j], v[i], acc[i]);
         }
       }
+      float sv[8];
+      sraw.to_float(sv);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int g = g0 + 32 * u + lane;
-        if (g < ng) {
-          if (shared_out != nullptr) {
-            float v[8];
-            load8(shared_out + t * d + 8 * g, v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] += v[i];
-          }
-          store8(y + t * d + 8 * g, acc[u]);
-        }
-      }
+      for (int i = 0; i < 8; ++i) acc[i] += sv[i];
+      store8(y + t * d + 8 * g, acc);
     }
   }
 }
@@ -114,13 +108,20 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ out_perm,
       rows[j] = r;
     }
     for (int g = lane; g < ng; g += 32) {
+      Raw8<T> graw, raw[kMaxK];
+      graw.load(dy + t * d + 8 * g);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && rows[j] >= 0) raw[j].load(out_perm + rows[j] * d + 8 * g);
+        else raw[j].zero();
+      }
       float g8[8];
-      load8(dy + t * d + 8 * g, g8);
+      graw.to_float(g8);
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         if (j < k && rows[j] >= 0) {
           float v[8], o[8];
-          load8(out_perm + rows[j] * d + 8 * g, v);
+          raw[j].to_float(v);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             dot[j] = fmaf(g8[i], v[i], dot[j]);

@@ -216,28 +216,32 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
       rows[j] = r;
     }
     for (int g = lane; g < ng; g += 32) {
-      float acc[8];
-      if (dx_router != nullptr) {
-        load8(dx_router + t * d + 8 * g, acc);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      }
+      Raw8<T> raw[kMaxK], sraw;
+      Raw8<float> rraw;
+      if (dx_router != nullptr) rraw.load(dx_router + t * d + 8 * g);
+      else rraw.zero();
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        if (j < k && rows[j] >= 0) {
+        if (j < k && rows[j] >= 0) raw[j].load(dx_perm + rows[j] * d + 8 * g);
+        else raw[j].zero();
+      }
+      if (dx_shared != nullptr) sraw.load(dx_shared + t * d + 8 * g);
+      else sraw.zero();
+      float acc[8];
+      rraw.to_float(acc);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
           float v[8];
-          load8(dx_perm + rows[j] * d + 8 * g, v);
+          raw[j].to_float(v);
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[i] += v[i];
         }
       }
-      if (dx_shared != nullptr) {
-        float v[8];
-        load8(dx_shared + t * d + 8 * g, v);
+      float sv[8];
+      sraw.to_float(sv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += v[i];
-      }
+      for (int i = 0; i < 8; ++i) acc[i] += sv[i];
       store8(dx + t * d + 8 * g, acc);
     }
   }

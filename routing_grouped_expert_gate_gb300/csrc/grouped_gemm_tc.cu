@@ -138,6 +138,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
       : "memory");
 }
+// Bring a tile into L2 ahead of its TMA load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -377,50 +384,82 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   if (warp == 0) {
     // ================= TMA producer =================
+    // Loads run up to STAGES k-blocks ahead of the MMAs; an L2 prefetch cursor
+    // runs PF k-blocks ahead of the loads (across tile boundaries), so weight
+    // tiles arriving from DRAM are already in L2 when their load is issued.
     if (lane == 0) {
+      constexpr int PF = 2 * STAGES;
+      // issue (or only prefetch) the A and B boxes of k-block kb of tile ti
+      auto kblock = [&](const Tile& ti, int kb, bool prefetch_only, uint8_t* a_dst, uint8_t* b_dst,
+                        uint64_t* bar) {
+        const int k0 = kb * BK;
+        if (!A_MN) {
+          if (prefetch_only) tma_prefetch_2d(&tmA, k0, ti.m0);
+          else tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
+        } else {
+          for (int h = 0; h < 2; ++h) {
+            if (prefetch_only) tma_prefetch_2d(&tmA, ti.m0 + 64 * h, ti.k_begin + k0);
+            else tma_load_2d(a_dst + 8192 * h, &tmA, bar, ti.m0 + 64 * h, ti.k_begin + k0);
+          }
+        }
+        if (!B_MN) {
+          if (EPI == EPI_SWIGLU_FWD) {
+            const int r0 = ti.grp * 2 * P.F;
+            for (int h = 0; h < 2; ++h) {
+              const int y = r0 + h * P.F + ti.n0;
+              if (prefetch_only) tma_prefetch_2d(&tmB, k0, y);
+              else tma_load_2d(b_dst + 16384 * h, &tmB, bar, k0, y);
+            }
+          } else {
+            const int y = ti.grp * P.b_group_rows + ti.n0;
+            if (prefetch_only) tma_prefetch_2d(&tmB, k0, y);
+            else tma_load_2d(b_dst, &tmB, bar, k0, y);
+          }
+        } else {
+          const int y = KGROUPED ? ti.k_begin + k0 : ti.grp * P.b_group_rows + k0;
+          for (int j = 0; j < 4; ++j) {
+            if (prefetch_only) tma_prefetch_2d(&tmB, ti.n0 + 64 * j, y);
+            else tma_load_2d(b_dst + j * 8192, &tmB, bar, ti.n0 + 64 * j, y);
+          }
+        }
+      };
+      // prefetch cursor
+      int pt = blockIdx.x, pkb = 0;
+      Tile pti;
+      if (pt < total) pti = decode_tile<KGROUPED, EPI>(sh, P, pt);
+      auto prefetch_next = [&]() {
+        while (pt < total && pkb >= pti.nk) {
+          pt += gridDim.x;
+          pkb = 0;
+          if (pt < total) pti = decode_tile<KGROUPED, EPI>(sh, P, pt);
+        }
+        if (pt < total) {
+          kblock(pti, pkb, true, nullptr, nullptr, nullptr);
+          ++pkb;
+        }
+      };
+      for (int i = 0; i < PF; ++i) prefetch_next();
+
       int stage = 0;
       uint32_t phase = 0;
-      int issued = 0;  // loads issued whose stage the MMA warp has not been seen to free
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh, P, 1)) { ok = false; break; }
           uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
-          uint8_t* b_dst = a_dst + A_STAGE_BYTES;
           uint64_t* bar = &sh.full[stage];
           mbar_expect_tx(bar, STAGE_BYTES);
-          const int k0 = kb * BK;
-          if (!A_MN) {
-            tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
-          } else {
-            tma_load_2d(a_dst, &tmA, bar, ti.m0, ti.k_begin + k0);
-            tma_load_2d(a_dst + 8192, &tmA, bar, ti.m0 + 64, ti.k_begin + k0);
-          }
-          if (!B_MN) {
-            if (EPI == EPI_SWIGLU_FWD) {
-              const int r0 = ti.grp * 2 * P.F;
-              tma_load_2d(b_dst, &tmB, bar, k0, r0 + ti.n0);
-              tma_load_2d(b_dst + 16384, &tmB, bar, k0, r0 + P.F + ti.n0);
-            } else {
-              tma_load_2d(b_dst, &tmB, bar, k0, ti.grp * P.b_group_rows + ti.n0);
-            }
-          } else {
-            const int y = KGROUPED ? ti.k_begin + k0 : ti.grp * P.b_group_rows + k0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + j * 8192, &tmB, bar, ti.n0 + 64 * j, y);
-          }
-          ++issued;
+          kblock(ti, kb, false, a_dst, a_dst + A_STAGE_BYTES, bar);
+          prefetch_next();
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
       if (!ok) {
         // let the copies already in flight land before the CTA exits
-        for (int s = 0; s < STAGES; ++s) mbar_try_wait(&sh.full[s], 0);
         const uint64_t t0 = global_timer_ns();
         while (global_timer_ns() - t0 < 2000000ull) { }
       }
-      (void)issued;
     }
   } else if (warp == 1) {
     // ================= MMA issuer (whole warp walks; lane 0 issues) =================

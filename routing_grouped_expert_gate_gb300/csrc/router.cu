@@ -120,7 +120,7 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 constexpr int RT_BT = 128, RT_BE = 64, RT_KC = 32;
 
 template <typename Tx>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
                     const float* __restrict__ logit_bias, float* __restrict__ logits,
                     int64_t T, int d, int E) {
@@ -140,51 +140,40 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
     for (int j = 0; j < 8; ++j) acc[i][j] = hi[i][j] = lo[i][j] = 0.f;
 
   // loader roles: x: 2 x (token = v & 127, group kg = v >> 7); W: expert tid & 63, kg tid >> 6
-  float xr[2][8], wr[8];
-  auto load_chunk = [&](int k0) {
+  auto stage_chunk = [&](int k0) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int v = tid + 256 * r;
       const int tok = v & 127, kg = v >> 7;
       const int64_t t = t_base + tok;
       const int kk = k0 + 8 * kg;
+      float xr[8];
       if (t < T && kk < d) {
-        load8(x + t * d + kk, xr[r]);
+        load8(x + t * d + kk, xr);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xr[r][i] = 0.f;
+        for (int i = 0; i < 8; ++i) xr[i] = 0.f;
       }
-    }
-    {
-      const int e = tid & 63, kg = tid >> 6;
-      const int kk = k0 + 8 * kg;
-      if (e_base + e < E && kk < d) {
-        load8(W + (int64_t)(e_base + e) * d + kk, wr);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wr[i] = 0.f;
-      }
-    }
-  };
-  auto store_chunk = [&]() {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int v = tid + 256 * r;
-      const int tok = v & 127, kg = v >> 7;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xs[kg * 8 + i][tok] = xr[r][i];
+      for (int i = 0; i < 8; ++i) xs[kg * 8 + i][tok] = xr[i];
     }
     const int e = tid & 63, kg = tid >> 6;
+    const int kk = k0 + 8 * kg;
+    float wr[8];
+    if (e_base + e < E && kk < d) {
+      load8(W + (int64_t)(e_base + e) * d + kk, wr);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wr[i] = 0.f;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) ws[kg * 8 + i][e] = wr[i];
   };
 
-  load_chunk(0);
   for (int k0 = 0; k0 < d; k0 += RT_KC) {
     __syncthreads();
-    store_chunk();
+    stage_chunk(k0);
     __syncthreads();
-    if (k0 + RT_KC < d) load_chunk(k0 + RT_KC);
 #pragma unroll
     for (int kk = 0; kk < RT_KC; ++kk) {
       const float4 a = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
