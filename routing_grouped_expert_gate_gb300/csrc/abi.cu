@@ -176,8 +176,12 @@ int moe_kernel_times(float* ms_total, int32_t* launches) {
 }
 
 int moe_set_grouped_gemm_impl(int impl) {
-  if (impl != MOE_GEMM_AUTO && impl != MOE_GEMM_CUDA_CORES) return MOE_ERR_INVALID_ARG;
-  return g_gemm_impl.exchange(impl);
+  if (impl != MOE_GEMM_AUTO && impl != MOE_GEMM_CUDA_CORES && impl != MOE_GEMM_TC_SINGLE_CTA)
+    return MOE_ERR_INVALID_ARG;
+  tc_set_single_cta(impl == MOE_GEMM_TC_SINGLE_CTA);
+  const int prev = g_gemm_impl.exchange(impl == MOE_GEMM_CUDA_CORES ? MOE_GEMM_CUDA_CORES
+                                                                   : MOE_GEMM_AUTO);
+  return prev;
 }
 
 int moe_last_device_status(moe_stream_t stream, int32_t* detail) {

@@ -113,7 +113,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false when the timeout ran out or another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Shared& sh,
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int& abort_flag,
                                           const Params& P, int site) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -121,10 +121,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Shared& 
   while (true) {
     if (mbar_try_wait(b, parity)) return true;
     if ((++n & 63u) == 0) {
-      if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) return false;
       if (global_timer_ns() - t0 > P.timeout_ns) {
         record_error(P.status, MOE_ERR_TIMEOUT, site);
-        *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+        *reinterpret_cast<volatile int*>(&abort_flag) = 1;
         return false;
       }
     }
@@ -293,6 +293,129 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
   return ti;
 }
 
+// ---------------------------------------------------------------- epilogues
+// One thread per accumulator row (TMEM lane): read the row's 256 fp32 columns
+// with tcgen05.ld (all lanes of the warp together) and write the outputs.
+template <int EPI>
+__device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
+                                           int row_in_tile) {
+  if (EPI == EPI_SWIGLU_FWD) {
+    const int r = ti.m0 + row_in_tile;
+    const bool rv = r < ti.m_end;
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      float g[32], u[32], h[32];
+      tmem_ld32(t_row + c, g);
+      tmem_ld32(t_row + BN / 2 + c, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
+      if (rv) {
+        const int f0 = ti.n0 + c;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (f0 + 8 * j < P.F) {
+            store_bf16x8(P.out0 + (int64_t)r * P.ld0 + f0 + 8 * j, h + 8 * j);
+            if (P.out1) {
+              bf16* pr = P.out1 + (int64_t)r * 2 * P.F;
+              store_bf16x8(pr + f0 + 8 * j, g + 8 * j);
+              store_bf16x8(pr + P.F + f0 + 8 * j, u + 8 * j);
+            }
+          }
+        }
+      }
+    }
+  } else if (EPI == EPI_STORE) {
+    const int r = ti.m0 + row_in_tile;
+    const bool rv = r < ti.m_end;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      float v[32];
+      tmem_ld32(t_row + c, v);
+      if (rv) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (ti.n0 + c + 8 * j < P.N_out)
+            store_bf16x8(P.out0 + (int64_t)r * P.ld0 + ti.n0 + c + 8 * j, v + 8 * j);
+      }
+    }
+  } else if (EPI == EPI_SWIGLU_BWD) {
+    // gate/up of the row are read from global memory; the loads of the next
+    // 32-column chunk are issued before the current chunk is computed, so
+    // their latency hides behind the TMEM read and the math.
+    const int r = ti.m0 + row_in_tile;
+    const bool rv = r < ti.m_end;
+    const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
+    bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
+    uint4 gq[4], uq[4], gn[4], un[4];
+    auto fetch = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int f = ti.n0 + c + 8 * j;
+        if (rv && f < P.F) {
+          g[j] = __ldg(reinterpret_cast<const uint4*>(pr + f));
+          u[j] = __ldg(reinterpret_cast<const uint4*>(pr + P.F + f));
+        } else {
+          g[j] = make_uint4(0, 0, 0, 0);
+          u[j] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    };
+    fetch(0, gq, uq);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (c + 32 < BN) fetch(c + 32, gn, un);
+      float dh[32];
+      tmem_ld32(t_row + c, dh);
+      if (rv) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int f = ti.n0 + c + 8 * j;
+          if (f < P.F) {
+            float gv[8], uv[8], dg[8], du[8];
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gq[j]);
+            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 a = __bfloat1622float2(g2[i]);
+              const float2 b2 = __bfloat1622float2(u2[i]);
+              gv[2 * i] = a.x; gv[2 * i + 1] = a.y;
+              uv[2 * i] = b2.x; uv[2 * i + 1] = b2.y;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float sg = 1.f / (1.f + __expf(-gv[i]));
+              const float d = dh[8 * j + i];
+              dg[i] = d * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
+              du[i] = d * gv[i] * sg;
+            }
+            store_bf16x8(dp + f, dg);
+            store_bf16x8(dp + P.F + f, du);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gq[j] = gn[j];
+        uq[j] = un[j];
+      }
+    }
+  } else {  // EPI_WGRAD
+    const int m = ti.m0 + row_in_tile;
+    const bool rv = m < P.M_out;
+    bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      float v[32];
+      tmem_ld32(t_row + c, v);
+      if (rv) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (ti.n0 + c + 8 * j < P.N_out) store_bf16x8(dst_row + ti.n0 + c + 8 * j, v + 8 * j);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -384,11 +507,10 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   if (warp == 0) {
     // ================= TMA producer =================
-    // Loads run up to STAGES k-blocks ahead of the MMAs; an L2 prefetch cursor
-    // runs PF k-blocks ahead of the loads (across tile boundaries), so weight
-    // tiles arriving from DRAM are already in L2 when their load is issued.
+    // Loads run up to STAGES k-blocks ahead of the MMAs. (An L2 prefetch of
+    // later k-blocks by every CTA was measured to slow the kernel down: the
+    // CTAs sharing a weight tile all prefetch it.)
     if (lane == 0) {
-      constexpr int PF = 2 * STAGES;
       // issue (or only prefetch) the A and B boxes of k-block kb of tile ti
       auto kblock = [&](const Tile& ti, int kb, bool prefetch_only, uint8_t* a_dst, uint8_t* b_dst,
                         uint64_t* bar) {
@@ -423,35 +545,17 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
       };
-      // prefetch cursor
-      int pt = blockIdx.x, pkb = 0;
-      Tile pti;
-      if (pt < total) pti = decode_tile<KGROUPED, EPI>(sh, P, pt);
-      auto prefetch_next = [&]() {
-        while (pt < total && pkb >= pti.nk) {
-          pt += gridDim.x;
-          pkb = 0;
-          if (pt < total) pti = decode_tile<KGROUPED, EPI>(sh, P, pt);
-        }
-        if (pt < total) {
-          kblock(pti, pkb, true, nullptr, nullptr, nullptr);
-          ++pkb;
-        }
-      };
-      for (int i = 0; i < PF; ++i) prefetch_next();
-
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh, P, 1)) { ok = false; break; }
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh.abort, P, 1)) { ok = false; break; }
           uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
           uint64_t* bar = &sh.full[stage];
           mbar_expect_tx(bar, STAGE_BYTES);
           kblock(ti, kb, false, a_dst, a_dst + A_STAGE_BYTES, bar);
-          prefetch_next();
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -472,11 +576,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
       if (ti.nk == 0) continue;  // empty segment: the epilogue writes zeros itself
-      if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh, P, 2)) { ok = false; break; }
+      if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 2)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < ti.nk; ++kb) {
-        if (!mbar_wait(&sh.full[stage], phase, sh, P, 3)) { ok = false; break; }
+        if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 3)) { ok = false; break; }
         tc_fence_after();
         uint8_t* a_s = stage_base + stage * STAGE_BYTES;
         uint8_t* b_s = a_s + A_STAGE_BYTES;
@@ -535,125 +639,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           continue;
         }
       }
-      if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh, P, 4)) break;
+      if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 4)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
-      if (EPI == EPI_SWIGLU_FWD) {
-        const int r = ti.m0 + row_in_tile;
-        const bool rv = r < ti.m_end;
-#pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          float g[32], u[32], h[32];
-          tmem_ld32(t_row + c, g);
-          tmem_ld32(t_row + BN / 2 + c, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
-          if (rv) {
-            const int f0 = ti.n0 + c;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (f0 + 8 * j < P.F) {
-                store_bf16x8(P.out0 + (int64_t)r * P.ld0 + f0 + 8 * j, h + 8 * j);
-                if (P.out1) {
-                  bf16* pr = P.out1 + (int64_t)r * 2 * P.F;
-                  store_bf16x8(pr + f0 + 8 * j, g + 8 * j);
-                  store_bf16x8(pr + P.F + f0 + 8 * j, u + 8 * j);
-                }
-              }
-            }
-          }
-        }
-      } else if (EPI == EPI_STORE) {
-        const int r = ti.m0 + row_in_tile;
-        const bool rv = r < ti.m_end;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(t_row + c, v);
-          if (rv) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (ti.n0 + c + 8 * j < P.N_out)
-                store_bf16x8(P.out0 + (int64_t)r * P.ld0 + ti.n0 + c + 8 * j, v + 8 * j);
-          }
-        }
-      } else if (EPI == EPI_SWIGLU_BWD) {
-        // gate/up of the row are read from global memory; the loads of the next
-        // 32-column chunk are issued before the current chunk is computed, so
-        // their latency hides behind the TMEM read and the math.
-        const int r = ti.m0 + row_in_tile;
-        const bool rv = r < ti.m_end;
-        const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
-        bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
-        uint4 gq[4], uq[4], gn[4], un[4];
-        auto fetch = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int f = ti.n0 + c + 8 * j;
-            if (rv && f < P.F) {
-              g[j] = __ldg(reinterpret_cast<const uint4*>(pr + f));
-              u[j] = __ldg(reinterpret_cast<const uint4*>(pr + P.F + f));
-            } else {
-              g[j] = make_uint4(0, 0, 0, 0);
-              u[j] = make_uint4(0, 0, 0, 0);
-            }
-          }
-        };
-        fetch(0, gq, uq);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          if (c + 32 < BN) fetch(c + 32, gn, un);
-          float dh[32];
-          tmem_ld32(t_row + c, dh);
-          if (rv) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int f = ti.n0 + c + 8 * j;
-              if (f < P.F) {
-                float gv[8], uv[8], dg[8], du[8];
-                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gq[j]);
-                const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float2 a = __bfloat1622float2(g2[i]);
-                  const float2 b2 = __bfloat1622float2(u2[i]);
-                  gv[2 * i] = a.x; gv[2 * i + 1] = a.y;
-                  uv[2 * i] = b2.x; uv[2 * i + 1] = b2.y;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float sg = 1.f / (1.f + __expf(-gv[i]));
-                  const float d = dh[8 * j + i];
-                  dg[i] = d * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
-                  du[i] = d * gv[i] * sg;
-                }
-                store_bf16x8(dp + f, dg);
-                store_bf16x8(dp + P.F + f, du);
-              }
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            gq[j] = gn[j];
-            uq[j] = un[j];
-          }
-        }
-      } else {  // EPI_WGRAD
-        const int m = ti.m0 + row_in_tile;
-        const bool rv = m < P.M_out;
-        bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(t_row + c, v);
-          if (rv) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (ti.n0 + c + 8 * j < P.N_out) store_bf16x8(dst_row + ti.n0 + c + 8 * j, v + 8 * j);
-          }
-        }
-      }
+      drain_tile<EPI>(P, ti, t_row, row_in_tile);
       tc_fence_before();
       mbar_arrive(&sh.tmem_empty[acc]);
       acc ^= 1;
@@ -666,6 +656,304 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- CTA-pair kernel
+// The M-grouped contractions on a pair of CTAs (a 2-CTA cluster on two SMs):
+// one tcgen05.mma.cta_group::2 instruction computes a 256 x 256 tile whose
+// rows 0..127 come from (and accumulate in) the even CTA and rows 128..255 in
+// the odd one; each CTA stages only its own 128 rows of A and its own half
+// (128 columns) of B. Per SM and per K step that is 32 KB of shared-memory
+// traffic each way instead of 48 KB in and 48 KB read by the single-CTA
+// kernel, and 6 pipeline stages fit instead of 4.
+// Protocol: both CTAs' TMA loads complete on the even CTA's `full` barrier;
+// the even CTA issues the MMAs and its commits arrive on both CTAs' `empty`
+// and `tmem_full` barriers; every epilogue warp of both CTAs arrives on the
+// even CTA's `tmem_empty`.
+constexpr int STAGES2 = 6;
+constexpr int A2_BYTES = BM * BK * 2;              // 16 KB: this CTA's 128 rows
+constexpr int B2_BYTES = (BN / 2) * BK * 2;        // 16 KB: this CTA's half of N
+constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KB
+constexpr int PAIR_ACC = 1;                        // accumulators per CTA (x 256 columns)
+
+struct __align__(8) Shared2 {
+  uint64_t full[STAGES2];
+  uint64_t empty[STAGES2];
+  uint64_t tmem_full[PAIR_ACC];
+  uint64_t tmem_empty[PAIR_ACC];
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int off[MAXG + 1];
+  int prefix[MAXG + 1];
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// TMA into this CTA's shared memory, completing on a barrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster_addr, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at this offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(su32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__host__ __device__ constexpr uint32_t make_idesc_pair(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
+}
+
+template <int EPI>
+__device__ __forceinline__ Tile decode_pair_tile(const Shared2& sh, const Params& P, int t,
+                                                 uint32_t rank) {
+  int lo = 0, hi = P.G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sh.prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int g = lo;
+  const int rows = sh.off[g + 1] - sh.off[g];
+  const int mp = (rows + 2 * BM - 1) / (2 * BM);
+  const int local = t - sh.prefix[g];
+  const int ni = local / mp, mi = local - ni * mp;
+  Tile ti;
+  ti.grp = g;
+  ti.m0 = sh.off[g] + mi * 2 * BM + (int)rank * BM;
+  ti.m_end = sh.off[g + 1];
+  ti.n0 = ni * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
+  ti.k_begin = 0;
+  ti.k_end = P.K;
+  ti.nk = (P.K + BK - 1) / BK;
+  return ti;
+}
+
+template <bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const Params P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stage_base = smem;
+  Shared2& sh = *reinterpret_cast<Shared2*>(smem + STAGES2 * STAGE2_BYTES);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int cluster_id = blockIdx.x >> 1;
+  const int n_clusters = gridDim.x >> 1;
+
+  if (tid == 0) {
+    sh.abort = 0;
+    for (int s2 = 0; s2 < STAGES2; ++s2) {
+      mbar_init(&sh.full[s2], 1);
+      mbar_init(&sh.empty[s2], 1);
+    }
+    for (int a = 0; a < PAIR_ACC; ++a) {
+      mbar_init(&sh.tmem_full[a], 1);
+      mbar_init(&sh.tmem_empty[a], 2 * 4);
+    }
+    fence_barrier_init();
+  }
+  for (int g = tid; g <= P.G; g += NUM_THREADS)
+    sh.off[g] = P.offsets ? P.offsets[g] : (g == 0 ? 0 : P.n_rows);
+  __syncthreads();
+  if (tid == 0) {
+    int prev = 0;
+    bool bad = false;
+    for (int g = 0; g <= P.G; ++g) {
+      int v = sh.off[g];
+      if (v < prev || v > P.n_rows || (g == 0 && v != 0)) {
+        bad = true;
+        v = prev;
+      }
+      sh.off[g] = v;
+      prev = v;
+    }
+    if (bad && leader) record_error(P.status, MOE_ERR_DEVICE_INDEX, -1);
+    int acc = 0;
+    for (int g = 0; g < P.G; ++g) {
+      sh.prefix[g] = acc;
+      acc += ((sh.off[g + 1] - sh.off[g] + 2 * BM - 1) / (2 * BM)) * P.NT;
+    }
+    sh.prefix[P.G] = acc;
+    sh.total_tiles = acc;
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&sh.tmem_base, PAIR_ACC * BN);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // both CTAs' barriers and TMEM exist before any remote access
+  tc_fence_after();
+
+  // both CTAs must hold their accumulators at the same TMEM address
+  const uint32_t tmem_base = sh.tmem_base;
+  const uint32_t peer_base = ld_shared_cluster_u32(mapa_shared(su32(&sh.tmem_base), rank ^ 1u));
+  const bool usable = (peer_base == tmem_base);
+  if (!usable && tid == 0 && leader) record_error(P.status, MOE_ERR_CUDA, 2000);
+  const int total = usable ? sh.total_tiles : 0;
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ================= TMA producer (both CTAs) =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = cluster_id; t < total && !aborted; t += n_clusters) {
+        const Tile ti = decode_pair_tile<EPI>(sh, P, t, rank);
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh.abort, P, 11)) { aborted = true; break; }
+          uint8_t* a_dst = stage_base + stage * STAGE2_BYTES;
+          uint8_t* b_dst = a_dst + A2_BYTES;
+          const uint32_t bar = mapa_shared(su32(&sh.full[stage]), 0);  // the even CTA's
+          if (leader) mbar_expect_tx(&sh.full[stage], 2 * STAGE2_BYTES);
+          const int k0 = kb * BK;
+          tma_load_2d_pair(a_dst, &tmA, bar, k0, ti.m0);
+          if (!B_MN) {
+            int y;
+            if (EPI == EPI_SWIGLU_FWD) y = ti.grp * 2 * P.F + (int)rank * P.F + ti.n0;
+            else y = ti.grp * P.b_group_rows + ti.n0 + (int)rank * (BN / 2);
+            tma_load_2d_pair(b_dst, &tmB, bar, k0, y);
+          } else {
+            const int y = ti.grp * P.b_group_rows + k0;
+            const int x0 = ti.n0 + (int)rank * (BN / 2);
+            tma_load_2d_pair(b_dst, &tmB, bar, x0, y);
+            tma_load_2d_pair(b_dst + 8192, &tmB, bar, x0 + 64, y);
+          }
+          if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer (the even CTA) =================
+    if (leader) {
+      constexpr uint32_t IDESC = make_idesc_pair(false, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = cluster_id; t < total && !aborted; t += n_clusters) {
+        const Tile ti = decode_pair_tile<EPI>(sh, P, t, rank);
+        if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 12)) { aborted = true; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 13)) { aborted = true; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = su32(stage_base + stage * STAGE2_BYTES);
+            const uint32_t b_addr = a_addr + A2_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = sw128_desc(a_addr + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sw128_desc(b_addr + kk * 2048, 8192, 1024)
+                                       : sw128_desc(b_addr + kk * 32, 16, 1024);
+              mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit_pair(&sh.empty[stage], 0x3);
+          }
+          __syncwarp();
+          if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+        }
+        if (aborted) break;
+        if (lane == 0) mma_commit_pair(&sh.tmem_full[acc], 0x3);
+        __syncwarp();
+        if (++acc == PAIR_ACC) { acc = 0; acc_phase ^= 1; }
+      }
+    }
+  } else {
+    // ================= epilogue: warps 2..5 of both CTAs =================
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t empty_base = mapa_shared(su32(&sh.tmem_empty[0]), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = cluster_id; t < total; t += n_clusters) {
+      const Tile ti = decode_pair_tile<EPI>(sh, P, t, rank);
+      if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      drain_tile<EPI>(P, ti, t_row, row_in_tile);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(empty_base + acc * 8);
+      if (++acc == PAIR_ACC) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  if (aborted || *reinterpret_cast<volatile int*>(&sh.abort)) {
+    // let copies and remote arrivals already in flight land before the CTAs exit
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 2000000ull) { }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // neither CTA leaves while the other may still address it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, PAIR_ACC * BN);
   }
 }
 
@@ -755,6 +1043,53 @@ static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtenso
   return e;
 }
 
+constexpr size_t kSmemBytes2 = 1024 + (size_t)STAGES2 * STAGE2_BYTES + sizeof(Shared2);
+
+// 0: M-grouped contractions on CTA pairs (default); 1: every contraction single-CTA
+static std::atomic<int> g_tc_mode{0};
+
+template <bool B_MN, int EPI>
+static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
+                               const Params& P, int kind) {
+  auto kern = tc_grouped_gemm_pair<B_MN, EPI>;
+  static std::atomic<uint64_t> attr_set_mask{0};
+  static int max_clusters[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = 1ull << (dev & 63);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes2;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!(attr_set_mask.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes2);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(c.sm_count & ~1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = c.sm_count / 2;
+    }
+    max_clusters[dev & 63] = n;
+    attr_set_mask.fetch_or(bit);
+  }
+  cfg.gridDim = dim3(2 * max_clusters[dev & 63]);
+  timing_mark(kind, c.stream, true);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, P);
+  note_launches(1);
+  timing_mark(kind, c.stream, false);
+  return e;
+}
+
 static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* offsets) {
   Params P{};
   P.G = G;
@@ -770,6 +1105,8 @@ static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* of
 bool tc_available() { return tc::get_encoder(); }
 
 size_t tc_grouped_ws_bytes(int) { return 0; }
+
+int tc_set_single_cta(int on) { return tc::g_tc_mode.exchange(on ? 1 : 0); }
 
 int tc_timing_enable(int on) {
   using namespace tc;
@@ -833,10 +1170,12 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   P.out0 = static_cast<bf16*>(h);
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
-  cudaError_t e = launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd);
+  const bool pair = g_tc_mode.load() == 0;
+  cudaError_t e = pair ? launch_pair<false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd)
+                       : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
   // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
-  if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, 256)) {
+  if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, pair ? 128 : 256)) {
     *err = MOE_ERR_CUDA;
     return cudaSuccess;
   }
@@ -847,7 +1186,8 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   Q.b_group_rows = d;
   Q.out0 = static_cast<bf16*>(out);
   Q.ld0 = d;
-  return launch_one<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd);
+  return pair ? launch_pair<false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd)
+              : launch_one<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd);
 }
 
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
@@ -873,7 +1213,9 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     P.b_group_rows = d;
     P.out0 = static_cast<bf16*>(d_pre);
     P.aux_in = static_cast<const bf16*>(pre_gu);
-    e = launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
+    const bool pair = g_tc_mode.load() == 0;
+    e = pair ? launch_pair<true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
+             : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
     if (!make_map(&mA, d_pre, n_rows, 2 * F, 128) || !make_map(&mB, w1, (int64_t)G * 2 * F, d, 64)) {
@@ -887,7 +1229,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     Q.b_group_rows = 2 * F;
     Q.out0 = static_cast<bf16*>(dx_rows);
     Q.ld0 = d;
-    e = launch_one<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad);
+    e = pair ? launch_pair<true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad)
+             : launch_one<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad);
     if (e != cudaSuccess) return e;
   }
   // fc2 wgrad: dW2_g [d, F] = d_outᵀ h : A = d_out [n_rows, d] MN-major, B = h [n_rows, F] MN-major
