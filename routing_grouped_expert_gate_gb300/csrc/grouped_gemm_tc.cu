@@ -675,7 +675,7 @@ constexpr int STAGES2 = 6;
 constexpr int A2_BYTES = BM * BK * 2;              // 16 KB: this CTA's 128 rows
 constexpr int B2_BYTES = (BN / 2) * BK * 2;        // 16 KB: this CTA's half of N
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KB
-constexpr int PAIR_ACC = 1;                        // accumulators per CTA (x 256 columns)
+constexpr int PAIR_ACC = 2;                        // accumulators per CTA (x 256 columns)
 
 struct __align__(8) Shared2 {
   uint64_t full[STAGES2];
