@@ -38,6 +38,7 @@ MOE_BF16 = 1
 MOE_GEMM_AUTO = 0
 MOE_GEMM_CUDA_CORES = 1
 MOE_GEMM_TC_SINGLE_CTA = 2
+MOE_GEMM_TC_PAIRS = 3
 
 MOE_WS_PERMUTE = 0
 MOE_WS_GROUPED = 1

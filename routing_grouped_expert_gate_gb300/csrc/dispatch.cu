@@ -73,10 +73,18 @@ permute_scan(int32_t* __restrict__ block_counts, int64_t nblk, int E,
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
-    for (int64_t b = 0; b < nblk; ++b) {
-      const int c = block_counts[b * E + e];
-      block_counts[b * E + e] = run;
-      run += c;
+    // eight independent loads in flight, then the running sum over them
+    for (int64_t b0 = 0; b0 < nblk; b0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (b0 + i < nblk) ? block_counts[(b0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (b0 + i < nblk) {
+          block_counts[(b0 + i) * E + e] = run;
+          run += v[i];
+        }
+      }
     }
     counts[e] = run;
     tot[e] = run;
@@ -93,8 +101,15 @@ permute_scan(int32_t* __restrict__ block_counts, int64_t nblk, int E,
   }
   __syncthreads();
   if (e < E) {
-    const int b0 = base[e];
-    for (int64_t b = 0; b < nblk; ++b) block_counts[b * E + e] += b0;
+    const int base_e = base[e];
+    for (int64_t b0 = 0; b0 < nblk; b0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (b0 + i < nblk) ? block_counts[(b0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (b0 + i < nblk) block_counts[(b0 + i) * E + e] = v[i] + base_e;
+    }
   }
 }
 
@@ -196,18 +211,19 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
 // ------------------------------------------------------------------ B1
 // dx[t] = dx_router[t] + sum_j dx_perm[row_of[t, j]] + dx_shared[t], in fp32 in
 // that order, rounded once. One warp per token, 8 elements per lane per step.
-template <typename T>
+template <typename T, int KK>
 __global__ void __launch_bounds__(256)
 permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ row_of,
                    const float* __restrict__ dx_router, const T* __restrict__ dx_shared,
                    T* __restrict__ dx, int64_t Tn, int k, int d, int64_t A, int* status) {
+  constexpr int U = KK >= 8 ? 1 : 8 / KK;  // 8-element groups per lane per step
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int ng = d >> 3;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
-    int64_t rows[kMaxK];
+    int64_t rows[KK];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KK; ++j) {
       int r = (j < k) ? row_of[t * k + j] : -1;
       if (j < k && (r < 0 || r >= A)) {
         if (lane == 0) record_error(status, MOE_ERR_DEVICE_INDEX, (int)t);
@@ -215,34 +231,43 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
       }
       rows[j] = r;
     }
-    for (int g = lane; g < ng; g += 32) {
-      Raw8<T> raw[kMaxK], sraw;
-      Raw8<float> rraw;
-      if (dx_router != nullptr) rraw.load(dx_router + t * d + 8 * g);
-      else rraw.zero();
+    for (int g0 = 0; g0 < ng; g0 += 32 * U) {
+      Raw8<T> raw[U][KK], sraw[U];
+      Raw8<float> rraw[U];
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k && rows[j] >= 0) raw[j].load(dx_perm + rows[j] * d + 8 * g);
-        else raw[j].zero();
-      }
-      if (dx_shared != nullptr) sraw.load(dx_shared + t * d + 8 * g);
-      else sraw.zero();
-      float acc[8];
-      rraw.to_float(acc);
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u + lane;
+        if (g < ng && dx_router != nullptr) rraw[u].load(dx_router + t * d + 8 * g);
+        else rraw[u].zero();
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          float v[8];
-          raw[j].to_float(v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] += v[i];
+        for (int j = 0; j < KK; ++j) {
+          if (g < ng && j < k && rows[j] >= 0) raw[u][j].load(dx_perm + rows[j] * d + 8 * g);
+          else raw[u][j].zero();
         }
+        if (g < ng && dx_shared != nullptr) sraw[u].load(dx_shared + t * d + 8 * g);
+        else sraw[u].zero();
       }
-      float sv[8];
-      sraw.to_float(sv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += sv[i];
-      store8(dx + t * d + 8 * g, acc);
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u + lane;
+        if (g >= ng) continue;
+        float acc[8];
+        rraw[u].to_float(acc);
+#pragma unroll
+        for (int j = 0; j < KK; ++j) {
+          if (j < k) {
+            float v[8];
+            raw[u][j].to_float(v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += v[i];
+          }
+        }
+        float sv[8];
+        sraw[u].to_float(sv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += sv[i];
+        store8(dx + t * d + 8 * g, acc);
+      }
     }
   }
 }
@@ -252,15 +277,28 @@ cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_
                                const void* dx_shared, void* dx) {
   if (cfg.T == 0) return cudaSuccess;
   const int64_t A = cfg.T * cfg.k;
-  if (cfg.act_dtype == MOE_BF16)
-    permute_bwd_kernel<bf16><<<copy_grid(c, cfg.T), 256, 0, c.stream>>>(
-        static_cast<const bf16*>(dx_perm), row_of, dx_router, static_cast<const bf16*>(dx_shared),
-        static_cast<bf16*>(dx), cfg.T, cfg.k, cfg.d, A, c.status);
-  else
-    permute_bwd_kernel<float><<<copy_grid(c, cfg.T), 256, 0, c.stream>>>(
-        static_cast<const float*>(dx_perm), row_of, dx_router,
-        static_cast<const float*>(dx_shared), static_cast<float*>(dx), cfg.T, cfg.k, cfg.d, A,
-        c.status);
+  const unsigned grid = copy_grid(c, cfg.T);
+#define MOE_PBWD(KK)                                                                          \
+  if (cfg.act_dtype == MOE_BF16)                                                             \
+    permute_bwd_kernel<bf16, KK><<<grid, 256, 0, c.stream>>>(                                 \
+        static_cast<const bf16*>(dx_perm), row_of, dx_router,                                \
+        static_cast<const bf16*>(dx_shared), static_cast<bf16*>(dx), cfg.T, cfg.k, cfg.d, A, \
+        c.status);                                                                           \
+  else                                                                                       \
+    permute_bwd_kernel<float, KK><<<grid, 256, 0, c.stream>>>(                                \
+        static_cast<const float*>(dx_perm), row_of, dx_router,                               \
+        static_cast<const float*>(dx_shared), static_cast<float*>(dx), cfg.T, cfg.k, cfg.d, A, \
+        c.status)
+  if (cfg.k <= 1) {
+    MOE_PBWD(1);
+  } else if (cfg.k <= 2) {
+    MOE_PBWD(2);
+  } else if (cfg.k <= 4) {
+    MOE_PBWD(4);
+  } else {
+    MOE_PBWD(8);
+  }
+#undef MOE_PBWD
   note_launches(1);
   return cudaGetLastError();
 }

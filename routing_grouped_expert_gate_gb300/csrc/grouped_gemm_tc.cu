@@ -50,7 +50,8 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int NUM_THREADS = 192;                // 6 warps
+constexpr int NUM_EPI_WARPS = 8;                 // two per TMEM lane quadrant
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // producer, MMA, epilogue warps
 constexpr int TMEM_COLS = 512;
 constexpr int MAXG = 256;
 
@@ -298,12 +299,13 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
 // with tcgen05.ld (all lanes of the warp together) and write the outputs.
 template <int EPI>
 __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
-                                           int row_in_tile) {
+                                           int row_in_tile, int half) {
+  // the two warps of a lane quadrant split the accumulator's columns in halves
   if (EPI == EPI_SWIGLU_FWD) {
     const int r = ti.m0 + row_in_tile;
     const bool rv = r < ti.m_end;
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
+    for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
       float g[32], u[32], h[32];
       tmem_ld32(t_row + c, g);
       tmem_ld32(t_row + BN / 2 + c, u);
@@ -328,7 +330,7 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
     const int r = ti.m0 + row_in_tile;
     const bool rv = r < ti.m_end;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
       float v[32];
       tmem_ld32(t_row + c, v);
       if (rv) {
@@ -360,10 +362,11 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
         }
       }
     };
-    fetch(0, gq, uq);
+    const int c_lo = half * (BN / 2), c_hi = c_lo + BN / 2;
+    fetch(c_lo, gq, uq);
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      if (c + 32 < BN) fetch(c + 32, gn, un);
+    for (int c = c_lo; c < c_hi; c += 32) {
+      if (c + 32 < c_hi) fetch(c + 32, gn, un);
       float dh[32];
       tmem_ld32(t_row + c, dh);
       if (rv) {
@@ -404,7 +407,7 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
     const bool rv = m < P.M_out;
     bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
       float v[32];
       tmem_ld32(t_row + c, v);
       if (rv) {
@@ -442,7 +445,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.tmem_full[a], 1);
-      mbar_init(&sh.tmem_empty[a], 4 * 32);
+      mbar_init(&sh.tmem_empty[a], NUM_EPI_WARPS * 32);
     }
     fence_barrier_init();
   }
@@ -622,6 +625,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   } else {
     // ================= epilogue: warps 2..5 =================
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -633,7 +637,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (ti.nk == 0) {
           if (m < P.M_out) {
             const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int c = 0; c < BN; c += 8)
+            for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 8)
               if (ti.n0 + c < P.N_out) store_bf16x8(dst_row + ti.n0 + c, z);
           }
           continue;
@@ -643,7 +647,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
-      drain_tile<EPI>(P, ti, t_row, row_in_tile);
+      drain_tile<EPI>(P, ti, t_row, row_in_tile, half);
       tc_fence_before();
       mbar_arrive(&sh.tmem_empty[acc]);
       acc ^= 1;
@@ -807,7 +811,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < PAIR_ACC; ++a) {
       mbar_init(&sh.tmem_full[a], 1);
-      mbar_init(&sh.tmem_empty[a], 2 * 4);
+      mbar_init(&sh.tmem_empty[a], 2 * NUM_EPI_WARPS);
     }
     fence_barrier_init();
   }
@@ -926,6 +930,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ================= epilogue: warps 2..5 of both CTAs =================
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     const uint32_t empty_base = mapa_shared(su32(&sh.tmem_empty[0]), 0);
     int acc = 0;
@@ -935,7 +940,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      drain_tile<EPI>(P, ti, t_row, row_in_tile);
+      drain_tile<EPI>(P, ti, t_row, row_in_tile, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(empty_base + acc * 8);
@@ -1045,8 +1050,16 @@ static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtenso
 
 constexpr size_t kSmemBytes2 = 1024 + (size_t)STAGES2 * STAGE2_BYTES + sizeof(Shared2);
 
-// 0: M-grouped contractions on CTA pairs (default); 1: every contraction single-CTA
+// 0: CTA pairs for long segments (default); 1: single CTAs only; 2: CTA pairs always
 static std::atomic<int> g_tc_mode{0};
+
+// CTA pairs compute 256-row tiles; when the experts' segments are short the
+// second half of many pair tiles would be empty rows, so small segments stay
+// on single CTAs (measured: a 256-row average is faster single-CTA).
+static bool use_pair(int G, int64_t n_rows) {
+  const int mode = g_tc_mode.load();
+  return mode == 2 || (mode == 0 && n_rows >= (int64_t)512 * G);
+}
 
 template <bool B_MN, int EPI>
 static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
@@ -1106,7 +1119,7 @@ bool tc_available() { return tc::get_encoder(); }
 
 size_t tc_grouped_ws_bytes(int) { return 0; }
 
-int tc_set_single_cta(int on) { return tc::g_tc_mode.exchange(on ? 1 : 0); }
+int tc_set_mode(int mode) { return tc::g_tc_mode.exchange(mode); }
 
 int tc_timing_enable(int on) {
   using namespace tc;
@@ -1170,7 +1183,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   P.out0 = static_cast<bf16*>(h);
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
-  const bool pair = g_tc_mode.load() == 0;
+  const bool pair = use_pair(G, n_rows);
   cudaError_t e = pair ? launch_pair<false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd)
                        : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
@@ -1213,7 +1226,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     P.b_group_rows = d;
     P.out0 = static_cast<bf16*>(d_pre);
     P.aux_in = static_cast<const bf16*>(pre_gu);
-    const bool pair = g_tc_mode.load() == 0;
+    const bool pair = use_pair(G, n_rows);
     e = pair ? launch_pair<true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
              : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
     if (e != cudaSuccess) return e;

@@ -97,7 +97,7 @@ size_t tc_grouped_ws_bytes(int n_groups);
 // kernel kinds of the grouped GEMM, for per-kernel timing
 enum TcKind { kFc1Fwd = 0, kFc2Fwd, kFc2Dgrad, kFc1Dgrad, kFc2Wgrad, kFc1Wgrad, kTcKinds };
 int tc_timing_enable(int on);
-int tc_set_single_cta(int on);  // returns the previous setting
+int tc_set_mode(int mode);  // 0 auto, 1 single-CTA only, 2 CTA pairs always
 int tc_timing_read(float* ms_total, int32_t* launches);
 
 // ---- misc

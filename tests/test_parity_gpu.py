@@ -33,6 +33,7 @@ SMALL = {
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
 CASES = ([(n, "native", "tcgen05") for n in SMALL if n != "tiny_fp32"]
          + [(n, "native", "tcgen05_1cta") for n in SMALL if n != "tiny_fp32"]
+         + [(n, "native", "tcgen05_pairs") for n in SMALL if n != "tiny_fp32"]
          + [(n, "native", "cudacores") for n in SMALL]
          + [(n, "f32", "cudacores") for n in SMALL if n != "tiny_fp32"])
 
@@ -54,6 +55,7 @@ def run_gpu(wl, seed=0, backward=True, impl="tcgen05"):
     b = layer.alloc_buffers(cfg, "cuda", backward=backward)
     old = L.set_grouped_gemm_impl({"tcgen05": L.MOE_GEMM_AUTO,
                                    "tcgen05_1cta": L.MOE_GEMM_TC_SINGLE_CTA,
+                                   "tcgen05_pairs": L.MOE_GEMM_TC_PAIRS,
                                    "cudacores": L.MOE_GEMM_CUDA_CORES}[impl])
     try:
         layer.forward(cfg, p, inp["x"], b)
@@ -141,7 +143,7 @@ def test_zero_load_experts_exist_in_skewed_case(built):
     assert (counts == 0).sum() >= 1 and counts.max() > 3 * counts.mean()
 
 
-@pytest.mark.parametrize("impl", ["tcgen05", "tcgen05_1cta", "cudacores"])
+@pytest.mark.parametrize("impl", ["tcgen05", "tcgen05_1cta", "tcgen05_pairs", "cudacores"])
 def test_deterministic_bytes(built, impl):
     wl = SMALL["fine_grained_small"]
     _, b1 = run_gpu(wl, backward=True, impl=impl)
