@@ -691,6 +691,7 @@ struct __align__(8) Shared2 {
   int total_tiles;
   int off[MAXG + 1];
   int prefix[MAXG + 1];
+  int order[MAXG];
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -708,6 +709,12 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
+}
+__device__ __forceinline__ void st_shared_cluster_zero16(uint32_t addr) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void fence_async_shared_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -761,34 +768,51 @@ __host__ __device__ constexpr uint32_t make_idesc_pair(bool a_mn, bool b_mn) {
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
-template <int EPI>
+template <bool KGROUPED, int EPI>
 __device__ __forceinline__ Tile decode_pair_tile(const Shared2& sh, const Params& P, int t,
                                                  uint32_t rank) {
-  int lo = 0, hi = P.G;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (sh.prefix[mid] <= t) lo = mid; else hi = mid;
-  }
-  const int g = lo;
-  const int rows = sh.off[g + 1] - sh.off[g];
-  const int mp = (rows + 2 * BM - 1) / (2 * BM);
-  const int local = t - sh.prefix[g];
-  const int ni = local / mp, mi = local - ni * mp;
   Tile ti;
-  ti.grp = g;
-  ti.m0 = sh.off[g] + mi * 2 * BM + (int)rank * BM;
-  ti.m_end = sh.off[g + 1];
-  ti.n0 = ni * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
-  ti.k_begin = 0;
-  ti.k_end = P.K;
-  ti.nk = (P.K + BK - 1) / BK;
+  if (!KGROUPED) {
+    int lo = 0, hi = P.G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sh.prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    const int rows = sh.off[g + 1] - sh.off[g];
+    const int mp = (rows + 2 * BM - 1) / (2 * BM);
+    const int local = t - sh.prefix[g];
+    const int ni = local / mp, mi = local - ni * mp;
+    ti.grp = g;
+    ti.m0 = sh.off[g] + mi * 2 * BM + (int)rank * BM;
+    ti.m_end = sh.off[g + 1];
+    ti.n0 = ni * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
+    ti.k_begin = 0;
+    ti.k_end = P.K;
+    ti.nk = (P.K + BK - 1) / BK;
+  } else {
+    // P.MT counts 256-row pair tiles along M
+    const int per = P.MT * P.NT;
+    const int gi = t / per;
+    const int local = t - gi * per;
+    const int g = sh.order[gi];
+    const int mi = local / P.NT, ni = local - mi * P.NT;
+    ti.grp = g;
+    ti.m0 = mi * 2 * BM + (int)rank * BM;
+    ti.m_end = P.M_out;
+    ti.n0 = ni * BN;
+    ti.k_begin = sh.off[g];
+    ti.k_end = sh.off[g + 1];
+    ti.nk = (ti.k_end - ti.k_begin + BK - 1) / BK;
+  }
   return ti;
 }
 
-template <bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const Params P) {
+  constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -831,13 +855,29 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       prev = v;
     }
     if (bad && leader) record_error(P.status, MOE_ERR_DEVICE_INDEX, -1);
-    int acc = 0;
-    for (int g = 0; g < P.G; ++g) {
-      sh.prefix[g] = acc;
-      acc += ((sh.off[g + 1] - sh.off[g] + 2 * BM - 1) / (2 * BM)) * P.NT;
+    if (!KGROUPED) {
+      int acc = 0;
+      for (int g = 0; g < P.G; ++g) {
+        sh.prefix[g] = acc;
+        acc += ((sh.off[g + 1] - sh.off[g] + 2 * BM - 1) / (2 * BM)) * P.NT;
+      }
+      sh.prefix[P.G] = acc;
+      sh.total_tiles = acc;
+    } else {
+      sh.total_tiles = P.G * P.MT * P.NT;
     }
-    sh.prefix[P.G] = acc;
-    sh.total_tiles = acc;
+  }
+  if (KGROUPED) {
+    __syncthreads();
+    for (int g = tid; g < P.G; g += NUM_THREADS) {  // longest segment first
+      const int ng = sh.off[g + 1] - sh.off[g];
+      int r = 0;
+      for (int h = 0; h < P.G; ++h) {
+        const int nh = sh.off[h + 1] - sh.off[h];
+        r += (nh > ng) || (nh == ng && h < g);
+      }
+      sh.order[r] = g;
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(&sh.tmem_base, PAIR_ACC * BN);
@@ -866,7 +906,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0;
       for (int t = cluster_id; t < total && !aborted; t += n_clusters) {
-        const Tile ti = decode_pair_tile<EPI>(sh, P, t, rank);
+        const Tile ti = decode_pair_tile<KGROUPED, EPI>(sh, P, t, rank);
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh.abort, P, 11)) { aborted = true; break; }
           uint8_t* a_dst = stage_base + stage * STAGE2_BYTES;
@@ -874,14 +914,19 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
           const uint32_t bar = mapa_shared(su32(&sh.full[stage]), 0);  // the even CTA's
           if (leader) mbar_expect_tx(&sh.full[stage], 2 * STAGE2_BYTES);
           const int k0 = kb * BK;
-          tma_load_2d_pair(a_dst, &tmA, bar, k0, ti.m0);
+          if (!A_MN) {
+            tma_load_2d_pair(a_dst, &tmA, bar, k0, ti.m0);
+          } else {
+            tma_load_2d_pair(a_dst, &tmA, bar, ti.m0, ti.k_begin + k0);
+            tma_load_2d_pair(a_dst + 8192, &tmA, bar, ti.m0 + 64, ti.k_begin + k0);
+          }
           if (!B_MN) {
             int y;
             if (EPI == EPI_SWIGLU_FWD) y = ti.grp * 2 * P.F + (int)rank * P.F + ti.n0;
             else y = ti.grp * P.b_group_rows + ti.n0 + (int)rank * (BN / 2);
             tma_load_2d_pair(b_dst, &tmB, bar, k0, y);
           } else {
-            const int y = ti.grp * P.b_group_rows + k0;
+            const int y = KGROUPED ? ti.k_begin + k0 : ti.grp * P.b_group_rows + k0;
             const int x0 = ti.n0 + (int)rank * (BN / 2);
             tma_load_2d_pair(b_dst, &tmB, bar, x0, y);
             tma_load_2d_pair(b_dst + 8192, &tmB, bar, x0 + 64, y);
@@ -893,25 +938,46 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ================= MMA issuer (the even CTA) =================
     if (leader) {
-      constexpr uint32_t IDESC = make_idesc_pair(false, B_MN);
+      constexpr uint32_t IDESC = make_idesc_pair(A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = cluster_id; t < total && !aborted; t += n_clusters) {
-        const Tile ti = decode_pair_tile<EPI>(sh, P, t, rank);
+        const Tile ti = decode_pair_tile<KGROUPED, EPI>(sh, P, t, rank);
+        if (ti.nk == 0) continue;  // empty segment: the epilogues write zeros themselves
         if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 12)) { aborted = true; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 13)) { aborted = true; break; }
           tc_fence_after();
+          uint8_t* a_s = stage_base + stage * STAGE2_BYTES;
+          if (KGROUPED && kb == ti.nk - 1) {
+            // K rows past the segment end belong to the next expert: zero them in
+            // both CTAs' A (this CTA's directly, the peer's through DSMEM)
+            const int valid = ti.k_end - (ti.k_begin + kb * BK);
+            if (valid < BK) {
+              const int n16 = (BK - valid) * 8;
+              for (int half = 0; half < 2; ++half) {
+                uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
+                const uint32_t zp = mapa_shared(su32(z), 1u);
+                for (int i = lane; i < n16; i += 32) {
+                  z[i] = make_uint4(0, 0, 0, 0);
+                  st_shared_cluster_zero16(zp + 16u * i);
+                }
+              }
+              fence_async_shared_cluster();
+              __syncwarp();
+            }
+          }
           if (lane == 0) {
-            const uint32_t a_addr = su32(stage_base + stage * STAGE2_BYTES);
+            const uint32_t a_addr = su32(a_s);
             const uint32_t b_addr = a_addr + A2_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = sw128_desc(a_addr + kk * 32, 16, 1024);
+              const uint64_t ad = A_MN ? sw128_desc(a_addr + kk * 2048, 8192, 1024)
+                                       : sw128_desc(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? sw128_desc(b_addr + kk * 2048, 8192, 1024)
                                        : sw128_desc(b_addr + kk * 32, 16, 1024);
               mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
@@ -928,7 +994,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       }
     }
   } else {
-    // ================= epilogue: warps 2..5 of both CTAs =================
+    // ================= epilogue: warps 2.. of both CTAs =================
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
@@ -936,7 +1002,17 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster_id; t < total; t += n_clusters) {
-      const Tile ti = decode_pair_tile<EPI>(sh, P, t, rank);
+      const Tile ti = decode_pair_tile<KGROUPED, EPI>(sh, P, t, rank);
+      if (KGROUPED && ti.nk == 0) {
+        const int m = ti.m0 + row_in_tile;
+        if (m < P.M_out) {
+          bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
+          const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 8)
+            if (ti.n0 + c < P.N_out) store_bf16x8(dst_row + ti.n0 + c, z);
+        }
+        continue;
+      }
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
@@ -1061,10 +1137,10 @@ static bool use_pair(int G, int64_t n_rows) {
   return mode == 2 || (mode == 0 && n_rows >= (int64_t)512 * G);
 }
 
-template <bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
                                const Params& P, int kind) {
-  auto kern = tc_grouped_gemm_pair<B_MN, EPI>;
+  auto kern = tc_grouped_gemm_pair<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   static int max_clusters[64];
   int dev = 0;
@@ -1184,7 +1260,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
   const bool pair = use_pair(G, n_rows);
-  cudaError_t e = pair ? launch_pair<false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd)
+  cudaError_t e = pair ? launch_pair<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd)
                        : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
   // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
@@ -1199,7 +1275,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   Q.b_group_rows = d;
   Q.out0 = static_cast<bf16*>(out);
   Q.ld0 = d;
-  return pair ? launch_pair<false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd)
+  return pair ? launch_pair<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd)
               : launch_one<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd);
 }
 
@@ -1227,7 +1303,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     P.out0 = static_cast<bf16*>(d_pre);
     P.aux_in = static_cast<const bf16*>(pre_gu);
     const bool pair = use_pair(G, n_rows);
-    e = pair ? launch_pair<true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
+    e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
              : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
@@ -1242,7 +1318,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     Q.b_group_rows = 2 * F;
     Q.out0 = static_cast<bf16*>(dx_rows);
     Q.ld0 = d;
-    e = pair ? launch_pair<true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad)
+    e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad)
              : launch_one<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad);
     if (e != cudaSuccess) return e;
   }
@@ -1257,10 +1333,12 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   Params R = base_params(c, G, n_rows, offsets);
   R.M_out = d;
   R.N_out = F;
-  R.MT = (d + BM - 1) / BM;
+  const bool wpair = g_tc_mode.load() != 1;  // weight gradients: CTA pairs unless single-CTA
+  R.MT = wpair ? (d + 2 * BM - 1) / (2 * BM) : (d + BM - 1) / BM;
   R.NT = (F + BN - 1) / BN;
   R.out0 = static_cast<bf16*>(dw2);
-  e = launch_one<true, true, EPI_WGRAD>(c, mA, mB, R, kFc2Wgrad);
+  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, R, kFc2Wgrad)
+            : launch_one<true, true, EPI_WGRAD>(c, mA, mB, R, kFc2Wgrad);
   if (e != cudaSuccess) return e;
   // fc1 wgrad: dW1_g [2F, d] = d_preᵀ x : A = d_pre [n_rows, 2F] MN-major, B = x_rows MN-major
   if (!make_map(&mA, n_rows > 0 ? d_pre : w1, mr, 2 * F, 64) ||
@@ -1271,10 +1349,11 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   Params S = base_params(c, G, n_rows, offsets);
   S.M_out = 2 * F;
   S.N_out = d;
-  S.MT = (2 * F + BM - 1) / BM;
+  S.MT = wpair ? (2 * F + 2 * BM - 1) / (2 * BM) : (2 * F + BM - 1) / BM;
   S.NT = (d + BN - 1) / BN;
   S.out0 = static_cast<bf16*>(dw1);
-  return launch_one<true, true, EPI_WGRAD>(c, mA, mB, S, kFc1Wgrad);
+  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, S, kFc1Wgrad)
+               : launch_one<true, true, EPI_WGRAD>(c, mA, mB, S, kFc1Wgrad);
 }
 
 }  // namespace moe
