@@ -431,7 +431,11 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
   b.C = part; b.c_sm = d; b.c_sg = (int64_t)E * d;
   b.n_groups = 1; b.alpha = 1.f; b.split_k = S;
   if (T > 0) {
-    MOE_LAUNCH(launch_simt_gemm(c, b));
+    if (E <= 16) {
+      MOE_LAUNCH(launch_router_dw_small(c, *cfg, x, d_logits, part, S));
+    } else {
+      MOE_LAUNCH(launch_simt_gemm(c, b));
+    }
     MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)E * d, S, (int64_t)E * d, dw_router, kF32, 0));
   } else {
     MOE_LAUNCH(cudaMemsetAsync(dw_router, 0, (size_t)E * d * sizeof(float), c.stream));

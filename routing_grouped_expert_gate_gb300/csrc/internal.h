@@ -22,6 +22,9 @@ cudaError_t launch_router_logits(const Ctx& c, const moe_cfg& cfg, const void* x
                                  float* logits);
 cudaError_t launch_router_topk(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                const float* sel_bias, int32_t* idx, float* w);
+// dW_r partials [splits][E][d] for E <= 16 (sum them in slice order)
+cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void* x,
+                                   const float* d_logits, float* part, int splits);
 cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                      const int32_t* idx, const float* dw, float* d_logits,
                                      int accumulate);

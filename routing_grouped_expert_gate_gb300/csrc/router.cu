@@ -115,17 +115,21 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 // Register-tiled fp32 SIMT GEMM: a CTA computes 128 tokens x 64 experts; a
 // thread computes 4 tokens x 8 experts ({4tx..4tx+3} and {32+4tx..32+4tx+3},
 // so that the eight threads of one shared-memory phase read 128 consecutive
-// bytes). K advances in chunks of 32; the next chunk is prefetched into
-// registers while the current one is multiplied.
-constexpr int RT_BT = 128, RT_BE = 64, RT_KC = 32;
+// bytes). K advances in chunks of 64 staged through shared memory (51 KB of
+// dynamic shared memory); two CTAs per SM overlap one CTA's loads with the
+// other's FMAs.
+constexpr int RT_BT = 128, RT_BE = 64, RT_KC = 64;
+constexpr int RT_XS = RT_KC * (RT_BT + 4), RT_WS = RT_KC * (RT_BE + 4);
+constexpr size_t RT_SMEM = (size_t)(RT_XS + RT_WS) * sizeof(float);
 
 template <typename Tx>
 __global__ void __launch_bounds__(256, 2)
 router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
                     const float* __restrict__ logit_bias, float* __restrict__ logits,
                     int64_t T, int d, int E) {
-  __shared__ __align__(16) float xs[RT_KC][RT_BT + 4];
-  __shared__ __align__(16) float ws[RT_KC][RT_BE + 4];
+  extern __shared__ __align__(16) float rt_smem[];
+  float (*xs)[RT_BT + 4] = reinterpret_cast<float (*)[RT_BT + 4]>(rt_smem);
+  float (*ws)[RT_BE + 4] = reinterpret_cast<float (*)[RT_BE + 4]>(rt_smem + RT_XS);
 
   const int tid = threadIdx.x;
   const int ty = tid >> 3;  // token group: tokens 4ty..4ty+3
@@ -139,10 +143,10 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = hi[i][j] = lo[i][j] = 0.f;
 
-  // loader roles: x: 2 x (token = v & 127, group kg = v >> 7); W: expert tid & 63, kg tid >> 6
+  // loader roles: x: 4 x (token = v & 127, group kg = v >> 7); W: 2 x (expert v & 63, kg v >> 6)
   auto stage_chunk = [&](int k0) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < 4; ++r) {
       const int v = tid + 256 * r;
       const int tok = v & 127, kg = v >> 7;
       const int64_t t = t_base + tok;
@@ -157,17 +161,21 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
 #pragma unroll
       for (int i = 0; i < 8; ++i) xs[kg * 8 + i][tok] = xr[i];
     }
-    const int e = tid & 63, kg = tid >> 6;
-    const int kk = k0 + 8 * kg;
-    float wr[8];
-    if (e_base + e < E && kk < d) {
-      load8(W + (int64_t)(e_base + e) * d + kk, wr);
-    } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wr[i] = 0.f;
+    for (int r = 0; r < 2; ++r) {
+      const int v = tid + 256 * r;
+      const int e = v & 63, kg = v >> 6;
+      const int kk = k0 + 8 * kg;
+      float wr[8];
+      if (e_base + e < E && kk < d) {
+        load8(W + (int64_t)(e_base + e) * d + kk, wr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wr[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ws[kg * 8 + i][e] = wr[i];
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ws[kg * 8 + i][e] = wr[i];
   };
 
   for (int k0 = 0; k0 < d; k0 += RT_KC) {
@@ -408,6 +416,60 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ B3, E <= 16
+// dW_r partials for few experts: part[s][e][c] = sum over the tokens of slice s
+// of d_logits[t][e] * x[t][c]. A thread owns 8 consecutive columns and every
+// expert; the d_logits row of a token is the same for the whole CTA (a
+// broadcast load). Slices are summed afterwards in slice order.
+template <typename Tx, int EMAX>
+__global__ void __launch_bounds__(256)
+router_dw_small(const Tx* __restrict__ x, const float* __restrict__ d_logits,
+                float* __restrict__ part, int64_t T, int d, int E, int64_t tok_per_slice) {
+  const int c0 = (blockIdx.x * 256 + threadIdx.x) * 8;
+  const int64_t t_beg = (int64_t)blockIdx.y * tok_per_slice;
+  const int64_t t_end = t_beg + tok_per_slice < T ? t_beg + tok_per_slice : T;
+  if (c0 >= d) return;
+  float acc[EMAX][8];
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[e][i] = 0.f;
+  for (int64_t t = t_beg; t < t_end; ++t) {
+    float xv[8];
+    load8(x + t * d + c0, xv);
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (e < E) {
+        const float g = __ldg(d_logits + t * E + e);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[e][i] = fmaf(g, xv[i], acc[e][i]);
+      }
+    }
+  }
+  float* out = part + (int64_t)blockIdx.y * E * d;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+    if (e < E) store8(out + (int64_t)e * d + c0, acc[e]);
+}
+
+cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void* x,
+                                   const float* d_logits, float* part, int splits) {
+  if (cfg.T == 0) return cudaSuccess;
+  const int64_t per = (cfg.T + splits - 1) / splits;
+  dim3 grid((unsigned)((cfg.d / 8 + 255) / 256), (unsigned)splits);
+#define MOE_DWS(TX, EM)                                                                   \
+  router_dw_small<TX, EM><<<grid, 256, 0, c.stream>>>(static_cast<const TX*>(x), d_logits, \
+                                                      part, cfg.T, cfg.d, cfg.E, per)
+  if (cfg.act_dtype == MOE_BF16) {
+    if (cfg.E <= 8) MOE_DWS(bf16, 8); else MOE_DWS(bf16, 16);
+  } else {
+    if (cfg.E <= 8) MOE_DWS(float, 8); else MOE_DWS(float, 16);
+  }
+#undef MOE_DWS
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ launchers
 template <typename Tx>
 static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, const Tx* x,
@@ -427,7 +489,17 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
         x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
   } else {
     dim3 grid((unsigned)((T + RT_BT - 1) / RT_BT), (unsigned)((cfg.E + RT_BE - 1) / RT_BE));
-    router_logits_tiled<Tx><<<grid, 256, 0, c.stream>>>(x, w_router, logit_bias, logits, T,
+    static bool attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_done[dev & 63]) {
+      cudaError_t e = cudaFuncSetAttribute(router_logits_tiled<Tx>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)RT_SMEM);
+      if (e != cudaSuccess) return e;
+      attr_done[dev & 63] = true;
+    }
+    router_logits_tiled<Tx><<<grid, 256, RT_SMEM, c.stream>>>(x, w_router, logit_bias, logits, T,
                                                          cfg.d, cfg.E);
   }
   note_launches(1);

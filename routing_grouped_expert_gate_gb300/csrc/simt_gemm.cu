@@ -8,8 +8,10 @@
 //     dW_r = d_logitsᵀ · x (K = T, split over K with partials reduced in a fixed
 //     order so the result is deterministic).
 //
-// A CTA computes a 64 x 64 tile of C with 256 threads (4 x 4 per thread); K
-// advances 16 at a time through shared memory. Operands are addressed through
+// A CTA computes a 128 x 64 tile of C with 256 threads (4 x 8 per thread: rows
+// 4ty..4ty+3, columns {4tx..4tx+3} and {32+4tx..32+4tx+3}, so the eight threads
+// of one shared-memory phase read 128 consecutive bytes); K advances 32 at a
+// time through shared memory. Operands are addressed through
 // element strides, so the same kernel reads K-contiguous or M/N-contiguous
 // matrices; consecutive threads always touch consecutive addresses.
 #include "common.cuh"
@@ -17,7 +19,7 @@
 
 namespace moe {
 
-constexpr int SG_BM = 64, SG_BN = 64, SG_KC = 16;
+constexpr int SG_BM = 128, SG_BN = 64, SG_KC = 32;
 
 template <typename T>
 __device__ __forceinline__ float ldf(const void* p, int64_t i) {
@@ -25,13 +27,13 @@ __device__ __forceinline__ float ldf(const void* p, int64_t i) {
 }
 
 template <typename TA, typename TB, typename TC>
-__global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemm g, int mode, int* status) {
+__global__ void __launch_bounds__(256, 2) simt_gemm_kernel(SimtGemm g, int mode, int* status) {
   __shared__ __align__(16) float As[SG_KC][SG_BM + 4];
   __shared__ __align__(16) float Bs[SG_KC][SG_BN + 4];
   __shared__ int s_info[4];
 
   const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;
+  const int ty = tid >> 3, tx = tid & 7;
 
   int64_t m0 = 0, m_lim = g.M, k_beg = 0, k_end = g.K;
   const void* Ap = g.A;
@@ -96,36 +98,43 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemm g, int mode, in
 
   const bool a_kc = (g.a_sk == 1);
   const bool b_kc = (g.b_sk == 1);
-  float acc[4][4];
+  float acc[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
   for (int64_t k0 = k_beg; k0 < k_end; k0 += SG_KC) {
+    // A: 128 x 32 elements, 16 per thread; B: 64 x 32, 8 per thread. Consecutive
+    // threads read consecutive addresses whichever way the operand is laid out.
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < 16; ++r) {
       const int lin = tid + 256 * r;
       int mm, kk;
-      if (a_kc) { mm = lin >> 4; kk = lin & 15; } else { kk = lin >> 6; mm = lin & 63; }
+      if (a_kc) { mm = lin >> 5; kk = lin & 31; } else { kk = lin >> 7; mm = lin & 127; }
       const int64_t gm = m0 + mm, gk = k0 + kk;
       As[kk][mm] = (gm < m_lim && gk < k_end) ? ldf<TA>(Ap, gm * g.a_sm + gk * g.a_sk) : 0.f;
-      int nn;
-      if (b_kc) { nn = lin >> 4; kk = lin & 15; } else { kk = lin >> 6; nn = lin & 63; }
-      const int64_t gn = n0 + nn, gk2 = k0 + kk;
-      Bs[kk][nn] = (gn < g.N && gk2 < k_end) ? ldf<TB>(Bp, gn * g.b_sn + gk2 * g.b_sk) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int lin = tid + 256 * r;
+      int nn, kk;
+      if (b_kc) { nn = lin >> 5; kk = lin & 31; } else { kk = lin >> 6; nn = lin & 63; }
+      const int64_t gn = n0 + nn, gk = k0 + kk;
+      Bs[kk][nn] = (gn < g.N && gk < k_end) ? ldf<TB>(Bp, gn * g.b_sn + gk * g.b_sk) : 0.f;
     }
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < SG_KC; ++kk) {
       const float4 a = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
-      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][32 + 4 * tx]);
       const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
@@ -136,8 +145,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemm g, int mode, in
     const int64_t gm = m0 + 4 * ty + i;
     if (gm >= m_lim) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t gn = n0 + 4 * tx + j;
+    for (int j = 0; j < 8; ++j) {
+      const int64_t gn = n0 + (j < 4 ? 4 * tx + j : 32 + 4 * tx + (j - 4));
       if (gn >= g.N) continue;
       float v = g.alpha * acc[i][j];
       TC* dst = C + gm * g.c_sm + gn;
