@@ -182,25 +182,31 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
     __syncthreads();
     stage_chunk(k0);
     __syncthreads();
+    // plain FMAs over 32 elements, then the partial sums fold into (hi, lo):
+    // the rounding that grows with d stays inside 32-term partial sums
 #pragma unroll
-    for (int kk = 0; kk < RT_KC; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&ws[kk][32 + 4 * tx]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    for (int half = 0; half < RT_KC / 32; ++half) {
+#pragma unroll
+      for (int k2 = 0; k2 < 32; ++k2) {
+        const int kk = half * 32 + k2;
+        const float4 a = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&ws[kk][32 + 4 * tx]);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) {
+          comp_add(hi[i][j], lo[i][j], acc[i][j]);
+          acc[i][j] = 0.f;
+        }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        comp_add(hi[i][j], lo[i][j], acc[i][j]);
-        acc[i][j] = 0.f;
-      }
   }
 
 #pragma unroll
