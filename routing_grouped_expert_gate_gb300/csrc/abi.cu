@@ -106,10 +106,12 @@ static int act_size(const moe_cfg& cfg) { return cfg.act_dtype == MOE_BF16 ? 2 :
     if (_e != cudaSuccess) return MOE_ERR_CUDA;   \
   } while (0)
 
+// K (token) slices of the dW_r reduction; partials [S][E][d] fp32 in the workspace
 static int route_bwd_splits(const moe_cfg& cfg) {
-  int64_t s = (cfg.T + 511) / 512;
+  int64_t s = (cfg.E <= 16) ? (cfg.T + 31) / 32 : (cfg.T + 511) / 512;
+  const int64_t cap = (cfg.E <= 16) ? 64 : 32;
   if (s < 1) s = 1;
-  if (s > 32) s = 32;
+  if (s > cap) s = cap;
   return (int)s;
 }
 
@@ -423,12 +425,14 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
   }
   const int S = route_bwd_splits(*cfg);
   float* part = static_cast<float*>(ws);
-  SimtGemm b{};  // dW_r = d_logitsᵀ · x  [E, d], K = T split S ways
-  b.mode = kGroupNone; b.M = E; b.N = d; b.K = T;
-  b.dtA = kF32; b.dtB = dtx; b.dtC = kF32;
-  b.A = d_logits; b.a_sm = 1; b.a_sk = E;
-  b.B = x; b.b_sn = 1; b.b_sk = d;
-  b.C = part; b.c_sm = d; b.c_sg = (int64_t)E * d;
+  // dW_r = d_logitsᵀ · x [E, d], K = T split S ways. Computed as its transpose
+  // (M = d, N = E) so that the 128-row tiles run along d, written back as [E, d].
+  SimtGemm b{};
+  b.mode = kGroupNone; b.M = d; b.N = E; b.K = T;
+  b.dtA = dtx; b.dtB = kF32; b.dtC = kF32;
+  b.A = x; b.a_sm = 1; b.a_sk = d;
+  b.B = d_logits; b.b_sn = 1; b.b_sk = E;
+  b.C = part; b.c_sm = 1; b.c_sn = d; b.c_sg = (int64_t)E * d;
   b.n_groups = 1; b.alpha = 1.f; b.split_k = S;
   if (T > 0) {
     if (E <= 16) {

@@ -56,7 +56,7 @@ cudaError_t launch_aux_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* l
 
 // ---- generic fp32-accumulating SIMT GEMM (simt_gemm.cu)
 // C(m, n) = alpha * sum_k A(m, k) * B(n, k)  (+ C(m, n) when accumulate)
-// A(m, k) = A[m*a_sm + k*a_sk], B(n, k) = B[n*b_sn + k*b_sk], C(m, n) = C[m*c_sm + n].
+// A(m, k) = A[m*a_sm + k*a_sk], B(n, k) = B[n*b_sn + k*b_sk], C(m, n) = C[m*c_sm + n*c_sn].
 enum SimtGrouping { kGroupNone = 0, kGroupM = 1, kGroupK = 2 };
 enum SimtDtype { kF32 = 0, kBF16 = 1 };
 struct SimtGemm {
@@ -66,6 +66,7 @@ struct SimtGemm {
   const void* A; int64_t a_sm, a_sk, a_sg;
   const void* B; int64_t b_sn, b_sk, b_sg;
   void* C; int64_t c_sm, c_sg;
+  int64_t c_sn;            // C(m, n) = C[m*c_sm + n*c_sn]; 0 means 1
   const int32_t* offsets;  // [n_groups + 1] device (grouped modes), NULL = one group
   int n_groups;
   float alpha;

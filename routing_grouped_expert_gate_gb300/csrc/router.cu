@@ -428,10 +428,10 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
 // expert; the d_logits row of a token is the same for the whole CTA (a
 // broadcast load). Slices are summed afterwards in slice order.
 template <typename Tx, int EMAX>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 router_dw_small(const Tx* __restrict__ x, const float* __restrict__ d_logits,
                 float* __restrict__ part, int64_t T, int d, int E, int64_t tok_per_slice) {
-  const int c0 = (blockIdx.x * 256 + threadIdx.x) * 8;
+  const int c0 = (blockIdx.x * 128 + threadIdx.x) * 8;
   const int64_t t_beg = (int64_t)blockIdx.y * tok_per_slice;
   const int64_t t_end = t_beg + tok_per_slice < T ? t_beg + tok_per_slice : T;
   if (c0 >= d) return;
@@ -462,9 +462,9 @@ cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void*
                                    const float* d_logits, float* part, int splits) {
   if (cfg.T == 0) return cudaSuccess;
   const int64_t per = (cfg.T + splits - 1) / splits;
-  dim3 grid((unsigned)((cfg.d / 8 + 255) / 256), (unsigned)splits);
+  dim3 grid((unsigned)((cfg.d / 8 + 127) / 128), (unsigned)splits);
 #define MOE_DWS(TX, EM)                                                                   \
-  router_dw_small<TX, EM><<<grid, 256, 0, c.stream>>>(static_cast<const TX*>(x), d_logits, \
+  router_dw_small<TX, EM><<<grid, 128, 0, c.stream>>>(static_cast<const TX*>(x), d_logits, \
                                                       part, cfg.T, cfg.d, cfg.E, per)
   if (cfg.act_dtype == MOE_BF16) {
     if (cfg.E <= 8) MOE_DWS(bf16, 8); else MOE_DWS(bf16, 16);

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(256, 2) simt_gemm_kernel(SimtGemm g, int mode,
       const int64_t gn = n0 + (j < 4 ? 4 * tx + j : 32 + 4 * tx + (j - 4));
       if (gn >= g.N) continue;
       float v = g.alpha * acc[i][j];
-      TC* dst = C + gm * g.c_sm + gn;
+      TC* dst = C + gm * g.c_sm + gn * (g.c_sn ? g.c_sn : 1);
       if (g.accumulate) v += to_f32<TC>(*dst);
       *dst = from_f32<TC>(v);
     }
@@ -178,6 +178,7 @@ cudaError_t launch_simt_gemm(const Ctx& c, const SimtGemm& g) {
   else if (g.dtA == kBF16 && g.dtB == kBF16 && g.dtC == kF32) MOE_SG(bf16, bf16, float);
   else if (g.dtA == kF32 && g.dtB == kBF16 && g.dtC == kF32) MOE_SG(float, bf16, float);
   else if (g.dtA == kF32 && g.dtB == kF32 && g.dtC == kBF16) MOE_SG(float, float, bf16);
+  else if (g.dtA == kBF16 && g.dtB == kF32 && g.dtC == kF32) MOE_SG(bf16, float, float);
   else return cudaErrorInvalidValue;
 #undef MOE_SG
   note_launches(1);
