@@ -132,27 +132,35 @@ def measured_peaks():
             "source": "fallback"}
 
 
+# the sources that define the tcgen05 grouped-GEMM kernels; a recorded DRAM
+# figure stays valid while none of them changes
+TC_SOURCES = ("grouped_gemm_tc.cu", "common.cuh", "internal.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "routing_grouped_expert_gate_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in TC_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+def recorded_traffic(workload, kernel_key):
+    """DRAM bytes (read + write) per launch of one grouped-GEMM kernel kind on
+    one workload, from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    ent = d.get(kernel_key)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if d.get("source_hash") != kernel_source_hash():
         return None
-    return ent.get("bytes_per_launch")
+    ent = d.get("workloads", {}).get(workload, {}).get(kernel_key)
+    if not ent:
+        return None
+    return ent["read"] + ent["write"]
 
 
 # ------------------------------------------------------------------ our arm
@@ -314,14 +322,22 @@ def run_ours(args, ws, rank, local):
 
     peaks = measured_peaks()
     work = stage_work(wl, backward)
+    # fp32 FMA peak of the CUDA cores at the SM clock sampled under load:
+    # SMs x 128 fp32 lanes x 2 flops per FMA x clock
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
+    fp32_peak = n_sm * 128 * 2 * mhz * 1e6 / 1e12
     stages = {}
     for n, ms in stage_ms.items():
         e = {"ms": round(ms, 4)}
         wk = work.get(n, {})
         if "flops" in wk:
             e["tflops"] = round(wk["flops"] / (ms * 1e-3) / 1e12, 2)
+            if n in ("route", "route_bwd"):
+                e["fp32_alu_frac"] = round(e["tflops"] / fp32_peak, 4)
         if "bytes" in wk:
             e["gbs"] = round(wk["bytes"] / (ms * 1e-3) / 1e9, 1)
+            e["hbm_frac"] = round(e["gbs"] / peaks["hbm_gbs"], 4)
         stages[n] = e
     grouped = [n for n in stage_ms if n in ("grouped_fwd", "grouped_bwd", "shared_fwd",
                                             "shared_bwd")]
@@ -353,7 +369,7 @@ def run_ours(args, ws, rank, local):
         achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": f"tc_grouped_gemm {dom}",
                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom),
+                    "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name, dom),
                     "peak_source": peak_src, "flops_per_launch": per_launch_flops,
                     "ms_per_launch": round(per_launch_ms, 4)}
     else:
@@ -376,7 +392,7 @@ def run_ours(args, ws, rank, local):
         "stages": stages,
         "gpu_launches": int(launches),
         "clocks": clk,
-        "peaks": peaks,
+        "peaks": dict(peaks, fp32_alu_tflops=round(fp32_peak, 2)),
     }
     out["value"] = round(ws * T / (ms_per_step * 1e-3), 1)
 

@@ -112,29 +112,46 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 }
 
 // ------------------------------------------------------------------ S1, E > 16
-// Register-tiled fp32 SIMT GEMM: a CTA computes 128 tokens x 64 experts; a
-// thread computes 4 tokens x 8 experts ({4tx..4tx+3} and {32+4tx..32+4tx+3},
-// so that the eight threads of one shared-memory phase read 128 consecutive
-// bytes). K advances in chunks of 64 staged through shared memory (51 KB of
-// dynamic shared memory); two CTAs per SM overlap one CTA's loads with the
-// other's FMAs.
-constexpr int RT_BT = 128, RT_BE = 64, RT_KC = 64;
-constexpr int RT_XS = RT_KC * (RT_BT + 4), RT_WS = RT_KC * (RT_BE + 4);
-constexpr size_t RT_SMEM = (size_t)(RT_XS + RT_WS) * sizeof(float);
+// Register-tiled fp32 SIMT GEMM on 256-thread CTAs. A CTA computes BT tokens x
+// 64 experts; its threads form KS = 128 / BT groups of 2*BT threads that split
+// K: group g takes the 64-wide K chunks g, g + KS, g + 2 KS, ... A thread
+// computes 4 tokens x 8 experts ({4tx..4tx+3} and {32+4tx..32+4tx+3}, so that
+// the eight threads of one shared-memory phase read 128 consecutive bytes).
+// Partial sums fold into the compensated (hi, lo) pair every 32 elements; at
+// the end group 0 adds the other groups' pairs in group order (deterministic).
+// Smaller BT (more K groups) gives more CTAs when T x E is small.
+constexpr int RT_BE = 64, RT_KC = 64, RT_THREADS = 256;
 
-template <typename Tx>
-__global__ void __launch_bounds__(256, 2)
+template <int BT>
+struct RouterTile {
+  static constexpr int kGroups = 128 / BT;
+  static constexpr int kGroupThreads = 2 * BT;
+  static constexpr int kXs = RT_KC * (BT + 4);
+  static constexpr int kWs = RT_KC * (RT_BE + 4);
+  static constexpr int kGroupFloats = kXs + kWs;
+  static constexpr size_t kSmem = (size_t)kGroups * kGroupFloats * sizeof(float);
+  static_assert((kGroups - 1) * kGroupThreads * 64 <= kGroups * kGroupFloats,
+                "the partial (hi, lo) pairs must fit in the staging buffers");
+};
+
+template <typename Tx, int BT>
+__global__ void __launch_bounds__(RT_THREADS, 2)
 router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
                     const float* __restrict__ logit_bias, float* __restrict__ logits,
                     int64_t T, int d, int E) {
+  using RT = RouterTile<BT>;
+  constexpr int KS = RT::kGroups;
+  constexpr int NT = RT::kGroupThreads;
   extern __shared__ __align__(16) float rt_smem[];
-  float (*xs)[RT_BT + 4] = reinterpret_cast<float (*)[RT_BT + 4]>(rt_smem);
-  float (*ws)[RT_BE + 4] = reinterpret_cast<float (*)[RT_BE + 4]>(rt_smem + RT_XS);
+  const int grp = threadIdx.x / NT;
+  const int tid = threadIdx.x % NT;
+  float* gbuf = rt_smem + grp * RT::kGroupFloats;
+  float (*xs)[BT + 4] = reinterpret_cast<float (*)[BT + 4]>(gbuf);
+  float (*ws)[RT_BE + 4] = reinterpret_cast<float (*)[RT_BE + 4]>(gbuf + RT::kXs);
 
-  const int tid = threadIdx.x;
   const int ty = tid >> 3;  // token group: tokens 4ty..4ty+3
   const int tx = tid & 7;   // expert group
-  const int64_t t_base = (int64_t)blockIdx.x * RT_BT;
+  const int64_t t_base = (int64_t)blockIdx.x * BT;
   const int e_base = blockIdx.y * RT_BE;
 
   float acc[4][8], hi[4][8], lo[4][8];
@@ -143,12 +160,12 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = hi[i][j] = lo[i][j] = 0.f;
 
-  // loader roles: x: 4 x (token = v & 127, group kg = v >> 7); W: 2 x (expert v & 63, kg v >> 6)
+  // loader roles: x: 4 x (token v % BT, group kg = v / BT); W: 512 / NT x (expert v & 63, kg v >> 6)
   auto stage_chunk = [&](int k0) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int v = tid + 256 * r;
-      const int tok = v & 127, kg = v >> 7;
+    for (int r = 0; r < (8 * BT) / NT; ++r) {
+      const int v = tid + NT * r;
+      const int tok = v % BT, kg = v / BT;
       const int64_t t = t_base + tok;
       const int kk = k0 + 8 * kg;
       float xr[8];
@@ -162,8 +179,8 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
       for (int i = 0; i < 8; ++i) xs[kg * 8 + i][tok] = xr[i];
     }
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int v = tid + 256 * r;
+    for (int r = 0; r < 512 / NT; ++r) {
+      const int v = tid + NT * r;
       const int e = v & 63, kg = v >> 6;
       const int kk = k0 + 8 * kg;
       float wr[8];
@@ -178,10 +195,15 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
     }
   };
 
-  for (int k0 = 0; k0 < d; k0 += RT_KC) {
+  const int n_chunks = (d + RT_KC - 1) / RT_KC;
+  const int rounds = (n_chunks + KS - 1) / KS;
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int chunk = rd * KS + grp;
+    const bool mine = chunk < n_chunks;  // uniform within a group
     __syncthreads();
-    stage_chunk(k0);
+    if (mine) stage_chunk(chunk * RT_KC);
     __syncthreads();
+    if (!mine) continue;
     // plain FMAs over 32 elements, then the partial sums fold into (hi, lo):
     // the rounding that grows with d stays inside 32-term partial sums
 #pragma unroll
@@ -209,6 +231,36 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
     }
   }
 
+  if constexpr (KS > 1) {
+    // groups 1..KS-1 park their pairs in the staging buffers; group 0 adds
+    // them in group order
+    __syncthreads();
+    float* park = rt_smem;  // [KS-1][NT][64], thread-major within a group
+    if (grp > 0) {
+      float* mine = park + ((size_t)(grp - 1) * NT + tid) * 64;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          mine[(i * 8 + j) * 2] = hi[i][j];
+          mine[(i * 8 + j) * 2 + 1] = lo[i][j];
+        }
+    }
+    __syncthreads();
+    if (grp > 0) return;
+#pragma unroll 1
+    for (int g = 1; g < KS; ++g) {
+      const float* theirs = park + ((size_t)(g - 1) * NT + tid) * 64;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          comp_add(hi[i][j], lo[i][j], theirs[(i * 8 + j) * 2]);
+          lo[i][j] += theirs[(i * 8 + j) * 2 + 1];
+        }
+    }
+  }
+
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t t = t_base + 4 * ty + i;
@@ -232,6 +284,26 @@ router_logits_tiled(const Tx* __restrict__ x, const float* __restrict__ W,
       }
     }
   }
+}
+
+template <typename Tx, int BT>
+static cudaError_t launch_router_tiled(const Ctx& c, const Tx* x, const float* w_router,
+                                       const float* logit_bias, float* logits, int64_t T, int d,
+                                       int E) {
+  constexpr size_t smem = RouterTile<BT>::kSmem;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_tiled<Tx, BT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev & 63] = true;
+  }
+  dim3 grid((unsigned)((T + BT - 1) / BT), (unsigned)((E + RT_BE - 1) / RT_BE));
+  router_logits_tiled<Tx, BT><<<grid, RT_THREADS, smem, c.stream>>>(x, w_router, logit_bias,
+                                                                     logits, T, d, E);
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------------------ S2
@@ -494,19 +566,30 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
     router_logits_small<Tx, 16, TPW><<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
         x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
   } else {
-    dim3 grid((unsigned)((T + RT_BT - 1) / RT_BT), (unsigned)((cfg.E + RT_BE - 1) / RT_BE));
-    static bool attr_done[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_done[dev & 63]) {
-      cudaError_t e = cudaFuncSetAttribute(router_logits_tiled<Tx>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)RT_SMEM);
-      if (e != cudaSuccess) return e;
-      attr_done[dev & 63] = true;
+    // token tile: the one whose busiest SM has the least work, among those
+    // that give every SM two CTAs where T x E allows (ties to the larger tile,
+    // which stages W fewer times)
+    const int64_t e_tiles = (cfg.E + RT_BE - 1) / RT_BE;
+    const int64_t sms = c.sm_count > 0 ? c.sm_count : 1;
+    int best_bt = 32;
+    int64_t best_cost = -1;
+    for (int bt : {128, 64, 32}) {
+      const int64_t ctas = ((T + bt - 1) / bt) * e_tiles;
+      if (ctas < 2 * sms && bt != 32) continue;
+      const int64_t cost = ((ctas + sms - 1) / sms) * bt * bt;  // CTAs per SM x (BT / KS)
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_bt = bt;
+      }
     }
-    router_logits_tiled<Tx><<<grid, 256, RT_SMEM, c.stream>>>(x, w_router, logit_bias, logits, T,
-                                                         cfg.d, cfg.E);
+    cudaError_t e;
+    if (best_bt == 128)
+      e = launch_router_tiled<Tx, 128>(c, x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+    else if (best_bt == 64)
+      e = launch_router_tiled<Tx, 64>(c, x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+    else
+      e = launch_router_tiled<Tx, 32>(c, x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+    if (e != cudaSuccess) return e;
   }
   note_launches(1);
   return cudaGetLastError();
