@@ -228,7 +228,8 @@ def run_ours(args, ws, rank, local):
     # the step, as a list of (stage, call) so that events can bracket each call
     def calls():
         c = [("route", lambda: L.route_topk(cfg, x, p["w_router"], p.get("logit_bias"),
-                                             p.get("sel_bias"), b["logits"], b["idx"], b["w"])),
+                                             p.get("sel_bias"), b["logits"], b["idx"], b["w"],
+                                             b["ws"])),
              ("permute", lambda: L.permute(cfg, x, b["idx"], b["counts"], b["offsets"], b["row_of"],
                                            b["src_tok"], b["x_perm"], b["ws"])),
              ("grouped_fwd", lambda: L.grouped_swiglu(cfg, E, T * k, F, b["offsets"], b["x_perm"],

@@ -75,6 +75,7 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
 #define MOE_WS_GROUPED_BWD  2
 #define MOE_WS_AUX          3
 #define MOE_WS_ROUTE_BWD    4
+#define MOE_WS_ROUTE        5
 
 /* Layer configuration. Names follow the flags the Handbook uses for the layer
  * (§2.5 and §3.4: --num-experts, --moe-ffn-hidden-size, --moe-router-topk,
@@ -116,11 +117,18 @@ int moe_check_cfg(const moe_cfg* cfg);
  *   logits     [T, E] fp32 out (kept for the backward and the aux loss)
  *   idx        [T, k] int32 out, by descending key; equal keys: lower index
  *   w          [T, k] fp32 out
- * The logits are accumulated with compensated fp32 sums, so their error is
- * far below the 1e-6 gap that separates a decided top-k from a near tie.   */
+ *   ws         >= moe_workspace_bytes(cfg, MOE_WS_ROUTE) bytes of scratch
+ *              (may be NULL when that size is 0); it holds the router weight
+ *              split into three bf16 planes for the tensor-core gate GEMM
+ * The logits keep fp32 accuracy either way: on the tensor cores (bf16 x, E a
+ * multiple of 64) W_r = W0 + W1 + W2 exactly in bf16 planes, every product
+ * with a bf16 x is exact, and the partial sums fold into compensated fp32
+ * pairs; on the CUDA cores the fp32 FMA sums fold the same way. Their error
+ * is far below the 1e-6 gap that separates a decided top-k from a near tie.
+ * MOE_ERR_WORKSPACE when ws_bytes is too small.                            */
 int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
                    const float* logit_bias, const float* sel_bias, float* logits,
-                   int32_t* idx, float* w, moe_stream_t stream);
+                   int32_t* idx, float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* S3. Dispatch: counts[e] = #{(t,j): idx[t,j] = e}; offsets = exclusive scan
  * (offsets[E] = T·k); stable permutation row(t,j) = offsets[e] +
@@ -271,6 +279,11 @@ size_t moe_workspace_bytes(const moe_cfg* cfg, int which);
 /* Static English text for a status code. */
 const char* moe_status_string(int status);
 
+/* "cudaErrorName: description" of the CUDA runtime error behind the calling
+ * thread's most recent MOE_ERR_CUDA, or "" if there was none. The string
+ * stays valid until the thread's next call of this function. */
+const char* moe_last_cuda_error(void);
+
 /* Synchronises `stream`, returns the first device-detected error recorded
  * on the current device since the previous call (MOE_OK if none) and clears
  * it. `detail` (may be NULL) receives the offending index or a site code. */
@@ -301,6 +314,27 @@ int moe_selftest_wait_timeout(moe_stream_t stream);
 #define MOE_GEMM_TC_SINGLE_CTA 2
 #define MOE_GEMM_TC_PAIRS      3
 int moe_set_grouped_gemm_impl(int impl);
+
+/* Which kernels compute the router's gate GEMM (moe_route_topk).
+ * MOE_ROUTER_AUTO (default): the tcgen05 kernel over three bf16 planes of W_r
+ * when x is bf16 and E is a multiple of 64 (E >= 64), the CUDA-core kernels
+ * otherwise. MOE_ROUTER_CUDA_CORES: always the CUDA-core kernels (for
+ * cross-checking). Process-wide; returns the previous setting, or
+ * MOE_ERR_INVALID_ARG. */
+#define MOE_ROUTER_AUTO       0
+#define MOE_ROUTER_CUDA_CORES 1
+int moe_set_router_impl(int impl);
+
+/* K elements per window of the tensor-core gate GEMM's main accumulator
+ * before the window's sums fold into the compensated pair (multiple of 16,
+ * 16..4096; default 32). Shorter windows bound the fp32 accumulation error
+ * more tightly and cost more folding. Returns the previous value, or
+ * MOE_ERR_INVALID_ARG. */
+int moe_set_router_fold(int fold_k);
+
+/* 1 when moe_route_topk would run its gate GEMM on the tensor cores for cfg
+ * under the current setting, else 0. */
+int moe_router_uses_tensor_cores(const moe_cfg* cfg);
 
 /* Per-kernel timing of the tcgen05 grouped GEMM kernels, for measurement.
  * moe_kernel_timing(1) starts recording a CUDA event pair around every such

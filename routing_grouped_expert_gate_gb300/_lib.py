@@ -45,6 +45,10 @@ MOE_WS_GROUPED = 1
 MOE_WS_GROUPED_BWD = 2
 MOE_WS_AUX = 3
 MOE_WS_ROUTE_BWD = 4
+MOE_WS_ROUTE = 5
+
+MOE_ROUTER_AUTO = 0
+MOE_ROUTER_CUDA_CORES = 1
 
 
 class MoeCfg(ctypes.Structure):
@@ -56,7 +60,10 @@ class MoeCfg(ctypes.Structure):
 class MoeError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {code} ({status_string(code)})")
+        msg = f"{where}: {code} ({status_string(code)})"
+        if code == MOE_ERR_CUDA:
+            msg += f" [{lib.moe_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 def _load():
@@ -75,7 +82,8 @@ lib = _load()
 _VP = c_void_p
 _SIGS = {
     "moe_check_cfg": (c_int, [POINTER(MoeCfg)]),
-    "moe_route_topk": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_route_topk": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, c_size_t,
+                               _VP]),
     "moe_permute": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
     "moe_grouped_swiglu": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP, _VP,
                                    _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
@@ -91,12 +99,16 @@ _SIGS = {
     "moe_permute_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_workspace_bytes": (c_size_t, [POINTER(MoeCfg), c_int]),
     "moe_status_string": (c_char_p, [c_int]),
+    "moe_last_cuda_error": (c_char_p, []),
     "moe_last_device_status": (c_int, [_VP, POINTER(c_int32)]),
     "moe_set_wait_timeout_ns": (c_uint64, [c_uint64]),
     "moe_selftest_wait_timeout": (c_int, [_VP]),
     "moe_version": (c_char_p, []),
     "moe_launch_count": (c_uint64, []),
     "moe_set_grouped_gemm_impl": (c_int, [c_int]),
+    "moe_set_router_impl": (c_int, [c_int]),
+    "moe_set_router_fold": (c_int, [c_int]),
+    "moe_router_uses_tensor_cores": (c_int, [POINTER(MoeCfg)]),
     "moe_kernel_timing": (c_int, [c_int]),
     "moe_kernel_times": (c_int, [POINTER(c_float), POINTER(c_int32)]),
     "moe_permute_noalloc": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -123,6 +135,26 @@ def set_grouped_gemm_impl(impl: int) -> int:
     if rc < 0:
         raise MoeError(rc, "moe_set_grouped_gemm_impl")
     return rc
+
+
+def set_router_impl(impl: int) -> int:
+    """MOE_ROUTER_AUTO (tensor cores where eligible) or MOE_ROUTER_CUDA_CORES."""
+    rc = int(lib.moe_set_router_impl(impl))
+    if rc < 0:
+        raise MoeError(rc, "moe_set_router_impl")
+    return rc
+
+
+def set_router_fold(fold_k: int) -> int:
+    """K elements per compensated window of the tensor-core gate GEMM."""
+    rc = int(lib.moe_set_router_fold(fold_k))
+    if rc < 0:
+        raise MoeError(rc, "moe_set_router_fold")
+    return rc
+
+
+def router_uses_tensor_cores(cfg) -> bool:
+    return bool(lib.moe_router_uses_tensor_cores(ctypes.byref(cfg)))
 
 
 KERNEL_KINDS = ["fc1_fwd", "fc2_fwd", "fc2_dgrad", "fc1_dgrad", "fc2_wgrad", "fc1_wgrad"]
@@ -201,9 +233,11 @@ def selftest_wait_timeout(stream=None):
 
 # ------------------------------------------------------------------ entry points
 
-def route_topk(cfg, x, w_router, logit_bias, sel_bias, logits, idx, w, stream=None):
+def route_topk(cfg, x, w_router, logit_bias, sel_bias, logits, idx, w, ws=None, stream=None):
     _check(lib.moe_route_topk(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias),
-                              _p(sel_bias), _p(logits), _p(idx), _p(w), _stream(stream)),
+                              _p(sel_bias), _p(logits), _p(idx), _p(w), _p(ws),
+                              0 if ws is None else ws.numel() * ws.element_size(),
+                              _stream(stream)),
            "moe_route_topk")
 
 

@@ -2,6 +2,7 @@
 // the device status word, workspace sizing, and the order in which each call
 // launches its kernels on the caller's stream.
 #include <atomic>
+#include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
@@ -100,10 +101,18 @@ static int act_size(const moe_cfg& cfg) { return cfg.act_dtype == MOE_BF16 ? 2 :
     const int _rc = make_ctx((cudaStream_t)(stream), &ctx);    \
     if (_rc != MOE_OK) return _rc;                             \
   } while (0)
-#define MOE_LAUNCH(expr)                          \
-  do {                                            \
-    const cudaError_t _e = (expr);                \
-    if (_e != cudaSuccess) return MOE_ERR_CUDA;   \
+// the CUDA error behind the calling thread's last MOE_ERR_CUDA
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+static int cuda_failed(cudaError_t e) {
+  g_last_cuda_error = e;
+  cudaGetLastError();  // clear a non-sticky error so later calls can run
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_LAUNCH(expr)                               \
+  do {                                                 \
+    const cudaError_t _e = (expr);                     \
+    if (_e != cudaSuccess) return cuda_failed(_e);     \
   } while (0)
 
 // K (token) slices of the dW_r reduction; partials [S][E][d] fp32 in the workspace
@@ -187,13 +196,35 @@ int moe_set_grouped_gemm_impl(int impl) {
   return g_public.exchange(impl);
 }
 
+int moe_set_router_impl(int impl) {
+  if (impl != MOE_ROUTER_AUTO && impl != MOE_ROUTER_CUDA_CORES) return MOE_ERR_INVALID_ARG;
+  return router_set_impl(impl == MOE_ROUTER_CUDA_CORES ? 1 : 0);
+}
+
+int moe_set_router_fold(int fold_k) {
+  if (fold_k < 16 || fold_k > 4096 || fold_k % 16 != 0) return MOE_ERR_INVALID_ARG;
+  return router_set_fold(fold_k);
+}
+
+const char* moe_last_cuda_error(void) {
+  static thread_local char buf[256];
+  if (g_last_cuda_error == cudaSuccess) return "";
+  snprintf(buf, sizeof(buf), "%s: %s", cudaGetErrorName(g_last_cuda_error),
+           cudaGetErrorString(g_last_cuda_error));
+  return buf;
+}
+
+int moe_router_uses_tensor_cores(const moe_cfg* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return router_tc_eligible(*cfg) ? 1 : 0;
+}
+
 int moe_last_device_status(moe_stream_t stream, int32_t* detail) {
   MOE_CTX(stream, c);
-  if (cudaStreamSynchronize(c.stream) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_LAUNCH(cudaStreamSynchronize(c.stream));
   int h[2] = {0, 0};
-  if (cudaMemcpy(h, c.status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (cudaMemset(c.status, 0, 2 * sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_LAUNCH(cudaMemcpy(h, c.status, sizeof(h), cudaMemcpyDeviceToHost));
+  MOE_LAUNCH(cudaMemset(c.status, 0, 2 * sizeof(int)));
   if (detail) *detail = h[1];
   return h[0];
 }
@@ -206,21 +237,26 @@ size_t moe_workspace_bytes(const moe_cfg* cfg, int which) {
     case MOE_WS_GROUPED_BWD: return grouped_bwd_ws(*cfg);
     case MOE_WS_AUX: return aux_ws_bytes(*cfg);
     case MOE_WS_ROUTE_BWD: return route_bwd_ws(*cfg);
+    case MOE_WS_ROUTE: return router_ws_bytes(*cfg);
     default: return 0;
   }
 }
 
 int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
                    const float* logit_bias, const float* sel_bias, float* logits, int32_t* idx,
-                   float* w, moe_stream_t stream) {
+                   float* w, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_CHECK_CFG(cfg);
   if (sel_bias != nullptr && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
   MOE_PTR(x); MOE_PTR(w_router); MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(w);
   MOE_REQUIRE(logit_bias == nullptr || (reinterpret_cast<uintptr_t>(logit_bias) & 3u) == 0, MOE_ERR_ALIGN);
   MOE_REQUIRE(sel_bias == nullptr || (reinterpret_cast<uintptr_t>(sel_bias) & 3u) == 0, MOE_ERR_ALIGN);
+  const size_t need = router_ws_bytes(*cfg);
+  MOE_REQUIRE(ws_bytes >= need, MOE_ERR_WORKSPACE);
+  if (need > 0) { MOE_PTR(ws); }
   MOE_CTX(stream, c);
-  MOE_LAUNCH(launch_router_logits(c, *cfg, x, w_router, logit_bias, logits));
+  MOE_LAUNCH(launch_router_logits(c, *cfg, x, w_router, logit_bias, logits,
+                                  need > 0 ? ws : nullptr));
   MOE_LAUNCH(launch_router_topk(c, *cfg, logits, sel_bias, idx, w));
   return MOE_OK;
 }

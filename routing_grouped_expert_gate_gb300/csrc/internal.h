@@ -16,10 +16,18 @@ struct Ctx {
   int sm_count;
 };
 
-// ---- router (router.cu)
+// ---- router (router.cu; tensor-core gate GEMM in router_tc.cu)
+// ws: the router workspace (router_ws_bytes) or NULL when that size is 0
 cudaError_t launch_router_logits(const Ctx& c, const moe_cfg& cfg, const void* x,
                                  const float* w_router, const float* logit_bias,
-                                 float* logits);
+                                 float* logits, void* ws);
+size_t router_ws_bytes(const moe_cfg& cfg);
+bool router_tc_eligible(const moe_cfg& cfg);
+int router_set_impl(int impl);    // 0 tensor cores where eligible, 1 CUDA cores
+int router_set_fold(int fold_k);  // K elements per compensated window (multiple of 16)
+cudaError_t launch_router_logits_tc(const Ctx& c, const moe_cfg& cfg, const void* x_bf16,
+                                    const float* w_router, const float* logit_bias,
+                                    float* logits, void* ws);
 cudaError_t launch_router_topk(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                const float* sel_bias, int32_t* idx, float* w);
 // dW_r partials [splits][E][d] for E <= 16 (sum them in slice order)

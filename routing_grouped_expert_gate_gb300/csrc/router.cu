@@ -119,7 +119,8 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 // the eight threads of one shared-memory phase read 128 consecutive bytes).
 // Partial sums fold into the compensated (hi, lo) pair every 32 elements; at
 // the end group 0 adds the other groups' pairs in group order (deterministic).
-// Smaller BT (more K groups) gives more CTAs when T x E is small.
+// Smaller BT (more K groups) gives more CTAs when T x E is small; with large
+// T x E the 128-token tile is fastest (W staged once per 128 tokens).
 constexpr int RT_BE = 64, RT_KC = 64, RT_THREADS = 256;
 
 template <int BT>
@@ -566,20 +567,15 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
     router_logits_small<Tx, 16, TPW><<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
         x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
   } else {
-    // token tile: the one whose busiest SM has the least work, among those
-    // that give every SM two CTAs where T x E allows (ties to the larger tile,
-    // which stages W fewer times)
+    // token tile: the largest that still gives every SM a CTA (a smaller tile
+    // splits K inside the CTA and stages W once per fewer tokens)
     const int64_t e_tiles = (cfg.E + RT_BE - 1) / RT_BE;
     const int64_t sms = c.sm_count > 0 ? c.sm_count : 1;
     int best_bt = 32;
-    int64_t best_cost = -1;
-    for (int bt : {128, 64, 32}) {
-      const int64_t ctas = ((T + bt - 1) / bt) * e_tiles;
-      if (ctas < 2 * sms && bt != 32) continue;
-      const int64_t cost = ((ctas + sms - 1) / sms) * bt * bt;  // CTAs per SM x (BT / KS)
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
+    for (int bt : {128, 64}) {
+      if (((T + bt - 1) / bt) * e_tiles >= sms) {
         best_bt = bt;
+        break;
       }
     }
     cudaError_t e;
@@ -597,7 +593,9 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
 
 cudaError_t launch_router_logits(const Ctx& c, const moe_cfg& cfg, const void* x,
                                  const float* w_router, const float* logit_bias,
-                                 float* logits) {
+                                 float* logits, void* ws) {
+  if (cfg.T > 0 && ws != nullptr && router_tc_eligible(cfg))
+    return launch_router_logits_tc(c, cfg, x, w_router, logit_bias, logits, ws);
   if (cfg.act_dtype == MOE_BF16)
     return router_logits_dispatch(c, cfg, static_cast<const bf16*>(x), w_router, logit_bias,
                                   logits);

@@ -51,7 +51,7 @@ def alloc_buffers(cfg, device, backward: bool = True) -> Dict[str, torch.Tensor]
     if Fs > 0:
         b.update({"pre_gu_s": e(T, 2 * Fs), "h_s": e(T, Fs), "y_s": e(T, d)})
     ws = max(L.workspace_bytes(cfg, L.MOE_WS_PERMUTE), L.workspace_bytes(cfg, L.MOE_WS_GROUPED),
-             L.workspace_bytes(cfg, L.MOE_WS_AUX))
+             L.workspace_bytes(cfg, L.MOE_WS_AUX), L.workspace_bytes(cfg, L.MOE_WS_ROUTE))
     if backward:
         b.update({
             "d_out_perm": e(A, d),
@@ -80,7 +80,7 @@ def forward(cfg, p: Dict[str, Optional[torch.Tensor]], x: torch.Tensor,
     T, k, E, F, Fs = cfg.T, cfg.k, cfg.E, cfg.F, cfg.F_shared
     ws = b["ws"]
     L.route_topk(cfg, x, p["w_router"], p.get("logit_bias"), p.get("sel_bias"), b["logits"],
-                 b["idx"], b["w"], stream)
+                 b["idx"], b["w"], ws, stream)
     L.permute(cfg, x, b["idx"], b["counts"], b["offsets"], b["row_of"], b["src_tok"],
               b["x_perm"], ws, stream)
     L.grouped_swiglu(cfg, E, T * k, F, b["offsets"], b["x_perm"], p["w1"], p["w2"], b["pre_gu"],

@@ -78,8 +78,25 @@ def test_top1_sigmoid_is_allowed(L):
 def test_selection_bias_with_softmax_refused_before_any_device_work(L):
     cfg = _cfg(L)
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: the call returns first
-    rc = L.lib.moe_route_topk(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake, None)
+    rc = L.lib.moe_route_topk(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake, None, 0,
+                              None)
     assert rc == L.MOE_ERR_INVALID_ARG
+
+
+def test_router_workspace_sizes_and_refusal(L):
+    # tensor-core gate GEMM: three bf16 planes of W_r when x is bf16 and E % 64 == 0
+    tc = _cfg(L, T=512, d=256, E=128, k=8, act_dtype="bf16")
+    assert L.workspace_bytes(tc, L.MOE_WS_ROUTE) == 3 * 128 * 256 * 2
+    for other in (_cfg(L, T=512, d=256, E=128, k=8, act_dtype="f32"),
+                  _cfg(L, T=512, d=256, E=8, k=2, act_dtype="bf16"),
+                  _cfg(L, T=512, d=256, E=96, k=8, act_dtype="bf16")):
+        assert L.workspace_bytes(other, L.MOE_WS_ROUTE) == 0
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: the size check comes first
+    rc = L.lib.moe_route_topk(ctypes.byref(tc), fake, fake, None, None, fake, fake, fake, fake,
+                              100, None)
+    assert rc == L.MOE_ERR_WORKSPACE
+    assert L.lib.moe_set_router_fold(24) == L.MOE_ERR_INVALID_ARG
+    assert L.lib.moe_set_router_impl(7) == L.MOE_ERR_INVALID_ARG
 
 
 def test_null_and_misaligned_pointers_refused(L):

@@ -57,6 +57,9 @@ def run_gpu(wl, seed=0, backward=True, impl="tcgen05"):
                                    "tcgen05_1cta": L.MOE_GEMM_TC_SINGLE_CTA,
                                    "tcgen05_pairs": L.MOE_GEMM_TC_PAIRS,
                                    "cudacores": L.MOE_GEMM_CUDA_CORES}[impl])
+    # the CUDA-core run also takes the router's gate GEMM off the tensor cores
+    old_r = L.set_router_impl(L.MOE_ROUTER_CUDA_CORES if impl == "cudacores"
+                              else L.MOE_ROUTER_AUTO)
     try:
         layer.forward(cfg, p, inp["x"], b)
         if backward:
@@ -64,6 +67,7 @@ def run_gpu(wl, seed=0, backward=True, impl="tcgen05"):
         torch.cuda.synchronize()
     finally:
         L.set_grouped_gemm_impl(old)
+        L.set_router_impl(old_r)
     rc, detail = moe._lib.last_device_status()
     assert rc == 0, f"device status {rc} ({moe.status_string(rc)}) detail {detail}"
     return inp, b
@@ -132,6 +136,46 @@ def test_layer_parity(built, name, dt, impl):
     empty = np.nonzero(f["counts"] == 0)[0]
     for e in empty:
         assert float(b["dw1"][e].abs().max()) == 0.0 and float(b["dw2"][e].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("name", ["fine_grained_small", "deepseek_small", "zipf_small"])
+@pytest.mark.parametrize("fold_k", [16, 32, 64])
+def test_router_gate_gemm_paths(built, name, fold_k):
+    """The tensor-core gate GEMM (three bf16 planes of W_r, compensated folds
+    every fold_k elements) and the CUDA-core one both keep every logit within
+    1e-6 of the float64 oracle and select the oracle's experts."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = SMALL[name]
+    inp = mi.make_inputs(wl, seed=3, device="cuda")
+    cfg = moe.cfg_from_workload(wl)
+    ref = {k: O.as_f64(v) for k, v in inp.items() if v is not None}
+    r = O.route(ref["x"], ref["w_router"], wl.k, wl.score, wl.scaling, ref.get("logit_bias"),
+                ref.get("sel_bias"))
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_ROUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+    old_f = L.set_router_fold(fold_k)
+    try:
+        for impl in (L.MOE_ROUTER_AUTO, L.MOE_ROUTER_CUDA_CORES):
+            old = L.set_router_impl(impl)
+            try:
+                assert L.router_uses_tensor_cores(cfg) == (impl == L.MOE_ROUTER_AUTO)
+                logits = torch.full((wl.T, wl.E), float("nan"), device="cuda")
+                idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+                w = torch.empty(wl.T, wl.k, device="cuda")
+                L.route_topk(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"),
+                             inp.get("sel_bias"), logits, idx, w, ws)
+                torch.cuda.synchronize()
+            finally:
+                L.set_router_impl(old)
+            assert L.last_device_status()[0] == 0
+            err = float(np.max(np.abs(to_np(logits) - r["logits"])))
+            assert err < 1e-6, (impl, fold_k, err)
+            decided = r["gap"] >= 1e-6
+            assert np.array_equal(to_np(idx)[decided], r["idx"][decided])
+            assert_close("w", to_np(w)[decided], r["w"][decided], TOL_F32)
+    finally:
+        L.set_router_fold(old_f)
 
 
 def test_zero_load_experts_exist_in_skewed_case(built):
