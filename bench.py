@@ -47,6 +47,9 @@ def parse():
                     help="override the workload's token count (smaller cases for profiling)")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the forward only (the workload's own pass if it has no backward)")
+    ap.add_argument("--stage", default=None, choices=["route"],
+                    help="time one stage alone at the workload's full size, drawing only its "
+                         "inputs (a profiling aid; prints a stage line, not the step line)")
     return ap.parse_args()
 
 
@@ -527,9 +530,58 @@ def run_reference(args, ws, rank):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_stage_route(args):
+    """moe_route_topk alone (gate GEMM + scores + top-k) on the full workload."""
+    import torch
+    import moe_inputs as mi
+    from routing_grouped_expert_gate_gb300 import build as B
+    B.build()
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = mi.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        wl = mi.shrink(wl, name=f"{wl.name}_T{args.tokens}", T=args.tokens)
+    cfg = moe.cfg_from_workload(wl)
+    inp = mi.make_inputs(wl, seed=0, device="cuda", only=("x", "w_router"))
+    T, E, k, d = wl.T, wl.E, wl.k, wl.d
+    logits = torch.empty(T, E, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_ROUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        L.route_topk(cfg, inp["x"], inp["w_router"], inp["logit_bias"], inp["sel_bias"], logits,
+                     idx, w, ws)
+
+    for _ in range(max(args.warmup, 0)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    rc, detail = L.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} ({L.status_string(rc)}) {detail}")
+    us = e0.elapsed_time(e1) / max(args.steps, 1) * 1e3
+    es = 2 if wl.act_dtype == "bf16" else 4
+    flops = 2.0 * T * d * E
+    nbytes = T * d * es + E * d * 4 + T * E * 4 + T * k * 8
+    return {"stage": "route", "workload": workload_desc(wl, False), "steps": args.steps,
+            "us_per_call": round(us, 2), "tensor_cores": L.router_uses_tensor_cores(cfg),
+            "tflops_algorithmic": round(flops / (us * 1e-6) / 1e12, 2),
+            "gbs_algorithmic": round(nbytes / (us * 1e-6) / 1e9, 1)}
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    if args.stage == "route":
+        print(json.dumps(run_stage_route(args)), flush=True)
+        return 0
     if args.impl == "reference":
         out = run_reference(args, ws, rank)
         if out is not None:

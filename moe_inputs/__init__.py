@@ -18,7 +18,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Dict, Optional
+from typing import Sequence, Dict, Optional
 
 import torch
 
@@ -120,24 +120,34 @@ def zipf_logit_offset(E: int, s: float) -> torch.Tensor:
 
 
 def make_inputs(w: Workload, seed: int = 0, device="cpu",
-                with_dy: Optional[bool] = None) -> Dict[str, Optional[torch.Tensor]]:
+                with_dy: Optional[bool] = None,
+                only: Optional[Sequence[str]] = None) -> Dict[str, Optional[torch.Tensor]]:
     """Draw every input tensor of the workload on `device`.
 
     Returns a dict with keys x [T,d], w_router [E,d] fp32, w1 [E,2F,d],
     w2 [E,d,F], w1_s [2F_s,d] / w2_s [d,F_s] (None without a shared expert),
     sel_bias [E] fp32 (or None), logit_bias [E] fp32 (or None), dy [T,d]
     (or None). Rows [0,F) of each w1[e] are the gate, rows [F,2F) the up part.
+    `only` restricts the draw to the named tensors among x, w_router, w1, w2
+    (the others come back None); every tensor has its own generator, so the
+    values drawn do not depend on which others are drawn.
     """
     device = torch.device(device)
     act = w.torch_act_dtype
     std = w.weight_std
     out: Dict[str, Optional[torch.Tensor]] = {}
-    out["x"] = _normal((w.T, w.d), 1.0, _gen(seed, "x", device), device, act)
-    out["w_router"] = _normal((w.E, w.d), std, _gen(seed, "w_router", device), device,
-                              torch.float32)
-    out["w1"] = _normal((w.E, 2 * w.F, w.d), std, _gen(seed, "w1", device), device, act)
-    out["w2"] = _normal((w.E, w.d, w.F), std, _gen(seed, "w2", device), device, act)
-    if w.F_shared > 0:
+
+    def want(name):
+        return only is None or name in only
+
+    out["x"] = _normal((w.T, w.d), 1.0, _gen(seed, "x", device), device, act) if want("x") else None
+    out["w_router"] = (_normal((w.E, w.d), std, _gen(seed, "w_router", device), device,
+                               torch.float32) if want("w_router") else None)
+    out["w1"] = (_normal((w.E, 2 * w.F, w.d), std, _gen(seed, "w1", device), device, act)
+                 if want("w1") else None)
+    out["w2"] = (_normal((w.E, w.d, w.F), std, _gen(seed, "w2", device), device, act)
+                 if want("w2") else None)
+    if w.F_shared > 0 and want("w1") and want("w2"):
         out["w1_s"] = _normal((2 * w.F_shared, w.d), std, _gen(seed, "w1_s", device),
                               device, act)
         out["w2_s"] = _normal((w.d, w.F_shared), std, _gen(seed, "w2_s", device),
@@ -156,5 +166,5 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu",
     if with_dy is None:
         with_dy = w.backward
     out["dy"] = (_normal((w.T, w.d), 1.0, _gen(seed, "dy", device), device, act)
-                 if with_dy else None)
+                 if with_dy and only is None else None)
     return out

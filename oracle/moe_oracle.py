@@ -82,6 +82,16 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z * sigmoid(z)
 
 
+def softplus(z: np.ndarray) -> np.ndarray:
+    """log(1 + exp(z)), evaluated without overflow for either sign."""
+    return np.logaddexp(0.0, np.asarray(z, dtype=np.float64))
+
+
+def logsumexp_rows(z: np.ndarray) -> np.ndarray:
+    m = z.max(axis=-1, keepdims=True)
+    return (m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True)))[..., 0]
+
+
 def softmax_rows(z: np.ndarray) -> np.ndarray:
     m = z.max(axis=-1, keepdims=True)
     e = np.exp(z - m)
@@ -106,16 +116,38 @@ def gate_logits(x: np.ndarray, w_router: np.ndarray,
     return logits
 
 
+SCORE_FUNCTIONS = ("softmax", "sigmoid", "sqrtsoftplus", "softmax_pre")
+
+
 def scores(logits: np.ndarray, score: str) -> np.ndarray:
     """Per-expert scores before selection.
 
     Handbook §3.1 "Gating function": softmax routing selects on the logits
-    themselves; sigmoid routing selects on sigmoid(logits).
+    themselves (the softmax over the chosen comes after the top-k); with the
+    pre-softmax setting ("Output scale": --moe-router-pre-softmax) the softmax
+    over all E experts comes first and the top-k ranks its probabilities;
+    sigmoid routing selects on sigmoid(logits); sqrt(softplus) routing on
+    sqrt(log(1 + exp(logits))).
     """
     if score == "softmax":
         return logits.copy()
+    if score == "softmax_pre":
+        return softmax_rows(logits)
     if score == "sigmoid":
         return sigmoid(logits)
+    if score == "sqrtsoftplus":
+        return np.sqrt(softplus(logits))
+    raise ValueError(score)
+
+
+def score_derivative(logits: np.ndarray, score: str) -> np.ndarray:
+    """d score / d logit, elementwise, for the sigmoid-like score functions."""
+    if score == "sigmoid":
+        s = sigmoid(logits)
+        return s * (1.0 - s)
+    if score == "sqrtsoftplus":
+        # d/dl sqrt(softplus(l)) = sigmoid(l) / (2 sqrt(softplus(l)))
+        return sigmoid(logits) / (2.0 * np.sqrt(softplus(logits)))
     raise ValueError(score)
 
 
@@ -128,7 +160,7 @@ def selection_keys(logits: np.ndarray, score: str,
     """
     s = scores(logits, score)
     if sel_bias is not None:
-        if score == "softmax":
+        if score in ("softmax", "softmax_pre"):
             raise ValueError("the selection bias is refused with softmax scores "
                              "(Handbook §3.1, Gating function)")
         s = s + sel_bias[None, :]
@@ -165,8 +197,10 @@ def mixing_weights(logits: np.ndarray, idx: np.ndarray, score: str,
     """Weights of the chosen experts.
 
     Handbook §3.1 "Gating function" and "Output scale": softmax routing takes
-    the softmax over the k chosen logits (the renormalised softmax); sigmoid
-    routing divides each chosen score by their sum plus 1e-20 when k > 1 (the
+    the softmax over the k chosen logits (the renormalised softmax); with the
+    pre-softmax setting the weights are the chosen experts' probabilities
+    under the softmax over all E, not renormalised; sigmoid and sqrt(softplus)
+    routing divide each chosen score by their sum plus 1e-20 when k > 1 (the
     expert bias never enters); then everything is multiplied by the routed
     scaling factor.
     """
@@ -174,8 +208,10 @@ def mixing_weights(logits: np.ndarray, idx: np.ndarray, score: str,
     sel_logits = np.take_along_axis(logits, idx, axis=1)
     if score == "softmax":
         p = softmax_rows(sel_logits)
+    elif score == "softmax_pre":
+        p = np.take_along_axis(softmax_rows(logits), idx, axis=1)
     else:
-        s = sigmoid(sel_logits)
+        s = scores(sel_logits, score)
         p = s / (s.sum(axis=1, keepdims=True) + SIGMOID_RENORM_EPS) if k > 1 else s
     return p * scaling
 
@@ -309,12 +345,12 @@ def combine(out_perm: np.ndarray, row_of: np.ndarray, w: np.ndarray,
 def aux_probs(logits: np.ndarray, score: str) -> np.ndarray:
     """Router probabilities the aux loss averages: softmax over all E experts.
 
-    For sigmoid scores the pages give no form; the reading here normalises
-    the scores over all experts, s / sum_e s.
+    For sigmoid and sqrt(softplus) scores the pages give no form; the reading
+    here normalises the scores over all experts, s / sum_e s.
     """
-    if score == "softmax":
+    if score in ("softmax", "softmax_pre"):
         return softmax_rows(logits)
-    s = sigmoid(logits)
+    s = scores(logits, score)
     return s / s.sum(axis=1, keepdims=True)
 
 
@@ -325,6 +361,100 @@ def aux_loss(logits: np.ndarray, counts: np.ndarray, k: int, coeff: float,
     P = aux_probs(logits, score)
     col = P.sum(axis=0)
     return float(np.sum(col * counts.astype(np.float64)) * (E * coeff / (k * T * T)))
+
+
+# ----------------------------------------------------------------------------
+# router z-loss
+# ----------------------------------------------------------------------------
+
+def z_loss(logits: np.ndarray, coeff: float) -> float:
+    """Handbook §3.1 "Router scoring", part "Precision" (z_loss_func): the mean over tokens of
+    the squared logsumexp of each token's logits, times the coefficient. (The
+    value Megatron logs is this divided by the coefficient, the mean squared
+    logsumexp.)"""
+    T = logits.shape[0]
+    if T == 0:
+        return 0.0
+    lse = logsumexp_rows(logits)
+    return float(coeff * np.mean(lse * lse))
+
+
+def z_loss_backward(logits: np.ndarray, coeff: float, g: float = 1.0,
+                    T_total: Optional[int] = None) -> np.ndarray:
+    """d(g * z_loss)/d(logits) = g * coeff * 2 * lse_t * softmax(l_t) / T."""
+    n = logits.shape[0]
+    T = n if T_total is None else T_total
+    lse = logsumexp_rows(logits)
+    return (g * coeff * 2.0 / T) * lse[:, None] * softmax_rows(logits)
+
+
+# ----------------------------------------------------------------------------
+# load-balance bookkeeping: sequence-wise aux loss, expert bias update
+# ----------------------------------------------------------------------------
+
+def sequence_of_tokens(T: int, seq_len: int, seq_major: bool) -> np.ndarray:
+    """Sequence index of every token of a micro-batch of T = B * seq_len tokens.
+
+    Batch-major storage (seq_major False): token t = b * seq_len + s. Sequence-
+    major storage, the [seq, batch] order Megatron's activations use: token
+    t = s * B + b.
+    """
+    B = T // seq_len
+    t = np.arange(T)
+    return (t % B) if seq_major else (t // seq_len)
+
+
+def seq_aux_loss(logits: np.ndarray, idx: np.ndarray, seq_len: int, k: int, coeff: float,
+                 score: str, seq_major: bool = False) -> float:
+    """Handbook §3.3 "Load balancing", part "Scope" (seq_aux_loss): the
+    Switch loss taken over each sequence on its own, with that sequence's
+    counts, probabilities and length, then averaged over the B sequences:
+      (1/B) sum_b coeff * E / (k * S^2) * sum_e c[b, e] * sum_{t in b} P[t, e]."""
+    T, E = logits.shape
+    B = T // seq_len
+    seq = sequence_of_tokens(T, seq_len, seq_major)
+    P = aux_probs(logits, score)
+    total = 0.0
+    for b in range(B):
+        rows = np.nonzero(seq == b)[0]
+        c = np.bincount(idx[rows].reshape(-1), minlength=E).astype(np.float64)
+        total += coeff * E / (k * seq_len * seq_len) * float(np.sum(c * P[rows].sum(axis=0)))
+    return total / B
+
+
+def seq_aux_loss_backward(logits, idx, seq_len: int, k: int, coeff: float, score: str,
+                          g: float = 1.0, seq_major: bool = False) -> np.ndarray:
+    """d(g * seq_aux_loss)/d(logits), counts held constant: each sequence's
+    tokens get the aux-loss gradient of their own sequence, scaled by 1/B."""
+    T, E = logits.shape
+    B = T // seq_len
+    seq = sequence_of_tokens(T, seq_len, seq_major)
+    out = np.zeros((T, E))
+    for b in range(B):
+        rows = np.nonzero(seq == b)[0]
+        c = np.bincount(idx[rows].reshape(-1), minlength=E)
+        out[rows] = aux_loss_backward(logits[rows], c, k, coeff, score, g / B, T_total=seq_len)
+    return out
+
+
+def accumulate_tokens_per_expert(acc: np.ndarray, counts: np.ndarray) -> np.ndarray:
+    """Handbook §3.3 "Loss-free bias": the router keeps the token count of
+    every expert in int64 and adds each micro-batch's counts to it."""
+    return np.asarray(acc, dtype=np.int64) + np.asarray(counts, dtype=np.int64)
+
+
+def expert_bias_update(tokens_per_expert: np.ndarray, bias: np.ndarray,
+                       rate: float) -> np.ndarray:
+    """Handbook §3.3 "Loss-free bias" (_update_router_expert_bias): every
+    expert's bias moves by the update rate towards balance,
+      bias += sign(total - count[e] * E) * rate,
+    the comparison with the mean load made on the integers (count * E against
+    the total), never on a floating-point mean."""
+    c = [int(v) for v in np.asarray(tokens_per_expert).reshape(-1)]
+    E = len(c)
+    total = sum(c)
+    direction = np.array([(total > v * E) - (total < v * E) for v in c], dtype=np.float64)
+    return np.asarray(bias, dtype=np.float64) + direction * rate
 
 
 # ----------------------------------------------------------------------------
@@ -418,14 +548,14 @@ def aux_loss_backward(logits, counts, k: int, coeff: float, score: str,
     T = n if T_total is None else T_total
     dP = np.broadcast_to(g_aux * coeff * E * counts.astype(np.float64) / (k * T * T),
                          (n, E))
-    if score == "softmax":
+    if score in ("softmax", "softmax_pre"):
         P = softmax_rows(logits)
         return P * (dP - np.sum(P * dP, axis=1, keepdims=True))
-    s = sigmoid(logits)
+    s = scores(logits, score)
     S = s.sum(axis=1, keepdims=True)
     P = s / S
     ds = (dP - np.sum(P * dP, axis=1, keepdims=True)) / S
-    return ds * s * (1.0 - s)
+    return ds * score_derivative(logits, score)
 
 
 def scores_backward(logits, idx, dw, score: str, scaling: float) -> np.ndarray:
@@ -433,25 +563,34 @@ def scores_backward(logits, idx, dw, score: str, scaling: float) -> np.ndarray:
 
     Softmax over the chosen logits: p = softmax(l_sel), w = c p,
       d l_sel = p * (c dw - <p, c dw>).
-    Sigmoid, k > 1: w = c s_sel / (S + eps), S = sum s_sel,
-      d s_sel = c (dw - <dw, s_sel> / (S + eps)) / (S + eps), d l = d s * s (1 - s);
-    sigmoid, k = 1: w = c s, d s = c dw.
+    Sigmoid / sqrt(softplus), k > 1: w = c s_sel / (S + eps), S = sum s_sel,
+      d s_sel = c (dw - <dw, s_sel> / (S + eps)) / (S + eps), d l = d s * s'(l);
+    k = 1: w = c s, d s = c dw.
+    Pre-softmax: w_j = c P[idx_j] with P the softmax over all E, so every
+    logit gets a gradient: d l_e = c P_e (g_e - sum_j P[idx_j] dw_j), where
+    g_e = dw_j if e = idx_j and 0 otherwise.
     """
     T, E = logits.shape
     k = idx.shape[1]
     sel = np.take_along_axis(logits, idx, axis=1)
+    if score == "softmax_pre":
+        P = softmax_rows(logits)
+        g = np.zeros((T, E))
+        np.put_along_axis(g, idx, scaling * dw, axis=1)
+        return P * (g - np.sum(np.take_along_axis(P, idx, axis=1) * scaling * dw, axis=1,
+                               keepdims=True))
     if score == "softmax":
         p = softmax_rows(sel)
         gp = scaling * dw
         dsel = p * (gp - np.sum(p * gp, axis=1, keepdims=True))
     else:
-        s = sigmoid(sel)
+        s = scores(sel, score)
         if k > 1:
             S = s.sum(axis=1, keepdims=True) + SIGMOID_RENORM_EPS
             ds = scaling * (dw - np.sum(dw * s, axis=1, keepdims=True) / S) / S
         else:
             ds = scaling * dw
-        dsel = ds * s * (1.0 - s)
+        dsel = ds * score_derivative(sel, score)
     d_logits = np.zeros((T, E))
     np.put_along_axis(d_logits, idx, dsel, axis=1)
     return d_logits

@@ -20,11 +20,10 @@
 // One CTA computes 128 tokens x 64 experts: warp 0 issues the TMA loads (x
 // tile + three W tiles per 64-wide K block), warp 1 owns 256 TMEM columns
 // (two 64-column window accumulators, one 64-column low-part accumulator) and
-// issues tcgen05.mma (M=128, N=64, K=16), warps 2..5 (one per TMEM lane
-// quadrant) fold the windows and write the logits. Each fold thread keeps its
-// token's 64 (hi, lo) pairs in registers: 6 warps of up to 255 registers fit
-// the SM's four 16K-register partitions (at most two warps each). Every
-// mbarrier wait is bounded (MOE_ERR_TIMEOUT + abort flag).
+// issues tcgen05.mma (M=128, N=64, K=16), warps 2..9 (two per TMEM lane
+// quadrant, 32 columns each) fold the windows and write the logits; each fold
+// thread keeps its token's 32 (hi, lo) pairs in registers. Every mbarrier
+// wait is bounded (MOE_ERR_TIMEOUT + abort flag).
 #include <algorithm>
 #include <atomic>
 
@@ -37,8 +36,8 @@ namespace rtc {
 
 using namespace tc;
 
-constexpr int R_THREADS = 192;
-constexpr int R_EPI_WARPS = 4;
+constexpr int R_THREADS = 320;
+constexpr int R_EPI_WARPS = 8;
 constexpr int R_TMEM_COLS = 256;
 constexpr int R_MAX_STAGES = 8;
 
@@ -76,7 +75,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  const RParams P) {
   using RT = RTile<BN>;
   constexpr int S = RT::kStages;
-  constexpr int NC = BN;  // columns per fold warp
+  constexpr int NC = BN / 2;  // columns per fold warp
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -185,10 +184,11 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     if (ok && lane == 0) mma_commit(&sh.lo_full);
     __syncwarp();
   } else {
-    // ================= fold + store: warps 2..5 =================
+    // ================= fold + store: warps 2..9 =================
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 (the warp's quadrant)
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
-    const uint32_t base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + half * NC;
     float hi[NC], lo[NC];
 #pragma unroll
     for (int j = 0; j < NC; ++j) hi[j] = lo[j] = 0.f;
@@ -217,7 +217,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         for (int i = 0; i < 32; ++i) lo[c + i] += v[i];
       }
       const int64_t t = (int64_t)m0 + row;
-      const int e0 = n0;
+      const int e0 = n0 + half * NC;
       if (t < P.T) {
         float* dst = P.logits + t * P.E + e0;
 #pragma unroll
