@@ -66,6 +66,14 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
 /* ---- enumerations ---- */
 #define MOE_SCORE_SOFTMAX 0 /* top-k on logits, softmax over the k chosen     */
 #define MOE_SCORE_SIGMOID 1 /* top-k on sigmoid(l)+bias, renormalised (+1e-20) */
+#define MOE_SCORE_SQRT_SOFTPLUS 2 /* top-k on sqrt(softplus(l))+bias, renormalised
+                                     (+1e-20) like sigmoid (Handbook §3.1
+                                     "Gating function")                      */
+#define MOE_SCORE_SOFTMAX_PRE 3 /* softmax over all E first, top-k on those
+                                   probabilities, weights = the chosen
+                                   probabilities, not renormalised (Megatron's
+                                   --moe-router-pre-softmax; Handbook §3.1
+                                   "Output scale"); allowed at k = 1          */
 #define MOE_F32  0
 #define MOE_BF16 1
 
@@ -76,6 +84,7 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
 #define MOE_WS_AUX          3
 #define MOE_WS_ROUTE_BWD    4
 #define MOE_WS_ROUTE        5
+#define MOE_WS_Z_LOSS       6
 
 /* Layer configuration. Names follow the flags the Handbook uses for the layer
  * (§2.5 and §3.4: --num-experts, --moe-ffn-hidden-size, --moe-router-topk,
@@ -88,7 +97,7 @@ typedef struct {
   int32_t k;         /* experts per token, 1..min(8, E)                       */
   int32_t F;         /* routed expert FFN width, multiple of 8                */
   int32_t F_shared;  /* shared expert FFN width (multiple of 8), 0 = none     */
-  int32_t score_fn;  /* MOE_SCORE_SOFTMAX | MOE_SCORE_SIGMOID                 */
+  int32_t score_fn;  /* MOE_SCORE_SOFTMAX | _SIGMOID | _SQRT_SOFTPLUS | _SOFTMAX_PRE */
   int32_t act_dtype; /* MOE_BF16 | MOE_F32                                    */
   float scaling;     /* routed scaling factor (1.0 = none)                    */
   float aux_coeff;   /* Switch aux-loss coefficient                           */
@@ -270,6 +279,60 @@ int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_
                     moe_stream_t stream);
 
 /* ---------------------------- utilities --------------------------------- */
+
+/* ------------------------------------------------------------------------ *
+ * Router z-loss (Handbook §3.1 "Router scoring", part "Precision",
+ * z_loss_func): z = coeff * mean over the T tokens of logsumexp(l_t)^2.
+ * (Megatron logs z / coeff, the mean squared logsumexp.)
+ *   logits [T, E] fp32;  z: device fp32 scalar out
+ *   ws >= moe_workspace_bytes(cfg, MOE_WS_Z_LOSS)
+ * moe_z_loss_bwd: d_logits[t, e] (+)= g_z * coeff * 2 * lse_t * softmax(l_t)_e / T
+ * (accumulate != 0 adds to d_logits, else overwrites). Deterministic.       */
+int moe_z_loss(const moe_cfg* cfg, const float* logits, float coeff, float* z, void* ws,
+               size_t ws_bytes, moe_stream_t stream);
+int moe_z_loss_bwd(const moe_cfg* cfg, const float* logits, float coeff, float g_z,
+                   float* d_logits, int32_t accumulate, moe_stream_t stream);
+
+/* Sequence-wise Switch loss (Handbook §3.3 "Load balancing", part "Scope",
+ * Megatron's seq_aux_loss): the aux loss of each sequence on its own - its
+ * counts, its router probabilities, its length S = seq_len - averaged over
+ * the B = T / seq_len sequences:
+ *   out = (1/B) sum_b coeff * E / (k S^2) * sum_e c[b, e] * sum_{t in b} P[t, e]
+ * with P as in moe_aux_loss. Token t of sequence b at position s is
+ * t = b * S + s (seq_major = 0) or t = s * B + b (seq_major = 1, the
+ * [seq, batch] order of Megatron's activations).
+ *   logits [T, E] fp32, idx [T, k] int32 (an index out of range is skipped and
+ *   recorded as MOE_ERR_DEVICE_INDEX); out: device fp32 scalar
+ *   ws >= moe_seq_aux_workspace_bytes(cfg, seq_len)
+ * seq_len must divide T (else MOE_ERR_INVALID_ARG). The backward adds
+ * g * d(out)/d(logits) (counts held constant) to d_logits, or overwrites it
+ * when accumulate == 0. Deterministic.                                     */
+size_t moe_seq_aux_workspace_bytes(const moe_cfg* cfg, int64_t seq_len);
+int moe_seq_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* idx,
+                     int64_t seq_len, int32_t seq_major, float coeff, float* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream);
+int moe_seq_aux_loss_bwd(const moe_cfg* cfg, const float* logits, const int32_t* idx,
+                         int64_t seq_len, int32_t seq_major, float coeff, float g,
+                         float* d_logits, int32_t accumulate, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Load-balance bookkeeping (Handbook §3.3 "Load balancing", part "Loss-free
+ * bias"; §3.2 "Routing strategy", part "Who selects", for MaxVio).
+ * moe_tokens_per_expert_accumulate: tokens_per_expert[e] += counts[e]
+ *   (counts [E] int32 from moe_permute; tokens_per_expert [E] int64, the
+ *   router's running count, zeroed by the caller when a step starts).
+ * moe_expert_bias_update: expert_bias[e] += sign(total - tokens_per_expert[e]
+ *   * E) * rate in fp32, total = sum of the counts; the comparison is made on
+ *   the int64 values, never on a floating-point mean.
+ * moe_max_vio: *max_vio = (max_e count - total / E) / (total / E), computed as
+ *   (max * E - total) / total in fp64 and stored as fp32; 0 when total = 0.
+ * All three are single small launches on `stream`.                         */
+int moe_tokens_per_expert_accumulate(const moe_cfg* cfg, const int32_t* counts,
+                                     int64_t* tokens_per_expert, moe_stream_t stream);
+int moe_expert_bias_update(const moe_cfg* cfg, const int64_t* tokens_per_expert,
+                           float* expert_bias, float rate, moe_stream_t stream);
+int moe_max_vio(const moe_cfg* cfg, const int64_t* tokens_per_expert, float* max_vio,
+                moe_stream_t stream);
 
 /* Bytes of scratch the call `which` (MOE_WS_*) needs for cfg. For
  * MOE_WS_GROUPED / MOE_WS_GROUPED_BWD the size covers the routed experts

@@ -34,7 +34,7 @@ class Workload:
     k: int            # experts chosen per token
     F: int            # routed expert FFN width
     F_shared: int     # shared expert FFN width, 0 = no shared expert
-    score: str        # "softmax" (renormalised over the top-k) or "sigmoid"
+    score: str        # "softmax" (renormalised over the top-k), "sigmoid", "sqrtsoftplus" or "softmax_pre"
     act_dtype: str    # "f32" or "bf16"
     backward: bool    # whether the workload runs the backward pass
     sel_bias_range: float = 0.0   # >0: selection-only expert bias ~ U(-r, r)

@@ -32,6 +32,10 @@ MOE_ERR_NO_DEVICE = -8
 
 MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID = 1
+MOE_SCORE_SQRT_SOFTPLUS = 2
+MOE_SCORE_SOFTMAX_PRE = 3
+SCORE_CODES = {"softmax": MOE_SCORE_SOFTMAX, "sigmoid": MOE_SCORE_SIGMOID,
+               "sqrtsoftplus": MOE_SCORE_SQRT_SOFTPLUS, "softmax_pre": MOE_SCORE_SOFTMAX_PRE}
 MOE_F32 = 0
 MOE_BF16 = 1
 
@@ -46,6 +50,7 @@ MOE_WS_GROUPED_BWD = 2
 MOE_WS_AUX = 3
 MOE_WS_ROUTE_BWD = 4
 MOE_WS_ROUTE = 5
+MOE_WS_Z_LOSS = 6
 
 MOE_ROUTER_AUTO = 0
 MOE_ROUTER_CUDA_CORES = 1
@@ -107,6 +112,16 @@ _SIGS = {
     "moe_launch_count": (c_uint64, []),
     "moe_set_grouped_gemm_impl": (c_int, [c_int]),
     "moe_set_router_impl": (c_int, [c_int]),
+    "moe_z_loss": (c_int, [POINTER(MoeCfg), _VP, c_float, _VP, _VP, c_size_t, _VP]),
+    "moe_z_loss_bwd": (c_int, [POINTER(MoeCfg), _VP, c_float, c_float, _VP, c_int32, _VP]),
+    "moe_seq_aux_workspace_bytes": (c_size_t, [POINTER(MoeCfg), c_int64]),
+    "moe_seq_aux_loss": (c_int, [POINTER(MoeCfg), _VP, _VP, c_int64, c_int32, c_float, _VP, _VP,
+                                 c_size_t, _VP]),
+    "moe_seq_aux_loss_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, c_int64, c_int32, c_float,
+                                     c_float, _VP, c_int32, _VP, c_size_t, _VP]),
+    "moe_tokens_per_expert_accumulate": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP]),
+    "moe_expert_bias_update": (c_int, [POINTER(MoeCfg), _VP, _VP, c_float, _VP]),
+    "moe_max_vio": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP]),
     "moe_set_router_fold": (c_int, [c_int]),
     "moe_router_uses_tensor_cores": (c_int, [POINTER(MoeCfg)]),
     "moe_kernel_timing": (c_int, [c_int]),
@@ -179,7 +194,7 @@ def version() -> str:
 def make_cfg(T, d, E, k, F, F_shared=0, score="softmax", act_dtype="bf16", scaling=1.0,
              aux_coeff=1e-3) -> MoeCfg:
     return MoeCfg(T=T, d=d, E=E, k=k, F=F, F_shared=F_shared,
-                  score_fn=MOE_SCORE_SOFTMAX if score == "softmax" else MOE_SCORE_SIGMOID,
+                  score_fn=SCORE_CODES[score],
                   act_dtype=MOE_BF16 if act_dtype == "bf16" else MOE_F32,
                   scaling=scaling, aux_coeff=aux_coeff)
 
@@ -296,6 +311,54 @@ def aux_loss_bwd(cfg, logits, counts, g_aux, d_logits, accumulate, stream=None):
     _check(lib.moe_aux_loss_bwd(ctypes.byref(cfg), _p(logits), _p(counts), float(g_aux),
                                 _p(d_logits), int(accumulate), _stream(stream)),
            "moe_aux_loss_bwd")
+
+
+def _nbytes(ws):
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+def z_loss(cfg, logits, coeff, z, ws, stream=None):
+    _check(lib.moe_z_loss(ctypes.byref(cfg), _p(logits), float(coeff), _p(z), _p(ws),
+                          _nbytes(ws), _stream(stream)), "moe_z_loss")
+
+
+def z_loss_bwd(cfg, logits, coeff, g_z, d_logits, accumulate, stream=None):
+    _check(lib.moe_z_loss_bwd(ctypes.byref(cfg), _p(logits), float(coeff), float(g_z),
+                              _p(d_logits), int(accumulate), _stream(stream)), "moe_z_loss_bwd")
+
+
+def seq_aux_workspace_bytes(cfg, seq_len) -> int:
+    return int(lib.moe_seq_aux_workspace_bytes(ctypes.byref(cfg), int(seq_len)))
+
+
+def seq_aux_loss(cfg, logits, idx, seq_len, seq_major, coeff, out, ws, stream=None):
+    _check(lib.moe_seq_aux_loss(ctypes.byref(cfg), _p(logits), _p(idx), int(seq_len),
+                                int(seq_major), float(coeff), _p(out), _p(ws), _nbytes(ws),
+                                _stream(stream)), "moe_seq_aux_loss")
+
+
+def seq_aux_loss_bwd(cfg, logits, idx, seq_len, seq_major, coeff, g, d_logits, accumulate, ws,
+                     stream=None):
+    _check(lib.moe_seq_aux_loss_bwd(ctypes.byref(cfg), _p(logits), _p(idx), int(seq_len),
+                                    int(seq_major), float(coeff), float(g), _p(d_logits),
+                                    int(accumulate), _p(ws), _nbytes(ws), _stream(stream)),
+           "moe_seq_aux_loss_bwd")
+
+
+def tokens_per_expert_accumulate(cfg, counts, tokens_per_expert, stream=None):
+    _check(lib.moe_tokens_per_expert_accumulate(ctypes.byref(cfg), _p(counts),
+                                                _p(tokens_per_expert), _stream(stream)),
+           "moe_tokens_per_expert_accumulate")
+
+
+def expert_bias_update(cfg, tokens_per_expert, expert_bias, rate, stream=None):
+    _check(lib.moe_expert_bias_update(ctypes.byref(cfg), _p(tokens_per_expert), _p(expert_bias),
+                                      float(rate), _stream(stream)), "moe_expert_bias_update")
+
+
+def max_vio(cfg, tokens_per_expert, out, stream=None):
+    _check(lib.moe_max_vio(ctypes.byref(cfg), _p(tokens_per_expert), _p(out), _stream(stream)),
+           "moe_max_vio")
 
 
 def route_topk_bwd(cfg, x, w_router, logits, idx, dw, d_logits, accumulate, dx_router,

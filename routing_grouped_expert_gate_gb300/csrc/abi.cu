@@ -68,7 +68,7 @@ static int check_cfg(const moe_cfg* cfg) {
   if (cfg->T < 0 || cfg->d <= 0 || cfg->E <= 0 || cfg->k <= 0 || cfg->F <= 0 ||
       cfg->F_shared < 0)
     return MOE_ERR_INVALID_ARG;
-  if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID)
+  if (cfg->score_fn < MOE_SCORE_SOFTMAX || cfg->score_fn > MOE_SCORE_SOFTMAX_PRE)
     return MOE_ERR_INVALID_ARG;
   if (cfg->act_dtype != MOE_F32 && cfg->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (cfg->k > cfg->E) return MOE_ERR_INVALID_ARG;
@@ -238,6 +238,7 @@ size_t moe_workspace_bytes(const moe_cfg* cfg, int which) {
     case MOE_WS_AUX: return aux_ws_bytes(*cfg);
     case MOE_WS_ROUTE_BWD: return route_bwd_ws(*cfg);
     case MOE_WS_ROUTE: return router_ws_bytes(*cfg);
+    case MOE_WS_Z_LOSS: return z_loss_ws_bytes(*cfg);
     default: return 0;
   }
 }
@@ -246,7 +247,7 @@ int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
                    const float* logit_bias, const float* sel_bias, float* logits, int32_t* idx,
                    float* w, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_CHECK_CFG(cfg);
-  if (sel_bias != nullptr && cfg->score_fn == MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+  if (sel_bias != nullptr && !score_takes_bias(cfg->score_fn)) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
   MOE_PTR(x); MOE_PTR(w_router); MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(w);
   MOE_REQUIRE(logit_bias == nullptr || (reinterpret_cast<uintptr_t>(logit_bias) & 3u) == 0, MOE_ERR_ALIGN);
@@ -432,6 +433,85 @@ int moe_aux_loss_bwd(const moe_cfg* cfg, const float* logits, const int32_t* cou
   MOE_PTR(logits); MOE_PTR(d_logits);
   MOE_CTX(stream, c);
   MOE_LAUNCH(launch_aux_loss_bwd(c, *cfg, logits, counts, g_aux, d_logits, accumulate));
+  return MOE_OK;
+}
+
+int moe_z_loss(const moe_cfg* cfg, const float* logits, float coeff, float* z, void* ws,
+               size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(z); MOE_PTR(ws);
+  if (cfg->T > 0) { MOE_PTR(logits); }
+  MOE_REQUIRE(ws_bytes >= z_loss_ws_bytes(*cfg), MOE_ERR_WORKSPACE);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_z_loss(c, *cfg, logits, coeff, z, ws));
+  return MOE_OK;
+}
+
+int moe_z_loss_bwd(const moe_cfg* cfg, const float* logits, float coeff, float g_z,
+                   float* d_logits, int32_t accumulate, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(logits); MOE_PTR(d_logits);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_z_loss_bwd(c, *cfg, logits, coeff, g_z, d_logits, accumulate));
+  return MOE_OK;
+}
+
+size_t moe_seq_aux_workspace_bytes(const moe_cfg* cfg, int64_t seq_len) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return seq_aux_ws_bytes(*cfg, seq_len);
+}
+
+int moe_seq_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* idx,
+                     int64_t seq_len, int32_t seq_major, float coeff, float* out, void* ws,
+                     size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(cfg->T > 0 && seq_len > 0 && cfg->T % seq_len == 0, MOE_ERR_INVALID_ARG);
+  MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(out); MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= seq_aux_ws_bytes(*cfg, seq_len), MOE_ERR_WORKSPACE);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_seq_aux_loss(c, *cfg, logits, idx, seq_len, seq_major != 0, coeff, out, ws));
+  return MOE_OK;
+}
+
+int moe_seq_aux_loss_bwd(const moe_cfg* cfg, const float* logits, const int32_t* idx,
+                         int64_t seq_len, int32_t seq_major, float coeff, float g,
+                         float* d_logits, int32_t accumulate, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(cfg->T > 0 && seq_len > 0 && cfg->T % seq_len == 0, MOE_ERR_INVALID_ARG);
+  MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(d_logits); MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= seq_aux_ws_bytes(*cfg, seq_len), MOE_ERR_WORKSPACE);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_seq_aux_loss_bwd(c, *cfg, logits, idx, seq_len, seq_major != 0, coeff, g,
+                                     d_logits, accumulate, ws));
+  return MOE_OK;
+}
+
+int moe_tokens_per_expert_accumulate(const moe_cfg* cfg, const int32_t* counts,
+                                     int64_t* tokens_per_expert, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(counts); MOE_PTR(tokens_per_expert);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_tokens_accumulate(c, *cfg, counts, tokens_per_expert));
+  return MOE_OK;
+}
+
+int moe_expert_bias_update(const moe_cfg* cfg, const int64_t* tokens_per_expert,
+                           float* expert_bias, float rate, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(tokens_per_expert); MOE_PTR(expert_bias);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_expert_bias_update(c, *cfg, tokens_per_expert, expert_bias, rate));
+  return MOE_OK;
+}
+
+int moe_max_vio(const moe_cfg* cfg, const int64_t* tokens_per_expert, float* max_vio,
+                moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(tokens_per_expert); MOE_PTR(max_vio);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_max_vio(c, *cfg, tokens_per_expert, max_vio));
   return MOE_OK;
 }
 

@@ -24,18 +24,20 @@ size_t aux_ws_bytes(const moe_cfg& cfg) {
   return ((n + 255) & ~(size_t)255) + 256;
 }
 
-// P row of one token into p[EPL] (lane holds experts lane + 32 i); returns S for
-// sigmoid (1 for softmax). Non-existent experts get 0.
+// P row of one token into p[EPL] (lane holds experts lane + 32 i): the softmax
+// over all E, or s / sum_e s for the sigmoid-like scores (s_out = s, returns
+// sum_e s; 1 for softmax). l_out receives the logits. Non-existent experts
+// get 0.
 template <int EPL>
 __device__ __forceinline__ float token_probs(const float* __restrict__ row, int E, int score_fn,
-                                             int lane, float (&p)[EPL], float (&s_out)[EPL]) {
-  float l[EPL];
+                                             int lane, float (&p)[EPL], float (&s_out)[EPL],
+                                             float (&l)[EPL]) {
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     l[i] = (e < E) ? row[e] : -INFINITY;
   }
-  if (score_fn == MOE_SCORE_SOFTMAX) {
+  if (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE) {
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) m = fmaxf(m, l[i]);
@@ -58,7 +60,7 @@ __device__ __forceinline__ float token_probs(const float* __restrict__ row, int 
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
-    s_out[i] = (lane + 32 * i < E) ? sigmoidf_acc(l[i]) : 0.f;
+    s_out[i] = (lane + 32 * i < E) ? bias_score(l[i], score_fn) : 0.f;
     s += s_out[i];
   }
   s = warp_sum(s);
@@ -81,8 +83,8 @@ aux_partials(const float* __restrict__ logits, int64_t T, int E, int score_fn,
   for (int tl = warp; tl < AUX_TOK; tl += 8) {
     const int64_t t = t0 + tl;
     if (t >= T) break;
-    float p[EPL], s[EPL];
-    token_probs<EPL>(logits + t * E, E, score_fn, lane, p, s);
+    float p[EPL], s[EPL], l[EPL];
+    token_probs<EPL>(logits + t * E, E, score_fn, lane, p, s, l);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) col[i] += p[i];
   }
@@ -134,8 +136,8 @@ aux_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ cou
     dP[i] = (e < E) ? g_scale * (float)counts[e] : 0.f;
   }
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
-    float p[EPL], s[EPL];
-    const float S = token_probs<EPL>(logits + t * E, E, score_fn, lane, p, s);
+    float p[EPL], s[EPL], l[EPL];
+    const float S = token_probs<EPL>(logits + t * E, E, score_fn, lane, p, s, l);
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) dot += p[i] * dP[i];
@@ -145,16 +147,377 @@ aux_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ cou
       const int e = lane + 32 * i;
       if (e < E) {
         float g;
-        if (score_fn == MOE_SCORE_SOFTMAX) {
+        if (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE) {
           g = p[i] * (dP[i] - dot);
         } else {
-          g = (dP[i] - dot) / S * s[i] * (1.f - s[i]);
+          g = (dP[i] - dot) / S * bias_score_deriv(l[i], s[i], score_fn);
         }
         float* dst = d_logits + t * E + e;
         *dst = accumulate ? *dst + g : g;
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- router z-loss
+// Handbook §3.1 "Router scoring", part "Precision" (z_loss_func):
+//   z = coeff * mean_t (logsumexp_t l)^2,  dz/dl[t, e] = coeff * 2 lse_t softmax(l_t)_e / T.
+// Deterministic like the aux loss: 64 tokens per CTA, fixed-order sums, fp64
+// partials added in block order by one thread.
+constexpr int Z_TOK = 64;
+
+size_t z_loss_ws_bytes(const moe_cfg& cfg) {
+  const size_t n = (size_t)((cfg.T + Z_TOK - 1) / Z_TOK) * sizeof(double);
+  return ((n + 255) & ~(size_t)255) + 256;
+}
+
+template <int EPL>
+__device__ __forceinline__ float token_lse(const float* __restrict__ row, int E, int lane,
+                                           float (&l)[EPL], float& m_out, float& sum_out) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    l[i] = (e < E) ? row[e] : -INFINITY;
+    m = fmaxf(m, l[i]);
+  }
+  m = warp_max(m);
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (lane + 32 * i < E) sum += expf(l[i] - m);
+  sum = warp_sum(sum);
+  m_out = m;
+  sum_out = sum;
+  return m + logf(sum);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256)
+z_partials(const float* __restrict__ logits, int64_t T, int E, double* __restrict__ part) {
+  __shared__ double wsum[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double acc = 0.0;
+  const int64_t t0 = (int64_t)blockIdx.x * Z_TOK;
+  for (int tl = warp; tl < Z_TOK; tl += 8) {
+    const int64_t t = t0 + tl;
+    if (t >= T) break;
+    float l[EPL], m, sum;
+    const float lse = token_lse<EPL>(logits + t * E, E, lane, l, m, sum);
+    acc += (double)lse * (double)lse;
+  }
+  if (lane == 0) wsum[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double v = 0.0;
+    for (int w = 0; w < 8; ++w) v += wsum[w];
+    part[blockIdx.x] = v;
+  }
+}
+
+__global__ void z_finalize(const double* __restrict__ part, int64_t nblk, int64_t T, float coeff,
+                           float* __restrict__ z) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double v = 0.0;
+  for (int64_t b = 0; b < nblk; ++b) v += part[b];
+  *z = (T > 0) ? (float)((double)coeff * v / (double)T) : 0.f;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256)
+z_bwd_kernel(const float* __restrict__ logits, int64_t T, int E, float g_scale,
+             float* __restrict__ d_logits, int accumulate) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    float l[EPL], m, sum;
+    const float lse = token_lse<EPL>(logits + t * E, E, lane, l, m, sum);
+    const float f = g_scale * lse / sum;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        const float g = f * expf(l[i] - m);
+        float* dst = d_logits + t * E + e;
+        *dst = accumulate ? *dst + g : g;
+      }
+    }
+  }
+}
+
+#define MOE_BY_EPL(EPLV, MACRO) \
+  switch (EPLV) {               \
+    case 1: MACRO(1); break;    \
+    case 2: MACRO(2); break;    \
+    case 3: case 4: MACRO(4); break; \
+    default: MACRO(8); break;   \
+  }
+
+cudaError_t launch_z_loss(const Ctx& c, const moe_cfg& cfg, const float* logits, float coeff,
+                          float* z, void* ws) {
+  const int64_t nblk = (cfg.T + Z_TOK - 1) / Z_TOK;
+  double* part = static_cast<double*>(ws);
+  const int epl = (cfg.E + 31) / 32;
+  if (nblk > 0) {
+#define MOE_ZP(N) z_partials<N><<<(unsigned)nblk, 256, 0, c.stream>>>(logits, cfg.T, cfg.E, part)
+    MOE_BY_EPL(epl, MOE_ZP)
+#undef MOE_ZP
+  }
+  z_finalize<<<1, 32, 0, c.stream>>>(part, nblk, cfg.T, coeff, z);
+  note_launches(nblk > 0 ? 2 : 1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_z_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits, float coeff,
+                              float g_z, float* d_logits, int accumulate) {
+  if (cfg.T == 0) return cudaSuccess;
+  const float g_scale = (float)((double)g_z * (double)coeff * 2.0 / (double)cfg.T);
+  const int64_t blocks = (cfg.T + 7) / 8;
+  const int64_t cap = (int64_t)c.sm_count * 8;
+  const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
+  const int epl = (cfg.E + 31) / 32;
+#define MOE_ZB(N)                                                                          \
+  z_bwd_kernel<N><<<grid, 256, 0, c.stream>>>(logits, cfg.T, cfg.E, g_scale, d_logits, \
+                                              accumulate)
+  MOE_BY_EPL(epl, MOE_ZB)
+#undef MOE_ZB
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- sequence-wise aux loss
+// Handbook §3.3 "Load balancing", part "Scope" (seq_aux_loss): the Switch loss
+// of each sequence on its own (its counts, its probabilities, its length S),
+// averaged over the B = T / S sequences:
+//   (1/B) sum_b coeff * E / (k * S^2) * sum_e c[b, e] * sum_{t in b} P[t, e].
+// Token t of sequence b, position s: t = b S + s (batch-major) or t = s B + b
+// (sequence-major, the [seq, batch] order of Megatron's activations).
+// A sequence is cut into `cps` chunks of up to `chunk` tokens; one CTA per
+// chunk writes its column sums of P and its expert counts; the sums over
+// chunks, experts and sequences then run in fixed order (deterministic).
+struct SeqPlan {
+  int64_t B, S, cps, chunk;
+};
+
+static SeqPlan seq_plan(const moe_cfg& cfg, int64_t S) {
+  SeqPlan p;
+  p.S = S;
+  p.B = cfg.T / S;
+  const int64_t max_cps = (S + 63) / 64;
+  int64_t cps = (1024 + p.B - 1) / p.B;  // about 1024 CTAs in all
+  if (cps > max_cps) cps = max_cps;
+  if (cps < 1) cps = 1;
+  p.cps = cps;
+  p.chunk = (S + cps - 1) / cps;
+  return p;
+}
+
+size_t seq_aux_ws_bytes(const moe_cfg& cfg, int64_t S) {
+  if (S <= 0 || cfg.T % S != 0) return 0;
+  const SeqPlan p = seq_plan(cfg, S);
+  const size_t n = (size_t)(p.B * p.cps) * (size_t)cfg.E;
+  const size_t a = ((n * sizeof(float) + 255) & ~(size_t)255);        // column sums
+  const size_t b = ((n * sizeof(int32_t) + 255) & ~(size_t)255);      // counts
+  const size_t c = (((size_t)p.B * sizeof(double) + 255) & ~(size_t)255);  // per-sequence losses
+  const size_t d = (((size_t)p.B * cfg.E * sizeof(int32_t) + 255) & ~(size_t)255);  // counts per sequence
+  return a + b + c + d + 256;
+}
+
+__device__ __forceinline__ int64_t seq_token(int64_t b, int64_t s, int64_t B, int64_t S,
+                                             int seq_major) {
+  return seq_major ? s * B + b : b * S + s;
+}
+
+// colsum may be NULL (counts only)
+template <int EPL>
+__global__ void __launch_bounds__(256)
+seq_partials(const float* __restrict__ logits, const int32_t* __restrict__ idx, int E, int k,
+             SeqPlan pl, int seq_major, int score_fn, float* __restrict__ colsum,
+             int32_t* __restrict__ cnt, int* status) {
+  __shared__ float wsum[8][kMaxE];
+  __shared__ int hist[kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t blk = blockIdx.x;
+  const int64_t b = blk / pl.cps, cidx = blk - b * pl.cps;
+  const int64_t s0 = cidx * pl.chunk;
+  int64_t s1 = s0 + pl.chunk;
+  if (s1 > pl.S) s1 = pl.S;
+  float col[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) col[i] = 0.f;
+  for (int64_t s = s0 + warp; s < s1; s += 8) {
+    const int64_t t = seq_token(b, s, pl.B, pl.S, seq_major);
+    if (colsum != nullptr) {
+      float p[EPL], sc[EPL], l[EPL];
+      token_probs<EPL>(logits + t * E, E, score_fn, lane, p, sc, l);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) col[i] += p[i];
+    }
+    if (lane < k) {
+      const int e = idx[t * k + lane];
+      if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+      else record_error(status, MOE_ERR_DEVICE_INDEX, (int)t);
+    }
+  }
+  if (colsum != nullptr) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) wsum[warp][e] = col[i];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    if (colsum != nullptr) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += wsum[w][e];
+      colsum[blk * E + e] = v;
+    }
+    cnt[blk * E + e] = hist[e];
+  }
+}
+
+// one CTA per sequence: its loss (fp64), and its counts summed over chunks
+__global__ void __launch_bounds__(256)
+seq_per_sequence(const float* __restrict__ colsum, const int32_t* __restrict__ cnt, int E, int k,
+                 SeqPlan pl, float coeff, double* __restrict__ loss_b,
+                 int32_t* __restrict__ cnt_b) {
+  __shared__ double term[kMaxE];
+  const int64_t b = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    double cs = 0.0;
+    int64_t n = 0;
+    for (int64_t c = 0; c < pl.cps; ++c) {
+      const int64_t r = (b * pl.cps + c) * E + e;
+      if (colsum != nullptr) cs += (double)colsum[r];
+      n += cnt[r];
+    }
+    term[e] = cs * (double)n;
+    if (cnt_b != nullptr) cnt_b[b * E + e] = (int32_t)n;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && loss_b != nullptr) {
+    double acc = 0.0;
+    for (int e = 0; e < E; ++e) acc += term[e];
+    const double S = (double)pl.S;
+    loss_b[b] = acc * (double)coeff * (double)E / ((double)k * S * S);
+  }
+}
+
+__global__ void seq_mean(const double* __restrict__ loss_b, int64_t B, float* __restrict__ out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double v = 0.0;
+  for (int64_t b = 0; b < B; ++b) v += loss_b[b];
+  *out = (B > 0) ? (float)(v / (double)B) : 0.f;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256)
+seq_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ cnt_b, int E,
+               int score_fn, SeqPlan pl, int seq_major, float g_scale,
+               float* __restrict__ d_logits, int accumulate) {
+  const int lane = threadIdx.x & 31;
+  const int64_t T = pl.B * pl.S;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    const int64_t b = seq_major ? t % pl.B : t / pl.S;
+    float p[EPL], s[EPL], l[EPL], dP[EPL];
+    const float S = token_probs<EPL>(logits + t * E, E, score_fn, lane, p, s, l);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      dP[i] = (e < E) ? g_scale * (float)cnt_b[b * E + e] : 0.f;
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) dot += p[i] * dP[i];
+    dot = warp_sum(dot);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        float g;
+        if (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE)
+          g = p[i] * (dP[i] - dot);
+        else
+          g = (dP[i] - dot) / S * bias_score_deriv(l[i], s[i], score_fn);
+        float* dst = d_logits + t * E + e;
+        *dst = accumulate ? *dst + g : g;
+      }
+    }
+  }
+}
+
+struct SeqWs {
+  float* colsum;
+  int32_t* cnt;
+  double* loss_b;
+  int32_t* cnt_b;
+};
+
+static SeqWs seq_ws(const moe_cfg& cfg, const SeqPlan& p, void* ws) {
+  const size_t n = (size_t)(p.B * p.cps) * (size_t)cfg.E;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  SeqWs w;
+  w.colsum = reinterpret_cast<float*>(base);
+  base += (n * sizeof(float) + 255) & ~(size_t)255;
+  w.cnt = reinterpret_cast<int32_t*>(base);
+  base += (n * sizeof(int32_t) + 255) & ~(size_t)255;
+  w.loss_b = reinterpret_cast<double*>(base);
+  base += ((size_t)p.B * sizeof(double) + 255) & ~(size_t)255;
+  w.cnt_b = reinterpret_cast<int32_t*>(base);
+  return w;
+}
+
+cudaError_t launch_seq_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                const int32_t* idx, int64_t S, int seq_major, float coeff,
+                                float* out, void* ws) {
+  const SeqPlan pl = seq_plan(cfg, S);
+  const SeqWs w = seq_ws(cfg, pl, ws);
+  const int epl = (cfg.E + 31) / 32;
+  const unsigned nblk = (unsigned)(pl.B * pl.cps);
+#define MOE_SP(N)                                                                          \
+  seq_partials<N><<<nblk, 256, 0, c.stream>>>(logits, idx, cfg.E, cfg.k, pl, seq_major,   \
+                                              cfg.score_fn, w.colsum, w.cnt, c.status)
+  MOE_BY_EPL(epl, MOE_SP)
+#undef MOE_SP
+  seq_per_sequence<<<(unsigned)pl.B, 256, 0, c.stream>>>(w.colsum, w.cnt, cfg.E, cfg.k, pl,
+                                                          coeff, w.loss_b, nullptr);
+  seq_mean<<<1, 32, 0, c.stream>>>(w.loss_b, pl.B, out);
+  note_launches(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seq_aux_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                    const int32_t* idx, int64_t S, int seq_major, float coeff,
+                                    float g, float* d_logits, int accumulate, void* ws) {
+  const SeqPlan pl = seq_plan(cfg, S);
+  const SeqWs w = seq_ws(cfg, pl, ws);
+  const int epl = (cfg.E + 31) / 32;
+  const unsigned nblk = (unsigned)(pl.B * pl.cps);
+#define MOE_SC(N)                                                                          \
+  seq_partials<N><<<nblk, 256, 0, c.stream>>>(logits, idx, cfg.E, cfg.k, pl, seq_major,   \
+                                              cfg.score_fn, nullptr, w.cnt, c.status)
+  MOE_BY_EPL(epl, MOE_SC)
+#undef MOE_SC
+  seq_per_sequence<<<(unsigned)pl.B, 256, 0, c.stream>>>(nullptr, w.cnt, cfg.E, cfg.k, pl, coeff,
+                                                          nullptr, w.cnt_b);
+  const double Sd = (double)S;
+  const float g_scale = (float)((double)g * (double)coeff * (double)cfg.E /
+                                ((double)cfg.k * Sd * Sd * (double)pl.B));
+  const int64_t blocks = (cfg.T + 7) / 8;
+  const int64_t cap = (int64_t)c.sm_count * 8;
+  const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
+#define MOE_SB(N)                                                                        \
+  seq_bwd_kernel<N><<<grid, 256, 0, c.stream>>>(logits, w.cnt_b, cfg.E, cfg.score_fn, pl, \
+                                                seq_major, g_scale, d_logits, accumulate)
+  MOE_BY_EPL(epl, MOE_SB)
+#undef MOE_SB
+  note_launches(3);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logits,

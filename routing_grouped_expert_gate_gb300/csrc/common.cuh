@@ -131,4 +131,21 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ float sigmoidf_acc(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// sqrt(softplus(z)) = sqrt(log(1 + exp(z))); softplus(z) = z + log1p(exp(-z))
+// for z > 0 (no overflow), log1p(exp(z)) otherwise.
+__device__ __forceinline__ float sqrt_softplusf(float z) {
+  const float sp = z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
+  return sqrtf(sp);
+}
+
+// Score of one logit for the sigmoid-like score functions (sigmoid and
+// sqrt(softplus)); d score / d logit through `deriv`.
+__device__ __forceinline__ float bias_score(float z, int score_fn) {
+  return score_fn == MOE_SCORE_SQRT_SOFTPLUS ? sqrt_softplusf(z) : sigmoidf_acc(z);
+}
+__device__ __forceinline__ float bias_score_deriv(float z, float s, int score_fn) {
+  // sigmoid: s (1 - s); sqrt(softplus): sigmoid(z) / (2 s)
+  return score_fn == MOE_SCORE_SQRT_SOFTPLUS ? sigmoidf_acc(z) / (2.f * s) : s * (1.f - s);
+}
+
 }  // namespace moe

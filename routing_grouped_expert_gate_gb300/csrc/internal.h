@@ -9,6 +9,12 @@
 
 namespace moe {
 
+// score functions that take the aux-loss-free selection bias (Megatron refuses
+// it with softmax, before or after the top-k)
+inline bool score_takes_bias(int score_fn) {
+  return score_fn == MOE_SCORE_SIGMOID || score_fn == MOE_SCORE_SQRT_SOFTPLUS;
+}
+
 struct Ctx {
   cudaStream_t stream;
   int* status;          // device status word of the current device
@@ -36,6 +42,30 @@ cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void*
 cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                      const int32_t* idx, const float* dw, float* d_logits,
                                      int accumulate);
+
+// ---- router z-loss and sequence-wise aux loss (aux_loss.cu)
+size_t z_loss_ws_bytes(const moe_cfg& cfg);
+cudaError_t launch_z_loss(const Ctx& c, const moe_cfg& cfg, const float* logits, float coeff,
+                          float* z, void* ws);
+cudaError_t launch_z_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits, float coeff,
+                              float g_z, float* d_logits, int accumulate);
+size_t seq_aux_ws_bytes(const moe_cfg& cfg, int64_t seq_len);  // 0: seq_len does not divide T
+cudaError_t launch_seq_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                const int32_t* idx, int64_t seq_len, int seq_major, float coeff,
+                                float* out, void* ws);
+cudaError_t launch_seq_aux_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                    const int32_t* idx, int64_t seq_len, int seq_major,
+                                    float coeff, float g, float* d_logits, int accumulate,
+                                    void* ws);
+
+// ---- load-balance bookkeeping (balance.cu)
+cudaError_t launch_tokens_accumulate(const Ctx& c, const moe_cfg& cfg, const int32_t* counts,
+                                     int64_t* tokens_per_expert);
+cudaError_t launch_expert_bias_update(const Ctx& c, const moe_cfg& cfg,
+                                      const int64_t* tokens_per_expert, float* expert_bias,
+                                      float rate);
+cudaError_t launch_max_vio(const Ctx& c, const moe_cfg& cfg, const int64_t* tokens_per_expert,
+                           float* out);
 
 // ---- dispatch (dispatch.cu)
 size_t permute_ws_bytes(const moe_cfg& cfg);

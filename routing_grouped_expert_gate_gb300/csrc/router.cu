@@ -331,10 +331,10 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       if (e < E) {
         const float l = logits[t * E + e];
         float kv;
-        if (score_fn == MOE_SCORE_SOFTMAX) {
-          kv = l;
+        if (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE) {
+          kv = l;  // pre-softmax: replaced by the probability below
         } else {
-          kv = sigmoidf_acc(l);
+          kv = bias_score(l, score_fn);
           if (sel_bias != nullptr) kv = __fadd_rn(kv, sel_bias[e]);
         }
         key[i] = (kv == kv) ? kv : -INFINITY;
@@ -345,6 +345,28 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
         lg[i] = 0.f;
         taken[i] = true;
       }
+    }
+    // pre-softmax: the key is the probability under the softmax over all E
+    float pre_inv = 0.f, pre_max = 0.f;
+    if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < E) m = fmaxf(m, lg[i]);
+      m = warp_max(m);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < E) sum += expf(lg[i] - m);
+      sum = warp_sum(sum);
+      pre_max = m;
+      pre_inv = 1.f / sum;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < E) {
+          const float pv = expf(lg[i] - m) * pre_inv;
+          key[i] = (pv == pv) ? pv : -INFINITY;
+        }
     }
     int sel_e[kMaxK];
     float sel_l[kMaxK];
@@ -398,11 +420,15 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       const float inv = scaling / s;
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) wv[j] *= inv;
+    } else if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        wv[j] = (j < k) ? expf(sel_l[j] - pre_max) * pre_inv * scaling : 0.f;
     } else {
       float s = 0.f;
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        wv[j] = (j < k) ? sigmoidf_acc(sel_l[j]) : 0.f;
+        wv[j] = (j < k) ? bias_score(sel_l[j], score_fn) : 0.f;
         s += wv[j];
       }
       const float inv = (k > 1) ? scaling / (s + 1e-20f) : scaling;
@@ -473,11 +499,34 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
       }
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) dl[j] = p[j] * (scaling * gj[j] - dot);
+    } else if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
+      // w_j = c P[idx_j] with P the softmax over all E: every logit moves,
+      // d l_e = c P_e (g_e - sum_j P[idx_j] dw_j)
+      float m = -INFINITY;
+      for (int e = lane; e < E; e += 32) m = fmaxf(m, logits[t * E + e]);
+      m = warp_max(m);
+      float sum = 0.f;
+      for (int e = lane; e < E; e += 32) sum += expf(logits[t * E + e] - m);
+      sum = warp_sum(sum);
+      const float inv = 1.f / sum;
+      float dot = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) dot += expf(lj[j] - m) * inv * (scaling * gj[j]);
+      for (int e = lane; e < E; e += 32) {
+        float ge = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+          if (j < k && ej[j] == e) ge = scaling * gj[j];
+        const float pe = expf(logits[t * E + e] - m) * inv;
+        d_logits[t * E + e] += pe * (ge - dot);
+      }
+      continue;
     } else {
       float sj[kMaxK], S = 0.f, dsd = 0.f;
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        sj[j] = (j < k) ? sigmoidf_acc(lj[j]) : 0.f;
+        sj[j] = (j < k) ? bias_score(lj[j], score_fn) : 0.f;
         S += sj[j];
         dsd += gj[j] * sj[j];
       }
@@ -485,7 +534,7 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         const float ds = (k > 1) ? scaling * (gj[j] - dsd / S) / S : scaling * gj[j];
-        dl[j] = ds * sj[j] * (1.f - sj[j]);
+        dl[j] = ds * bias_score_deriv(lj[j], sj[j], score_fn);
       }
     }
     __syncwarp();

@@ -28,6 +28,16 @@ SMALL = {
     "deepseek_small": mi.shrink(W["deepseek_v3_shaped"], name="deepseek_small", T=256, d=512,
                                 F=128, F_shared=192, backward=True),
     "zipf_small": mi.shrink(W["zipf_imbalance"], name="zipf_small", T=1024, d=192, F=136),
+    # router variants (Handbook §3.1): sqrt(softplus) with the selection bias and a
+    # routed scaling factor; pre-softmax at top-1 and at top-4 with a skewed router
+    "sqrtsoftplus_small": mi.shrink(W["deepseek_v3_shaped"], name="sqrtsoftplus_small",
+                                    score="sqrtsoftplus", T=384, d=256, E=64, k=6, F=96,
+                                    F_shared=64, scaling=2.5, backward=True),
+    "presoftmax_top1_small": mi.shrink(W["fine_grained_64e"], name="presoftmax_top1_small",
+                                       score="softmax_pre", T=333, d=192, E=16, k=1, F=128,
+                                       F_shared=0),
+    "presoftmax_small": mi.shrink(W["zipf_imbalance"], name="presoftmax_small",
+                                  score="softmax_pre", T=257, d=128, E=32, k=4, F=64),
 }
 # bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
