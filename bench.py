@@ -47,6 +47,9 @@ def parse():
                     help="override the workload's token count (smaller cases for profiling)")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the forward only (the workload's own pass if it has no backward)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip timing the router's optional companions (z-loss, sequence "
+                         "aux loss, bias update, MaxVio) after the step")
     ap.add_argument("--stage", default=None, choices=["route"],
                     help="time one stage alone at the workload's full size, drawing only its "
                          "inputs (a profiling aid; prints a stage line, not the step line)")
@@ -167,6 +170,59 @@ def recorded_traffic(workload, kernel_key):
 
 
 # ------------------------------------------------------------------ our arm
+def time_extras(L, cfg, b, T, K):
+    """The router's optional companions, timed one by one on the step's own
+    logits, indices and counts after the timed step (not part of the step):
+    router z-loss, sequence-wise aux loss (sequences of min(T, 4096) tokens),
+    token-count accumulation, expert-bias update and MaxVio."""
+    import torch
+    E = cfg.E
+    dev = b["logits"].device
+    S = T if T <= 4096 or T % 4096 else 4096
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_Z_LOSS),
+                         L.seq_aux_workspace_bytes(cfg, S), 256), dtype=torch.uint8, device=dev)
+    z = torch.empty(1, device=dev)
+    d = torch.zeros_like(b["logits"])
+    tpe = torch.zeros(E, dtype=torch.int64, device=dev)
+    bias = torch.zeros(E, device=dev)
+    mv = torch.empty(1, device=dev)
+    calls = {
+        "z_loss": lambda: L.z_loss(cfg, b["logits"], 1e-3, z, ws),
+        "z_loss_bwd": lambda: L.z_loss_bwd(cfg, b["logits"], 1e-3, 1.0, d, 1),
+        "seq_aux_loss": lambda: L.seq_aux_loss(cfg, b["logits"], b["idx"], S, 0, 1e-4, z, ws),
+        "seq_aux_loss_bwd": lambda: L.seq_aux_loss_bwd(cfg, b["logits"], b["idx"], S, 0, 1e-4,
+                                                       1.0, d, 1, ws),
+        "tokens_per_expert_accumulate": lambda: L.tokens_per_expert_accumulate(cfg, b["counts"],
+                                                                               tpe),
+        "expert_bias_update": lambda: L.expert_bias_update(cfg, tpe, bias, 1e-3),
+        "max_vio": lambda: L.max_vio(cfg, tpe, mv),
+    }
+    logit_bytes = T * E * 4
+    nbytes = {"z_loss": logit_bytes, "z_loss_bwd": 3 * logit_bytes,
+              "seq_aux_loss": logit_bytes + T * cfg.k * 4,
+              "seq_aux_loss_bwd": 3 * logit_bytes + T * cfg.k * 4}
+    out = {"seq_len": S}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / K * 1e3
+        ent = {"us": round(us, 2)}
+        if name in nbytes:
+            ent["gbs"] = round(nbytes[name] / (us * 1e-6) / 1e9, 1)
+        out[name] = ent
+    rc, detail = L.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after the extras: {rc} {detail}")
+    return out
+
+
 def stage_work(wl, cfg_backward):
     """Algorithmic FLOPs / bytes of each ABI call of one step."""
     es = 2 if wl.act_dtype == "bf16" else 4
@@ -399,6 +455,8 @@ def run_ours(args, ws, rank, local):
         "peaks": dict(peaks, fp32_alu_tflops=round(fp32_peak, 2)),
     }
     out["value"] = round(ws * T / (ms_per_step * 1e-3), 1)
+    if not args.no_extras:
+        out["extras"] = time_extras(L, cfg, b, T, K)
 
     # ---- end to end: host inputs in, result out, through the same calls
     if not args.no_e2e:

@@ -458,6 +458,61 @@ def expert_bias_update(tokens_per_expert: np.ndarray, bias: np.ndarray,
 
 
 # ----------------------------------------------------------------------------
+# quantile balancing
+# ----------------------------------------------------------------------------
+
+def _kth_largest(values: np.ndarray, r: int) -> float:
+    """The r-th largest entry (1-based) of a 1-D array, by a full sort."""
+    return float(np.sort(values)[::-1][r - 1])
+
+
+def quantile_route(logits: np.ndarray, beta: np.ndarray, k: int, score: str,
+                   scaling: float = 1.0, solve: bool = True) -> Dict[str, np.ndarray]:
+    """Handbook §3.3 "Load balancing", part "Quantile" (the quantile-balancing
+    router): selection on the scores minus the per-expert quantile bias beta,
+    top-(k+1) per token; the first k are the chosen experts and the (k+1)-th
+    key is the token's threshold alpha. Each expert's local solution is the
+    (col_target+1)-th largest of (score - alpha) over the micro-batch's
+    tokens, col_target = T k / E (T k must be divisible by E).
+
+    The router computes in fp32, so the rank decisions and the quantile are
+    taken here on fp32 values: the scores rounded to fp32, then fp32
+    subtractions (numpy float32 arithmetic rounds like the device). The
+    mixing weights are those of the score function over the chosen experts:
+    beta, like the expert bias, only selects.
+    """
+    T, E = logits.shape
+    if not k < E:
+        raise ValueError("quantile routing needs k < E (it ranks k + 1 experts)")
+    s32 = scores(logits, score).astype(np.float32)
+    v32 = s32 - beta.astype(np.float32)[None, :]
+    order = np.argsort(-v32, axis=1, kind="stable")[:, :k + 1]
+    idx = order[:, :k].astype(np.int64)
+    alpha = v32[np.arange(T), order[:, k]]
+    out = {"idx": idx, "alpha": alpha.astype(np.float64),
+           "w": mixing_weights(logits, idx, score, scaling),
+           "keys": v32.astype(np.float64), "gap": kth_gap(v32.astype(np.float64), k)}
+    if solve:
+        if (T * k) % E != 0:
+            raise ValueError("quantile balancing needs T * k divisible by E")
+        col_target = T * k // E
+        d32 = s32 - alpha[:, None]
+        out["beta_local"] = np.array([_kth_largest(d32[:, e], col_target + 1)
+                                      for e in range(E)], dtype=np.float64)
+    return out
+
+
+def quantile_beta_update(beta: np.ndarray, accum: np.ndarray, count: int,
+                         ema: float) -> np.ndarray:
+    """Handbook §3.3 "Quantile": the micro-batches' solutions averaged
+    (accum / max(count, 1)), mixed into the running beta by the EMA
+    (ema * beta + (1 - ema) * average), then centred to zero mean."""
+    local = np.asarray(accum, dtype=np.float64) / max(int(count), 1)
+    nb = ema * np.asarray(beta, dtype=np.float64) + (1.0 - ema) * local
+    return nb - nb.mean()
+
+
+# ----------------------------------------------------------------------------
 # whole layer, forward
 # ----------------------------------------------------------------------------
 

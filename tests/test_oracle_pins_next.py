@@ -239,3 +239,71 @@ def test_token_counts_accumulate_over_micro_batches():
         all_idx.append(idx)
     np.testing.assert_array_equal(acc, O.dispatch(np.concatenate(all_idx), E)["counts"])
     assert acc.dtype == np.int64
+
+
+# ---------------------------------------------------------------- quantile balancing
+
+def test_quantile_route_selects_top_k_of_scores_minus_beta():
+    rng = np.random.default_rng(31)
+    T, E, k = 48, 8, 2
+    logits = rng.standard_normal((T, E))
+    beta = rng.standard_normal(E) * 0.3
+    r = O.quantile_route(logits, beta, k, "softmax")
+    v = (logits.astype(np.float32) - beta.astype(np.float32)).astype(np.float64)
+    for t in range(T):
+        ranked = sorted(range(E), key=lambda e: (-v[t, e], e))
+        assert list(r["idx"][t]) == ranked[:k]
+        assert r["alpha"][t] == v[t, ranked[k]]
+    # the weights ignore beta: the same as plain routing with those experts
+    np.testing.assert_allclose(r["w"], O.mixing_weights(logits, r["idx"], "softmax", 1.0))
+
+
+def test_quantile_solution_by_brute_force():
+    rng = np.random.default_rng(32)
+    T, E, k = 12, 4, 2  # col_target = 6
+    logits = rng.standard_normal((T, E))
+    beta = np.zeros(E)
+    r = O.quantile_route(logits, beta, k, "sigmoid")
+    s32 = O.scores(logits, "sigmoid").astype(np.float32)
+    for e in range(E):
+        col = [float(np.float32(s32[t, e] - np.float32(r["alpha"][t]))) for t in range(T)]
+        col.sort(reverse=True)
+        assert r["beta_local"][e] == col[T * k // E]  # the 7th largest
+    with pytest.raises(ValueError):
+        O.quantile_route(logits[:11], beta, k, "sigmoid")  # 11 * 2 not divisible by 4
+
+
+def test_quantile_balancing_evens_the_load_faster_than_the_sign_update():
+    g = G["quantile_balancing"]
+    rng = np.random.default_rng(33)
+    T, E, k = 512, 16, 2
+    skew = np.log(np.arange(1, E + 1, dtype=np.float64) ** -1.2)
+    logits = rng.standard_normal((T, E)) + 2.0 * skew[None, :]
+    target = T * k // E
+    beta = np.zeros(E)
+    bias = np.zeros(E)
+    for _ in range(g["steps"]):
+        r = O.quantile_route(logits, beta, k, "sigmoid")
+        beta = O.quantile_beta_update(beta, r["beta_local"], 1, ema=0.0)
+        keys = O.selection_keys(logits, "sigmoid", bias)
+        counts = O.dispatch(O.topk_sorted(keys, k), E)["counts"]
+        bias = O.expert_bias_update(counts, bias, 1e-3)
+    q_counts = O.dispatch(O.quantile_route(logits, beta, k, "sigmoid", solve=False)["idx"],
+                          E)["counts"]
+    s_counts = O.dispatch(O.topk_sorted(O.selection_keys(logits, "sigmoid", bias), k),
+                          E)["counts"]
+    assert q_counts.sum() == s_counts.sum() == T * k
+    assert O.max_vio(q_counts) < 0.25
+    assert O.max_vio(q_counts) < 0.25 * O.max_vio(s_counts)
+    assert abs(q_counts - target).max() < abs(s_counts - target).max()
+
+
+def test_quantile_beta_update_ema_and_centring():
+    beta = np.array([0.5, -0.25, 1.0, 0.0])
+    accum = np.array([1.0, 2.0, 3.0, 6.0])
+    nb = O.quantile_beta_update(beta, accum, 2, ema=0.75)
+    want = 0.75 * beta + 0.25 * accum / 2
+    np.testing.assert_allclose(nb, want - want.mean(), rtol=1e-15)
+    assert abs(nb.mean()) < 1e-15
+    np.testing.assert_allclose(O.quantile_beta_update(beta, accum, 0, ema=1.0),
+                               beta - beta.mean())
