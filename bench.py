@@ -174,7 +174,8 @@ def time_extras(L, cfg, b, T, K):
     """The router's optional companions, timed one by one on the step's own
     logits, indices and counts after the timed step (not part of the step):
     router z-loss, sequence-wise aux loss (sequences of min(T, 4096) tokens),
-    token-count accumulation, expert-bias update and MaxVio."""
+    token-count accumulation, expert-bias update, MaxVio and the quantile-
+    balancing router (ranking, per-expert quantile, accumulation, update)."""
     import torch
     E = cfg.E
     dev = b["logits"].device
@@ -197,10 +198,25 @@ def time_extras(L, cfg, b, T, K):
         "expert_bias_update": lambda: L.expert_bias_update(cfg, tpe, bias, 1e-3),
         "max_vio": lambda: L.max_vio(cfg, tpe, mv),
     }
+    if cfg.k < E and (T * cfg.k) % E == 0 and cfg.score_fn != L.MOE_SCORE_SOFTMAX_PRE:
+        qidx = torch.empty_like(b["idx"])
+        qw = torch.empty_like(b["w"])
+        alpha = torch.empty(T, device=dev)
+        beta = torch.zeros(E, device=dev)
+        bl = torch.empty(E, device=dev)
+        acc = torch.zeros(E, device=dev)
+        cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+        calls["quantile_route_and_solve"] = lambda: L.quantile_route(cfg, b["logits"], beta, qidx,
+                                                                     qw, alpha, bl)
+        calls["quantile_accumulate"] = lambda: L.quantile_accumulate(cfg, bl, acc, cnt)
+        calls["quantile_beta_update"] = lambda: L.quantile_beta_update(cfg, beta, acc, cnt, 0.9)
     logit_bytes = T * E * 4
     nbytes = {"z_loss": logit_bytes, "z_loss_bwd": 3 * logit_bytes,
               "seq_aux_loss": logit_bytes + T * cfg.k * 4,
-              "seq_aux_loss_bwd": 3 * logit_bytes + T * cfg.k * 4}
+              "seq_aux_loss_bwd": 3 * logit_bytes + T * cfg.k * 4,
+              # the per-token ranking reads the logits once; the per-expert
+              # radix select reads its column four times
+              "quantile_route_and_solve": 5 * logit_bytes + T * cfg.k * 8 + T * 4}
     out = {"seq_len": S}
     for name, fn in calls.items():
         for _ in range(3):

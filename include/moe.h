@@ -280,6 +280,39 @@ int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_
 
 /* ---------------------------- utilities --------------------------------- */
 
+/* S1 alone: logits = x·W_rᵀ (+ logit_bias), exactly as moe_route_topk
+ * computes them (same kernels, same accuracy, same workspace
+ * MOE_WS_ROUTE), for routers that select by other rules (quantile). */
+int moe_gate_logits(const moe_cfg* cfg, const void* x, const float* w_router,
+                    const float* logit_bias, float* logits, void* ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Quantile balancing (Handbook §3.3 "Load balancing", part "Quantile").
+ * moe_quantile_route: per token, rank the experts by key = score - beta[e]
+ *   (score: the logit for softmax, sigmoid(l) or sqrt(softplus(l)); fp32
+ *   subtraction), keep the first k in idx (descending key, ties to the lower
+ *   index) with the mixing weights of cfg's score function over them (beta
+ *   only selects), and write the (k+1)-th key to alpha[t]. When beta_local is
+ *   not NULL, also solve each expert's quantile: beta_local[e] = the
+ *   (T k / E + 1)-th largest of score[t, e] - alpha[t] over the T tokens
+ *   (exact: a radix select on the fp32 values; T k must be divisible by E).
+ *   Needs k < E. MOE_SCORE_SOFTMAX_PRE is refused (MOE_ERR_UNSUPPORTED).
+ *   logits [T, E] fp32; beta [E] fp32; idx [T, k] int32 out; w [T, k] fp32
+ *   out; alpha [T] fp32 out; beta_local [E] fp32 out or NULL.
+ * moe_quantile_accumulate: accum[e] += beta_local[e]; *count += 1 (the
+ *   micro-batches of one global batch).
+ * moe_quantile_beta_update: beta = ema * beta + (1 - ema) * accum / max(count,
+ *   1), then beta -= mean(beta); accum and count are reset to 0.
+ *   0 <= ema <= 1, else MOE_ERR_INVALID_ARG.                              */
+int moe_quantile_route(const moe_cfg* cfg, const float* logits, const float* beta,
+                       int32_t* idx, float* w, float* alpha, float* beta_local,
+                       moe_stream_t stream);
+int moe_quantile_accumulate(const moe_cfg* cfg, const float* beta_local, float* accum,
+                            int32_t* count, moe_stream_t stream);
+int moe_quantile_beta_update(const moe_cfg* cfg, float* beta, float* accum, int32_t* count,
+                             float ema, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Router z-loss (Handbook §3.1 "Router scoring", part "Precision",
  * z_loss_func): z = coeff * mean over the T tokens of logsumexp(l_t)^2.

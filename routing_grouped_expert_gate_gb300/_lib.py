@@ -112,6 +112,10 @@ _SIGS = {
     "moe_launch_count": (c_uint64, []),
     "moe_set_grouped_gemm_impl": (c_int, [c_int]),
     "moe_set_router_impl": (c_int, [c_int]),
+    "moe_gate_logits": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
+    "moe_quantile_route": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_quantile_accumulate": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP]),
+    "moe_quantile_beta_update": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, c_float, _VP]),
     "moe_z_loss": (c_int, [POINTER(MoeCfg), _VP, c_float, _VP, _VP, c_size_t, _VP]),
     "moe_z_loss_bwd": (c_int, [POINTER(MoeCfg), _VP, c_float, c_float, _VP, c_int32, _VP]),
     "moe_seq_aux_workspace_bytes": (c_size_t, [POINTER(MoeCfg), c_int64]),
@@ -315,6 +319,28 @@ def aux_loss_bwd(cfg, logits, counts, g_aux, d_logits, accumulate, stream=None):
 
 def _nbytes(ws):
     return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+def gate_logits(cfg, x, w_router, logit_bias, logits, ws=None, stream=None):
+    _check(lib.moe_gate_logits(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias),
+                               _p(logits), _p(ws), _nbytes(ws), _stream(stream)),
+           "moe_gate_logits")
+
+
+def quantile_route(cfg, logits, beta, idx, w, alpha, beta_local=None, stream=None):
+    _check(lib.moe_quantile_route(ctypes.byref(cfg), _p(logits), _p(beta), _p(idx), _p(w),
+                                  _p(alpha), _p(beta_local), _stream(stream)),
+           "moe_quantile_route")
+
+
+def quantile_accumulate(cfg, beta_local, accum, count, stream=None):
+    _check(lib.moe_quantile_accumulate(ctypes.byref(cfg), _p(beta_local), _p(accum), _p(count),
+                                       _stream(stream)), "moe_quantile_accumulate")
+
+
+def quantile_beta_update(cfg, beta, accum, count, ema, stream=None):
+    _check(lib.moe_quantile_beta_update(ctypes.byref(cfg), _p(beta), _p(accum), _p(count),
+                                        float(ema), _stream(stream)), "moe_quantile_beta_update")
 
 
 def z_loss(cfg, logits, coeff, z, ws, stream=None):

@@ -515,6 +515,59 @@ int moe_max_vio(const moe_cfg* cfg, const int64_t* tokens_per_expert, float* max
   return MOE_OK;
 }
 
+int moe_gate_logits(const moe_cfg* cfg, const void* x, const float* w_router,
+                    const float* logit_bias, float* logits, void* ws, size_t ws_bytes,
+                    moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(x); MOE_PTR(w_router); MOE_PTR(logits);
+  MOE_REQUIRE(logit_bias == nullptr || (reinterpret_cast<uintptr_t>(logit_bias) & 3u) == 0, MOE_ERR_ALIGN);
+  const size_t need = router_ws_bytes(*cfg);
+  MOE_REQUIRE(ws_bytes >= need, MOE_ERR_WORKSPACE);
+  if (need > 0) { MOE_PTR(ws); }
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_router_logits(c, *cfg, x, w_router, logit_bias, logits,
+                                  need > 0 ? ws : nullptr));
+  return MOE_OK;
+}
+
+int moe_quantile_route(const moe_cfg* cfg, const float* logits, const float* beta,
+                       int32_t* idx, float* w, float* alpha, float* beta_local,
+                       moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(cfg->score_fn != MOE_SCORE_SOFTMAX_PRE, MOE_ERR_UNSUPPORTED);
+  MOE_REQUIRE(cfg->k < cfg->E, MOE_ERR_INVALID_ARG);
+  if (beta_local != nullptr) {
+    MOE_REQUIRE(cfg->T > 0 && (cfg->T * (int64_t)cfg->k) % cfg->E == 0, MOE_ERR_INVALID_ARG);
+    MOE_PTR(beta_local);
+  }
+  MOE_PTR(beta); MOE_PTR(alpha);
+  if (cfg->T > 0) { MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(w); }
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_router_topk_q(c, *cfg, logits, nullptr, beta, alpha, idx, w));
+  if (beta_local != nullptr) MOE_LAUNCH(launch_quantile_solve(c, *cfg, logits, alpha, beta_local));
+  return MOE_OK;
+}
+
+int moe_quantile_accumulate(const moe_cfg* cfg, const float* beta_local, float* accum,
+                            int32_t* count, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(beta_local); MOE_PTR(accum); MOE_PTR(count);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_quantile_accumulate(c, *cfg, beta_local, accum, count));
+  return MOE_OK;
+}
+
+int moe_quantile_beta_update(const moe_cfg* cfg, float* beta, float* accum, int32_t* count,
+                             float ema, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(ema >= 0.f && ema <= 1.f, MOE_ERR_INVALID_ARG);
+  MOE_PTR(beta); MOE_PTR(accum); MOE_PTR(count);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_quantile_beta_update(c, *cfg, beta, accum, count, ema));
+  return MOE_OK;
+}
+
 int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
                        const float* logits, const int32_t* idx, const float* dw, float* d_logits,
                        int32_t accumulate, float* dx_router, float* dw_router, void* ws,

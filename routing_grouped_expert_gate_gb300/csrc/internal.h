@@ -36,6 +36,18 @@ cudaError_t launch_router_logits_tc(const Ctx& c, const moe_cfg& cfg, const void
                                     float* logits, void* ws);
 cudaError_t launch_router_topk(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                const float* sel_bias, int32_t* idx, float* w);
+// top-k with a quantile bias: key = score - beta, k + 1 ranked, alpha[t] =
+// the (k+1)-th key (beta, alpha NULL: plain top-k)
+cudaError_t launch_router_topk_q(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                 const float* sel_bias, const float* beta, float* alpha,
+                                 int32_t* idx, float* w);
+// quantile balancing (quantile.cu)
+cudaError_t launch_quantile_solve(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                  const float* alpha, float* beta_local);
+cudaError_t launch_quantile_accumulate(const Ctx& c, const moe_cfg& cfg, const float* beta_local,
+                                       float* accum, int32_t* count);
+cudaError_t launch_quantile_beta_update(const Ctx& c, const moe_cfg& cfg, float* beta,
+                                        float* accum, int32_t* count, float ema);
 // dW_r partials [splits][E][d] for E <= 16 (sum them in slice order)
 cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void* x,
                                    const float* d_logits, float* part, int splits);

@@ -315,11 +315,16 @@ __device__ __forceinline__ bool outranks(float ka, int ea, float kb, int eb) {
   return ka > kb || (ka == kb && ea < eb);
 }
 
+// Quantile routing (beta != NULL): the key is the score minus beta, k + 1
+// experts are ranked, the first k are chosen and the (k+1)-th key is written
+// to alpha[t] (the token's threshold).
 template <int EPL>
 __global__ void __launch_bounds__(256)
 router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias,
+            const float* __restrict__ beta, float* __restrict__ alpha,
             int32_t* __restrict__ idx, float* __restrict__ w, int64_t T, int E, int k,
             int score_fn, float scaling) {
+  const int ksel = (alpha != nullptr) ? k + 1 : k;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
@@ -330,14 +335,9 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       const int e = lane + 32 * i;
       if (e < E) {
         const float l = logits[t * E + e];
-        float kv;
-        if (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE) {
-          kv = l;  // pre-softmax: replaced by the probability below
-        } else {
-          kv = bias_score(l, score_fn);
-          if (sel_bias != nullptr) kv = __fadd_rn(kv, sel_bias[e]);
-        }
-        key[i] = (kv == kv) ? kv : -INFINITY;
+        // pre-softmax: replaced by the probability below
+        key[i] = (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE)
+                     ? l : bias_score(l, score_fn);
         lg[i] = l;
         taken[i] = false;
       } else {
@@ -363,18 +363,27 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       pre_inv = 1.f / sum;
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < E) {
-          const float pv = expf(lg[i] - m) * pre_inv;
-          key[i] = (pv == pv) ? pv : -INFINITY;
-        }
+        if (lane + 32 * i < E) key[i] = expf(lg[i] - m) * pre_inv;
     }
-    int sel_e[kMaxK];
-    float sel_l[kMaxK];
+    // selection bias (added) or quantile bias (subtracted); NaN ranks last
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        float kv = key[i];
+        if (sel_bias != nullptr) kv = __fadd_rn(kv, sel_bias[e]);
+        if (beta != nullptr) kv = __fsub_rn(kv, beta[e]);
+        key[i] = (kv == kv) ? kv : -INFINITY;
+      }
+    }
+    int sel_e[kMaxK + 1];
+    float sel_l[kMaxK + 1], sel_key[kMaxK + 1];
+#pragma unroll
+    for (int j = 0; j < kMaxK + 1; ++j) {
       sel_e[j] = 0;
       sel_l[j] = 0.f;
-      if (j < k) {
+      sel_key[j] = 0.f;
+      if (j < ksel) {
         float bk = -INFINITY;
         int be = 0x7fffffff;
 #pragma unroll
@@ -401,9 +410,11 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
             l_own = lg[i];
           }
         sel_e[j] = be;
+        sel_key[j] = bk;
         sel_l[j] = __shfl_sync(0xffffffffu, l_own, owner);
       }
     }
+    if (alpha != nullptr && lane == 0) alpha[t] = sel_key[k];
     // mixing weights of the chosen experts
     float wv[kMaxK];
     if (score_fn == MOE_SCORE_SOFTMAX) {
@@ -660,12 +671,18 @@ static unsigned warp_grid(const Ctx& c, int64_t items) {
 
 cudaError_t launch_router_topk(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                const float* sel_bias, int32_t* idx, float* w) {
+  return launch_router_topk_q(c, cfg, logits, sel_bias, nullptr, nullptr, idx, w);
+}
+
+cudaError_t launch_router_topk_q(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                 const float* sel_bias, const float* beta, float* alpha,
+                                 int32_t* idx, float* w) {
   if (cfg.T == 0) return cudaSuccess;
   const unsigned grid = warp_grid(c, cfg.T);
   const int epl = (cfg.E + 31) / 32;
 #define MOE_TOPK(N)                                                                        \
-  router_topk<N><<<grid, 256, 0, c.stream>>>(logits, sel_bias, idx, w, cfg.T, cfg.E, cfg.k, \
-                                             cfg.score_fn, cfg.scaling)
+  router_topk<N><<<grid, 256, 0, c.stream>>>(logits, sel_bias, beta, alpha, idx, w, cfg.T, \
+                                             cfg.E, cfg.k, cfg.score_fn, cfg.scaling)
   switch (epl) {
     case 1: MOE_TOPK(1); break;
     case 2: MOE_TOPK(2); break;

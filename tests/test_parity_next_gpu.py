@@ -142,3 +142,111 @@ def test_max_vio_all_on_one_expert(L):
     out = torch.empty(1, device="cuda")
     L.max_vio(cfg, tpe, out)
     assert float(out.item()) == 7.0
+
+
+# ---------------------------------------------------------------- quantile balancing
+
+def _quantile_inputs(T, E, seed, skew=0.0):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    logits = torch.randn(T, E, generator=g, device="cuda") * 2.0
+    if skew:
+        off = torch.log(torch.arange(1, E + 1, device="cuda", dtype=torch.float32) ** -1.2)
+        logits = logits + skew * off[None, :]
+    beta = (torch.randn(E, generator=g, device="cuda") * 0.3).contiguous()
+    return logits.contiguous(), beta
+
+
+def _run_quantile(L, cfg, logits, beta, solve=True):
+    T, E, k = cfg.T, cfg.E, cfg.k
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    alpha = torch.empty(T, device="cuda")
+    bl = torch.empty(E, device="cuda") if solve else None
+    L.quantile_route(cfg, logits, beta, idx, w, alpha, bl)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    return idx, w, alpha, bl
+
+
+@pytest.mark.parametrize("T,E,k", [(4096, 64, 4), (1000, 8, 2), (256, 256, 8)])
+def test_quantile_route_softmax_is_exact(L, T, E, k):
+    cfg = L.make_cfg(T=T, d=64, E=E, k=k, F=64, score="softmax")
+    logits, beta = _quantile_inputs(T, E, 70 + T)
+    idx, w, alpha, bl = _run_quantile(L, cfg, logits, beta)
+    r = O.quantile_route(O.as_f64(logits), O.as_f64(beta), k, "softmax")
+    # the keys are fp32 differences of the same fp32 inputs on both sides
+    assert np.array_equal(idx.cpu().numpy(), r["idx"])
+    assert np.array_equal(alpha.cpu().numpy().astype(np.float64), r["alpha"])
+    assert np.array_equal(bl.cpu().numpy().astype(np.float64), r["beta_local"])
+    assert_close("w", w, r["w"], TOL_F32)
+
+
+@pytest.mark.parametrize("score", ["sigmoid", "sqrtsoftplus"])
+def test_quantile_route_sigmoid_like(L, score):
+    T, E, k = 2048, 32, 4
+    cfg = L.make_cfg(T=T, d=64, E=E, k=k, F=64, score=score)
+    logits, beta = _quantile_inputs(T, E, 80)
+    idx, w, alpha, bl = _run_quantile(L, cfg, logits, beta)
+    r = O.quantile_route(O.as_f64(logits), O.as_f64(beta), k, score)
+    decided = r["gap"] >= 1e-6
+    assert np.array_equal(idx.cpu().numpy()[decided], r["idx"][decided])
+    assert np.max(np.abs(alpha.cpu().numpy() - r["alpha"])) < 1e-6
+    assert np.max(np.abs(bl.cpu().numpy() - r["beta_local"])) < 1e-6
+    assert_close("w", to_np(w)[decided], r["w"][decided], TOL_F32)
+
+
+def test_quantile_accumulate_and_update(L):
+    E = 64
+    cfg = L.make_cfg(T=1024, d=64, E=E, k=4, F=64, score="sigmoid")
+    accum = torch.zeros(E, device="cuda")
+    count = torch.zeros(1, dtype=torch.int32, device="cuda")
+    beta = torch.zeros(E, device="cuda")
+    sols = []
+    for seed in range(3):
+        logits, _ = _quantile_inputs(1024, E, 90 + seed, skew=1.0)
+        _, _, _, bl = _run_quantile(L, cfg, logits, beta)
+        L.quantile_accumulate(cfg, bl, accum, count)
+        sols.append(O.as_f64(bl))
+    beta0 = torch.linspace(-0.1, 0.2, E, device="cuda")
+    beta.copy_(beta0)
+    L.quantile_beta_update(cfg, beta, accum, count, 0.9)
+    want = O.quantile_beta_update(O.as_f64(beta0), np.sum(sols, axis=0), 3, 0.9)
+    assert np.max(np.abs(O.as_f64(beta) - want)) < 1e-6
+    assert int(count.item()) == 0 and float(accum.abs().max()) == 0.0
+    assert abs(float(beta.double().mean())) < 1e-6
+
+
+def test_quantile_balancing_loop_evens_the_load(L):
+    T, E, k = 4096, 32, 4
+    cfg = L.make_cfg(T=T, d=64, E=E, k=k, F=64, score="sigmoid")
+    logits, _ = _quantile_inputs(T, E, 100, skew=2.0)
+    beta = torch.zeros(E, device="cuda")
+    accum = torch.zeros(E, device="cuda")
+    count = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = None
+    for _ in range(5):
+        idx, _, _, bl = _run_quantile(L, cfg, logits, beta)
+        c = np.bincount(idx.cpu().numpy().reshape(-1), minlength=E)
+        first = O.max_vio(c) if first is None else first
+        L.quantile_accumulate(cfg, bl, accum, count)
+        L.quantile_beta_update(cfg, beta, accum, count, 0.0)
+    idx, _, _, _ = _run_quantile(L, cfg, logits, beta, solve=False)
+    c = np.bincount(idx.cpu().numpy().reshape(-1), minlength=E)
+    assert c.sum() == T * k
+    assert O.max_vio(c) < 0.25 < first
+
+
+def test_quantile_refusals(L):
+    logits = torch.zeros(10, 8, device="cuda")
+    beta = torch.zeros(8, device="cuda")
+    idx = torch.empty(10, 3, dtype=torch.int32, device="cuda")
+    w = torch.empty(10, 3, device="cuda")
+    alpha = torch.empty(10, device="cuda")
+    bl = torch.empty(8, device="cuda")
+    with pytest.raises(L.MoeError):  # 10 * 3 is not divisible by 8
+        L.quantile_route(L.make_cfg(T=10, d=64, E=8, k=3, F=64, score="sigmoid"), logits, beta,
+                         idx, w, alpha, bl)
+    with pytest.raises(L.MoeError):  # pre-softmax is not a quantile score
+        L.quantile_route(L.make_cfg(T=10, d=64, E=8, k=3, F=64, score="softmax_pre"), logits,
+                         beta, idx, w, alpha, None)
