@@ -42,6 +42,15 @@ class Workload:
     scaling: float = 1.0          # routed scaling factor
     aux_coeff: float = 1e-3       # Switch load-balancing loss coefficient
     weight_std: float = 0.02
+    # expert activation: "swiglu", "swiglu_clamp" (act_clamp > 0) or "situ_glu"
+    # (act_gate_scale > 0, optional act_linear_scale); glu_linear_offset is
+    # added to the linear half
+    act_fn: str = "swiglu"
+    act_clamp: float = 0.0
+    act_gate_scale: float = 0.0
+    act_linear_scale: float = 0.0
+    glu_linear_offset: float = 0.0
+    shared_gate: bool = False     # sigmoid gate on the shared expert's output
 
     @property
     def A(self) -> int:
@@ -85,7 +94,7 @@ def shrink(w: Workload, **changes) -> Workload:
 
 # Order of the independent per-tensor streams; a tensor's stream never
 # depends on which other tensors a workload has.
-_STREAMS = ["x", "w_router", "w1", "w2", "w1_s", "w2_s", "sel_bias", "dy"]
+_STREAMS = ["x", "w_router", "w1", "w2", "w1_s", "w2_s", "sel_bias", "dy", "w_gate_s"]
 
 
 def _gen(seed: int, name: str, device) -> torch.Generator:
@@ -127,7 +136,8 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu",
     Returns a dict with keys x [T,d], w_router [E,d] fp32, w1 [E,2F,d],
     w2 [E,d,F], w1_s [2F_s,d] / w2_s [d,F_s] (None without a shared expert),
     sel_bias [E] fp32 (or None), logit_bias [E] fp32 (or None), dy [T,d]
-    (or None). Rows [0,F) of each w1[e] are the gate, rows [F,2F) the up part.
+    (or None), w_gate_s [d] fp32 (the shared expert's gate weight, or None).
+    Rows [0,F) of each w1[e] are the gate, rows [F,2F) the up part.
     `only` restricts the draw to the named tensors among x, w_router, w1, w2
     (the others come back None); every tensor has its own generator, so the
     values drawn do not depend on which others are drawn.
@@ -155,6 +165,10 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu",
     else:
         out["w1_s"] = None
         out["w2_s"] = None
+    # the shared expert's sigmoid gate weight [d], fp32 like the router's
+    out["w_gate_s"] = (_normal((w.d,), std, _gen(seed, "w_gate_s", device), device,
+                               torch.float32)
+                       if w.F_shared > 0 and w.shared_gate and want("w1") else None)
     if w.sel_bias_range > 0:
         g = _gen(seed, "sel_bias", device)
         r = w.sel_bias_range

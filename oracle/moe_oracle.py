@@ -47,6 +47,8 @@ inputs) and returns float64 / int64 arrays.
 """
 from __future__ import annotations
 
+import dataclasses
+import math
 from typing import Dict, Optional, Sequence
 
 import numpy as np
@@ -276,28 +278,116 @@ def max_vio(counts: np.ndarray) -> float:
 
 
 # ----------------------------------------------------------------------------
+# GLU activations of the experts
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class GluAct:
+    """The expert activation applied to fc1's [gate | linear] halves.
+
+    Handbook §3.4 "Experts", part "Activation" and its code: glu() computes
+    act(x_glu) * (x_linear + glu_linear_offset) with SiLU; a clamp value c
+    clips x_glu from above at c and x_linear to [-c, c] first (SwiGLU with a
+    hard clamp; c must be finite and > 0, and the offset zero); SiTU-GLU
+    replaces the gate by situ(x, s) = s tanh(x / s) sigmoid(x) and, with a
+    linear scale, soft-clamps x_linear to s_l tanh(x_linear / s_l).
+    """
+    kind: str = "swiglu"        # "swiglu" | "swiglu_clamp" | "situ_glu"
+    clamp: float = 0.0
+    gate_scale: float = 0.0
+    linear_scale: float = 0.0   # 0: the linear half is not soft-clamped
+    offset: float = 0.0
+
+    def check(self) -> "GluAct":
+        if self.kind == "swiglu_clamp":
+            if not (math.isfinite(self.clamp) and self.clamp > 0):
+                raise ValueError("the SwiGLU clamp value must be finite and > 0")
+            if self.offset != 0.0:
+                raise ValueError("glu_linear_offset must be 0 with the SwiGLU clamp")
+        elif self.kind == "situ_glu":
+            if not self.gate_scale > 0:
+                raise ValueError("SiTU-GLU needs a gate scale > 0")
+        elif self.kind != "swiglu":
+            raise ValueError(self.kind)
+        return self
+
+
+SWIGLU = GluAct()
+
+
+def act_of(wl) -> GluAct:
+    """The activation a workload asks for (SwiGLU when it names none)."""
+    return GluAct(getattr(wl, "act_fn", "swiglu"), getattr(wl, "act_clamp", 0.0),
+                  getattr(wl, "act_gate_scale", 0.0), getattr(wl, "act_linear_scale", 0.0),
+                  getattr(wl, "glu_linear_offset", 0.0)).check()
+
+
+def glu_forward(g: np.ndarray, u: np.ndarray, act: GluAct = SWIGLU) -> np.ndarray:
+    if act.kind == "swiglu":
+        return silu(g) * (u + act.offset)
+    if act.kind == "swiglu_clamp":
+        c = act.clamp
+        return silu(np.minimum(g, c)) * np.clip(u, -c, c)
+    s = act.gate_scale
+    gate = s * np.tanh(g / s) * sigmoid(g)
+    lin = act.linear_scale * np.tanh(u / act.linear_scale) if act.linear_scale > 0 else u
+    return gate * (lin + act.offset)
+
+
+def glu_backward(g: np.ndarray, u: np.ndarray, dh: np.ndarray, act: GluAct = SWIGLU):
+    """(dg, du) of h = glu_forward(g, u). A clipped input passes no gradient
+    (the clip is the identity, derivative 1, on [-c, c] ends included)."""
+    sg = sigmoid(g)
+    if act.kind == "swiglu":
+        dsilu = sg * (1.0 + g * (1.0 - sg))
+        return dh * (u + act.offset) * dsilu, dh * (g * sg)
+    if act.kind == "swiglu_clamp":
+        c = act.clamp
+        gc = np.minimum(g, c)
+        uc = np.clip(u, -c, c)
+        sgc = sigmoid(gc)
+        dg = dh * uc * sgc * (1.0 + gc * (1.0 - sgc)) * (g <= c)
+        du = dh * (gc * sgc) * ((u >= -c) & (u <= c))
+        return dg, du
+    s = act.gate_scale
+    th = np.tanh(g / s)
+    gate = s * th * sg
+    dgate = (1.0 - th * th) * sg + s * th * sg * (1.0 - sg)
+    if act.linear_scale > 0:
+        tl = np.tanh(u / act.linear_scale)
+        lin = act.linear_scale * tl
+        dlin = 1.0 - tl * tl
+    else:
+        lin = u
+        dlin = np.ones_like(u)
+    return dh * (lin + act.offset) * dgate, dh * gate * dlin
+
+
+# ----------------------------------------------------------------------------
 # S4 / S5: SwiGLU experts
 # ----------------------------------------------------------------------------
 
-def swiglu_ffn(xs: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> Dict[str, np.ndarray]:
+def swiglu_ffn(xs: np.ndarray, w1: np.ndarray, w2: np.ndarray,
+               act: GluAct = SWIGLU) -> Dict[str, np.ndarray]:
     """One bias-free SwiGLU expert on the rows xs [n, d].
 
     Handbook §3.4 "Count and size": fc1 has twice the FFN width, fc2 maps the
     FFN width F back to d; "Activation": fc1's output is split in two halves,
     the first is the gate (through SiLU), the second the linear part, and the
-    two are multiplied. w1 is [2F, d], w2 is [d, F].
+    two are multiplied (glu_forward: SiLU by default, or a clamped / SiTU
+    variant). w1 is [2F, d], w2 is [d, F].
     """
     F = w2.shape[1]
     gu = xs @ w1.T
     g = gu[:, :F]
     u = gu[:, F:]
-    h = silu(g) * u
+    h = glu_forward(g, u, act)
     out = h @ w2.T
     return {"g": g, "u": u, "h": h, "out": out}
 
 
 def grouped_swiglu(x_perm: np.ndarray, offsets: np.ndarray, w1: np.ndarray,
-                   w2: np.ndarray) -> Dict[str, np.ndarray]:
+                   w2: np.ndarray, act: GluAct = SWIGLU) -> Dict[str, np.ndarray]:
     """Each expert e runs its FFN on its own contiguous segment of rows."""
     A = x_perm.shape[0]
     E, twoF, _ = w1.shape
@@ -311,7 +401,7 @@ def grouped_swiglu(x_perm: np.ndarray, offsets: np.ndarray, w1: np.ndarray,
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
-        res = swiglu_ffn(x_perm[r0:r1], w1[e], w2[e])
+        res = swiglu_ffn(x_perm[r0:r1], w1[e], w2[e], act)
         g[r0:r1], u[r0:r1], h[r0:r1], out[r0:r1] = res["g"], res["u"], res["h"], res["out"]
     return {"g": g, "u": u, "h": h, "out": out}
 
@@ -319,6 +409,13 @@ def grouped_swiglu(x_perm: np.ndarray, offsets: np.ndarray, w1: np.ndarray,
 # ----------------------------------------------------------------------------
 # S6: combine
 # ----------------------------------------------------------------------------
+
+def shared_gate(x: np.ndarray, w_gate: np.ndarray) -> np.ndarray:
+    """Handbook §3.4 "Shared experts" (--moe-shared-expert-gate): a sigmoid
+    gate on the shared expert's output, sigmoid(x · w_gate) per token, from a
+    [d] gate weight."""
+    return sigmoid(x @ w_gate)
+
 
 def combine(out_perm: np.ndarray, row_of: np.ndarray, w: np.ndarray,
             y_shared: Optional[np.ndarray] = None) -> np.ndarray:
@@ -520,18 +617,23 @@ def layer_forward(wl, inp: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
     """S1..S7 for a workload `wl` (moe_inputs.Workload) on float64 inputs."""
     r = route(inp["x"], inp["w_router"], wl.k, wl.score, wl.scaling,
               inp.get("logit_bias"), inp.get("sel_bias"))
+    act = act_of(wl)
     dsp = dispatch(r["idx"], wl.E)
     x_perm = permute_rows(inp["x"], dsp["src_tok"])
-    ex = grouped_swiglu(x_perm, dsp["offsets"], inp["w1"], inp["w2"])
+    ex = grouped_swiglu(x_perm, dsp["offsets"], inp["w1"], inp["w2"], act)
     out = dict(r)
     out.update(dsp)
     out["x_perm"] = x_perm
     out.update({"g": ex["g"], "u": ex["u"], "h": ex["h"], "out_perm": ex["out"]})
     y_s = None
     if inp.get("w1_s") is not None:
-        sh = swiglu_ffn(inp["x"], inp["w1_s"], inp["w2_s"])
+        # the shared expert is an MLP of the same configuration: same activation
+        sh = swiglu_ffn(inp["x"], inp["w1_s"], inp["w2_s"], act)
         out.update({"g_s": sh["g"], "u_s": sh["u"], "h_s": sh["h"], "y_s": sh["out"]})
         y_s = sh["out"]
+        if inp.get("w_gate_s") is not None:
+            out["gate_s"] = shared_gate(inp["x"], inp["w_gate_s"])
+            y_s = out["gate_s"][:, None] * y_s
     out["y"] = combine(ex["out"], dsp["row_of"], r["w"], y_s)
     out["aux"] = aux_loss(r["logits"], dsp["counts"], wl.k, wl.aux_coeff, wl.score)
     return out
@@ -554,23 +656,23 @@ def combine_backward(dy: np.ndarray, out_perm: np.ndarray, row_of: np.ndarray,
     return d_out_perm, dw
 
 
-def swiglu_ffn_backward(xs, w1, w2, g, u, h, d_out) -> Dict[str, np.ndarray]:
-    """B5 + B4 for one expert: gradients of out = (silu(g) * u) @ w2.T, [g u] = xs @ w1.T.
+def swiglu_ffn_backward(xs, w1, w2, g, u, h, d_out,
+                        act: GluAct = SWIGLU) -> Dict[str, np.ndarray]:
+    """B5 + B4 for one expert: gradients of out = glu(g, u) @ w2.T, [g u] = xs @ w1.T.
 
-    d/dg silu(g) = sigmoid(g) * (1 + g * (1 - sigmoid(g))).
+    For SwiGLU d/dg silu(g) = sigmoid(g) * (1 + g * (1 - sigmoid(g))); the
+    variants' derivatives are in glu_backward.
     """
     dh = d_out @ w2
     dW2 = d_out.T @ h
-    sg = sigmoid(g)
-    dg = dh * u * sg * (1.0 + g * (1.0 - sg))
-    du = dh * (g * sg)
+    dg, du = glu_backward(g, u, dh, act)
     d_pre = np.concatenate([dg, du], axis=1)
     dxs = d_pre @ w1
     dW1 = d_pre.T @ xs
     return {"dh": dh, "d_pre": d_pre, "dxs": dxs, "dW1": dW1, "dW2": dW2}
 
 
-def grouped_swiglu_backward(x_perm, offsets, w1, w2, g, u, h, d_out_perm):
+def grouped_swiglu_backward(x_perm, offsets, w1, w2, g, u, h, d_out_perm, act: GluAct = SWIGLU):
     A, d = x_perm.shape
     E, twoF, _ = w1.shape
     d_pre = np.zeros((A, twoF))
@@ -582,7 +684,7 @@ def grouped_swiglu_backward(x_perm, offsets, w1, w2, g, u, h, d_out_perm):
         if r1 == r0:
             continue  # an expert with no rows has zero weight gradient
         res = swiglu_ffn_backward(x_perm[r0:r1], w1[e], w2[e], g[r0:r1], u[r0:r1],
-                                  h[r0:r1], d_out_perm[r0:r1])
+                                  h[r0:r1], d_out_perm[r0:r1], act)
         d_pre[r0:r1] = res["d_pre"]
         dx_perm[r0:r1] = res["dxs"]
         dW1[e] = res["dW1"]
@@ -662,9 +764,10 @@ def permute_backward(dx_perm: np.ndarray, row_of: np.ndarray) -> np.ndarray:
 
 def layer_backward(wl, inp, fwd, dy: np.ndarray, g_aux: float = 1.0) -> Dict[str, np.ndarray]:
     """Gradients of  <dy, y> + g_aux * aux  w.r.t. x, the router and expert weights."""
+    act = act_of(wl)
     d_out_perm, dw = combine_backward(dy, fwd["out_perm"], fwd["row_of"], fwd["w"])
     ex = grouped_swiglu_backward(fwd["x_perm"], fwd["offsets"], inp["w1"], inp["w2"],
-                                 fwd["g"], fwd["u"], fwd["h"], d_out_perm)
+                                 fwd["g"], fwd["u"], fwd["h"], d_out_perm, act)
     d_logits = scores_backward(fwd["logits"], fwd["idx"], dw, wl.score, wl.scaling)
     d_logits = d_logits + aux_loss_backward(fwd["logits"], fwd["counts"], wl.k,
                                             wl.aux_coeff, wl.score, g_aux)
@@ -674,10 +777,18 @@ def layer_backward(wl, inp, fwd, dy: np.ndarray, g_aux: float = 1.0) -> Dict[str
            "dx_perm": ex["dx_perm"], "dW1": ex["dW1"], "dW2": ex["dW2"],
            "d_logits": d_logits, "dW_r": d_logits.T @ inp["x"]}
     if inp.get("w1_s") is not None:
+        dy_s = dy
+        if inp.get("w_gate_s") is not None:
+            gate = fwd["gate_s"]
+            dy_s = gate[:, None] * dy
+            d_gl = np.sum(dy * fwd["y_s"], axis=1) * gate * (1.0 - gate)
+            out["d_gate_logit_s"] = d_gl
+            out["dW_gate_s"] = d_gl @ inp["x"]
+            dx = dx + d_gl[:, None] * inp["w_gate_s"][None, :]
         sh = swiglu_ffn_backward(inp["x"], inp["w1_s"], inp["w2_s"], fwd["g_s"],
-                                 fwd["u_s"], fwd["h_s"], dy)
+                                 fwd["u_s"], fwd["h_s"], dy_s, act)
         out.update({"dW1_s": sh["dW1"], "dW2_s": sh["dW2"], "dx_s": sh["dxs"],
-                    "d_pre_s": sh["d_pre"]})
+                    "d_pre_s": sh["d_pre"], "dy_s": dy_s})
         dx = dx + sh["dxs"]
     out["dx"] = dx
     return out
@@ -708,13 +819,17 @@ def tokens_forward(wl, inp, tokens: Sequence[int], routing=None) -> Dict[str, np
         idx, w = r["idx"], r["w"]
     else:
         idx, w = routing["idx"][tokens], routing["w"][tokens]
+    act = act_of(wl)
     y = np.zeros((len(tokens), wl.d))
     for i in range(len(tokens)):
         for j in range(wl.k):
-            res = swiglu_ffn(x[i:i + 1], inp["w1"][idx[i, j]], inp["w2"][idx[i, j]])
+            res = swiglu_ffn(x[i:i + 1], inp["w1"][idx[i, j]], inp["w2"][idx[i, j]], act)
             y[i] += w[i, j] * res["out"][0]
     if inp.get("w1_s") is not None:
-        y = y + swiglu_ffn(x, inp["w1_s"], inp["w2_s"])["out"]
+        y_s = swiglu_ffn(x, inp["w1_s"], inp["w2_s"], act)["out"]
+        if inp.get("w_gate_s") is not None:
+            y_s = shared_gate(x, inp["w_gate_s"])[:, None] * y_s
+        y = y + y_s
     return {"idx": idx, "w": w, "y": y}
 
 
@@ -731,15 +846,16 @@ def tokens_backward(wl, inp, tokens: Sequence[int], routing, counts, dy_rows,
     idx = routing["idx"][tokens]
     w = routing["w"][tokens]
     n = len(tokens)
+    act = act_of(wl)
     dw = np.zeros((n, wl.k))
     dx = np.zeros((n, wl.d))
     for i in range(n):
         for j in range(wl.k):
             e = idx[i, j]
-            f = swiglu_ffn(x[i:i + 1], inp["w1"][e], inp["w2"][e])
+            f = swiglu_ffn(x[i:i + 1], inp["w1"][e], inp["w2"][e], act)
             dw[i, j] = float(np.sum(dy_rows[i] * f["out"][0]))
             b = swiglu_ffn_backward(x[i:i + 1], inp["w1"][e], inp["w2"][e], f["g"], f["u"],
-                                    f["h"], w[i, j] * dy_rows[i:i + 1])
+                                    f["h"], w[i, j] * dy_rows[i:i + 1], act)
             dx[i] += b["dxs"][0]
     # the aux-loss gradient of a token needs its own logits, the global counts and T
     d_aux = aux_loss_backward(logits, counts, wl.k, wl.aux_coeff, wl.score, g_aux,
@@ -747,13 +863,20 @@ def tokens_backward(wl, inp, tokens: Sequence[int], routing, counts, dy_rows,
     d_logits = scores_backward(logits, idx, dw, wl.score, wl.scaling) + d_aux
     dx += d_logits @ inp["w_router"]
     if inp.get("w1_s") is not None:
-        f = swiglu_ffn(x, inp["w1_s"], inp["w2_s"])
-        b = swiglu_ffn_backward(x, inp["w1_s"], inp["w2_s"], f["g"], f["u"], f["h"], dy_rows)
+        f = swiglu_ffn(x, inp["w1_s"], inp["w2_s"], act)
+        dy_s = dy_rows
+        if inp.get("w_gate_s") is not None:
+            gate = shared_gate(x, inp["w_gate_s"])
+            dy_s = gate[:, None] * dy_rows
+            d_gl = np.sum(dy_rows * f["out"], axis=1) * gate * (1.0 - gate)
+            dx += d_gl[:, None] * inp["w_gate_s"][None, :]
+        b = swiglu_ffn_backward(x, inp["w1_s"], inp["w2_s"], f["g"], f["u"], f["h"], dy_s, act)
         dx += b["dxs"]
     return {"dw": dw, "d_logits": d_logits, "dx": dx}
 
 
-def expert_grad_columns(x_rows, d_out_rows, w1_e, w2_e, cols: Sequence[int]) -> Dict[str, np.ndarray]:
+def expert_grad_columns(x_rows, d_out_rows, w1_e, w2_e, cols: Sequence[int],
+                        act: GluAct = SWIGLU) -> Dict[str, np.ndarray]:
     """Weight gradients of one expert restricted to FFN columns `cols`.
 
     The SwiGLU definitions separate per FFN column f: h[:, f] needs only gate
@@ -766,8 +889,8 @@ def expert_grad_columns(x_rows, d_out_rows, w1_e, w2_e, cols: Sequence[int]) -> 
     F = w2_e.shape[1]
     w1s = np.concatenate([w1_e[cols], w1_e[F + cols]], axis=0)
     w2s = w2_e[:, cols]
-    f = swiglu_ffn(x_rows, w1s, w2s)
-    b = swiglu_ffn_backward(x_rows, w1s, w2s, f["g"], f["u"], f["h"], d_out_rows)
+    f = swiglu_ffn(x_rows, w1s, w2s, act)
+    b = swiglu_ffn_backward(x_rows, w1s, w2s, f["g"], f["u"], f["h"], d_out_rows, act)
     n = len(cols)
     return {"dW2_cols": b["dW2"], "dW1_gate": b["dW1"][:n], "dW1_up": b["dW1"][n:]}
 

@@ -25,10 +25,10 @@ def _load(name):
 
 
 def _tiny(score="softmax", E=4, k=2, F=6, d=8, T=16, F_shared=0, sel=0.0, zipf=0.0,
-          scaling=1.0, coeff=1e-2, seed=0):
+          scaling=1.0, coeff=1e-2, seed=0, **act):
     wl = mi.Workload("pin", T=T, d=d, E=E, k=k, F=F, F_shared=F_shared, score=score,
                      act_dtype="f32", backward=True, sel_bias_range=sel, zipf_s=zipf,
-                     scaling=scaling, aux_coeff=coeff, weight_std=0.5)
+                     scaling=scaling, aux_coeff=coeff, weight_std=0.5, **act)
     inp = {kk: O.as_f64(v) for kk, v in mi.make_inputs(wl, seed=seed).items()}
     return wl, inp
 
@@ -313,7 +313,7 @@ def _fd_check(wl, inp, keys, eps=1e-6, rtol=2e-6, atol=1e-9):
     assert np.min(f["gap"]) > 1e-3  # no near ties: selection is locally constant
     b = O.layer_backward(wl, inp, f, dy)
     grad_of = {"x": "dx", "w_router": "dW_r", "w1": "dW1", "w2": "dW2",
-               "w1_s": "dW1_s", "w2_s": "dW2_s"}
+               "w1_s": "dW1_s", "w2_s": "dW2_s", "w_gate_s": "dW_gate_s"}
     for name in keys:
         base = inp[name]
         g_an = b[grad_of[name]]

@@ -307,3 +307,90 @@ def test_quantile_beta_update_ema_and_centring():
     assert abs(nb.mean()) < 1e-15
     np.testing.assert_allclose(O.quantile_beta_update(beta, accum, 0, ema=1.0),
                                beta - beta.mean())
+
+
+# ---------------------------------------------------------------- expert activations
+
+GA = json.load(open(os.path.join(GOLDEN, "expert_activations.json")))
+
+
+def _gu(seed=40, n=400):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((n, 7)) * 12, rng.standard_normal((n, 7)) * 12
+
+
+def test_clamp_validation_follows_the_pages():
+    c = GA["swiglu_clamp_value"]["clamp"]
+    O.GluAct("swiglu_clamp", clamp=c).check()
+    for bad in (0.0, -1.0, math.inf, math.nan):
+        with pytest.raises(ValueError):
+            O.GluAct("swiglu_clamp", clamp=bad).check()
+    with pytest.raises(ValueError):
+        O.GluAct("swiglu_clamp", clamp=c, offset=0.5).check()
+
+
+def test_clamped_swiglu_limits_and_bound():
+    g, u = _gu()
+    c = GA["swiglu_clamp_value"]["clamp"]
+    plain = O.glu_forward(g, u, O.SWIGLU)
+    # a limit no activation reaches changes nothing
+    np.testing.assert_array_equal(O.glu_forward(g, u, O.GluAct("swiglu_clamp", clamp=1e9)),
+                                  plain)
+    h = O.glu_forward(g, u, O.GluAct("swiglu_clamp", clamp=c))
+    # the point of the clamp: |h| <= silu(c) * c, while plain SwiGLU exceeds it here
+    bound = c * c / (1.0 + math.exp(-c))
+    assert np.abs(h).max() <= bound * (1 + 1e-15)
+    assert np.abs(plain).max() > bound
+    # inside the box the two agree
+    inside = (g <= c) & (np.abs(u) <= c)
+    np.testing.assert_array_equal(h[inside], plain[inside])
+
+
+def test_situ_glu_limits_and_bound():
+    g, u = _gu(41)
+    sg, sl = GA["situ_glu"]["gate_scale"], GA["situ_glu"]["linear_scale"]
+    # a huge scale is SwiGLU: s tanh(x / s) -> x
+    big = O.glu_forward(g, u, O.GluAct("situ_glu", gate_scale=1e7))
+    np.testing.assert_allclose(big, O.glu_forward(g, u, O.SWIGLU), rtol=1e-9, atol=1e-12)
+    # the smooth cap: the gate stays below s, the linear half below s_l
+    act = O.GluAct("situ_glu", gate_scale=sg, linear_scale=sl)
+    h = O.glu_forward(g, u, act)
+    gate_only = O.glu_forward(g, np.ones_like(u), O.GluAct("situ_glu", gate_scale=sg))
+    assert np.abs(gate_only).max() < sg
+    lin_only = O.glu_forward(np.full_like(g, 50.0), u,
+                             O.GluAct("situ_glu", gate_scale=1e7, linear_scale=sl)) / 50.0
+    assert np.abs(lin_only).max() < sl
+    assert np.abs(h).max() < sg * sl
+
+
+@pytest.mark.parametrize("act", [
+    {"act_fn": "swiglu_clamp", "act_clamp": 0.6},
+    {"act_fn": "situ_glu", "act_gate_scale": 0.8, "act_linear_scale": 0.9},
+    {"act_fn": "situ_glu", "act_gate_scale": 1.5},
+    {"act_fn": "swiglu", "glu_linear_offset": 0.3},
+])
+def test_finite_differences_expert_activations(act):
+    wl, inp = _tiny(E=4, k=2, F=3, d=4, T=6, F_shared=2, coeff=0.5, seed=42, **act)
+    if act["act_fn"] == "swiglu_clamp":
+        # some inputs are clipped, none sits on the edge (where the derivative jumps)
+        f = O.layer_forward(wl, inp)
+        c = act["act_clamp"]
+        g = np.concatenate([f["g"].ravel(), f["g_s"].ravel()])
+        u = np.concatenate([f["u"].ravel(), f["u_s"].ravel()])
+        assert np.any(g > c) and np.any(np.abs(u) > c)
+        assert np.min(np.abs(g - c)) > 1e-4 and np.min(np.abs(np.abs(u) - c)) > 1e-4
+    _fd_check(wl, inp, ["x", "w_router", "w1", "w2", "w1_s", "w2_s"])
+
+
+def test_shared_gate_half_at_zero_weight_and_gradients():
+    wl, inp = _tiny(E=4, k=2, F=3, d=4, T=6, F_shared=2, coeff=0.5, seed=43, shared_gate=True)
+    assert inp["w_gate_s"] is not None and inp["w_gate_s"].shape == (4,)
+    f = O.layer_forward(wl, inp)
+    ungated = dict(inp, w_gate_s=None)
+    f0 = O.layer_forward(wl, ungated)
+    zero = dict(inp, w_gate_s=np.zeros(4))
+    fz = O.layer_forward(wl, zero)
+    routed = f0["y"] - f0["y_s"]
+    np.testing.assert_allclose(fz["y"], routed + 0.5 * f0["y_s"], rtol=1e-14, atol=1e-15)
+    assert not np.allclose(f["y"], f0["y"])
+    _fd_check(wl, inp, ["x", "w_router", "w1_s", "w2_s", "w_gate_s"])
