@@ -76,6 +76,9 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
                                    "Output scale"); allowed at k = 1          */
 #define MOE_F32  0
 #define MOE_BF16 1
+#define MOE_ACT_SWIGLU       0
+#define MOE_ACT_SWIGLU_CLAMP 1
+#define MOE_ACT_SITU_GLU     2
 
 /* which workspace moe_workspace_bytes() sizes */
 #define MOE_WS_PERMUTE      0
@@ -85,6 +88,7 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
 #define MOE_WS_ROUTE_BWD    4
 #define MOE_WS_ROUTE        5
 #define MOE_WS_Z_LOSS       6
+#define MOE_WS_SHARED_GATE_BWD 7
 
 /* Layer configuration. Names follow the flags the Handbook uses for the layer
  * (§2.5 and §3.4: --num-experts, --moe-ffn-hidden-size, --moe-router-topk,
@@ -101,6 +105,21 @@ typedef struct {
   int32_t act_dtype; /* MOE_BF16 | MOE_F32                                    */
   float scaling;     /* routed scaling factor (1.0 = none)                    */
   float aux_coeff;   /* Switch aux-loss coefficient                           */
+  /* expert activation on fc1's [gate | linear] halves (routed and shared
+   * experts alike; Handbook §3.4 "Experts", part "Activation"):
+   *   MOE_ACT_SWIGLU (0):        silu(g) * (u + glu_linear_offset)
+   *   MOE_ACT_SWIGLU_CLAMP (1):  silu(min(g, c)) * clamp(u, -c, c),
+   *                              c = act_clamp, finite > 0, offset 0
+   *   MOE_ACT_SITU_GLU (2):      s tanh(g/s) sigmoid(g) * (lin(u) + offset),
+   *                              s = act_gate_scale > 0, lin(u) =
+   *                              act_linear_scale * tanh(u / act_linear_scale)
+   *                              when act_linear_scale > 0, else u
+   * A zero-initialised tail is plain SwiGLU.                                 */
+  int32_t act_fn;
+  float act_clamp;
+  float act_gate_scale;
+  float act_linear_scale;
+  float glu_linear_offset;
 } moe_cfg;
 
 /* Validates cfg the way the Handbook says Megatron does: softmax with top-1
@@ -180,13 +199,15 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
                        size_t ws_bytes, moe_stream_t stream);
 
 /* S6. Weighted unpermute-combine: y[t] = Σ_{j<k} w[t,j]·out_perm[row_of[t,j]]
- * (+ shared_out[t]), accumulated in fp32 in j order, then rounded once.
+ * (+ g_t · shared_out[t]), accumulated in fp32 in j order, then rounded once.
  * LeCompute, "An expert transforms numbers inside the model"; Handbook §3.4
- * "Shared experts" (shared output added at weight 1).
- *   out_perm [T·k, d], shared_out [T, d] or NULL, y [T, d] out: act dtype  */
+ * "Shared experts" (shared output added at weight 1, or through the sigmoid
+ * shared-expert gate: g_t = shared_gate[t] from moe_shared_gate).
+ *   out_perm [T·k, d], shared_out [T, d] or NULL, y [T, d] out: act dtype
+ *   shared_gate [T] fp32 or NULL (weight 1); needs shared_out              */
 int moe_unpermute_combine(const moe_cfg* cfg, const void* out_perm, const int32_t* row_of,
-                          const float* w, const void* shared_out, void* y,
-                          moe_stream_t stream);
+                          const float* w, const void* shared_out, const float* shared_gate,
+                          void* y, moe_stream_t stream);
 
 /* S7. Switch load-balancing loss (Handbook §3.3 "Aux loss"):
  * aux = coeff · E / (k · T²) · Σ_e counts[e] · Σ_t P[t,e], with P the softmax
@@ -270,13 +291,15 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
                        float* dw_router, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* B1. Backward of the permutation, fused with the other input gradients:
- * dx[t] = Σ_j dx_perm[row_of[t,j]] (+ dx_router[t]) (+ dx_shared[t]), summed
- * in fp32 and rounded once to the act dtype.
+ * dx[t] = Σ_j dx_perm[row_of[t,j]] (+ dx_router[t]) (+ dx_shared[t])
+ *         (+ d_gate_logit[t] · w_gate), summed in fp32 and rounded once to the
+ * act dtype.
  *   dx_perm [T·k, d] act dtype; dx_router [T, d] fp32 or NULL;
- *   dx_shared [T, d] act dtype or NULL; dx [T, d] act dtype out            */
+ *   dx_shared [T, d] act dtype or NULL; d_gate_logit [T] and w_gate [d]
+ *   fp32, both or neither (the shared-expert gate's path); dx [T, d] out   */
 int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_of,
-                    const float* dx_router, const void* dx_shared, void* dx,
-                    moe_stream_t stream);
+                    const float* dx_router, const void* dx_shared, const float* d_gate_logit,
+                    const float* w_gate, void* dx, moe_stream_t stream);
 
 /* ---------------------------- utilities --------------------------------- */
 
@@ -312,6 +335,26 @@ int moe_quantile_accumulate(const moe_cfg* cfg, const float* beta_local, float* 
                             int32_t* count, moe_stream_t stream);
 int moe_quantile_beta_update(const moe_cfg* cfg, float* beta, float* accum, int32_t* count,
                              float ema, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * The shared expert's sigmoid gate (Handbook §3.4 "Shared experts",
+ * --moe-shared-expert-gate): the shared output is multiplied per token by
+ * g_t = sigmoid(x[t] · w_gate), w_gate a [d] fp32 weight.
+ * moe_shared_gate: gate[t] = g_t (fp32 [T] out; fp32 dot over d).
+ * moe_shared_gate_bwd, for the loss's gradient dy [T, d] and the ungated
+ *   shared output shared_out [T, d] (act dtype):
+ *     dy_shared[t]    = g_t · dy[t]            (act dtype out: the shared
+ *                                               expert's upstream gradient)
+ *     d_gate_logit[t] = <dy[t], shared_out[t]> g_t (1 - g_t)   (fp32 [T] out)
+ *     dw_gate         = Σ_t d_gate_logit[t] · x[t]             (fp32 [d] out,
+ *                       deterministic slice sums)
+ *   ws >= moe_workspace_bytes(cfg, MOE_WS_SHARED_GATE_BWD). The input's share,
+ *   d_gate_logit[t] · w_gate, is added by moe_permute_bwd.                  */
+int moe_shared_gate(const moe_cfg* cfg, const void* x, const float* w_gate, float* gate,
+                    moe_stream_t stream);
+int moe_shared_gate_bwd(const moe_cfg* cfg, const void* x, const float* gate, const void* dy,
+                        const void* shared_out, void* dy_shared, float* d_gate_logit,
+                        float* dw_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Router z-loss (Handbook §3.1 "Router scoring", part "Precision",

@@ -334,20 +334,26 @@ def glu_forward(g: np.ndarray, u: np.ndarray, act: GluAct = SWIGLU) -> np.ndarra
     return gate * (lin + act.offset)
 
 
-def glu_backward(g: np.ndarray, u: np.ndarray, dh: np.ndarray, act: GluAct = SWIGLU):
+def glu_backward(g: np.ndarray, u: np.ndarray, dh: np.ndarray, act: GluAct = SWIGLU,
+                 decide=None):
     """(dg, du) of h = glu_forward(g, u). A clipped input passes no gradient
-    (the clip is the identity, derivative 1, on [-c, c] ends included)."""
+    (the clip is the identity, derivative 1, on [-c, c] ends included).
+
+    `decide` = (g', u'): the values the clip decisions are taken on, when
+    they must be those of a lower-precision copy (a bf16 layer keeps its
+    pre-activations in bf16 for the backward)."""
     sg = sigmoid(g)
     if act.kind == "swiglu":
         dsilu = sg * (1.0 + g * (1.0 - sg))
         return dh * (u + act.offset) * dsilu, dh * (g * sg)
     if act.kind == "swiglu_clamp":
         c = act.clamp
+        gd, ud = (g, u) if decide is None else decide
         gc = np.minimum(g, c)
         uc = np.clip(u, -c, c)
         sgc = sigmoid(gc)
-        dg = dh * uc * sgc * (1.0 + gc * (1.0 - sgc)) * (g <= c)
-        du = dh * (gc * sgc) * ((u >= -c) & (u <= c))
+        dg = dh * uc * sgc * (1.0 + gc * (1.0 - sgc)) * (gd <= c)
+        du = dh * (gc * sgc) * ((ud >= -c) & (ud <= c))
         return dg, du
     s = act.gate_scale
     th = np.tanh(g / s)
@@ -657,7 +663,7 @@ def combine_backward(dy: np.ndarray, out_perm: np.ndarray, row_of: np.ndarray,
 
 
 def swiglu_ffn_backward(xs, w1, w2, g, u, h, d_out,
-                        act: GluAct = SWIGLU) -> Dict[str, np.ndarray]:
+                        act: GluAct = SWIGLU, decide=None) -> Dict[str, np.ndarray]:
     """B5 + B4 for one expert: gradients of out = glu(g, u) @ w2.T, [g u] = xs @ w1.T.
 
     For SwiGLU d/dg silu(g) = sigmoid(g) * (1 + g * (1 - sigmoid(g))); the
@@ -665,14 +671,31 @@ def swiglu_ffn_backward(xs, w1, w2, g, u, h, d_out,
     """
     dh = d_out @ w2
     dW2 = d_out.T @ h
-    dg, du = glu_backward(g, u, dh, act)
+    dg, du = glu_backward(g, u, dh, act, decide)
     d_pre = np.concatenate([dg, du], axis=1)
     dxs = d_pre @ w1
     dW1 = d_pre.T @ xs
     return {"dh": dh, "d_pre": d_pre, "dxs": dxs, "dW1": dW1, "dW2": dW2}
 
 
-def grouped_swiglu_backward(x_perm, offsets, w1, w2, g, u, h, d_out_perm, act: GluAct = SWIGLU):
+def round_to(a: np.ndarray, act_dtype: str) -> np.ndarray:
+    """a rounded to the layer's activation dtype (round to nearest even), back in float64."""
+    import torch
+    dt = torch.bfloat16 if act_dtype == "bf16" else torch.float32
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dt).double().numpy()
+
+
+def clip_decisions(g, u, act: GluAct, act_dtype: str):
+    """Where the SwiGLU clamp decides on the stored pre-activations: a bf16
+    layer keeps gate|up in bf16 for the backward, so its clip decisions are
+    taken on those values (the same precision on both sides of a check)."""
+    if act.kind != "swiglu_clamp" or act_dtype != "bf16":
+        return None
+    return round_to(g, act_dtype), round_to(u, act_dtype)
+
+
+def grouped_swiglu_backward(x_perm, offsets, w1, w2, g, u, h, d_out_perm, act: GluAct = SWIGLU,
+                            act_dtype: str = "f32"):
     A, d = x_perm.shape
     E, twoF, _ = w1.shape
     d_pre = np.zeros((A, twoF))
@@ -684,7 +707,8 @@ def grouped_swiglu_backward(x_perm, offsets, w1, w2, g, u, h, d_out_perm, act: G
         if r1 == r0:
             continue  # an expert with no rows has zero weight gradient
         res = swiglu_ffn_backward(x_perm[r0:r1], w1[e], w2[e], g[r0:r1], u[r0:r1],
-                                  h[r0:r1], d_out_perm[r0:r1], act)
+                                  h[r0:r1], d_out_perm[r0:r1], act,
+                                  clip_decisions(g[r0:r1], u[r0:r1], act, act_dtype))
         d_pre[r0:r1] = res["d_pre"]
         dx_perm[r0:r1] = res["dxs"]
         dW1[e] = res["dW1"]
@@ -767,7 +791,7 @@ def layer_backward(wl, inp, fwd, dy: np.ndarray, g_aux: float = 1.0) -> Dict[str
     act = act_of(wl)
     d_out_perm, dw = combine_backward(dy, fwd["out_perm"], fwd["row_of"], fwd["w"])
     ex = grouped_swiglu_backward(fwd["x_perm"], fwd["offsets"], inp["w1"], inp["w2"],
-                                 fwd["g"], fwd["u"], fwd["h"], d_out_perm, act)
+                                 fwd["g"], fwd["u"], fwd["h"], d_out_perm, act, wl.act_dtype)
     d_logits = scores_backward(fwd["logits"], fwd["idx"], dw, wl.score, wl.scaling)
     d_logits = d_logits + aux_loss_backward(fwd["logits"], fwd["counts"], wl.k,
                                             wl.aux_coeff, wl.score, g_aux)
@@ -786,7 +810,8 @@ def layer_backward(wl, inp, fwd, dy: np.ndarray, g_aux: float = 1.0) -> Dict[str
             out["dW_gate_s"] = d_gl @ inp["x"]
             dx = dx + d_gl[:, None] * inp["w_gate_s"][None, :]
         sh = swiglu_ffn_backward(inp["x"], inp["w1_s"], inp["w2_s"], fwd["g_s"],
-                                 fwd["u_s"], fwd["h_s"], dy_s, act)
+                                 fwd["u_s"], fwd["h_s"], dy_s, act,
+                                 clip_decisions(fwd["g_s"], fwd["u_s"], act, wl.act_dtype))
         out.update({"dW1_s": sh["dW1"], "dW2_s": sh["dW2"], "dx_s": sh["dxs"],
                     "d_pre_s": sh["d_pre"], "dy_s": dy_s})
         dx = dx + sh["dxs"]

@@ -51,6 +51,7 @@ MOE_WS_AUX = 3
 MOE_WS_ROUTE_BWD = 4
 MOE_WS_ROUTE = 5
 MOE_WS_Z_LOSS = 6
+MOE_WS_SHARED_GATE_BWD = 7
 
 MOE_ROUTER_AUTO = 0
 MOE_ROUTER_CUDA_CORES = 1
@@ -59,7 +60,9 @@ MOE_ROUTER_CUDA_CORES = 1
 class MoeCfg(ctypes.Structure):
     _fields_ = [("T", c_int64), ("d", c_int32), ("E", c_int32), ("k", c_int32),
                 ("F", c_int32), ("F_shared", c_int32), ("score_fn", c_int32),
-                ("act_dtype", c_int32), ("scaling", c_float), ("aux_coeff", c_float)]
+                ("act_dtype", c_int32), ("scaling", c_float), ("aux_coeff", c_float),
+                ("act_fn", c_int32), ("act_clamp", c_float), ("act_gate_scale", c_float),
+                ("act_linear_scale", c_float), ("glu_linear_offset", c_float)]
 
 
 class MoeError(RuntimeError):
@@ -92,7 +95,10 @@ _SIGS = {
     "moe_permute": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
     "moe_grouped_swiglu": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP, _VP,
                                    _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
-    "moe_unpermute_combine": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_unpermute_combine": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_shared_gate": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP]),
+    "moe_shared_gate_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                    c_size_t, _VP]),
     "moe_aux_loss": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, c_size_t, _VP]),
     "moe_unpermute_combine_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_grouped_swiglu_bwd": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP,
@@ -101,7 +107,7 @@ _SIGS = {
     "moe_aux_loss_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, c_float, _VP, c_int32, _VP]),
     "moe_route_topk_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, c_int32, _VP,
                                    _VP, _VP, c_size_t, _VP]),
-    "moe_permute_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_permute_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_workspace_bytes": (c_size_t, [POINTER(MoeCfg), c_int]),
     "moe_status_string": (c_char_p, [c_int]),
     "moe_last_cuda_error": (c_char_p, []),
@@ -195,17 +201,28 @@ def version() -> str:
     return lib.moe_version().decode()
 
 
+MOE_ACT_SWIGLU = 0
+MOE_ACT_SWIGLU_CLAMP = 1
+MOE_ACT_SITU_GLU = 2
+ACT_CODES = {"swiglu": MOE_ACT_SWIGLU, "swiglu_clamp": MOE_ACT_SWIGLU_CLAMP,
+             "situ_glu": MOE_ACT_SITU_GLU}
+
+
 def make_cfg(T, d, E, k, F, F_shared=0, score="softmax", act_dtype="bf16", scaling=1.0,
-             aux_coeff=1e-3) -> MoeCfg:
+             aux_coeff=1e-3, act_fn="swiglu", act_clamp=0.0, act_gate_scale=0.0,
+             act_linear_scale=0.0, glu_linear_offset=0.0) -> MoeCfg:
     return MoeCfg(T=T, d=d, E=E, k=k, F=F, F_shared=F_shared,
                   score_fn=SCORE_CODES[score],
                   act_dtype=MOE_BF16 if act_dtype == "bf16" else MOE_F32,
-                  scaling=scaling, aux_coeff=aux_coeff)
+                  scaling=scaling, aux_coeff=aux_coeff, act_fn=ACT_CODES[act_fn],
+                  act_clamp=act_clamp, act_gate_scale=act_gate_scale,
+                  act_linear_scale=act_linear_scale, glu_linear_offset=glu_linear_offset)
 
 
 def cfg_from_workload(wl, T: Optional[int] = None) -> MoeCfg:
     return make_cfg(wl.T if T is None else T, wl.d, wl.E, wl.k, wl.F, wl.F_shared, wl.score,
-                    wl.act_dtype, wl.scaling, wl.aux_coeff)
+                    wl.act_dtype, wl.scaling, wl.aux_coeff, wl.act_fn, wl.act_clamp,
+                    wl.act_gate_scale, wl.act_linear_scale, wl.glu_linear_offset)
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -283,10 +300,22 @@ def grouped_swiglu(cfg, n_groups, n_rows, F, offsets, x_rows, w1, w2, pre_gu, h,
            "moe_grouped_swiglu")
 
 
-def unpermute_combine(cfg, out_perm, row_of, w, shared_out, y, stream=None):
+def unpermute_combine(cfg, out_perm, row_of, w, shared_out, y, stream=None, shared_gate=None):
     _check(lib.moe_unpermute_combine(ctypes.byref(cfg), _p(out_perm), _p(row_of), _p(w),
-                                     _p(shared_out), _p(y), _stream(stream)),
+                                     _p(shared_out), _p(shared_gate), _p(y), _stream(stream)),
            "moe_unpermute_combine")
+
+
+def shared_gate(cfg, x, w_gate, gate, stream=None):
+    _check(lib.moe_shared_gate(ctypes.byref(cfg), _p(x), _p(w_gate), _p(gate), _stream(stream)),
+           "moe_shared_gate")
+
+
+def shared_gate_bwd(cfg, x, gate, dy, shared_out, dy_shared, d_gate_logit, dw_gate, ws,
+                    stream=None):
+    _check(lib.moe_shared_gate_bwd(ctypes.byref(cfg), _p(x), _p(gate), _p(dy), _p(shared_out),
+                                   _p(dy_shared), _p(d_gate_logit), _p(dw_gate), _p(ws),
+                                   _nbytes(ws), _stream(stream)), "moe_shared_gate_bwd")
 
 
 def aux_loss(cfg, logits, counts, aux, ws, stream=None):
@@ -397,7 +426,9 @@ def route_topk_bwd(cfg, x, w_router, logits, idx, dw, d_logits, accumulate, dx_r
            "moe_route_topk_bwd")
 
 
-def permute_bwd(cfg, dx_perm, row_of, dx_router, dx_shared, dx, stream=None):
+def permute_bwd(cfg, dx_perm, row_of, dx_router, dx_shared, dx, stream=None,
+                d_gate_logit=None, w_gate=None):
     _check(lib.moe_permute_bwd(ctypes.byref(cfg), _p(dx_perm), _p(row_of), _p(dx_router),
-                               _p(dx_shared), _p(dx), _stream(stream)),
+                               _p(dx_shared), _p(d_gate_logit), _p(w_gate), _p(dx),
+                               _stream(stream)),
            "moe_permute_bwd")

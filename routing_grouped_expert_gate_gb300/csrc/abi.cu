@@ -2,6 +2,7 @@
 // the device status word, workspace sizing, and the order in which each call
 // launches its kernels on the caller's stream.
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 
@@ -57,6 +58,7 @@ static int make_ctx(cudaStream_t stream, Ctx* c) {
   c->status = g_status_ptr[dev];
   c->timeout_ns = g_timeout_ns.load();
   c->sm_count = g_sm_count[dev];
+  c->act = GluAct{MOE_ACT_SWIGLU, 0.f, 0.f, 0.f, 0.f};
   return MOE_OK;
 }
 
@@ -79,8 +81,26 @@ static int check_cfg(const moe_cfg* cfg) {
   if (cfg->E > kMaxE || cfg->k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if ((cfg->d & 7) || (cfg->F & 7) || (cfg->F_shared & 7)) return MOE_ERR_ALIGN;
   if (cfg->T * (int64_t)cfg->k >= (int64_t)0x7fffffff) return MOE_ERR_UNSUPPORTED;
+  // expert activation (Handbook §3.4 "Activation"): the SwiGLU clamp value
+  // must be finite and > 0 with a zero linear offset; SiTU needs a gate scale
+  switch (cfg->act_fn) {
+    case MOE_ACT_SWIGLU: break;
+    case MOE_ACT_SWIGLU_CLAMP:
+      if (!(std::isfinite(cfg->act_clamp) && cfg->act_clamp > 0.f) ||
+          cfg->glu_linear_offset != 0.f)
+        return MOE_ERR_INVALID_ARG;
+      break;
+    case MOE_ACT_SITU_GLU:
+      if (!(std::isfinite(cfg->act_gate_scale) && cfg->act_gate_scale > 0.f) ||
+          !(std::isfinite(cfg->act_linear_scale) && cfg->act_linear_scale >= 0.f))
+        return MOE_ERR_INVALID_ARG;
+      break;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(cfg->glu_linear_offset)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
+static_assert(sizeof(moe_cfg) == 64, "moe_cfg layout");
 
 static int act_size(const moe_cfg& cfg) { return cfg.act_dtype == MOE_BF16 ? 2 : 4; }
 
@@ -149,6 +169,12 @@ static size_t grouped_bwd_ws(const moe_cfg& cfg) {
 
 static size_t route_bwd_ws(const moe_cfg& cfg) {
   return round256((size_t)route_bwd_splits(cfg) * cfg.E * cfg.d * sizeof(float));
+}
+
+static size_t shared_gate_bwd_ws(const moe_cfg& cfg) {
+  moe_cfg one = cfg;
+  one.E = 1;
+  return round256((size_t)route_bwd_splits(one) * cfg.d * sizeof(float));
 }
 
 }  // namespace moe
@@ -239,6 +265,7 @@ size_t moe_workspace_bytes(const moe_cfg* cfg, int which) {
     case MOE_WS_ROUTE_BWD: return route_bwd_ws(*cfg);
     case MOE_WS_ROUTE: return router_ws_bytes(*cfg);
     case MOE_WS_Z_LOSS: return z_loss_ws_bytes(*cfg);
+    case MOE_WS_SHARED_GATE_BWD: return shared_gate_bwd_ws(*cfg);
     default: return 0;
   }
 }
@@ -288,6 +315,7 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
   MOE_PTR(w1); MOE_PTR(w2); MOE_OPT_PTR(pre_gu); MOE_OPT_PTR(offsets);
   if (n_rows > 0) { MOE_PTR(x_rows); MOE_PTR(h); MOE_PTR(out); }
   MOE_CTX(stream, c);
+  c.act = glu_act_of(*cfg);
   if (n_rows == 0) return MOE_OK;
   const int dt = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
   const int d = cfg->d;
@@ -313,7 +341,7 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
   g1.C = pre; g1.c_sm = 2 * F; g1.c_sg = 0;
   g1.offsets = offsets; g1.n_groups = n_groups; g1.alpha = 1.f;
   MOE_LAUNCH(launch_simt_gemm(c, g1));
-  MOE_LAUNCH(launch_swiglu_fwd_elem(c, dt, pre, h, n_rows, F));
+  MOE_LAUNCH(launch_swiglu_fwd_elem(c, dt, pre, h, n_rows, F));  // c.act
   SimtGemm g2{};
   g2.mode = kGroupM; g2.M = (int)n_rows; g2.N = d; g2.K = F;
   g2.dtA = g2.dtB = g2.dtC = dt;
@@ -326,12 +354,55 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
 }
 
 int moe_unpermute_combine(const moe_cfg* cfg, const void* out_perm, const int32_t* row_of,
-                          const float* w, const void* shared_out, void* y, moe_stream_t stream) {
+                          const float* w, const void* shared_out, const float* shared_gate,
+                          void* y, moe_stream_t stream) {
   MOE_CHECK_CFG(cfg);
   if (cfg->T == 0) return MOE_OK;
   MOE_PTR(out_perm); MOE_PTR(row_of); MOE_PTR(w); MOE_PTR(y); MOE_OPT_PTR(shared_out);
+  MOE_REQUIRE(shared_gate == nullptr || shared_out != nullptr, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE(shared_gate == nullptr || (reinterpret_cast<uintptr_t>(shared_gate) & 3u) == 0,
+              MOE_ERR_ALIGN);
   MOE_CTX(stream, c);
-  MOE_LAUNCH(launch_combine(c, *cfg, out_perm, row_of, w, shared_out, y));
+  MOE_LAUNCH(launch_combine(c, *cfg, out_perm, row_of, w, shared_out, shared_gate, y));
+  return MOE_OK;
+}
+
+int moe_shared_gate(const moe_cfg* cfg, const void* x, const float* w_gate, float* gate,
+                    moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (cfg->T == 0) return MOE_OK;
+  MOE_PTR(x); MOE_PTR(w_gate); MOE_PTR(gate);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_shared_gate(c, *cfg, x, w_gate, gate));
+  return MOE_OK;
+}
+
+int moe_shared_gate_bwd(const moe_cfg* cfg, const void* x, const float* gate, const void* dy,
+                        const void* shared_out, void* dy_shared, float* d_gate_logit,
+                        float* dw_gate, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_PTR(dw_gate); MOE_PTR(ws);
+  MOE_REQUIRE(ws_bytes >= shared_gate_bwd_ws(*cfg), MOE_ERR_WORKSPACE);
+  if (cfg->T > 0) {
+    MOE_PTR(x); MOE_PTR(gate); MOE_PTR(dy); MOE_PTR(shared_out); MOE_PTR(dy_shared);
+    MOE_PTR(d_gate_logit);
+  }
+  MOE_CTX(stream, c);
+  if (cfg->T == 0) {
+    MOE_LAUNCH(cudaMemsetAsync(dw_gate, 0, (size_t)cfg->d * sizeof(float), c.stream));
+    return MOE_OK;
+  }
+  MOE_LAUNCH(launch_shared_gate_bwd_tokens(c, *cfg, dy, shared_out, gate, dy_shared,
+                                           d_gate_logit));
+  // dw_gate = sum_t d_gate_logit[t] x[t]: the router's weight-gradient kernel
+  // for a single expert, token slices summed in slice order
+  moe_cfg one = *cfg;
+  one.E = 1;
+  const int S = route_bwd_splits(one);
+  float* part = static_cast<float*>(ws);
+  MOE_LAUNCH(launch_router_dw_small(c, one, x, d_gate_logit, part, S));
+  MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)cfg->d, S, (int64_t)cfg->d, dw_gate, kF32,
+                                    0));
   return MOE_OK;
 }
 
@@ -375,6 +446,7 @@ int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows,
   }
   const size_t need_dh = round256((size_t)n_rows * F * sizeof(float));
   MOE_CTX(stream, c);
+  c.act = glu_act_of(*cfg);
   const int dt = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
   const int d = cfg->d;
   if (use_tc(dt)) {
@@ -617,13 +689,16 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
 }
 
 int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_of,
-                    const float* dx_router, const void* dx_shared, void* dx,
-                    moe_stream_t stream) {
+                    const float* dx_router, const void* dx_shared, const float* d_gate_logit,
+                    const float* w_gate, void* dx, moe_stream_t stream) {
   MOE_CHECK_CFG(cfg);
   if (cfg->T == 0) return MOE_OK;
   MOE_PTR(dx_perm); MOE_PTR(row_of); MOE_PTR(dx); MOE_OPT_PTR(dx_router); MOE_OPT_PTR(dx_shared);
+  MOE_REQUIRE((d_gate_logit == nullptr) == (w_gate == nullptr), MOE_ERR_INVALID_ARG);
+  MOE_OPT_PTR(d_gate_logit); MOE_OPT_PTR(w_gate);
   MOE_CTX(stream, c);
-  MOE_LAUNCH(launch_permute_bwd(c, *cfg, dx_perm, row_of, dx_router, dx_shared, dx));
+  MOE_LAUNCH(launch_permute_bwd(c, *cfg, dx_perm, row_of, dx_router, dx_shared, d_gate_logit,
+                                w_gate, dx));
   return MOE_OK;
 }
 

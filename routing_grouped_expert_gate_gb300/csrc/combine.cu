@@ -4,7 +4,7 @@
 // transforms numbers inside the model": the block returns each chosen expert's
 // output times its weight, summed coordinate by coordinate. The Ultimate MoE
 // Training Handbook, §3.4 "Shared experts": the shared expert's output is added
-// at weight 1.
+// at weight 1, or times sigmoid(x · w_gate) with the shared-expert gate.
 //
 // Both kernels run one warp per token with 16-byte accesses (8 bf16 or 4+4
 // fp32 per lane per step): the gather, the scaling and the accumulation happen
@@ -49,7 +49,8 @@ template <typename T, int KK>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ out_perm, const int32_t* __restrict__ row_of,
                const float* __restrict__ w, const T* __restrict__ shared_out,
-               T* __restrict__ y, int64_t Tn, int k, int d, int64_t A, int* status) {
+               const float* __restrict__ shared_gate, T* __restrict__ y, int64_t Tn, int k,
+               int d, int64_t A, int* status) {
   constexpr int U = KK >= 8 ? 1 : 8 / KK;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -58,6 +59,7 @@ combine_kernel(const T* __restrict__ out_perm, const int32_t* __restrict__ row_o
     int64_t rows[KK];
     float wj[KK];
     token_rows<KK>(row_of, w, t, k, A, lane, status, rows, wj);
+    const float gs = shared_gate != nullptr ? shared_gate[t] : 1.f;
     for (int g0 = 0; g0 < ng; g0 += 32 * U) {
       Raw8<T> raw[U][KK], sraw[U];
 #pragma unroll
@@ -90,7 +92,7 @@ combine_kernel(const T* __restrict__ out_perm, const int32_t* __restrict__ row_o
         float sv[8];
         sraw[u].to_float(sv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += sv[i];
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(gs, sv[i], acc[i]);
         store8(y + t * d + 8 * g, acc);
       }
     }
@@ -174,7 +176,7 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ out_perm,
 
 cudaError_t launch_combine(const Ctx& c, const moe_cfg& cfg, const void* out_perm,
                            const int32_t* row_of, const float* w, const void* shared_out,
-                           void* y) {
+                           const float* shared_gate, void* y) {
   if (cfg.T == 0) return cudaSuccess;
   const int64_t A = cfg.T * cfg.k;
   const unsigned grid = token_grid(c, cfg.T);
@@ -182,12 +184,12 @@ cudaError_t launch_combine(const Ctx& c, const moe_cfg& cfg, const void* out_per
   if (cfg.act_dtype == MOE_BF16)                                                             \
     combine_kernel<bf16, KK><<<grid, 256, 0, c.stream>>>(                                     \
         static_cast<const bf16*>(out_perm), row_of, w, static_cast<const bf16*>(shared_out), \
-        static_cast<bf16*>(y), cfg.T, cfg.k, cfg.d, A, c.status);                            \
+        shared_gate, static_cast<bf16*>(y), cfg.T, cfg.k, cfg.d, A, c.status);               \
   else                                                                                       \
     combine_kernel<float, KK><<<grid, 256, 0, c.stream>>>(                                    \
         static_cast<const float*>(out_perm), row_of, w,                                      \
-        static_cast<const float*>(shared_out), static_cast<float*>(y), cfg.T, cfg.k, cfg.d, A, \
-        c.status)
+        static_cast<const float*>(shared_out), shared_gate, static_cast<float*>(y), cfg.T,   \
+        cfg.k, cfg.d, A, c.status)
   MOE_BY_K(cfg.k, MOE_COMBINE);
 #undef MOE_COMBINE
   note_launches(1);

@@ -215,6 +215,7 @@ template <typename T, int KK>
 __global__ void __launch_bounds__(256)
 permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ row_of,
                    const float* __restrict__ dx_router, const T* __restrict__ dx_shared,
+                   const float* __restrict__ d_gate_logit, const float* __restrict__ w_gate,
                    T* __restrict__ dx, int64_t Tn, int k, int d, int64_t A, int* status) {
   constexpr int U = KK >= 8 ? 1 : 8 / KK;  // 8-element groups per lane per step
   const int lane = threadIdx.x & 31;
@@ -231,6 +232,7 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
       }
       rows[j] = r;
     }
+    const float dgl = d_gate_logit != nullptr ? d_gate_logit[t] : 0.f;
     for (int g0 = 0; g0 < ng; g0 += 32 * U) {
       Raw8<T> raw[U][KK], sraw[U];
       Raw8<float> rraw[U];
@@ -266,6 +268,13 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
         sraw[u].to_float(sv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] += sv[i];
+        if (d_gate_logit != nullptr) {
+          // the shared-expert gate's path: d(logit) * w_gate
+          float wg[8];
+          load8(w_gate + 8 * g, wg);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(dgl, wg[i], acc[i]);
+        }
         store8(dx + t * d + 8 * g, acc);
       }
     }
@@ -274,7 +283,8 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
 
 cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_perm,
                                const int32_t* row_of, const float* dx_router,
-                               const void* dx_shared, void* dx) {
+                               const void* dx_shared, const float* d_gate_logit,
+                               const float* w_gate, void* dx) {
   if (cfg.T == 0) return cudaSuccess;
   const int64_t A = cfg.T * cfg.k;
   const unsigned grid = copy_grid(c, cfg.T);
@@ -282,13 +292,13 @@ cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_
   if (cfg.act_dtype == MOE_BF16)                                                             \
     permute_bwd_kernel<bf16, KK><<<grid, 256, 0, c.stream>>>(                                 \
         static_cast<const bf16*>(dx_perm), row_of, dx_router,                                \
-        static_cast<const bf16*>(dx_shared), static_cast<bf16*>(dx), cfg.T, cfg.k, cfg.d, A, \
-        c.status);                                                                           \
+        static_cast<const bf16*>(dx_shared), d_gate_logit, w_gate, static_cast<bf16*>(dx),   \
+        cfg.T, cfg.k, cfg.d, A, c.status);                                                   \
   else                                                                                       \
     permute_bwd_kernel<float, KK><<<grid, 256, 0, c.stream>>>(                                \
         static_cast<const float*>(dx_perm), row_of, dx_router,                               \
-        static_cast<const float*>(dx_shared), static_cast<float*>(dx), cfg.T, cfg.k, cfg.d, A, \
-        c.status)
+        static_cast<const float*>(dx_shared), d_gate_logit, w_gate, static_cast<float*>(dx), \
+        cfg.T, cfg.k, cfg.d, A, c.status)
   if (cfg.k <= 1) {
     MOE_PBWD(1);
   } else if (cfg.k <= 2) {

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "glu_act.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -74,6 +75,7 @@ struct Params {
   const bf16* aux_in; // fc2 dgrad: gate|up input
   int* status;
   uint64_t timeout_ns;
+  GluAct act;         // expert activation (SwiGLU epilogues)
 };
 
 struct __align__(8) Shared {
@@ -177,24 +179,32 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
     const bool rv = r < ti.m_end;
 #pragma unroll 1
     for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
-      float g[32], u[32], h[32];
+      float g[32], u[32];
       tmem_ld32(t_row + c, g);
       tmem_ld32(t_row + BN / 2 + c, u);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
-      if (rv) {
-        const int f0 = ti.n0 + c;
+      const int f0 = ti.n0 + c;
+      if (rv && P.out1) {
+        // the pre-activation gate|up first: h then overwrites g in place
+        bf16* pr = P.out1 + (int64_t)r * 2 * P.F;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (f0 + 8 * j < P.F) {
-            store_bf16x8(P.out0 + (int64_t)r * P.ld0 + f0 + 8 * j, h + 8 * j);
-            if (P.out1) {
-              bf16* pr = P.out1 + (int64_t)r * 2 * P.F;
-              store_bf16x8(pr + f0 + 8 * j, g + 8 * j);
-              store_bf16x8(pr + P.F + f0 + 8 * j, u + 8 * j);
-            }
+            store_bf16x8(pr + f0 + 8 * j, g + 8 * j);
+            store_bf16x8(pr + P.F + f0 + 8 * j, u + 8 * j);
           }
         }
+      }
+      if (glu_is_plain(P.act)) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = glu_fwd(g[i], u[i], P.act);
+      }
+      if (rv) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (f0 + 8 * j < P.F) store_bf16x8(P.out0 + (int64_t)r * P.ld0 + f0 + 8 * j, g + 8 * j);
       }
     }
   } else if (EPI == EPI_STORE) {
@@ -255,12 +265,17 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
               gv[2 * i] = a.x; gv[2 * i + 1] = a.y;
               uv[2 * i] = b2.x; uv[2 * i + 1] = b2.y;
             }
+            if (glu_is_plain(P.act)) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float sg = 1.f / (1.f + __expf(-gv[i]));
-              const float d = dh[8 * j + i];
-              dg[i] = d * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
-              du[i] = d * gv[i] * sg;
+              for (int i = 0; i < 8; ++i) {
+                const float sg = 1.f / (1.f + __expf(-gv[i]));
+                const float d = dh[8 * j + i];
+                dg[i] = d * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
+                du[i] = d * gv[i] * sg;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) glu_bwd(gv[i], uv[i], dh[8 * j + i], P.act, dg[i], du[i]);
             }
             store_bf16x8(dp + f, dg);
             store_bf16x8(dp + P.F + f, du);
@@ -1059,6 +1074,7 @@ static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* of
   P.offsets = offsets;
   P.status = c.status;
   P.timeout_ns = c.timeout_ns;
+  P.act = c.act;
   return P;
 }
 

@@ -15,11 +15,25 @@ inline bool score_takes_bias(int score_fn) {
   return score_fn == MOE_SCORE_SIGMOID || score_fn == MOE_SCORE_SQRT_SOFTPLUS;
 }
 
+// expert activation (moe_cfg's act_* fields); fn = MOE_ACT_*
+struct GluAct {
+  int fn;
+  float clamp, gate_scale, linear_scale, offset;
+};
+inline GluAct glu_act_of(const moe_cfg& cfg) {
+  return GluAct{cfg.act_fn, cfg.act_clamp, cfg.act_gate_scale, cfg.act_linear_scale,
+                cfg.glu_linear_offset};
+}
+__host__ __device__ inline bool glu_is_plain(const GluAct& a) {
+  return a.fn == MOE_ACT_SWIGLU && a.offset == 0.f;
+}
+
 struct Ctx {
   cudaStream_t stream;
   int* status;          // device status word of the current device
   uint64_t timeout_ns;  // bound of every spin-wait
   int sm_count;
+  GluAct act;           // the call's expert activation (grouped SwiGLU calls)
 };
 
 // ---- router (router.cu; tensor-core gate GEMM in router_tc.cu)
@@ -86,12 +100,19 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
                            int32_t* src_tok, void* x_perm, void* ws);
 cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_perm,
                                const int32_t* row_of, const float* dx_router,
-                               const void* dx_shared, void* dx);
+                               const void* dx_shared, const float* d_gate_logit,
+                               const float* w_gate, void* dx);
 
 // ---- combine (combine.cu)
 cudaError_t launch_combine(const Ctx& c, const moe_cfg& cfg, const void* out_perm,
                            const int32_t* row_of, const float* w, const void* shared_out,
-                           void* y);
+                           const float* shared_gate, void* y);
+// the shared expert's sigmoid gate (shared_gate.cu)
+cudaError_t launch_shared_gate(const Ctx& c, const moe_cfg& cfg, const void* x,
+                               const float* w_gate, float* gate);
+cudaError_t launch_shared_gate_bwd_tokens(const Ctx& c, const moe_cfg& cfg, const void* dy,
+                                          const void* shared_out, const float* gate,
+                                          void* dy_shared, float* d_gate_logit);
 cudaError_t launch_combine_bwd(const Ctx& c, const moe_cfg& cfg, const void* dy,
                                const void* out_perm, const int32_t* row_of, const float* w,
                                void* d_out_perm, float* dw);

@@ -16,6 +16,7 @@
 // matrices; consecutive threads always touch consecutive addresses.
 #include "common.cuh"
 #include "internal.h"
+#include "glu_act.cuh"
 
 namespace moe {
 
@@ -216,10 +217,10 @@ cudaError_t launch_reduce_partials(const Ctx& c, const float* part, int64_t stri
 
 // ------------------------------------------------------------------ SwiGLU elementwise
 // Handbook §3.4 "Activation": the first half of fc1's output is the gate,
-// h = silu(gate) * up.
+// h = act(gate, up): SwiGLU or one of its variants (glu_fwd).
 template <typename T>
 __global__ void __launch_bounds__(256)
-swiglu_fwd_elem(const T* __restrict__ pre, T* __restrict__ h, int64_t rows, int F) {
+swiglu_fwd_elem(const T* __restrict__ pre, T* __restrict__ h, int64_t rows, int F, GluAct act) {
   const int64_t n = rows * F;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -227,15 +228,15 @@ swiglu_fwd_elem(const T* __restrict__ pre, T* __restrict__ h, int64_t rows, int 
     const int f = (int)(i - r * F);
     const float gt = to_f32<T>(pre[r * 2 * F + f]);
     const float up = to_f32<T>(pre[r * 2 * F + F + f]);
-    h[i] = from_f32<T>(gt * sigmoidf_acc(gt) * up);
+    h[i] = from_f32<T>(glu_fwd(gt, up, act));
   }
 }
 
-// d_pre = [dh * up * s (1 + g (1 - s)) | dh * g * s],  s = sigmoid(g)
+// d_pre = [dh * d h / d g | dh * d h / d u] of the activation (glu_bwd)
 template <typename T>
 __global__ void __launch_bounds__(256)
 swiglu_bwd_elem(const float* __restrict__ dh, const T* __restrict__ pre, T* __restrict__ d_pre,
-                int64_t rows, int F) {
+                int64_t rows, int F, GluAct act) {
   const int64_t n = rows * F;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -243,10 +244,10 @@ swiglu_bwd_elem(const float* __restrict__ dh, const T* __restrict__ pre, T* __re
     const int f = (int)(i - r * F);
     const float gt = to_f32<T>(pre[r * 2 * F + f]);
     const float up = to_f32<T>(pre[r * 2 * F + F + f]);
-    const float s = sigmoidf_acc(gt);
-    const float g = dh[i];
-    d_pre[r * 2 * F + f] = from_f32<T>(g * up * s * (1.f + gt * (1.f - s)));
-    d_pre[r * 2 * F + F + f] = from_f32<T>(g * gt * s);
+    float dg, du;
+    glu_bwd(gt, up, dh[i], act, dg, du);
+    d_pre[r * 2 * F + f] = from_f32<T>(dg);
+    d_pre[r * 2 * F + F + f] = from_f32<T>(du);
   }
 }
 
@@ -261,10 +262,10 @@ cudaError_t launch_swiglu_fwd_elem(const Ctx& c, int dt, const void* pre_gu, voi
   if (rows * F == 0) return cudaSuccess;
   if (dt == kBF16)
     swiglu_fwd_elem<bf16><<<elem_grid(c, rows * F), 256, 0, c.stream>>>(
-        static_cast<const bf16*>(pre_gu), static_cast<bf16*>(h), rows, F);
+        static_cast<const bf16*>(pre_gu), static_cast<bf16*>(h), rows, F, c.act);
   else
     swiglu_fwd_elem<float><<<elem_grid(c, rows * F), 256, 0, c.stream>>>(
-        static_cast<const float*>(pre_gu), static_cast<float*>(h), rows, F);
+        static_cast<const float*>(pre_gu), static_cast<float*>(h), rows, F, c.act);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -274,10 +275,10 @@ cudaError_t launch_swiglu_bwd_elem(const Ctx& c, int dt, const float* dh, const 
   if (rows * F == 0) return cudaSuccess;
   if (dt == kBF16)
     swiglu_bwd_elem<bf16><<<elem_grid(c, rows * F), 256, 0, c.stream>>>(
-        dh, static_cast<const bf16*>(pre_gu), static_cast<bf16*>(d_pre), rows, F);
+        dh, static_cast<const bf16*>(pre_gu), static_cast<bf16*>(d_pre), rows, F, c.act);
   else
     swiglu_bwd_elem<float><<<elem_grid(c, rows * F), 256, 0, c.stream>>>(
-        dh, static_cast<const float*>(pre_gu), static_cast<float*>(d_pre), rows, F);
+        dh, static_cast<const float*>(pre_gu), static_cast<float*>(d_pre), rows, F, c.act);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -5,10 +5,13 @@ ABI calls in order on one stream; every step of the layer runs in libmoe's
 CUDA kernels:
 
   forward : route_topk -> permute -> grouped_swiglu (routed) [-> grouped_swiglu
-            (shared)] -> unpermute_combine -> aux_loss
+            (shared) [-> shared_gate]] -> unpermute_combine -> aux_loss
   backward: unpermute_combine_bwd -> grouped_swiglu_bwd (routed) [->
-            grouped_swiglu_bwd (shared)] -> aux_loss_bwd -> route_topk_bwd ->
-            permute_bwd
+            [shared_gate_bwd ->] grouped_swiglu_bwd (shared)] -> aux_loss_bwd ->
+            route_topk_bwd -> permute_bwd
+
+The shared expert's sigmoid gate is used when the parameters hold its weight
+("w_gate_s", [d] fp32).
 
 The backward returns the gradients of  <dy, y> + g_aux * aux  with respect to
 x, the router weight and the expert weights.
@@ -49,7 +52,8 @@ def alloc_buffers(cfg, device, backward: bool = True) -> Dict[str, torch.Tensor]
         "aux": e(1, dt=torch.float32),
     }
     if Fs > 0:
-        b.update({"pre_gu_s": e(T, 2 * Fs), "h_s": e(T, Fs), "y_s": e(T, d)})
+        b.update({"pre_gu_s": e(T, 2 * Fs), "h_s": e(T, Fs), "y_s": e(T, d),
+                  "gate_s": e(T, dt=torch.float32)})
     ws = max(L.workspace_bytes(cfg, L.MOE_WS_PERMUTE), L.workspace_bytes(cfg, L.MOE_WS_GROUPED),
              L.workspace_bytes(cfg, L.MOE_WS_AUX), L.workspace_bytes(cfg, L.MOE_WS_ROUTE))
     if backward:
@@ -67,9 +71,12 @@ def alloc_buffers(cfg, device, backward: bool = True) -> Dict[str, torch.Tensor]
         })
         if Fs > 0:
             b.update({"d_pre_s": e(T, 2 * Fs), "dx_s": e(T, d), "dw1_s": e(1, 2 * Fs, d),
-                      "dw2_s": e(1, d, Fs)})
+                      "dw2_s": e(1, d, Fs), "dy_s": e(T, d),
+                      "d_gate_logit_s": e(T, dt=torch.float32),
+                      "dw_gate_s": e(d, dt=torch.float32)})
         ws = max(ws, L.workspace_bytes(cfg, L.MOE_WS_GROUPED_BWD),
-                 L.workspace_bytes(cfg, L.MOE_WS_ROUTE_BWD))
+                 L.workspace_bytes(cfg, L.MOE_WS_ROUTE_BWD),
+                 L.workspace_bytes(cfg, L.MOE_WS_SHARED_GATE_BWD))
     b["ws"] = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
     return b
 
@@ -86,11 +93,16 @@ def forward(cfg, p: Dict[str, Optional[torch.Tensor]], x: torch.Tensor,
     L.grouped_swiglu(cfg, E, T * k, F, b["offsets"], b["x_perm"], p["w1"], p["w2"], b["pre_gu"],
                      b["h"], b["out_perm"], ws, stream)
     y_s = None
+    gate = None
     if Fs > 0:
         L.grouped_swiglu(cfg, 1, T, Fs, None, x, p["w1_s"], p["w2_s"], b["pre_gu_s"], b["h_s"],
                          b["y_s"], ws, stream)
         y_s = b["y_s"]
-    L.unpermute_combine(cfg, b["out_perm"], b["row_of"], b["w"], y_s, b["y"], stream)
+        if p.get("w_gate_s") is not None:
+            L.shared_gate(cfg, x, p["w_gate_s"], b["gate_s"], stream)
+            gate = b["gate_s"]
+    L.unpermute_combine(cfg, b["out_perm"], b["row_of"], b["w"], y_s, b["y"], stream,
+                        shared_gate=gate)
     L.aux_loss(cfg, b["logits"], b["counts"], b["aux"], ws, stream)
     return b
 
@@ -106,15 +118,23 @@ def backward(cfg, p: Dict[str, Optional[torch.Tensor]], x: torch.Tensor, dy: tor
                          b["pre_gu"], b["h"], b["d_out_perm"], b["d_pre"], b["dx_perm"], b["dw1"],
                          b["dw2"], ws, stream)
     dx_s = None
+    gated = Fs > 0 and p.get("w_gate_s") is not None
     if Fs > 0:
+        dy_s = dy
+        if gated:
+            L.shared_gate_bwd(cfg, x, b["gate_s"], dy, b["y_s"], b["dy_s"], b["d_gate_logit_s"],
+                              b["dw_gate_s"], ws, stream)
+            dy_s = b["dy_s"]
         L.grouped_swiglu_bwd(cfg, 1, T, Fs, None, x, p["w1_s"], p["w2_s"], b["pre_gu_s"],
-                             b["h_s"], dy, b["d_pre_s"], b["dx_s"], b["dw1_s"], b["dw2_s"], ws,
+                             b["h_s"], dy_s, b["d_pre_s"], b["dx_s"], b["dw1_s"], b["dw2_s"], ws,
                              stream)
         dx_s = b["dx_s"]
     L.aux_loss_bwd(cfg, b["logits"], b["counts"], g_aux, b["d_logits"], 0, stream)
     L.route_topk_bwd(cfg, x, p["w_router"], b["logits"], b["idx"], b["dw"], b["d_logits"], 1,
                      b["dx_router"], b["dw_router"], ws, stream)
-    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], b["dx_router"], dx_s, b["dx"], stream)
+    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], b["dx_router"], dx_s, b["dx"], stream,
+                  d_gate_logit=b["d_gate_logit_s"] if gated else None,
+                  w_gate=p["w_gate_s"] if gated else None)
     return b
 
 
@@ -124,4 +144,5 @@ def params_from_inputs(inp: Dict[str, Optional[torch.Tensor]]) -> Dict[str, Opti
     if inp.get("w1_s") is not None:
         p["w1_s"] = inp["w1_s"].unsqueeze(0)
         p["w2_s"] = inp["w2_s"].unsqueeze(0)
+        p["w_gate_s"] = inp.get("w_gate_s")
     return p

@@ -103,9 +103,9 @@ def test_null_and_misaligned_pointers_refused(L):
     cfg = _cfg(L)
     good = ctypes.c_void_p(0x10000)
     bad = ctypes.c_void_p(0x10008)
-    rc = L.lib.moe_unpermute_combine(ctypes.byref(cfg), None, good, good, None, good, None)
+    rc = L.lib.moe_unpermute_combine(ctypes.byref(cfg), None, good, good, None, None, good, None)
     assert rc == L.MOE_ERR_INVALID_ARG
-    rc = L.lib.moe_unpermute_combine(ctypes.byref(cfg), bad, good, good, None, good, None)
+    rc = L.lib.moe_unpermute_combine(ctypes.byref(cfg), bad, good, good, None, None, good, None)
     assert rc == L.MOE_ERR_ALIGN
     rc = L.lib.moe_permute(ctypes.byref(cfg), good, good, good, good, good, good, good, good, 0,
                            None)
@@ -121,6 +121,22 @@ def test_status_strings_and_timeout_setter(L):
 
 
 def test_cfg_struct_layout(L):
-    # int64 T, seven int32, two floats: 44 bytes, padded to 48 like the C struct
-    assert ctypes.sizeof(L.MoeCfg) == 48
+    # int64 T, seven int32, two floats, the activation (int32 + four floats): 64 bytes
+    assert ctypes.sizeof(L.MoeCfg) == 64
     assert L.MoeCfg.scaling.offset == 36 and L.MoeCfg.aux_coeff.offset == 40
+
+
+def test_activation_settings_validated(L):
+    ok = [dict(act_fn="swiglu"), dict(act_fn="swiglu", glu_linear_offset=0.5),
+          dict(act_fn="swiglu_clamp", act_clamp=10.0),
+          dict(act_fn="situ_glu", act_gate_scale=4.0, act_linear_scale=25.0),
+          dict(act_fn="situ_glu", act_gate_scale=4.0)]
+    bad = [dict(act_fn="swiglu_clamp", act_clamp=0.0), dict(act_fn="swiglu_clamp", act_clamp=-1.0),
+           dict(act_fn="swiglu_clamp", act_clamp=float("inf")),
+           dict(act_fn="swiglu_clamp", act_clamp=10.0, glu_linear_offset=0.5),
+           dict(act_fn="situ_glu", act_gate_scale=0.0),
+           dict(act_fn="situ_glu", act_gate_scale=4.0, act_linear_scale=-1.0)]
+    for kw in ok:
+        assert L.check_cfg(_cfg(L, **kw)) == L.MOE_OK, kw
+    for kw in bad:
+        assert L.check_cfg(_cfg(L, **kw)) == L.MOE_ERR_INVALID_ARG, kw

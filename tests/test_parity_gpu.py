@@ -38,6 +38,17 @@ SMALL = {
                                        F_shared=0),
     "presoftmax_small": mi.shrink(W["zipf_imbalance"], name="presoftmax_small",
                                   score="softmax_pre", T=257, d=128, E=32, k=4, F=64),
+    # expert activations (Handbook §3.4 "Activation") and the gated shared expert:
+    # a clamp value that clips about a sixth of the gate inputs (a bf16 value, so
+    # that the clip decisions on the stored bf16 pre-activations are unambiguous);
+    # SiTU-GLU with scales inside the activations' range and a linear offset
+    "clamp_small": mi.shrink(W["mixtral_style"], name="clamp_small", T=300, d=256, F=320,
+                             act_fn="swiglu_clamp", act_clamp=0.3125),
+    "situ_small": mi.shrink(W["fine_grained_64e"], name="situ_small", T=517, d=320, F=192,
+                            F_shared=128, act_fn="situ_glu", act_gate_scale=0.25,
+                            act_linear_scale=0.2, glu_linear_offset=0.1),
+    "gated_shared_small": mi.shrink(W["fine_grained_64e"], name="gated_shared_small", T=517,
+                                    d=320, F=192, F_shared=128, shared_gate=True),
 }
 # bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
@@ -123,6 +134,8 @@ def test_layer_parity(built, name, dt, impl):
     assert_close("out_perm", to_np(b["out_perm"])[gr], f["out_perm"][orow], tol)
     if wl.F_shared:
         assert_close("y_shared", b["y_s"], f["y_s"], tol)
+    if inp.get("w_gate_s") is not None:
+        assert_close("shared gate", b["gate_s"], f["gate_s"], TOL_F32)
     # S6, S7
     assert_close("y", to_np(b["y"])[ok], f["y"][ok], tol)
     aux = float(b["aux"].item())
@@ -142,6 +155,10 @@ def test_layer_parity(built, name, dt, impl):
         if wl.F_shared:
             assert_close("dW1_s", b["dw1_s"][0], g["dW1_s"], tol)
             assert_close("dW2_s", b["dw2_s"][0], g["dW2_s"], tol)
+    if inp.get("w_gate_s") is not None:
+        assert_close("d shared-gate logit", b["d_gate_logit_s"], g["d_gate_logit_s"], tol)
+        assert_close("dW_gate_s", b["dw_gate_s"], g["dW_gate_s"], tol)
+        assert_close("dy_s", b["dy_s"], g["dy_s"], tol)
     # experts that received no rows get an exactly zero weight gradient
     empty = np.nonzero(f["counts"] == 0)[0]
     for e in empty:
