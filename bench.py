@@ -73,6 +73,8 @@ def workload_desc(wl, backward):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi clocks, power and throttle reasons every 20 ms; stop() keeps
+    the samples taken inside the timed window (host monotonic time)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -86,7 +88,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -95,9 +97,9 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -105,22 +107,31 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons, power = [], None, set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for ts, ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-                power.append(float(parts[3]))
+                rows.append((ts, float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
+        inside = rows
+        if window is not None:
+            inside = [r for r in rows if window[0] <= r[0] <= window[1]]
+            if not inside and rows:  # a window shorter than the sampling period
+                mid = 0.5 * (window[0] + window[1])
+                inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for nm, v in zip(names, r[4]):
                 if v.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+        sm = [r[1] for r in inside]
+        power = [r[3] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": inside[-1][2] if inside else None,
                 "reasons": sorted(reasons), "samples": len(sm),
                 "power_w_max": max(power) if power else None}
 
@@ -370,6 +381,7 @@ def run_ours(args, ws, rank, local):
     L.kernel_timing(True)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    host_t0 = time.monotonic()
     t_start.record(stream)
     for i in range(K):
         ev[i][0].record(stream)
@@ -378,10 +390,11 @@ def run_ours(args, ws, rank, local):
             ev[i][j + 1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    host_t1 = time.monotonic()
     launches = L.launch_count() - launches0
     L.kernel_timing(False)
     ktimes = L.kernel_times()
-    clk = clocks.stop()
+    clk = clocks.stop(window=(host_t0, host_t1))
     if dist:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -409,7 +422,11 @@ def run_ours(args, ws, rank, local):
         wk = work.get(n, {})
         if "flops" in wk:
             e["tflops"] = round(wk["flops"] / (ms * 1e-3) / 1e12, 2)
-            if n in ("route", "route_bwd"):
+            if n == "route" and L.router_uses_tensor_cores(cfg):
+                # three bf16 MMAs per product (exact planes of the fp32 weight)
+                e["tensor_cores"] = True
+                e["tensor_frac"] = round(3 * e["tflops"] / peaks["bf16_tflops"], 4)
+            elif n in ("route", "route_bwd"):
                 e["fp32_alu_frac"] = round(e["tflops"] / fp32_peak, 4)
         if "bytes" in wk:
             e["gbs"] = round(wk["bytes"] / (ms * 1e-3) / 1e9, 1)
