@@ -63,6 +63,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(dist, value, device):
+    """The largest of every rank's value (the job's time is its slowest rank's);
+    the value itself when there is no process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world_size, tokens_per_rank, ms_per_step):
+    """Whole-job tokens/s: every rank processes its own tokens_per_rank per step
+    (replicas, weak scaling), and a step lasts as long as the slowest rank."""
+    return round(world_size * tokens_per_rank / (ms_per_step * 1e-3), 1)
+
+
 def workload_desc(wl, backward):
     s = (f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} top-{wl.k} {wl.score} F={wl.F}"
          f"{' shared F=' + str(wl.F_shared) if wl.F_shared else ''} {wl.act_dtype} "
@@ -397,11 +414,7 @@ def run_ours(args, ws, rank, local):
     clk = clocks.stop(window=(host_t0, host_t1))
     if dist:
         dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
     ms_per_step = total_ms / K
     stage_ms = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
                 for j, n in enumerate(names)}
@@ -487,7 +500,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clk,
         "peaks": dict(peaks, fp32_alu_tflops=round(fp32_peak, 2)),
     }
-    out["value"] = round(ws * T / (ms_per_step * 1e-3), 1)
+    out["value"] = job_throughput(ws, T, ms_per_step)
     if not args.no_extras:
         out["extras"] = time_extras(L, cfg, b, T, K)
 
@@ -526,14 +539,10 @@ def run_ours(args, ws, rank, local):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
         bi = xh.numel() * xh.element_size() + (dyh.numel() * dyh.element_size() if backward else 0)
         bo = yh.numel() * yh.element_size() + 4
-        out["e2e"] = {"value": round(ws * T / (e_ms / K * 1e-3), 1), "unit": UNIT,
+        out["e2e"] = {"value": job_throughput(ws, T, e_ms / K), "unit": UNIT,
                       "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                       "ms_per_step": round(e_ms / K, 4)}
         x, dy = x_saved, dy_saved
