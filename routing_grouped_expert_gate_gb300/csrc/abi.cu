@@ -1,6 +1,7 @@
 // The extern "C" entry points declared in include/moe.h: argument checks,
 // the device status word, workspace sizing, and the order in which each call
 // launches its kernels on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -168,7 +169,8 @@ static size_t grouped_bwd_ws(const moe_cfg& cfg) {
 }
 
 static size_t route_bwd_ws(const moe_cfg& cfg) {
-  return round256((size_t)route_bwd_splits(cfg) * cfg.E * cfg.d * sizeof(float));
+  const size_t simt = round256((size_t)route_bwd_splits(cfg) * cfg.E * cfg.d * sizeof(float));
+  return router_bwd_tc_shape(cfg) ? std::max(simt, round256(router_bwd_tc_ws_bytes(cfg))) : simt;
 }
 
 static size_t shared_gate_bwd_ws(const moe_cfg& cfg) {
@@ -654,6 +656,10 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
   const int dtx = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
   const int T = (int)cfg->T, E = cfg->E, d = cfg->d;
   MOE_LAUNCH(launch_router_scores_bwd(c, *cfg, logits, idx, dw, d_logits, accumulate));
+  if (T > 0 && router_bwd_tc_eligible(*cfg)) {
+    MOE_LAUNCH(launch_router_bwd_tc(c, *cfg, x, w_router, d_logits, dx_router, dw_router, ws));
+    return MOE_OK;
+  }
   if (T > 0) {
     SimtGemm a{};  // dx_router = d_logits · W_r   [T, d], K = E
     a.mode = kGroupNone; a.M = T; a.N = d; a.K = E;

@@ -44,6 +44,14 @@ cudaError_t launch_router_logits(const Ctx& c, const moe_cfg& cfg, const void* x
 size_t router_ws_bytes(const moe_cfg& cfg);
 bool router_tc_eligible(const moe_cfg& cfg);
 int router_set_impl(int impl);    // 0 tensor cores where eligible, 1 CUDA cores
+bool router_tensor_cores_enabled();
+// router backward on the tensor cores (router_bwd_tc.cu): dx_router and dW_r
+bool router_bwd_tc_shape(const moe_cfg& cfg);     // a shape the kernels take
+bool router_bwd_tc_eligible(const moe_cfg& cfg);  // shape, setting and driver allow it
+size_t router_bwd_tc_ws_bytes(const moe_cfg& cfg);
+cudaError_t launch_router_bwd_tc(const Ctx& c, const moe_cfg& cfg, const void* x,
+                                 const float* w_router, const float* d_logits, float* dx_router,
+                                 float* dw_router, void* ws);
 int router_set_fold(int fold_k);  // K elements per compensated window (multiple of 16)
 cudaError_t launch_router_logits_tc(const Ctx& c, const moe_cfg& cfg, const void* x_bf16,
                                     const float* w_router, const float* logit_bias,

@@ -309,6 +309,8 @@ size_t router_ws_bytes(const moe_cfg& cfg) {
 
 int router_set_impl(int impl) { return rtc::g_router_impl.exchange(impl); }
 
+bool router_tensor_cores_enabled() { return rtc::g_router_impl.load() == 0; }
+
 int router_set_fold(int fold_k) { return rtc::g_router_fold.exchange(fold_k); }
 
 cudaError_t launch_router_logits_tc(const Ctx& c, const moe_cfg& cfg, const void* x,
