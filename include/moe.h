@@ -260,7 +260,11 @@ int moe_unpermute_combine_bwd(const moe_cfg* cfg, const void* dy, const void* ou
  *   pre_gu [n_rows, 2F] and h [n_rows, F] from the forward; d_out [n_rows, d]
  *   d_pre [n_rows, 2F] act dtype out; dx_rows [n_rows, d] act dtype out;
  *   dw1 [n_groups, 2F, d], dw2 [n_groups, d, F] act dtype out (fp32 sums).
- *   ws >= moe_workspace_bytes(cfg, MOE_WS_GROUPED_BWD)                     */
+ *   ws >= moe_workspace_bytes(cfg, MOE_WS_GROUPED_BWD)
+ * On the tensor cores with d < 4096 and a workspace of at least n_rows·F·2
+ * bytes, dh is stored in bf16 and the activation's derivative runs as a
+ * separate elementwise pass (a short-K tile cannot hide it); otherwise it
+ * runs in the dgrad epilogue on the fp32 accumulators.                     */
 int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows,
                            int32_t F, const int32_t* offsets, const void* x_rows,
                            const void* w1, const void* w2, const void* pre_gu,

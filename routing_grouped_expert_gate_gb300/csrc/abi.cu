@@ -456,7 +456,7 @@ int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows,
     int err = MOE_OK;
     MOE_LAUNCH(launch_tc_grouped_swiglu_bwd(c, n_groups, n_rows, F, d, offsets, x_rows, w1, w2,
                                             pre_gu, h, d_out, d_pre, dx_rows, dw1, dw2, ws,
-                                            &err));
+                                            ws_bytes, &err));
     return err;
   }
   MOE_REQUIRE(ws_bytes >= need_dh, MOE_ERR_WORKSPACE);

@@ -924,6 +924,49 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// ---------------------------------------------------------------- SwiGLU backward, elementwise
+// d_pre[r] = [dh * d act/d g | dh * d act/d u] from dh [rows, F] and the stored
+// gate|up [rows, 2F] (bf16 each), 8 columns per thread with 16-byte accesses.
+__global__ void __launch_bounds__(256)
+glu_bwd_rows(const bf16* __restrict__ dh, const bf16* __restrict__ gu, bf16* __restrict__ d_pre,
+             int64_t rows, int F, GluAct act) {
+  const int per_row = F >> 3;
+  const int64_t n = rows * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int f = (int)(i - r * per_row) * 8;
+    float d8[8], g8[8], u8[8], dg[8], du[8];
+    load_bf16x8(dh + r * F + f, d8);
+    load_bf16x8(gu + r * 2 * F + f, g8);
+    load_bf16x8(gu + r * 2 * F + F + f, u8);
+    if (glu_is_plain(act)) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float sg = 1.f / (1.f + __expf(-g8[j]));
+        dg[j] = d8[j] * u8[j] * sg * (1.f + g8[j] * (1.f - sg));
+        du[j] = d8[j] * g8[j] * sg;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) glu_bwd(g8[j], u8[j], d8[j], act, dg[j], du[j]);
+    }
+    store_bf16x8(d_pre + r * 2 * F + f, dg);
+    store_bf16x8(d_pre + r * 2 * F + F + f, du);
+  }
+}
+
+static cudaError_t launch_glu_bwd_rows(const Ctx& c, const bf16* dh, const bf16* gu, bf16* d_pre,
+                                       int64_t rows, int F) {
+  const int64_t n = rows * (F / 8);
+  const int64_t blocks = (n + 255) / 256;
+  const int64_t cap = (int64_t)c.sm_count * 16;
+  glu_bwd_rows<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, c.stream>>>(dh, gu, d_pre, rows,
+                                                                              F, c.act);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- host side
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::mutex g_mu;
@@ -1172,13 +1215,19 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
                                          const int32_t* offsets, const void* x_rows,
                                          const void* w1, const void* w2, const void* pre_gu,
                                          const void* h, const void* d_out, void* d_pre,
-                                         void* dx_rows, void* dw1, void* dw2, void*, int* err) {
+                                         void* dx_rows, void* dw1, void* dw2, void* ws,
+                                         size_t ws_bytes, int* err) {
   using namespace tc;
   *err = MOE_OK;
   CUtensorMap mA, mB;
   cudaError_t e;
   if (n_rows > 0) {
-    // fc2 dgrad + SwiGLU backward: A = d_out [n_rows, d] K-major; B = W2 [G*d, F] MN-major
+    // fc2 dgrad: A = d_out [n_rows, d] K-major; B = W2 [G*d, F] MN-major. With a
+    // short K (d < 4096) a tile's MMAs do not hide the SwiGLU-backward
+    // epilogue, so the GEMM stores dh (bf16) and an elementwise pass applies
+    // the derivative; with d >= 4096 the derivative runs in the epilogue.
+    const size_t dh_bytes = ((size_t)n_rows * F * 2 + 255) & ~(size_t)255;
+    const bool split = d < 4096 && ws != nullptr && ws_bytes >= dh_bytes;
     if (!make_map(&mA, d_out, n_rows, d, 128) || !make_map(&mB, w2, (int64_t)G * d, F, 64)) {
       *err = MOE_ERR_CUDA;
       return cudaSuccess;
@@ -1189,11 +1238,21 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     P.N_out = F;
     P.NT = (F + BN - 1) / BN;
     P.b_group_rows = d;
-    P.out0 = static_cast<bf16*>(d_pre);
-    P.aux_in = static_cast<const bf16*>(pre_gu);
     const bool pair = use_pair(G, n_rows);
-    e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
-             : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
+    if (split) {
+      P.out0 = static_cast<bf16*>(ws);
+      P.ld0 = F;
+      e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_STORE>(c, mA, mB, P, kFc2Dgrad);
+      if (e != cudaSuccess) return e;
+      e = launch_glu_bwd_rows(c, static_cast<const bf16*>(ws), static_cast<const bf16*>(pre_gu),
+                              static_cast<bf16*>(d_pre), n_rows, F);
+    } else {
+      P.out0 = static_cast<bf16*>(d_pre);
+      P.aux_in = static_cast<const bf16*>(pre_gu);
+      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
+    }
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
     if (!make_map(&mA, d_pre, n_rows, 2 * F, 128) || !make_map(&mB, w1, (int64_t)G * 2 * F, d, 64)) {

@@ -175,7 +175,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int n_groups, int64_t n_r
                                          const void* w1, const void* w2, const void* pre_gu,
                                          const void* h, const void* d_out, void* d_pre,
                                          void* dx_rows, void* dw1, void* dw2, void* ws,
-                                         int* err);
+                                         size_t ws_bytes, int* err);
 size_t tc_grouped_ws_bytes(int n_groups);
 // kernel kinds of the grouped GEMM, for per-kernel timing
 enum TcKind { kFc1Fwd = 0, kFc2Fwd, kFc2Dgrad, kFc1Dgrad, kFc2Wgrad, kFc1Wgrad, kTcKinds };
