@@ -108,7 +108,9 @@ aux_finalize(const float* __restrict__ part, int64_t nblk, const int32_t* __rest
   __shared__ double term[kMaxE];
   const int e = threadIdx.x;
   if (e < E) {
+    // fixed block order; the loads run ahead of the dependent adds
     double col = 0.0;
+#pragma unroll 8
     for (int64_t b = 0; b < nblk; ++b) col += (double)part[b * E + e];
     term[e] = col * (double)counts[e];
   }
@@ -219,6 +221,7 @@ __global__ void z_finalize(const double* __restrict__ part, int64_t nblk, int64_
                            float* __restrict__ z) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   double v = 0.0;
+#pragma unroll 8
   for (int64_t b = 0; b < nblk; ++b) v += part[b];
   *z = (T > 0) ? (float)((double)coeff * v / (double)T) : 0.f;
 }
