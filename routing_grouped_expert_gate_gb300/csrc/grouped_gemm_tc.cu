@@ -56,6 +56,9 @@ constexpr int NUM_EPI_WARPS = 8;                 // two per TMEM lane quadrant
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // producer, MMA, epilogue warps
 constexpr int TMEM_COLS = 512;
 constexpr int MAXG = 256;
+// per epilogue warp: one 32 x 32 bf16 output box staged for a TMA store
+constexpr int EPI_BOX_BYTES = 32 * 32 * 2;
+constexpr int EPI_BUF_BYTES = NUM_EPI_WARPS * EPI_BOX_BYTES;  // 16 KB
 
 enum Epi { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_WGRAD = 3 };
 
@@ -76,6 +79,7 @@ struct Params {
   int* status;
   uint64_t timeout_ns;
   GluAct act;         // expert activation (SwiGLU epilogues)
+  int tma_out;        // 1: plain outputs go out through the output tensor map
 };
 
 struct __align__(8) Shared {
@@ -115,6 +119,45 @@ __device__ __forceinline__ void load_bf16x8(const bf16* p, float* v) {
     float2 f = __bfloat1622float2(h[i]);
     v[2 * i] = f.x;
     v[2 * i + 1] = f.y;
+  }
+}
+
+// One row (thread = lane = row) of a 32 x 32 bf16 box into the warp's staging
+// buffer, laid out as the output tensor map's 64-byte swizzle expects: the
+// 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3) of the row's 64
+// bytes. Eight consecutive rows then cover all 32 banks, so the warp's 16-byte
+// stores are free of bank conflicts. The buffer is 1024-byte aligned.
+__device__ __forceinline__ void stage_box_row(uint32_t buf, int lane, const float* v) {
+  const uint32_t row = buf + (uint32_t)lane * 64u;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((uint32_t)(j ^ sw) << 4)),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                 : "memory");
+  }
+}
+
+// Store the warp's 32 rows x 32 columns through its staging buffer: wait until
+// the previous box has left the buffer, stage, hand it to the TMA unit. The
+// tensor map clips rows and columns outside the output.
+template <bool K3D>
+__device__ __forceinline__ void store_box(const CUtensorMap* map, uint32_t buf, int lane,
+                                          const float* v, int x, int y, int z) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  stage_box_row(buf, lane, v);
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    if (K3D) tma_store_3d(map, buf, x, y, z);
+    else tma_store_2d(map, buf, x, y);
   }
 }
 
@@ -172,7 +215,8 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
 // with tcgen05.ld (all lanes of the warp together) and write the outputs.
 template <int EPI>
 __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
-                                           int row_in_tile, int half) {
+                                           int row_in_tile, int half, const CUtensorMap* tmC,
+                                           uint32_t ebuf) {
   // the two warps of a lane quadrant split the accumulator's columns in halves
   if (EPI == EPI_SWIGLU_FWD) {
     const int r = ti.m0 + row_in_tile;
@@ -210,11 +254,17 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
   } else if (EPI == EPI_STORE) {
     const int r = ti.m0 + row_in_tile;
     const bool rv = r < ti.m_end;
+    // the warp's 32 rows all in the segment: whole boxes through the TMA unit
+    const int lane = row_in_tile & 31;
+    const int y0 = r - lane;
+    const bool boxed = P.tma_out && y0 + 32 <= ti.m_end;
 #pragma unroll 1
     for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
       float v[32];
       tmem_ld32(t_row + c, v);
-      if (rv) {
+      if (boxed) {
+        if (ti.n0 + c < P.N_out) store_box<false>(tmC, ebuf, lane, v, ti.n0 + c, y0, 0);
+      } else if (rv) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (ti.n0 + c + 8 * j < P.N_out)
@@ -291,12 +341,16 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
   } else {  // EPI_WGRAD
     const int m = ti.m0 + row_in_tile;
     const bool rv = m < P.M_out;
+    const int lane = row_in_tile & 31;
     bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
 #pragma unroll 1
     for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
       float v[32];
       tmem_ld32(t_row + c, v);
-      if (rv) {
+      if (P.tma_out) {
+        if (ti.n0 + c < P.N_out && m - lane < P.M_out)
+          store_box<true>(tmC, ebuf, lane, v, ti.n0 + c, m - lane, ti.grp);
+      } else if (rv) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (ti.n0 + c + 8 * j < P.N_out) store_bf16x8(dst_row + ti.n0 + c + 8 * j, v + 8 * j);
@@ -305,18 +359,39 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
   }
 }
 
+// An empty expert's weight-gradient tile: zeros, without touching TMEM.
+__device__ __forceinline__ void zero_wgrad_tile(const Params& P, const Tile& ti, int row_in_tile,
+                                                int half, const CUtensorMap* tmC, uint32_t ebuf) {
+  const int m = ti.m0 + row_in_tile;
+  if (P.tma_out) {
+    const int lane = row_in_tile & 31;
+    float z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32)
+      if (ti.n0 + c < P.N_out && m - lane < P.M_out)
+        store_box<true>(tmC, ebuf, lane, z, ti.n0 + c, m - lane, ti.grp);
+  } else if (m < P.M_out) {
+    bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
+    const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 8)
+      if (ti.n0 + c < P.N_out) store_bf16x8(dst_row + ti.n0 + c, z);
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const Params P) {
+                const __grid_constant__ CUtensorMap tmC, const Params P) {
   constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled stages
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
-  Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi_buf = smem + STAGES * STAGE_BYTES;  // 1024-byte aligned
+  Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES + EPI_BUF_BYTES);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -473,16 +548,22 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tc_fence_after();
         uint8_t* a_s = stage_base + stage * STAGE_BYTES;
         uint8_t* b_s = a_s + A_STAGE_BYTES;
+        int nkk = BK / 16;  // K16 steps of this stage that hold rows of the segment
         if (KGROUPED && kb == ti.nk - 1) {
-          // rows past the segment end belong to the next expert: zero them in A
+          // rows past the segment end belong to the next expert: the K16 steps
+          // wholly past it are not issued, and the rest of the last partial one
+          // is zeroed in A
           const int valid = ti.k_end - (ti.k_begin + kb * BK);
           if (valid < BK) {
-            for (int half = 0; half < 2; ++half) {
-              uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
-              const int n16 = (BK - valid) * 8;
-              for (int i = lane; i < n16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+            nkk = (valid + 15) >> 4;
+            const int n16 = (nkk * 16 - valid) * 8;
+            if (n16 > 0) {
+              for (int half = 0; half < 2; ++half) {
+                uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
+                for (int i = lane; i < n16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+              }
+              fence_async_shared();
             }
-            fence_async_shared();
             __syncwarp();
           }
         }
@@ -490,6 +571,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const uint32_t a_addr = su32(a_s), b_addr = su32(b_s);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= nkk) break;
             uint64_t ad, bd;
             if (!A_MN) ad = sw128_desc(a_addr + kk * 32, 16, 1024);
             else ad = sw128_desc(a_addr + kk * 2048, 8192, 1024);
@@ -513,32 +595,26 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
     const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
+    const uint32_t ebuf = su32(epi_buf) + (uint32_t)(warp - 2) * EPI_BOX_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
-      if (EPI == EPI_WGRAD) {
-        const int m = ti.m0 + row_in_tile;
-        bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
-        if (ti.nk == 0) {
-          if (m < P.M_out) {
-            const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 8)
-              if (ti.n0 + c < P.N_out) store_bf16x8(dst_row + ti.n0 + c, z);
-          }
-          continue;
-        }
+      if (EPI == EPI_WGRAD && ti.nk == 0) {
+        zero_wgrad_tile(P, ti, row_in_tile, half, &tmC, ebuf);
+        continue;
       }
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 4)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
-      drain_tile<EPI>(P, ti, t_row, row_in_tile, half);
+      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, ebuf);
       tc_fence_before();
       mbar_arrive(&sh.tmem_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed
   }
 
   tc_fence_before();
@@ -697,13 +773,15 @@ __device__ __forceinline__ Tile decode_pair_tile(const Shared2& sh, const Params
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const Params P) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const Params P) {
   constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stage_base = smem;
-  Shared2& sh = *reinterpret_cast<Shared2*>(smem + STAGES2 * STAGE2_BYTES);
+  uint8_t* epi_buf = smem + STAGES2 * STAGE2_BYTES;  // 1024-byte aligned
+  Shared2& sh = *reinterpret_cast<Shared2*>(smem + STAGES2 * STAGE2_BYTES + EPI_BUF_BYTES);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -839,21 +917,27 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
           if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 13)) { aborted = true; break; }
           tc_fence_after();
           uint8_t* a_s = stage_base + stage * STAGE2_BYTES;
+          int nkk = BK / 16;  // K16 steps of this stage that hold rows of the segment
           if (KGROUPED && kb == ti.nk - 1) {
-            // K rows past the segment end belong to the next expert: zero them in
-            // both CTAs' A (this CTA's directly, the peer's through DSMEM)
+            // K rows past the segment end belong to the next expert: the K16
+            // steps wholly past it are not issued, and the rest of the last
+            // partial one is zeroed in both CTAs' A (this CTA's directly, the
+            // peer's through DSMEM)
             const int valid = ti.k_end - (ti.k_begin + kb * BK);
             if (valid < BK) {
-              const int n16 = (BK - valid) * 8;
-              for (int half = 0; half < 2; ++half) {
-                uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
-                const uint32_t zp = mapa_shared(su32(z), 1u);
-                for (int i = lane; i < n16; i += 32) {
-                  z[i] = make_uint4(0, 0, 0, 0);
-                  st_shared_cluster_zero16(zp + 16u * i);
+              nkk = (valid + 15) >> 4;
+              const int n16 = (nkk * 16 - valid) * 8;
+              if (n16 > 0) {
+                for (int half = 0; half < 2; ++half) {
+                  uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
+                  const uint32_t zp = mapa_shared(su32(z), 1u);
+                  for (int i = lane; i < n16; i += 32) {
+                    z[i] = make_uint4(0, 0, 0, 0);
+                    st_shared_cluster_zero16(zp + 16u * i);
+                  }
                 }
+                fence_async_shared_cluster();
               }
-              fence_async_shared_cluster();
               __syncwarp();
             }
           }
@@ -862,6 +946,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
             const uint32_t b_addr = a_addr + A2_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
+              if (kk >= nkk) break;
               const uint64_t ad = A_MN ? sw128_desc(a_addr + kk * 2048, 8192, 1024)
                                        : sw128_desc(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? sw128_desc(b_addr + kk * 2048, 8192, 1024)
@@ -885,29 +970,25 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     const uint32_t empty_base = mapa_shared(su32(&sh.tmem_empty[0]), 0);
+    const uint32_t ebuf = su32(epi_buf) + (uint32_t)(warp - 2) * EPI_BOX_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster_id; t < total; t += n_clusters) {
       const Tile ti = decode_pair_tile<KGROUPED, EPI>(sh, P, t, rank);
       if (KGROUPED && ti.nk == 0) {
-        const int m = ti.m0 + row_in_tile;
-        if (m < P.M_out) {
-          bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
-          const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 8)
-            if (ti.n0 + c < P.N_out) store_bf16x8(dst_row + ti.n0 + c, z);
-        }
+        zero_wgrad_tile(P, ti, row_in_tile, half, &tmC, ebuf);
         continue;
       }
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      drain_tile<EPI>(P, ti, t_row, row_in_tile, half);
+      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, ebuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(empty_base + acc * 8);
       if (++acc == PAIR_ACC) { acc = 0; acc_phase ^= 1; }
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed
   }
 
   if (aborted || *reinterpret_cast<volatile int*>(&sh.abort)) {
@@ -1002,7 +1083,34 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
   return make_map_bf16(m, base, rows, cols, box_rows);
 }
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Shared);
+// Output maps for the epilogues' TMA stores: bf16, 32 x 32 boxes, 64-byte
+// swizzle (the staging layout of stage_box_row). The M-grouped epilogue
+// (EPI_STORE) issues 2-D stores into [rows, cols] with a row pitch of `ld`
+// elements; the weight-gradient epilogue issues 3-D stores into a dense
+// [G][rows][cols]. False (plain stores then) when the address or the pitch is
+// not a multiple of 16 bytes.
+static bool make_out_map(CUtensorMap* m, void* base, int rank, int64_t G, int64_t rows,
+                         int64_t cols, int64_t ld) {
+  if (base == nullptr || rows <= 0 || cols <= 0 || G <= 0 || (rank != 2 && rank != 3) ||
+      (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (ld * 2) % 16 != 0 || !get_encoder())
+    return false;
+  cuuint64_t gdim[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)G};
+  cuuint64_t gstride[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(ld * 2 * rows)};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t estride[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, base, gdim, gstride,
+                        box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+static bool make_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
+  return make_out_map(m, base, 2, 1, rows, cols, ld);
+}
+static bool make_wgrad_map(CUtensorMap* m, void* base, int64_t G, int64_t rows, int64_t cols) {
+  return make_out_map(m, base, 3, G, rows, cols, cols);
+}
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BUF_BYTES + sizeof(Shared);
 
 // ---- optional per-kernel timing (CUDA events on the launching stream)
 struct KernelTiming {
@@ -1035,7 +1143,7 @@ static void timing_mark(int kind, cudaStream_t s, bool start) {
 
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
-                              const Params& P, int kind) {
+                              const CUtensorMap& mc, const Params& P, int kind) {
   auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   int dev = 0;
@@ -1048,14 +1156,14 @@ static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtenso
     attr_set_mask.fetch_or(bit);
   }
   timing_mark(kind, c.stream, true);
-  kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, P);
+  kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, mc, P);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   timing_mark(kind, c.stream, false);
   return e;
 }
 
-constexpr size_t kSmemBytes2 = 1024 + (size_t)STAGES2 * STAGE2_BYTES + sizeof(Shared2);
+constexpr size_t kSmemBytes2 = 1024 + (size_t)STAGES2 * STAGE2_BYTES + EPI_BUF_BYTES + sizeof(Shared2);
 
 // 0: CTA pairs for long segments (default); 1: single CTAs only; 2: CTA pairs always
 static std::atomic<int> g_tc_mode{0};
@@ -1070,7 +1178,7 @@ static bool use_pair(int G, int64_t n_rows) {
 
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
-                               const Params& P, int kind) {
+                               const CUtensorMap& mc, const Params& P, int kind) {
   auto kern = tc_grouped_gemm_pair<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   static int max_clusters[64];
@@ -1104,7 +1212,7 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
   }
   cfg.gridDim = dim3(2 * max_clusters[dev & 63]);
   timing_mark(kind, c.stream, true);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, P);
   note_launches(1);
   timing_mark(kind, c.stream, false);
   return e;
@@ -1192,8 +1300,8 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
   const bool pair = use_pair(G, n_rows);
-  cudaError_t e = pair ? launch_pair<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd)
-                       : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, P, kFc1Fwd);
+  cudaError_t e = pair ? launch_pair<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mA, P, kFc1Fwd)
+                       : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mA, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
   // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
   if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, pair ? 128 : 256)) {
@@ -1207,8 +1315,11 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   Q.b_group_rows = d;
   Q.out0 = static_cast<bf16*>(out);
   Q.ld0 = d;
-  return pair ? launch_pair<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd)
-              : launch_one<false, false, EPI_STORE>(c, mA, mB, Q, kFc2Fwd);
+  CUtensorMap mC;
+  Q.tma_out = make_store_map(&mC, out, n_rows, d, d);
+  if (!Q.tma_out) mC = mA;
+  return pair ? launch_pair<false, false, EPI_STORE>(c, mA, mB, mC, Q, kFc2Fwd)
+              : launch_one<false, false, EPI_STORE>(c, mA, mB, mC, Q, kFc2Fwd);
 }
 
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
@@ -1219,7 +1330,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
                                          size_t ws_bytes, int* err) {
   using namespace tc;
   *err = MOE_OK;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mC;
   cudaError_t e;
   if (n_rows > 0) {
     // fc2 dgrad: A = d_out [n_rows, d] K-major; B = W2 [G*d, F] MN-major. With a
@@ -1242,16 +1353,18 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     if (split) {
       P.out0 = static_cast<bf16*>(ws);
       P.ld0 = F;
-      e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_STORE>(c, mA, mB, P, kFc2Dgrad);
+      P.tma_out = make_store_map(&mC, ws, n_rows, F, F);
+      if (!P.tma_out) mC = mA;
+      e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, P, kFc2Dgrad);
       if (e != cudaSuccess) return e;
       e = launch_glu_bwd_rows(c, static_cast<const bf16*>(ws), static_cast<const bf16*>(pre_gu),
                               static_cast<bf16*>(d_pre), n_rows, F);
     } else {
       P.out0 = static_cast<bf16*>(d_pre);
       P.aux_in = static_cast<const bf16*>(pre_gu);
-      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, P, kFc2Dgrad);
+      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, P, kFc2Dgrad);
     }
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
@@ -1266,8 +1379,10 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     Q.b_group_rows = 2 * F;
     Q.out0 = static_cast<bf16*>(dx_rows);
     Q.ld0 = d;
-    e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad)
-             : launch_one<false, true, EPI_STORE>(c, mA, mB, Q, kFc1Dgrad);
+    Q.tma_out = make_store_map(&mC, dx_rows, n_rows, d, d);
+    if (!Q.tma_out) mC = mA;
+    e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, Q, kFc1Dgrad)
+             : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, Q, kFc1Dgrad);
     if (e != cudaSuccess) return e;
   }
   // fc2 wgrad: dW2_g [d, F] = d_outᵀ h : A = d_out [n_rows, d] MN-major, B = h [n_rows, F] MN-major
@@ -1285,8 +1400,10 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   R.MT = wpair ? (d + 2 * BM - 1) / (2 * BM) : (d + BM - 1) / BM;
   R.NT = (F + BN - 1) / BN;
   R.out0 = static_cast<bf16*>(dw2);
-  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, R, kFc2Wgrad)
-            : launch_one<true, true, EPI_WGRAD>(c, mA, mB, R, kFc2Wgrad);
+  R.tma_out = make_wgrad_map(&mC, dw2, G, d, F);
+  if (!R.tma_out) mC = mA;
+  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, R, kFc2Wgrad)
+            : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, R, kFc2Wgrad);
   if (e != cudaSuccess) return e;
   // fc1 wgrad: dW1_g [2F, d] = d_preᵀ x : A = d_pre [n_rows, 2F] MN-major, B = x_rows MN-major
   if (!make_map(&mA, n_rows > 0 ? d_pre : w1, mr, 2 * F, 64) ||
@@ -1300,8 +1417,10 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   S.MT = wpair ? (2 * F + 2 * BM - 1) / (2 * BM) : (2 * F + BM - 1) / BM;
   S.NT = (d + BN - 1) / BN;
   S.out0 = static_cast<bf16*>(dw1);
-  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, S, kFc1Wgrad)
-               : launch_one<true, true, EPI_WGRAD>(c, mA, mB, S, kFc1Wgrad);
+  S.tma_out = make_wgrad_map(&mC, dw1, G, 2 * F, d);
+  if (!S.tma_out) mC = mA;
+  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, S, kFc1Wgrad)
+               : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, S, kFc1Wgrad);
 }
 
 }  // namespace moe
