@@ -264,7 +264,12 @@ int moe_unpermute_combine_bwd(const moe_cfg* cfg, const void* dy, const void* ou
  * On the tensor cores with d < 4096 and a workspace of at least n_rows·F·2
  * bytes, dh is stored in bf16 and the activation's derivative runs as a
  * separate elementwise pass (a short-K tile cannot hide it); otherwise it
- * runs in the dgrad epilogue on the fp32 accumulators.                     */
+ * runs in the dgrad epilogue on the fp32 accumulators. The last
+ * 2·n_groups·128 + 128 bytes of a workspace that has them hold per-group
+ * copies of the weight gradients' A tensor maps whose rows end at the
+ * group's end (built on the device each call), so that a group's last K
+ * block reads the next group's rows as zeros; without them those rows are
+ * zeroed in shared memory.                                                 */
 int moe_grouped_swiglu_bwd(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows,
                            int32_t F, const int32_t* offsets, const void* x_rows,
                            const void* w1, const void* w2, const void* pre_gu,

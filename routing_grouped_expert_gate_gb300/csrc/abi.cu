@@ -165,7 +165,7 @@ static size_t grouped_bwd_ws(const moe_cfg& cfg) {
     const size_t s = round256(rows_s * cfg.F_shared * sizeof(float));
     if (s > need) need = s;
   }
-  return need + round256(tc_grouped_ws_bytes(cfg.E));
+  return need + round256(tc_grouped_ws_bytes(cfg.E)) + round256(tc_tail_maps_bytes(cfg.E));
 }
 
 static size_t route_bwd_ws(const moe_cfg& cfg) {

@@ -80,6 +80,10 @@ struct Params {
   uint64_t timeout_ns;
   GluAct act;         // expert activation (SwiGLU epilogues)
   int tma_out;        // 1: plain outputs go out through the output tensor map
+  // K-grouped: per group, the A map with its rows ending at the group's last
+  // row (rows after it read as zeros), for the group's last K block; NULL =
+  // the MMA warp zeroes those rows in shared memory instead
+  const CUtensorMap* tail_maps;
 };
 
 struct __align__(8) Shared {
@@ -878,11 +882,19 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
           const uint32_t bar = mapa_shared(su32(&sh.full[stage]), 0);  // the even CTA's
           if (leader) mbar_expect_tx(&sh.full[stage], 2 * STAGE2_BYTES);
           const int k0 = kb * BK;
+          const CUtensorMap* amap = &tmA;
+          if (KGROUPED && P.tail_maps != nullptr && kb == ti.nk - 1 &&
+              ti.k_end - ti.k_begin - k0 < BK && ti.k_end < P.n_rows) {
+            // the expert's last block through its own map: the next expert's
+            // rows arrive as zeros (past the last row the common map does that)
+            amap = P.tail_maps + ti.grp;
+            tensormap_acquire(amap);
+          }
           if (!A_MN) {
-            tma_load_2d_pair(a_dst, &tmA, bar, k0, ti.m0);
+            tma_load_2d_pair(a_dst, amap, bar, k0, ti.m0);
           } else {
-            tma_load_2d_pair(a_dst, &tmA, bar, ti.m0, ti.k_begin + k0);
-            tma_load_2d_pair(a_dst + 8192, &tmA, bar, ti.m0 + 64, ti.k_begin + k0);
+            tma_load_2d_pair(a_dst, amap, bar, ti.m0, ti.k_begin + k0);
+            tma_load_2d_pair(a_dst + 8192, amap, bar, ti.m0 + 64, ti.k_begin + k0);
           }
           if (!B_MN) {
             int y;
@@ -921,13 +933,14 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
           if (KGROUPED && kb == ti.nk - 1) {
             // K rows past the segment end belong to the next expert: the K16
             // steps wholly past it are not issued, and the rest of the last
-            // partial one is zeroed in both CTAs' A (this CTA's directly, the
-            // peer's through DSMEM)
+            // partial one arrives as zeros through the expert's own A map, or
+            // without the maps is zeroed here in both CTAs' A (this CTA's
+            // directly, the peer's through DSMEM)
             const int valid = ti.k_end - (ti.k_begin + kb * BK);
             if (valid < BK) {
               nkk = (valid + 15) >> 4;
               const int n16 = (nkk * 16 - valid) * 8;
-              if (n16 > 0) {
+              if (n16 > 0 && P.tail_maps == nullptr) {
                 for (int half = 0; half < 2; ++half) {
                   uint4* z = reinterpret_cast<uint4*>(a_s + half * 8192 + valid * 128);
                   const uint32_t zp = mapa_shared(su32(z), 1u);
@@ -944,14 +957,21 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
           if (lane == 0) {
             const uint32_t a_addr = su32(a_s);
             const uint32_t b_addr = a_addr + A2_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              if (kk >= nkk) break;
+            auto issue = [&](int kk) {
               const uint64_t ad = A_MN ? sw128_desc(a_addr + kk * 2048, 8192, 1024)
                                        : sw128_desc(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? sw128_desc(b_addr + kk * 2048, 8192, 1024)
                                        : sw128_desc(b_addr + kk * 32, 16, 1024);
               mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            };
+            // a full stage as straight-line MMAs (measured: a bounds check in
+            // the unrolled loop slowed the weight gradients by about 7%)
+            if (nkk == BK / 16) {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) issue(kk);
+            } else {
+#pragma unroll 1
+              for (int kk = 0; kk < nkk; ++kk) issue(kk);
             }
             mma_commit_pair(&sh.empty[stage], 0x3);
           }
@@ -1046,6 +1066,39 @@ static cudaError_t launch_glu_bwd_rows(const Ctx& c, const bf16* dh, const bf16*
                                                                               F, c.act);
   note_launches(1);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- per-expert tail maps
+// For the weight gradients: per group g, copies of the two A maps (fc2: d_out,
+// fc1: d_pre) whose row extent is the group's end offset, so that a TMA load
+// of the group's last K block reads the following groups' rows as zeros. The
+// offsets are checked as the GEMM checks them (monotone, within n_rows); the
+// extent is at least 1 row.
+__global__ void __launch_bounds__(256)
+build_tail_maps(const __grid_constant__ CUtensorMap t0, const __grid_constant__ CUtensorMap t1,
+                const int32_t* __restrict__ offsets, int G, int n_rows, CUtensorMap* out) {
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    int end = offsets ? offsets[g + 1] : n_rows;
+    end = end < 1 ? 1 : (end > n_rows ? n_rows : end);
+    const uint4* s0 = reinterpret_cast<const uint4*>(&t0);
+    const uint4* s1 = reinterpret_cast<const uint4*>(&t1);
+    uint4* d0 = reinterpret_cast<uint4*>(out + g);
+    uint4* d1 = reinterpret_cast<uint4*>(out + G + g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      d0[i] = s0[i];
+      d1[i] = s1[i];
+    }
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(out + g)),
+                 "r"(end)
+                 : "memory");
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(out + G + g)),
+                 "r"(end)
+                 : "memory");
+  }
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- host side
@@ -1235,6 +1288,8 @@ bool tc_available() { return tc::get_encoder(); }
 
 size_t tc_grouped_ws_bytes(int) { return 0; }
 
+size_t tc_tail_maps_bytes(int n_groups) { return (size_t)2 * n_groups * sizeof(CUtensorMap) + 128; }
+
 int tc_set_mode(int mode) { return tc::g_tc_mode.exchange(mode); }
 
 int tc_timing_enable(int on) {
@@ -1332,6 +1387,15 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   *err = MOE_OK;
   CUtensorMap mA, mB, mC;
   cudaError_t e;
+  // the weight gradients' per-expert tail maps sit at the end of the workspace
+  const bool wpair = g_tc_mode.load() != 1;  // weight gradients: CTA pairs unless single-CTA
+  CUtensorMap* tail_maps = nullptr;
+  if (n_rows > 0 && wpair && ws != nullptr && ws_bytes >= tc_tail_maps_bytes(G)) {
+    const uintptr_t end = reinterpret_cast<uintptr_t>(ws) + ws_bytes;
+    tail_maps = reinterpret_cast<CUtensorMap*>((end - 2 * (size_t)G * sizeof(CUtensorMap)) &
+                                               ~(uintptr_t)127);
+    ws_bytes -= tc_tail_maps_bytes(G);
+  }
   if (n_rows > 0) {
     // fc2 dgrad: A = d_out [n_rows, d] K-major; B = W2 [G*d, F] MN-major. With a
     // short K (d < 4096) a tile's MMAs do not hide the SwiGLU-backward
@@ -1393,10 +1457,21 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     *err = MOE_ERR_CUDA;
     return cudaSuccess;
   }
+  if (tail_maps != nullptr) {
+    CUtensorMap mA1;  // fc1 wgrad's A: d_pre [n_rows, 2F]
+    if (!make_map(&mA1, d_pre, mr, 2 * F, 64)) {
+      *err = MOE_ERR_CUDA;
+      return cudaSuccess;
+    }
+    build_tail_maps<<<1, 256, 0, c.stream>>>(mA, mA1, offsets, G, (int)n_rows, tail_maps);
+    note_launches(1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   Params R = base_params(c, G, n_rows, offsets);
   R.M_out = d;
   R.N_out = F;
-  const bool wpair = g_tc_mode.load() != 1;  // weight gradients: CTA pairs unless single-CTA
+  R.tail_maps = tail_maps;
   R.MT = wpair ? (d + 2 * BM - 1) / (2 * BM) : (d + BM - 1) / BM;
   R.NT = (F + BN - 1) / BN;
   R.out0 = static_cast<bf16*>(dw2);
@@ -1414,6 +1489,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   Params S = base_params(c, G, n_rows, offsets);
   S.M_out = 2 * F;
   S.N_out = d;
+  S.tail_maps = tail_maps != nullptr ? tail_maps + G : nullptr;
   S.MT = wpair ? (2 * F + 2 * BM - 1) / (2 * BM) : (2 * F + BM - 1) / BM;
   S.NT = (d + BN - 1) / BN;
   S.out0 = static_cast<bf16*>(dw1);

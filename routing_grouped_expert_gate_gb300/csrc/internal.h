@@ -177,6 +177,9 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int n_groups, int64_t n_r
                                          void* dx_rows, void* dw1, void* dw2, void* ws,
                                          size_t ws_bytes, int* err);
 size_t tc_grouped_ws_bytes(int n_groups);
+// workspace the grouped backward uses, when present, for the weight
+// gradients' per-expert tail tensor maps (two per group)
+size_t tc_tail_maps_bytes(int n_groups);
 // kernel kinds of the grouped GEMM, for per-kernel timing
 enum TcKind { kFc1Fwd = 0, kFc2Fwd, kFc2Dgrad, kFc1Dgrad, kFc2Wgrad, kFc1Wgrad, kTcKinds };
 int tc_timing_enable(int on);
