@@ -660,7 +660,9 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
     MOE_LAUNCH(launch_router_bwd_tc(c, *cfg, x, w_router, d_logits, dx_router, dw_router, ws));
     return MOE_OK;
   }
-  if (T > 0) {
+  if (T > 0 && E <= 16) {
+    MOE_LAUNCH(launch_router_dx_small(c, *cfg, d_logits, w_router, dx_router));
+  } else if (T > 0) {
     SimtGemm a{};  // dx_router = d_logits · W_r   [T, d], K = E
     a.mode = kGroupNone; a.M = T; a.N = d; a.K = E;
     a.dtA = kF32; a.dtB = kF32; a.dtC = kF32;

@@ -73,6 +73,9 @@ cudaError_t launch_quantile_beta_update(const Ctx& c, const moe_cfg& cfg, float*
 // dW_r partials [splits][E][d] for E <= 16 (sum them in slice order)
 cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void* x,
                                    const float* d_logits, float* part, int splits);
+// dx_router = d_logits · W_r for E <= 16 (fp32, experts summed in order)
+cudaError_t launch_router_dx_small(const Ctx& c, const moe_cfg& cfg, const float* d_logits,
+                                   const float* w_router, float* dx_router);
 cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                      const int32_t* idx, const float* dw, float* d_logits,
                                      int accumulate);

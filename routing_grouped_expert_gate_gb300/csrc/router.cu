@@ -20,31 +20,46 @@
 namespace moe {
 
 // ------------------------------------------------------------------ S1, E <= 16
-// One warp per TPW tokens; lane l reads the 8-element groups l, l+32, ... of
-// the hidden dimension, so a token row is read once, 16 B per lane at a time.
-// The 32 lane partials are combined by a butterfly of compensated sums.
-template <typename Tx, int EMAX, int TPW>
+// One CTA per TB tokens. The 8 warps split the hidden dimension into eight
+// ranges of 8-element groups; lane l of warp w reads groups l, l+32, ... of
+// range w, so a token row is read once, 16 B per lane at a time, and every W
+// value a lane loads serves the CTA's TB tokens. Per lane, the products of up
+// to four groups (32 elements) are added in fp32 FMAs and folded into a
+// compensated (hi, lo) pair; the pairs are combined by a butterfly over the
+// lanes and then over the warps in warp order, every step a TwoSum, so the
+// result does not depend on scheduling. FOLD = false when no lane has more than
+// four groups (d <= 8192): its fp32 sum is then the chunk sum itself.
+template <typename Tx, int EMAX, int TB, bool FOLD>
 __global__ void __launch_bounds__(256)
 router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
                     const float* __restrict__ logit_bias, float* __restrict__ logits,
                     int64_t T, int d, int E) {
+  __shared__ float s_hi[8][TB * EMAX];
+  __shared__ float s_lo[8][TB * EMAX];
   const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t t0 = warp * TPW;
-  if (t0 >= T) return;
-
-  float hi[TPW][EMAX], lo[TPW][EMAX], acc[TPW][EMAX];
-#pragma unroll
-  for (int a = 0; a < TPW; ++a)
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = acc[a][e] = 0.f;
-
+  const int warp = threadIdx.x >> 5;
+  const int64_t t0 = (int64_t)blockIdx.x * TB;
   const int ngroups = d >> 3;
-  int cnt = 0;
-  for (int g = lane; g < ngroups; g += 32) {
-    float xv[TPW][8];
+  const int g_lo = (int)((int64_t)ngroups * warp / 8);
+  const int g_hi = (int)((int64_t)ngroups * (warp + 1) / 8);
+
+  float hi[TB][EMAX], lo[TB][EMAX], acc[TB][EMAX];
 #pragma unroll
-    for (int a = 0; a < TPW; ++a) {
+  for (int a = 0; a < TB; ++a)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[a][e] = 0.f;
+  if (FOLD) {
+#pragma unroll
+    for (int a = 0; a < TB; ++a)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = 0.f;
+  }
+
+  int cnt = 0;
+  for (int g = g_lo + lane; g < g_hi; g += 32) {
+    float xv[TB][8];
+#pragma unroll
+    for (int a = 0; a < TB; ++a) {
       if (t0 + a < T) {
         load8(x + (t0 + a) * (int64_t)d + 8 * g, xv[a]);
       } else {
@@ -58,14 +73,14 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
         float wv[8];
         load8(W + (int64_t)e * d + 8 * g, wv);
 #pragma unroll
-        for (int a = 0; a < TPW; ++a)
+        for (int a = 0; a < TB; ++a)
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[a][e] = fmaf(xv[a][i], wv[i], acc[a][e]);
       }
     }
-    if (++cnt == 4) {  // 32 elements per lane
+    if (FOLD && ++cnt == 4) {  // 32 elements per lane
 #pragma unroll
-      for (int a = 0; a < TPW; ++a)
+      for (int a = 0; a < TB; ++a)
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
           comp_add(hi[a][e], lo[a][e], acc[a][e]);
@@ -75,39 +90,57 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
     }
   }
 #pragma unroll
-  for (int a = 0; a < TPW; ++a)
+  for (int a = 0; a < TB; ++a)
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) comp_add(hi[a][e], lo[a][e], acc[a][e]);
+    for (int e = 0; e < EMAX; ++e) {
+      if (FOLD) {
+        comp_add(hi[a][e], lo[a][e], acc[a][e]);
+      } else {
+        hi[a][e] = acc[a][e];
+        lo[a][e] = 0.f;
+      }
+    }
 
   // Butterfly over lanes. Both partners compute the same (hi, lo): TwoSum's
   // error term is exact, hence symmetric in its operands.
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
-    for (int a = 0; a < TPW; ++a)
+    for (int a = 0; a < TB; ++a)
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) {
         float oh = __shfl_xor_sync(0xffffffffu, hi[a][e], off);
         float ol = __shfl_xor_sync(0xffffffffu, lo[a][e], off);
-        float s, er;
-        two_sum(hi[a][e], oh, s, er);
-        hi[a][e] = s;
+        float s2, er;
+        two_sum(hi[a][e], oh, s2, er);
+        hi[a][e] = s2;
         lo[a][e] = __fadd_rn(__fadd_rn(lo[a][e], ol), er);
       }
   }
+  if (lane == 0) {
 #pragma unroll
-  for (int a = 0; a < TPW; ++a) {
-    if (t0 + a >= T) break;
-    float v = 0.f;
+    for (int a = 0; a < TB; ++a)
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-      if (lane == e) {
-        float h = hi[a][e], l = lo[a][e];
-        if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
-        v = __fadd_rn(h, l);
+      for (int e = 0; e < EMAX; ++e) {
+        s_hi[warp][a * EMAX + e] = hi[a][e];
+        s_lo[warp][a * EMAX + e] = lo[a][e];
       }
+  }
+  __syncthreads();
+  // the eight warp partials of one logit, in warp order
+  for (int q = threadIdx.x; q < TB * EMAX; q += blockDim.x) {
+    const int a = q / EMAX, e = q - a * EMAX;
+    if (e >= E || t0 + a >= T) continue;
+    float h = s_hi[0][q], l = s_lo[0][q];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      float s2, er;
+      two_sum(h, s_hi[w][q], s2, er);
+      h = s2;
+      l = __fadd_rn(__fadd_rn(l, s_lo[w][q]), er);
     }
-    if (lane < E) logits[(t0 + a) * (int64_t)E + lane] = v;
+    if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
+    logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
   }
 }
 
@@ -559,11 +592,14 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
 // dW_r partials for few experts: part[s][e][c] = sum over the tokens of slice s
 // of d_logits[t][e] * x[t][c]. A thread owns 8 consecutive columns and every
 // expert; the d_logits row of a token is the same for the whole CTA (a
-// broadcast load). Slices are summed afterwards in slice order.
+// broadcast load). The tokens of a slice go in groups of U whose loads are
+// issued together, and are added in token order. Slices are summed afterwards
+// in slice order.
 template <typename Tx, int EMAX>
 __global__ void __launch_bounds__(128)
 router_dw_small(const Tx* __restrict__ x, const float* __restrict__ d_logits,
                 float* __restrict__ part, int64_t T, int d, int E, int64_t tok_per_slice) {
+  constexpr int U = EMAX <= 8 ? 4 : 2;
   const int c0 = (blockIdx.x * 128 + threadIdx.x) * 8;
   const int64_t t_beg = (int64_t)blockIdx.y * tok_per_slice;
   const int64_t t_end = t_beg + tok_per_slice < T ? t_beg + tok_per_slice : T;
@@ -573,7 +609,23 @@ router_dw_small(const Tx* __restrict__ x, const float* __restrict__ d_logits,
   for (int e = 0; e < EMAX; ++e)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[e][i] = 0.f;
-  for (int64_t t = t_beg; t < t_end; ++t) {
+  int64_t t = t_beg;
+  for (; t + U <= t_end; t += U) {
+    float xv[U][8], g[U][EMAX];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      load8(x + (t + u) * d + c0, xv[u]);
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) g[u][e] = e < E ? __ldg(d_logits + (t + u) * E + e) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[e][i] = fmaf(g[u][e], xv[u][i], acc[e][i]);
+  }
+  for (; t < t_end; ++t) {
     float xv[8];
     load8(x + t * d + c0, xv);
 #pragma unroll
@@ -609,6 +661,56 @@ cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void*
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ B3 dx, E <= 16
+// dx_router[t][c] = sum over e of d_logits[t][e] * W_r[e][c] (fp32, e in
+// order). A thread keeps W_r's 4 consecutive columns for every expert in
+// registers and walks the CTA's tokens; a warp writes 512 contiguous bytes of
+// a row at a time. grid.x covers d in 1024-column chunks, grid.y the tokens in
+// tiles of 32.
+template <int EMAX>
+__global__ void __launch_bounds__(256)
+router_dx_small(const float* __restrict__ d_logits, const float* __restrict__ W,
+                float* __restrict__ dx, int64_t T, int d, int E) {
+  constexpr int TT = 32;
+  const int c0 = (blockIdx.x * 256 + threadIdx.x) * 4;
+  if (c0 >= d) return;
+  float4 w[EMAX];
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+    w[e] = e < E ? __ldg(reinterpret_cast<const float4*>(W + (int64_t)e * d + c0))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t t_beg = (int64_t)blockIdx.y * TT;
+  const int64_t t_end = t_beg + TT < T ? t_beg + TT : T;
+  for (int64_t t = t_beg; t < t_end; ++t) {
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (e < E) {
+        const float g = __ldg(d_logits + t * E + e);
+        o.x = fmaf(g, w[e].x, o.x);
+        o.y = fmaf(g, w[e].y, o.y);
+        o.z = fmaf(g, w[e].z, o.z);
+        o.w = fmaf(g, w[e].w, o.w);
+      }
+    }
+    *reinterpret_cast<float4*>(dx + t * d + c0) = o;
+  }
+}
+
+cudaError_t launch_router_dx_small(const Ctx& c, const moe_cfg& cfg, const float* d_logits,
+                                   const float* w_router, float* dx_router) {
+  if (cfg.T == 0) return cudaSuccess;
+  dim3 grid((unsigned)((cfg.d / 4 + 255) / 256), (unsigned)((cfg.T + 31) / 32));
+  if (cfg.E <= 8)
+    router_dx_small<8><<<grid, 256, 0, c.stream>>>(d_logits, w_router, dx_router, cfg.T, cfg.d,
+                                                   cfg.E);
+  else
+    router_dx_small<16><<<grid, 256, 0, c.stream>>>(d_logits, w_router, dx_router, cfg.T,
+                                                    cfg.d, cfg.E);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ launchers
 template <typename Tx>
 static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, const Tx* x,
@@ -616,16 +718,22 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
                                           float* logits) {
   const int64_t T = cfg.T;
   if (T == 0) return cudaSuccess;
-  if (cfg.E <= 8) {
-    constexpr int TPW = 2;
-    const int64_t warps = (T + TPW - 1) / TPW;
-    router_logits_small<Tx, 8, TPW><<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
-        x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
-  } else if (cfg.E <= 16) {
-    constexpr int TPW = 1;
-    const int64_t warps = T;
-    router_logits_small<Tx, 16, TPW><<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
-        x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+  if (cfg.E <= 16) {
+    // groups of 8 per lane: d / 8 split over 8 warps of 32 lanes
+    const bool fold = (cfg.d / 8 + 255) / 256 > 4;
+    const unsigned grid8 = (unsigned)((T + 3) / 4), grid16 = (unsigned)((T + 1) / 2);
+    if (cfg.E <= 8 && !fold)
+      router_logits_small<Tx, 8, 4, false><<<grid8, 256, 0, c.stream>>>(x, w_router, logit_bias,
+                                                                        logits, T, cfg.d, cfg.E);
+    else if (cfg.E <= 8)
+      router_logits_small<Tx, 8, 4, true><<<grid8, 256, 0, c.stream>>>(x, w_router, logit_bias,
+                                                                       logits, T, cfg.d, cfg.E);
+    else if (!fold)
+      router_logits_small<Tx, 16, 2, false><<<grid16, 256, 0, c.stream>>>(
+          x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+    else
+      router_logits_small<Tx, 16, 2, true><<<grid16, 256, 0, c.stream>>>(
+          x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
   } else {
     // token tile: the largest that still gives every SM a CTA (a smaller tile
     // splits K inside the CTA and stages W once per fewer tokens)

@@ -205,6 +205,36 @@ def test_router_gate_gemm_paths(built, name, fold_k):
         L.set_router_fold(old_f)
 
 
+@pytest.mark.parametrize("E", [8, 16])
+@pytest.mark.parametrize("d", [4096, 8704])
+def test_small_router_hidden_sizes(built, E, d):
+    """The few-expert gate GEMM (E <= 16) on both of its accumulation forms:
+    one fp32 chunk per lane (d <= 8192) and 32-element chunks folded into
+    compensated pairs (d > 8192); a ragged token count that leaves the last
+    CTA partly empty. Logits within 1e-6 of the float64 oracle, the oracle's
+    experts selected."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = mi.shrink(W["mixtral_style"], name=f"router_e{E}_d{d}", T=37, d=d, E=E, F=64)
+    inp = mi.make_inputs(wl, seed=5, device="cuda", with_dy=False)
+    cfg = moe.cfg_from_workload(wl)
+    ref = {k: O.as_f64(v) for k, v in inp.items() if v is not None}
+    r = O.route(ref["x"], ref["w_router"], wl.k, wl.score, wl.scaling, ref.get("logit_bias"),
+                ref.get("sel_bias"))
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_ROUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+    logits = torch.full((wl.T, wl.E), float("nan"), device="cuda")
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.T, wl.k, device="cuda")
+    L.route_topk(cfg, inp["x"], inp["w_router"], None, None, logits, idx, w, ws)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    err = float(np.max(np.abs(to_np(logits) - r["logits"])))
+    assert err < 1e-6, err
+    decided = r["gap"] >= 1e-6
+    assert np.array_equal(to_np(idx)[decided], r["idx"][decided])
+
+
 def test_zero_load_experts_exist_in_skewed_case(built):
     wl = SMALL["zipf_small"]
     inp = mi.make_inputs(wl, seed=0)
