@@ -102,25 +102,41 @@ aux_partials(const float* __restrict__ logits, int64_t T, int E, int score_fn,
   }
 }
 
-__global__ void __launch_bounds__(256)
+// 1024 threads: thread (j, e) sums the block partials b = j, j + J, j + 2J,
+// ... of column e in fp64 (J = 1024 / E lanes of a column), the J sums of a
+// column are added in j order, and the E terms by a fixed pairwise tree: the
+// same order on every run, with dependent fp64 chains J times shorter than one
+// thread per column would give.
+__global__ void __launch_bounds__(1024)
 aux_finalize(const float* __restrict__ part, int64_t nblk, const int32_t* __restrict__ counts,
              int64_t T, int E, int k, float coeff, float* __restrict__ aux) {
+  __shared__ double colj[1024];
   __shared__ double term[kMaxE];
-  const int e = threadIdx.x;
-  if (e < E) {
-    // fixed block order; the loads run ahead of the dependent adds
+  const int J = E > 0 ? (1024 / E > 0 ? 1024 / E : 1) : 1;
+  for (int q = threadIdx.x; q < J * E; q += blockDim.x) {
+    const int j = q / E, e = q - j * E;
+    double v = 0.0;
+#pragma unroll 4
+    for (int64_t b = j; b < nblk; b += J) v += (double)part[b * E + e];
+    colj[q] = v;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     double col = 0.0;
-#pragma unroll 8
-    for (int64_t b = 0; b < nblk; ++b) col += (double)part[b * E + e];
+    for (int j = 0; j < J; ++j) col += colj[j * E + e];
     term[e] = col * (double)counts[e];
   }
   __syncthreads();
+  // pairwise tree over the E terms (E <= 256)
+  for (int width = 1; width < E; width <<= 1) {
+    for (int i = threadIdx.x * 2 * width; i + width < E; i += blockDim.x * 2 * width)
+      term[i] += term[i + width];
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
-    double acc = 0.0;
-    for (int i = 0; i < E; ++i) acc += term[i];
     const double scale =
         (T > 0) ? (double)coeff * (double)E / ((double)k * (double)T * (double)T) : 0.0;
-    *aux = (float)(acc * scale);
+    *aux = (float)((E > 0 ? term[0] : 0.0) * scale);
   }
 }
 
@@ -539,8 +555,8 @@ cudaError_t launch_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logit
     }
 #undef MOE_AUXP
   }
-  aux_finalize<<<1, 256, 0, c.stream>>>(part, nblk, counts, cfg.T, cfg.E, cfg.k, cfg.aux_coeff,
-                                        aux);
+  aux_finalize<<<1, 1024, 0, c.stream>>>(part, nblk, counts, cfg.T, cfg.E, cfg.k, cfg.aux_coeff,
+                                         aux);
   note_launches(nblk > 0 ? 2 : 1);
   return cudaGetLastError();
 }

@@ -25,8 +25,8 @@ namespace moe {
 // range w, so a token row is read once, 16 B per lane at a time, and every W
 // value a lane loads serves the CTA's TB tokens. Per lane, the products of up
 // to four groups (32 elements) are added in fp32 FMAs and folded into a
-// compensated (hi, lo) pair; the pairs are combined by a butterfly over the
-// lanes and then over the warps in warp order, every step a TwoSum, so the
+// compensated (hi, lo) pair; the pairs are combined by a reduce-scatter over
+// the lanes and then over the warps in warp order, every step a TwoSum, so the
 // result does not depend on scheduling. FOLD = false when no lane has more than
 // four groups (d <= 8192): its fp32 sum is then the chunk sum itself.
 template <typename Tx, int EMAX, int TB, bool FOLD>
@@ -101,31 +101,39 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
       }
     }
 
-  // Butterfly over lanes. Both partners compute the same (hi, lo): TwoSum's
-  // error term is exact, hence symmetric in its operands.
+  // Reduce-scatter over the lanes: at each halving step a lane keeps one half
+  // of its pairs (the upper half when its lane bit is set), gives the other
+  // half to its partner and adds what it receives with a TwoSum, so lane q
+  // ends with the warp's sum of pair q = a * EMAX + e (31 exchanges per lane
+  // instead of 5 x 32 for a full butterfly).
+  static_assert(TB * EMAX == 32, "one pair per lane after the reduce-scatter");
+  float vh[32], vl[32];
+#pragma unroll
+  for (int a = 0; a < TB; ++a)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      vh[a * EMAX + e] = hi[a][e];
+      vl[a * EMAX + e] = lo[a][e];
+    }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
+    const bool upper = (lane & off) != 0;
 #pragma unroll
-    for (int a = 0; a < TB; ++a)
-#pragma unroll
-      for (int e = 0; e < EMAX; ++e) {
-        float oh = __shfl_xor_sync(0xffffffffu, hi[a][e], off);
-        float ol = __shfl_xor_sync(0xffffffffu, lo[a][e], off);
-        float s2, er;
-        two_sum(hi[a][e], oh, s2, er);
-        hi[a][e] = s2;
-        lo[a][e] = __fadd_rn(__fadd_rn(lo[a][e], ol), er);
-      }
+    for (int q = 0; q < off; ++q) {
+      const float sh_ = upper ? vh[q] : vh[q + off];
+      const float sl_ = upper ? vl[q] : vl[q + off];
+      const float kh = upper ? vh[q + off] : vh[q];
+      const float kl = upper ? vl[q + off] : vl[q];
+      const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
+      const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
+      float s2, er;
+      two_sum(kh, rh, s2, er);
+      vh[q] = s2;
+      vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
+    }
   }
-  if (lane == 0) {
-#pragma unroll
-    for (int a = 0; a < TB; ++a)
-#pragma unroll
-      for (int e = 0; e < EMAX; ++e) {
-        s_hi[warp][a * EMAX + e] = hi[a][e];
-        s_lo[warp][a * EMAX + e] = lo[a][e];
-      }
-  }
+  s_hi[warp][lane] = vh[0];
+  s_lo[warp][lane] = vl[0];
   __syncthreads();
   // the eight warp partials of one logit, in warp order
   for (int q = threadIdx.x; q < TB * EMAX; q += blockDim.x) {
