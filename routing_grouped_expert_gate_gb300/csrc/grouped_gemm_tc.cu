@@ -220,18 +220,28 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
 template <int EPI>
 __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
                                            int row_in_tile, int half, const CUtensorMap* tmC,
-                                           uint32_t ebuf) {
+                                           const CUtensorMap* tmD, uint32_t ebuf) {
   // the two warps of a lane quadrant split the accumulator's columns in halves
   if (EPI == EPI_SWIGLU_FWD) {
     const int r = ti.m0 + row_in_tile;
     const bool rv = r < ti.m_end;
+    // whole 32 x 32 boxes through the TMA unit (h: tmC, gate|up: tmD) when the
+    // warp's 32 rows are in the segment and the 32 columns inside F (a gate
+    // box past F would land on the up columns of the same rows)
+    const int lane = row_in_tile & 31;
+    const int y0 = r - lane;
+    const bool rows_boxed = P.tma_out && y0 + 32 <= ti.m_end;
 #pragma unroll 1
     for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
       float g[32], u[32];
       tmem_ld32(t_row + c, g);
       tmem_ld32(t_row + BN / 2 + c, u);
       const int f0 = ti.n0 + c;
-      if (rv && P.out1) {
+      const bool boxed = rows_boxed && f0 + 32 <= P.F;
+      if (boxed && P.out1) {
+        store_box<false>(tmD, ebuf, lane, g, f0, y0, 0);
+        store_box<false>(tmD, ebuf, lane, u, P.F + f0, y0, 0);
+      } else if (rv && P.out1) {
         // the pre-activation gate|up first: h then overwrites g in place
         bf16* pr = P.out1 + (int64_t)r * 2 * P.F;
 #pragma unroll
@@ -249,7 +259,9 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
 #pragma unroll
         for (int i = 0; i < 32; ++i) g[i] = glu_fwd(g[i], u[i], P.act);
       }
-      if (rv) {
+      if (boxed) {
+        store_box<false>(tmC, ebuf, lane, g, f0, y0, 0);
+      } else if (rv) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (f0 + 8 * j < P.F) store_bf16x8(P.out0 + (int64_t)r * P.ld0 + f0 + 8 * j, g + 8 * j);
@@ -387,7 +399,8 @@ __device__ __forceinline__ void zero_wgrad_tile(const Params& P, const Tile& ti,
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const Params P) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                const Params P) {
   constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled stages
@@ -612,7 +625,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
-      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, ebuf);
+      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf);
       tc_fence_before();
       mbar_arrive(&sh.tmem_empty[acc]);
       acc ^= 1;
@@ -778,7 +791,8 @@ template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const Params P) {
+                     const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ CUtensorMap tmD, const Params P) {
   constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1002,7 +1016,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, ebuf);
+      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(empty_base + acc * 8);
@@ -1196,7 +1210,8 @@ static void timing_mark(int kind, cudaStream_t s, bool start) {
 
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
-                              const CUtensorMap& mc, const Params& P, int kind) {
+                              const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
+                              int kind) {
   auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   int dev = 0;
@@ -1209,7 +1224,7 @@ static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtenso
     attr_set_mask.fetch_or(bit);
   }
   timing_mark(kind, c.stream, true);
-  kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, mc, P);
+  kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, mc, md, P);
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   timing_mark(kind, c.stream, false);
@@ -1231,7 +1246,8 @@ static bool use_pair(int G, int64_t n_rows) {
 
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
-                               const CUtensorMap& mc, const Params& P, int kind) {
+                               const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
+                               int kind) {
   auto kern = tc_grouped_gemm_pair<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   static int max_clusters[64];
@@ -1265,7 +1281,7 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
   }
   cfg.gridDim = dim3(2 * max_clusters[dev & 63]);
   timing_mark(kind, c.stream, true);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, P);
   note_launches(1);
   timing_mark(kind, c.stream, false);
   return e;
@@ -1355,8 +1371,14 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
   const bool pair = use_pair(G, n_rows);
-  cudaError_t e = pair ? launch_pair<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mA, P, kFc1Fwd)
-                       : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mA, P, kFc1Fwd);
+  // h and gate|up stored through the TMA unit (both maps, or neither)
+  CUtensorMap mH, mGU;
+  P.tma_out = make_store_map(&mH, h, n_rows, F, F) &&
+              (pre_gu == nullptr || make_store_map(&mGU, pre_gu, n_rows, 2 * F, 2 * F));
+  if (!P.tma_out) mH = mA;
+  if (!P.tma_out || pre_gu == nullptr) mGU = mH;
+  cudaError_t e = pair ? launch_pair<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mH, mGU, P, kFc1Fwd)
+                       : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mH, mGU, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
   // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
   if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, pair ? 128 : 256)) {
@@ -1373,8 +1395,8 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   CUtensorMap mC;
   Q.tma_out = make_store_map(&mC, out, n_rows, d, d);
   if (!Q.tma_out) mC = mA;
-  return pair ? launch_pair<false, false, EPI_STORE>(c, mA, mB, mC, Q, kFc2Fwd)
-              : launch_one<false, false, EPI_STORE>(c, mA, mB, mC, Q, kFc2Fwd);
+  return pair ? launch_pair<false, false, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc2Fwd)
+              : launch_one<false, false, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc2Fwd);
 }
 
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
@@ -1419,16 +1441,16 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
       P.ld0 = F;
       P.tma_out = make_store_map(&mC, ws, n_rows, F, F);
       if (!P.tma_out) mC = mA;
-      e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, P, kFc2Dgrad);
+      e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, mC, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, mC, P, kFc2Dgrad);
       if (e != cudaSuccess) return e;
       e = launch_glu_bwd_rows(c, static_cast<const bf16*>(ws), static_cast<const bf16*>(pre_gu),
                               static_cast<bf16*>(d_pre), n_rows, F);
     } else {
       P.out0 = static_cast<bf16*>(d_pre);
       P.aux_in = static_cast<const bf16*>(pre_gu);
-      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, P, kFc2Dgrad);
+      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, mA, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, mA, P, kFc2Dgrad);
     }
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
@@ -1445,8 +1467,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     Q.ld0 = d;
     Q.tma_out = make_store_map(&mC, dx_rows, n_rows, d, d);
     if (!Q.tma_out) mC = mA;
-    e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, Q, kFc1Dgrad)
-             : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, Q, kFc1Dgrad);
+    e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc1Dgrad)
+             : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc1Dgrad);
     if (e != cudaSuccess) return e;
   }
   // fc2 wgrad: dW2_g [d, F] = d_outᵀ h : A = d_out [n_rows, d] MN-major, B = h [n_rows, F] MN-major
@@ -1477,8 +1499,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   R.out0 = static_cast<bf16*>(dw2);
   R.tma_out = make_wgrad_map(&mC, dw2, G, d, F);
   if (!R.tma_out) mC = mA;
-  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, R, kFc2Wgrad)
-            : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, R, kFc2Wgrad);
+  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, R, kFc2Wgrad)
+            : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, R, kFc2Wgrad);
   if (e != cudaSuccess) return e;
   // fc1 wgrad: dW1_g [2F, d] = d_preᵀ x : A = d_pre [n_rows, 2F] MN-major, B = x_rows MN-major
   if (!make_map(&mA, n_rows > 0 ? d_pre : w1, mr, 2 * F, 64) ||
@@ -1495,8 +1517,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   S.out0 = static_cast<bf16*>(dw1);
   S.tma_out = make_wgrad_map(&mC, dw1, G, 2 * F, d);
   if (!S.tma_out) mC = mA;
-  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, S, kFc1Wgrad)
-               : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, S, kFc1Wgrad);
+  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, S, kFc1Wgrad)
+               : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, S, kFc1Wgrad);
 }
 
 }  // namespace moe
