@@ -148,6 +148,23 @@ __device__ __forceinline__ void stage_box_row(uint32_t buf, int lane, const floa
   }
 }
 
+// One row of a 32-row x 16-column bf16 box (8 values = 16 B chunk j of the
+// row's 32 bytes) into a 1 KB half of the warp's buffer, in the 32-byte
+// swizzle of its tensor map: chunk j of row r sits at chunk j ^ ((r >> 2) & 1)
+// (eight consecutive rows then cover all 32 banks).
+__device__ __forceinline__ void stage_box16_chunk(uint32_t buf, int lane, int j, const float* v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  const uint32_t a = buf + (uint32_t)lane * 32u + ((uint32_t)(j ^ ((lane >> 2) & 1)) << 4);
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
+               : "memory");
+}
+
 // Store the warp's 32 rows x 32 columns through its staging buffer: wait until
 // the previous box has left the buffer, stage, hand it to the TMA unit. The
 // tensor map clips rows and columns outside the output.
@@ -295,6 +312,11 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
     const bool rv = r < ti.m_end;
     const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
     bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
+    // d_pre in 32-row x 16-column boxes through the TMA unit (tmC) when the
+    // warp's 32 rows are in the segment and the columns inside F
+    const int lane = row_in_tile & 31;
+    const int y0 = r - lane;
+    const bool rows_boxed = P.tma_out && y0 + 32 <= ti.m_end;
     uint4 gq[4], uq[4], gn[4], un[4];
     auto fetch = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
 #pragma unroll
@@ -316,11 +338,19 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
       if (c + 32 < c_hi) fetch(c + 32, gn, un);
       float dh[32];
       tmem_ld32(t_row + c, dh);
-      if (rv) {
+      const int fc = ti.n0 + c;
+      const bool boxed = rows_boxed && fc + 32 <= P.F;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int f = ti.n0 + c + 8 * j;
-          if (f < P.F) {
+      for (int s2 = 0; s2 < 2; ++s2) {
+        if (boxed) {  // the buffer's previous two boxes have been read
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * s2 + jj;
+          const int f = fc + 8 * j;
+          if (rv && f < P.F) {
             float gv[8], uv[8], dg[8], du[8];
             const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gq[j]);
             const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
@@ -343,8 +373,21 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
 #pragma unroll
               for (int i = 0; i < 8; ++i) glu_bwd(gv[i], uv[i], dh[8 * j + i], P.act, dg[i], du[i]);
             }
-            store_bf16x8(dp + f, dg);
-            store_bf16x8(dp + P.F + f, du);
+            if (boxed) {
+              stage_box16_chunk(ebuf, lane, jj, dg);
+              stage_box16_chunk(ebuf + 1024, lane, jj, du);
+            } else {
+              store_bf16x8(dp + f, dg);
+              store_bf16x8(dp + P.F + f, du);
+            }
+          }
+        }
+        if (boxed) {
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmC, ebuf, fc + 16 * s2, y0);
+            tma_store_2d(tmC, ebuf + 1024, P.F + fc + 16 * s2, y0);
           }
         }
       }
@@ -1157,21 +1200,26 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 // [G][rows][cols]. False (plain stores then) when the address or the pitch is
 // not a multiple of 16 bytes.
 static bool make_out_map(CUtensorMap* m, void* base, int rank, int64_t G, int64_t rows,
-                         int64_t cols, int64_t ld) {
+                         int64_t cols, int64_t ld, int box_cols = 32) {
   if (base == nullptr || rows <= 0 || cols <= 0 || G <= 0 || (rank != 2 && rank != 3) ||
       (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (ld * 2) % 16 != 0 || !get_encoder())
     return false;
   cuuint64_t gdim[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)G};
   cuuint64_t gstride[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(ld * 2 * rows)};
-  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, 32u, 1u};
   cuuint32_t estride[3] = {1u, 1u, 1u};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, base, gdim, gstride,
-                        box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 static bool make_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
   return make_out_map(m, base, 2, 1, rows, cols, ld);
+}
+// 16-column boxes (32-byte swizzle, stage_box16_chunk's layout)
+static bool make_store_map16(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
+  return make_out_map(m, base, 2, 1, rows, cols, ld, 16);
 }
 static bool make_wgrad_map(CUtensorMap* m, void* base, int64_t G, int64_t rows, int64_t cols) {
   return make_out_map(m, base, 3, G, rows, cols, cols);
@@ -1449,8 +1497,10 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     } else {
       P.out0 = static_cast<bf16*>(d_pre);
       P.aux_in = static_cast<const bf16*>(pre_gu);
-      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, mA, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mA, mA, P, kFc2Dgrad);
+      P.tma_out = make_store_map16(&mC, d_pre, n_rows, 2 * F, 2 * F);
+      if (!P.tma_out) mC = mA;
+      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mC, mC, P, kFc2Dgrad)
+               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mC, mC, P, kFc2Dgrad);
     }
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
