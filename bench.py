@@ -168,7 +168,7 @@ def measured_peaks():
 
 # the sources that define the tcgen05 grouped-GEMM kernels; a recorded DRAM
 # figure stays valid while none of them changes
-TC_SOURCES = ("grouped_gemm_tc.cu", "common.cuh", "internal.h")
+TC_SOURCES = ("grouped_gemm_tc.cu", "tc_ptx.cuh", "glu_act.cuh", "common.cuh", "internal.h")
 
 
 def kernel_source_hash():
