@@ -182,6 +182,53 @@ __device__ __forceinline__ void store_box(const CUtensorMap* map, uint32_t buf, 
   }
 }
 
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_cluster_zero16(uint32_t addr) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void fence_async_shared_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// TMA load of one box into the same shared-memory offset of every CTA in
+// `mask`, each copy completing on the barrier at `bar`'s offset in its CTA
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                               int x, int y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar)), "h"(mask)
+      : "memory");
+}
+// commit of this CTA's MMAs, arriving on the barrier at `bar`'s offset in
+// every CTA of `mask`
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(su32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tile schedule
 struct Tile {
   int grp;
@@ -193,8 +240,11 @@ struct Tile {
   int nk;       // k-blocks
 };
 
-template <bool KGROUPED, int EPI>
-__device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, int t) {
+// MCAST: the two CTAs of a cluster take neighbouring N tiles (2j, 2j + 1) of
+// the same expert and M tile; t counts such tile pairs.
+template <bool KGROUPED, int EPI, bool MCAST = false>
+__device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, int t,
+                                            uint32_t rank = 0) {
   Tile ti;
   if (!KGROUPED) {
     int lo = 0, hi = P.G;
@@ -206,7 +256,8 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
     const int rows = sh.off[g + 1] - sh.off[g];
     const int mt = (rows + BM - 1) / BM;
     const int local = t - sh.prefix[g];
-    const int ni = local / mt, mi = local - ni * mt;
+    const int nj = local / mt, mi = local - nj * mt;
+    const int ni = MCAST ? 2 * nj + (int)rank : nj;
     ti.grp = g;
     ti.m0 = sh.off[g] + mi * BM;
     ti.m_end = sh.off[g + 1];
@@ -439,7 +490,12 @@ __device__ __forceinline__ void zero_wgrad_tile(const Params& P, const Tile& ti,
 }
 
 // ---------------------------------------------------------------- the kernel
-template <bool A_MN, bool B_MN, int EPI>
+// MCAST (M-grouped, K-major A, an even number of N tiles): a 2-CTA cluster
+// computes the two neighbouring N tiles of one M tile; each CTA loads half of
+// the shared A tile (64 rows) and multicasts it into both CTAs, so a CTA reads
+// 40 KB per K block from L2 instead of 48 KB. A stage is free again once both
+// CTAs' MMAs have read it (each commit arrives on both CTAs' `empty`).
+template <bool A_MN, bool B_MN, int EPI, bool MCAST>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -453,16 +509,20 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint8_t* epi_buf = smem + STAGES * STAGE_BYTES;  // 1024-byte aligned
   Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES + EPI_BUF_BYTES);
 
+  static_assert(!MCAST || (!A_MN && EPI != EPI_WGRAD), "multicast: M-grouped, K-major A");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const uint32_t rank = MCAST ? cluster_ctarank() : 0u;
+  const int tile0 = MCAST ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = MCAST ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   // ---- set-up: segment offsets, tile prefix, barriers, TMEM
   if (tid == 0) {
     sh.abort = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);
+      mbar_init(&sh.empty[s], MCAST ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.tmem_full[a], 1);
@@ -493,7 +553,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int acc = 0;
       for (int g = 0; g < P.G; ++g) {
         sh.prefix[g] = acc;
-        acc += ((sh.off[g + 1] - sh.off[g] + BM - 1) / BM) * P.NT;
+        acc += ((sh.off[g + 1] - sh.off[g] + BM - 1) / BM) * (MCAST ? P.NT / 2 : P.NT);
       }
       sh.prefix[P.G] = acc;
       sh.total_tiles = acc;
@@ -524,6 +584,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
+  if (MCAST) cluster_barrier();  // the peer's barriers exist before any multicast
   tc_fence_after();
 
   const int total = sh.total_tiles;
@@ -539,7 +600,10 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       auto kblock = [&](const Tile& ti, int kb, bool prefetch_only, uint8_t* a_dst, uint8_t* b_dst,
                         uint64_t* bar) {
         const int k0 = kb * BK;
-        if (!A_MN) {
+        if (MCAST) {  // this CTA's 64 rows of the A tile, into both CTAs
+          if (prefetch_only) tma_prefetch_2d(&tmA, k0, ti.m0 + 64 * (int)rank);
+          else tma_load_2d_mc(a_dst + 8192 * rank, &tmA, bar, k0, ti.m0 + 64 * (int)rank, 0x3);
+        } else if (!A_MN) {
           if (prefetch_only) tma_prefetch_2d(&tmA, k0, ti.m0);
           else tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
         } else {
@@ -572,8 +636,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+      for (int t = tile0; t < total && ok; t += tstep) {
+        const Tile ti = decode_tile<KGROUPED, EPI, MCAST>(sh, P, t, rank);
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh.abort, P, 1)) { ok = false; break; }
           uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
@@ -597,8 +661,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+    for (int t = tile0; t < total && ok; t += tstep) {
+      const Tile ti = decode_tile<KGROUPED, EPI, MCAST>(sh, P, t, rank);
       if (ti.nk == 0) continue;  // empty segment: the epilogue writes zeros itself
       if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 2)) { ok = false; break; }
       tc_fence_after();
@@ -639,7 +703,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             else bd = sw128_desc(b_addr + kk * 2048, 8192, 1024);
             mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(&sh.empty[stage]);
+          if (MCAST) mma_commit_mc(&sh.empty[stage], 0x3);
+          else mma_commit(&sh.empty[stage]);
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -658,8 +723,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t ebuf = su32(epi_buf) + (uint32_t)(warp - 2) * EPI_BOX_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+    for (int t = tile0; t < total; t += tstep) {
+      const Tile ti = decode_tile<KGROUPED, EPI, MCAST>(sh, P, t, rank);
       if (EPI == EPI_WGRAD && ti.nk == 0) {
         zero_wgrad_tile(P, ti, row_in_tile, half, &tmC, ebuf);
         continue;
@@ -679,6 +744,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
+  if (MCAST) cluster_barrier();  // neither CTA leaves while the other may still address it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -716,32 +782,6 @@ struct __align__(8) Shared2 {
   int order[MAXG];
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// address of the same shared variable in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t d;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
-  return d;
-}
-__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_shared_cluster_zero16(uint32_t addr) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-}
-__device__ __forceinline__ void fence_async_shared_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
@@ -1256,25 +1296,47 @@ static void timing_mark(int kind, cudaStream_t s, bool start) {
   v.push_back(e);
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool MCAST = false>
 static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
                               const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
                               int kind) {
-  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
+  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI, MCAST>;
   static std::atomic<uint64_t> attr_set_mask{0};
+  static int max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = c.stream;
+  cfg.attrs = MCAST ? attr : nullptr;
+  cfg.numAttrs = MCAST ? 1 : 0;
   if (!(attr_set_mask.load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    int n = c.sm_count / 2;
+    if (MCAST) {
+      cfg.gridDim = dim3(c.sm_count & ~1);
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = c.sm_count / 2;
+      }
+    }
+    max_clusters[dev & 63] = n;
     attr_set_mask.fetch_or(bit);
   }
+  cfg.gridDim = dim3(MCAST ? 2 * max_clusters[dev & 63] : c.sm_count);
   timing_mark(kind, c.stream, true);
-  kern<<<c.sm_count, NUM_THREADS, kSmemBytes, c.stream>>>(ma, mb, mc, md, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, P);
   note_launches(1);
-  cudaError_t e = cudaGetLastError();
   timing_mark(kind, c.stream, false);
   return e;
 }
@@ -1333,6 +1395,21 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
   note_launches(1);
   timing_mark(kind, c.stream, false);
   return e;
+}
+
+// M-grouped contractions (K-major A): CTA pairs; else single CTAs whose
+// clusters multicast the A tile along N when the N tiles pair up (not in mode
+// 3, single CTAs without multicast); else plain single CTAs.
+template <bool B_MN, int EPI>
+static cudaError_t launch_mgrouped(const Ctx& c, bool pair, const CUtensorMap& ma, const void* a,
+                                   int64_t a_rows, int64_t a_cols, const CUtensorMap& mb,
+                                   const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
+                                   int kind) {
+  if (pair) return launch_pair<false, B_MN, EPI>(c, ma, mb, mc, md, P, kind);
+  CUtensorMap ma64;
+  if (g_tc_mode.load() != 3 && P.NT % 2 == 0 && make_map(&ma64, a, a_rows, a_cols, 64))
+    return launch_one<false, B_MN, EPI, true>(c, ma64, mb, mc, md, P, kind);
+  return launch_one<false, B_MN, EPI, false>(c, ma, mb, mc, md, P, kind);
 }
 
 static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* offsets) {
@@ -1425,8 +1502,8 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
               (pre_gu == nullptr || make_store_map(&mGU, pre_gu, n_rows, 2 * F, 2 * F));
   if (!P.tma_out) mH = mA;
   if (!P.tma_out || pre_gu == nullptr) mGU = mH;
-  cudaError_t e = pair ? launch_pair<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mH, mGU, P, kFc1Fwd)
-                       : launch_one<false, false, EPI_SWIGLU_FWD>(c, mA, mB, mH, mGU, P, kFc1Fwd);
+  cudaError_t e = launch_mgrouped<false, EPI_SWIGLU_FWD>(c, pair, mA, x_rows, n_rows, d, mB, mH,
+                                                         mGU, P, kFc1Fwd);
   if (e != cudaSuccess) return e;
   // fc2: A = h [n_rows, F], B = W2 [G*d, F] (K-major, 256-row boxes)
   if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, pair ? 128 : 256)) {
@@ -1443,8 +1520,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   CUtensorMap mC;
   Q.tma_out = make_store_map(&mC, out, n_rows, d, d);
   if (!Q.tma_out) mC = mA;
-  return pair ? launch_pair<false, false, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc2Fwd)
-              : launch_one<false, false, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc2Fwd);
+  return launch_mgrouped<false, EPI_STORE>(c, pair, mA, h, n_rows, F, mB, mC, mC, Q, kFc2Fwd);
 }
 
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
@@ -1458,7 +1534,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   CUtensorMap mA, mB, mC;
   cudaError_t e;
   // the weight gradients' per-expert tail maps sit at the end of the workspace
-  const bool wpair = g_tc_mode.load() != 1;  // weight gradients: CTA pairs unless single-CTA
+  const int mode = g_tc_mode.load();
+  const bool wpair = mode != 1 && mode != 3;  // weight gradients: CTA pairs unless single-CTA
   CUtensorMap* tail_maps = nullptr;
   if (n_rows > 0 && wpair && ws != nullptr && ws_bytes >= tc_tail_maps_bytes(G)) {
     const uintptr_t end = reinterpret_cast<uintptr_t>(ws) + ws_bytes;
@@ -1489,8 +1566,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
       P.ld0 = F;
       P.tma_out = make_store_map(&mC, ws, n_rows, F, F);
       if (!P.tma_out) mC = mA;
-      e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, mC, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, mC, P, kFc2Dgrad);
+      e = launch_mgrouped<true, EPI_STORE>(c, pair, mA, d_out, n_rows, d, mB, mC, mC, P,
+                                           kFc2Dgrad);
       if (e != cudaSuccess) return e;
       e = launch_glu_bwd_rows(c, static_cast<const bf16*>(ws), static_cast<const bf16*>(pre_gu),
                               static_cast<bf16*>(d_pre), n_rows, F);
@@ -1499,8 +1576,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
       P.aux_in = static_cast<const bf16*>(pre_gu);
       P.tma_out = make_store_map16(&mC, d_pre, n_rows, 2 * F, 2 * F);
       if (!P.tma_out) mC = mA;
-      e = pair ? launch_pair<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mC, mC, P, kFc2Dgrad)
-               : launch_one<false, true, EPI_SWIGLU_BWD>(c, mA, mB, mC, mC, P, kFc2Dgrad);
+      e = launch_mgrouped<true, EPI_SWIGLU_BWD>(c, pair, mA, d_out, n_rows, d, mB, mC, mC, P,
+                                                kFc2Dgrad);
     }
     if (e != cudaSuccess) return e;
     // fc1 dgrad: A = d_pre [n_rows, 2F] K-major; B = W1 [G*2F, d] MN-major
@@ -1517,8 +1594,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     Q.ld0 = d;
     Q.tma_out = make_store_map(&mC, dx_rows, n_rows, d, d);
     if (!Q.tma_out) mC = mA;
-    e = pair ? launch_pair<false, true, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc1Dgrad)
-             : launch_one<false, true, EPI_STORE>(c, mA, mB, mC, mC, Q, kFc1Dgrad);
+    e = launch_mgrouped<true, EPI_STORE>(c, pair, mA, d_pre, n_rows, 2 * F, mB, mC, mC, Q,
+                                         kFc1Dgrad);
     if (e != cudaSuccess) return e;
   }
   // fc2 wgrad: dW2_g [d, F] = d_outᵀ h : A = d_out [n_rows, d] MN-major, B = h [n_rows, F] MN-major
