@@ -439,6 +439,11 @@ def run_ours(args, ws, rank, local):
                 # three bf16 MMAs per product (exact planes of the fp32 weight)
                 e["tensor_cores"] = True
                 e["tensor_frac"] = round(3 * e["tflops"] / peaks["bf16_tflops"], 4)
+            elif n == "route_bwd" and L.router_bwd_uses_tensor_cores(cfg):
+                # six plane products for dx_router and three for dW_r against
+                # the two algorithmic products: 4.5 bf16 MMAs per product
+                e["tensor_cores"] = True
+                e["tensor_frac"] = round(4.5 * e["tflops"] / peaks["bf16_tflops"], 4)
             elif n in ("route", "route_bwd"):
                 e["fp32_alu_frac"] = round(e["tflops"] / fp32_peak, 4)
         if "bytes" in wk:

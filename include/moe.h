@@ -487,6 +487,11 @@ int moe_set_router_fold(int fold_k);
  * under the current setting, else 0. */
 int moe_router_uses_tensor_cores(const moe_cfg* cfg);
 
+/* 1 when moe_route_topk_bwd would run dx_router and dW_r on the tensor cores
+ * (bf16 activations, E >= 32, E a multiple of 8, tensor-core router setting),
+ * else 0. */
+int moe_router_bwd_uses_tensor_cores(const moe_cfg* cfg);
+
 /* Per-kernel timing of the tcgen05 grouped GEMM kernels, for measurement.
  * moe_kernel_timing(1) starts recording a CUDA event pair around every such
  * launch on the current device (on the launching stream) and discards earlier

@@ -135,6 +135,7 @@ _SIGS = {
     "moe_max_vio": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP]),
     "moe_set_router_fold": (c_int, [c_int]),
     "moe_router_uses_tensor_cores": (c_int, [POINTER(MoeCfg)]),
+    "moe_router_bwd_uses_tensor_cores": (c_int, [POINTER(MoeCfg)]),
     "moe_kernel_timing": (c_int, [c_int]),
     "moe_kernel_times": (c_int, [POINTER(c_float), POINTER(c_int32)]),
     "moe_permute_noalloc": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -181,6 +182,10 @@ def set_router_fold(fold_k: int) -> int:
 
 def router_uses_tensor_cores(cfg) -> bool:
     return bool(lib.moe_router_uses_tensor_cores(ctypes.byref(cfg)))
+
+
+def router_bwd_uses_tensor_cores(cfg) -> bool:
+    return bool(lib.moe_router_bwd_uses_tensor_cores(ctypes.byref(cfg)))
 
 
 KERNEL_KINDS = ["fc1_fwd", "fc2_fwd", "fc2_dgrad", "fc1_dgrad", "fc2_wgrad", "fc1_wgrad"]

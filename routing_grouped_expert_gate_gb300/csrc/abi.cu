@@ -250,6 +250,11 @@ int moe_router_uses_tensor_cores(const moe_cfg* cfg) {
   return router_tc_eligible(*cfg) ? 1 : 0;
 }
 
+int moe_router_bwd_uses_tensor_cores(const moe_cfg* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return router_bwd_tc_eligible(*cfg) ? 1 : 0;
+}
+
 int moe_last_device_status(moe_stream_t stream, int32_t* detail) {
   MOE_CTX(stream, c);
   MOE_LAUNCH(cudaStreamSynchronize(c.stream));
