@@ -103,28 +103,37 @@ aux_partials(const float* __restrict__ logits, int64_t T, int E, int score_fn,
 }
 
 // 1024 threads: thread (j, e) sums the block partials b = j, j + J, j + 2J,
-// ... of column e in fp64 (J = 1024 / E lanes of a column), the J sums of a
-// column are added in j order, and the E terms by a fixed pairwise tree: the
-// same order on every run, with dependent fp64 chains J times shorter than one
-// thread per column would give.
+// ... of column e into a compensated fp32 pair (J = min(1024 / E, 32) lanes
+// per column), the J pairs of a column are added in j order (TwoSum), the
+// column total times the count is formed in fp64, and the E terms are added
+// by a fixed pairwise tree: the same order on every run, and short dependent
+// chains of cheap operations (fp64 is slow on this part).
 __global__ void __launch_bounds__(1024)
 aux_finalize(const float* __restrict__ part, int64_t nblk, const int32_t* __restrict__ counts,
              int64_t T, int E, int k, float coeff, float* __restrict__ aux) {
-  __shared__ double colj[1024];
+  __shared__ float colh[1024];
+  __shared__ float coll[1024];
   __shared__ double term[kMaxE];
-  const int J = E > 0 ? (1024 / E > 0 ? 1024 / E : 1) : 1;
+  int J = E > 0 ? 1024 / E : 1;
+  J = J < 1 ? 1 : (J > 32 ? 32 : J);
   for (int q = threadIdx.x; q < J * E; q += blockDim.x) {
     const int j = q / E, e = q - j * E;
-    double v = 0.0;
+    float hi = 0.f, lo = 0.f;
 #pragma unroll 4
-    for (int64_t b = j; b < nblk; b += J) v += (double)part[b * E + e];
-    colj[q] = v;
+    for (int64_t b = j; b < nblk; b += J) comp_add(hi, lo, part[b * E + e]);
+    colh[q] = hi;
+    coll[q] = lo;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    double col = 0.0;
-    for (int j = 0; j < J; ++j) col += colj[j * E + e];
-    term[e] = col * (double)counts[e];
+    float hi = colh[e], lo = coll[e];
+    for (int j = 1; j < J; ++j) {
+      float s, er;
+      two_sum(hi, colh[j * E + e], s, er);
+      hi = s;
+      lo = __fadd_rn(__fadd_rn(lo, coll[j * E + e]), er);
+    }
+    term[e] = ((double)hi + (double)lo) * (double)counts[e];
   }
   __syncthreads();
   // pairwise tree over the E terms (E <= 256)

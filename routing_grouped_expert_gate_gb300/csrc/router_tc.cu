@@ -189,20 +189,34 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + half * NC;
-    float hi[NC], lo[NC];
+    // Two levels: the window sums of a group of GROUP windows are added in
+    // plain fp32 (round to nearest; the group's sum is a fraction of the
+    // logit, so these roundings are far below the logit's ulp), and each
+    // group sum folds into the compensated (hi, lo) pair with a TwoSum.
+    constexpr int GROUP = 4;
+    float hi[NC], lo[NC], grp[NC];
 #pragma unroll
-    for (int j = 0; j < NC; ++j) hi[j] = lo[j] = 0.f;
+    for (int j = 0; j < NC; ++j) hi[j] = lo[j] = grp[j] = 0.f;
     bool ok = true;
     for (int win = 0; win < n_win; ++win) {
       const int buf = win & 1;
       if (!mbar_wait(&sh.acc_full[buf], (win >> 1) & 1, sh.abort, P, 24)) { ok = false; break; }
       tc_fence_after();
+      const bool fold_now = (win % GROUP == GROUP - 1) || win == n_win - 1;
 #pragma unroll
       for (int c = 0; c < NC; c += 32) {
         float v[32];
         tmem_ld32(base + buf * BN + c, v);
+        if (fold_now) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) comp_add(hi[c + i], lo[c + i], v[i]);
+          for (int i = 0; i < 32; ++i) {
+            comp_add(hi[c + i], lo[c + i], __fadd_rn(grp[c + i], v[i]));
+            grp[c + i] = 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) grp[c + i] = __fadd_rn(grp[c + i], v[i]);
+        }
       }
       tc_fence_before();
       mbar_arrive(&sh.acc_empty[buf]);
