@@ -91,6 +91,7 @@ struct __align__(8) Shared {
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
+  uint64_t epi_load[NUM_EPI_WARPS];  // TMA loads into an epilogue warp's buffer
   uint32_t tmem_base;
   int abort;
   int total_tiles;
@@ -239,9 +240,11 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
 // One thread per accumulator row (TMEM lane): read the row's 256 fp32 columns
 // with tcgen05.ld (all lanes of the warp together) and write the outputs.
 template <int EPI>
-__device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
+__device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
                                            int row_in_tile, int half, const CUtensorMap* tmC,
-                                           const CUtensorMap* tmD, uint32_t ebuf) {
+                                           const CUtensorMap* tmD, uint32_t ebuf,
+                                           uint64_t* load_bar, uint32_t& load_phase,
+                                           int& abort_flag) {
   // the two warps of a lane quadrant split the accumulator's columns in halves
   if (EPI == EPI_SWIGLU_FWD) {
     const int r = ti.m0 + row_in_tile;
@@ -309,55 +312,62 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
       }
     }
   } else if (EPI == EPI_SWIGLU_BWD) {
-    // gate/up of the row are read from global memory; the loads of the next
-    // 32-column chunk are issued before the current chunk is computed, so
-    // their latency hides behind the TMEM read and the math.
+    // The warp's 32 rows inside the segment and the columns inside F: gate/up
+    // come in and d_pre goes out through the warp's buffer, 16 columns at a
+    // time, as 32 x 16 boxes in the 32-byte swizzle (tmD: gate|up, tmC:
+    // d_pre); each thread reads its row's chunks and writes dg/du in place.
+    // Elsewhere each thread loads and stores its row directly.
     const int r = ti.m0 + row_in_tile;
     const bool rv = r < ti.m_end;
-    const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
-    bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
-    // d_pre in 32-row x 16-column boxes through the TMA unit (tmC) when the
-    // warp's 32 rows are in the segment and the columns inside F
     const int lane = row_in_tile & 31;
     const int y0 = r - lane;
     const bool rows_boxed = P.tma_out && y0 + 32 <= ti.m_end;
-    uint4 gq[4], uq[4], gn[4], un[4];
-    auto fetch = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
+    const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
+    bf16* dp = P.out0 + (int64_t)r * 2 * P.F;
+    auto deriv8 = [&](const float* gv, const float* uv, const float* d, float* dg, float* du) {
+      if (glu_is_plain(P.act)) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int f = ti.n0 + c + 8 * j;
-        if (rv && f < P.F) {
-          g[j] = __ldg(reinterpret_cast<const uint4*>(pr + f));
-          u[j] = __ldg(reinterpret_cast<const uint4*>(pr + P.F + f));
-        } else {
-          g[j] = make_uint4(0, 0, 0, 0);
-          u[j] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 8; ++i) {
+          const float sg = 1.f / (1.f + __expf(-gv[i]));
+          dg[i] = d[i] * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
+          du[i] = d[i] * gv[i] * sg;
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) glu_bwd(gv[i], uv[i], d[i], P.act, dg[i], du[i]);
       }
     };
     const int c_lo = half * (BN / 2), c_hi = c_lo + BN / 2;
-    fetch(c_lo, gq, uq);
 #pragma unroll 1
     for (int c = c_lo; c < c_hi; c += 32) {
-      if (c + 32 < c_hi) fetch(c + 32, gn, un);
       float dh[32];
       tmem_ld32(t_row + c, dh);
       const int fc = ti.n0 + c;
-      const bool boxed = rows_boxed && fc + 32 <= P.F;
+      if (rows_boxed && fc + 32 <= P.F) {
 #pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2) {
-        if (boxed) {  // the buffer's previous two boxes have been read
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-        }
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int x = fc + 16 * s2;
+          if (lane == 0) {
+            bulk_wait_read<0>();  // the previous boxes have left the buffer
+            mbar_expect_tx(load_bar, 2048);
+            tma_load_2d_s(ebuf, tmD, su32(load_bar), x, y0);
+            tma_load_2d_s(ebuf + 1024, tmD, su32(load_bar), P.F + x, y0);
+          }
+          if (!mbar_wait(load_bar, load_phase, abort_flag, P, 16)) return false;
+          load_phase ^= 1;
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * s2 + jj;
-          const int f = fc + 8 * j;
-          if (rv && f < P.F) {
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t off = (uint32_t)lane * 32u + ((uint32_t)(jj ^ ((lane >> 2) & 1)) << 4);
+            uint4 gq, uq;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(gq.x), "=r"(gq.y), "=r"(gq.z), "=r"(gq.w)
+                         : "r"(ebuf + off));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(uq.x), "=r"(uq.y), "=r"(uq.z), "=r"(uq.w)
+                         : "r"(ebuf + 1024 + off));
             float gv[8], uv[8], dg[8], du[8];
-            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gq[j]);
-            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uq[j]);
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gq);
+            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uq);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float2 a = __bfloat1622float2(g2[i]);
@@ -365,40 +375,30 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
               gv[2 * i] = a.x; gv[2 * i + 1] = a.y;
               uv[2 * i] = b2.x; uv[2 * i + 1] = b2.y;
             }
-            if (glu_is_plain(P.act)) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float sg = 1.f / (1.f + __expf(-gv[i]));
-                const float d = dh[8 * j + i];
-                dg[i] = d * uv[i] * sg * (1.f + gv[i] * (1.f - sg));
-                du[i] = d * gv[i] * sg;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) glu_bwd(gv[i], uv[i], dh[8 * j + i], P.act, dg[i], du[i]);
-            }
-            if (boxed) {
-              stage_box16_chunk(ebuf, lane, jj, dg);
-              stage_box16_chunk(ebuf + 1024, lane, jj, du);
-            } else {
-              store_bf16x8(dp + f, dg);
-              store_bf16x8(dp + P.F + f, du);
-            }
+            deriv8(gv, uv, dh + 16 * s2 + 8 * jj, dg, du);
+            stage_box16_chunk(ebuf, lane, jj, dg);
+            stage_box16_chunk(ebuf + 1024, lane, jj, du);
           }
-        }
-        if (boxed) {
           fence_async_shared();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(tmC, ebuf, fc + 16 * s2, y0);
-            tma_store_2d(tmC, ebuf + 1024, P.F + fc + 16 * s2, y0);
+            tma_store_2d(tmC, ebuf, x, y0);
+            tma_store_2d(tmC, ebuf + 1024, P.F + x, y0);
           }
         }
-      }
+      } else if (rv) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        gq[j] = gn[j];
-        uq[j] = un[j];
+        for (int j = 0; j < 4; ++j) {
+          const int f = fc + 8 * j;
+          if (f < P.F) {
+            float gv[8], uv[8], dg[8], du[8];
+            load_bf16x8(pr + f, gv);
+            load_bf16x8(pr + P.F + f, uv);
+            deriv8(gv, uv, dh + 8 * j, dg, du);
+            store_bf16x8(dp + f, dg);
+            store_bf16x8(dp + P.F + f, du);
+          }
+        }
       }
     }
   } else {  // EPI_WGRAD
@@ -420,6 +420,7 @@ __device__ __forceinline__ void drain_tile(const Params& P, const Tile& ti, uint
       }
     }
   }
+  return true;
 }
 
 // An empty expert's weight-gradient tile: zeros, without touching TMEM.
@@ -481,6 +482,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(&sh.tmem_full[a], 1);
       mbar_init(&sh.tmem_empty[a], NUM_EPI_WARPS * 32);
     }
+    for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(&sh.epi_load[w], 1);
     fence_barrier_init();
   }
   for (int g = tid; g <= P.G; g += NUM_THREADS) {
@@ -674,6 +676,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     const uint32_t ebuf = su32(epi_buf) + (uint32_t)(warp - 2) * EPI_BOX_BYTES;
+    uint32_t epi_phase = 0;  // parity of this warp's epi_load barrier
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = tile0; t < total; t += tstep) {
@@ -686,7 +689,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
-      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf);
+      if (!drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf,
+                           &sh.epi_load[warp - 2], epi_phase, sh.abort))
+        break;
       tc_fence_before();
       mbar_arrive(&sh.tmem_empty[acc]);
       acc ^= 1;
@@ -725,6 +730,7 @@ constexpr int PAIR_ACC = 2;                        // accumulators per CTA (x 25
 struct __align__(8) Shared2 {
   uint64_t full[STAGES2];
   uint64_t empty[STAGES2];
+  uint64_t epi_load[NUM_EPI_WARPS];  // TMA loads into an epilogue warp's buffer
   uint64_t tmem_full[PAIR_ACC];
   uint64_t tmem_empty[PAIR_ACC];
   uint32_t tmem_base;
@@ -855,6 +861,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       mbar_init(&sh.tmem_full[a], 1);
       mbar_init(&sh.tmem_empty[a], 2 * NUM_EPI_WARPS);
     }
+    for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(&sh.epi_load[w], 1);
     fence_barrier_init();
   }
   for (int g = tid; g <= P.G; g += NUM_THREADS)
@@ -1041,6 +1048,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     const int row_in_tile = q * 32 + lane;
     const uint32_t empty_base = mapa_shared(su32(&sh.tmem_empty[0]), 0);
     const uint32_t ebuf = su32(epi_buf) + (uint32_t)(warp - 2) * EPI_BOX_BYTES;
+    uint32_t epi_phase = 0;  // parity of this warp's epi_load barrier
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster_id; t < total; t += n_clusters) {
@@ -1052,7 +1060,11 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf);
+      if (!drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf,
+                           &sh.epi_load[warp - 2], epi_phase, sh.abort)) {
+        aborted = true;
+        break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(empty_base + acc * 8);
@@ -1527,9 +1539,12 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     } else {
       P.out0 = static_cast<bf16*>(d_pre);
       P.aux_in = static_cast<const bf16*>(pre_gu);
-      P.tma_out = make_store_map16(&mC, d_pre, n_rows, 2 * F, 2 * F);
-      if (!P.tma_out) mC = mA;
-      e = launch_mgrouped<true, EPI_SWIGLU_BWD>(c, pair, mA, d_out, n_rows, d, mB, mC, mC, P,
+      // d_pre out (tmC) and gate|up in (tmD) as 32 x 16 boxes
+      CUtensorMap mGU;
+      P.tma_out = make_store_map16(&mC, d_pre, n_rows, 2 * F, 2 * F) &&
+                  make_store_map16(&mGU, const_cast<void*>(pre_gu), n_rows, 2 * F, 2 * F);
+      if (!P.tma_out) mC = mGU = mA;
+      e = launch_mgrouped<true, EPI_SWIGLU_BWD>(c, pair, mA, d_out, n_rows, d, mB, mC, mGU, P,
                                                 kFc2Dgrad);
     }
     if (e != cudaSuccess) return e;
