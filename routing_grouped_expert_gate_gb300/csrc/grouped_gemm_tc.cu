@@ -551,41 +551,28 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // later k-blocks by every CTA was measured to slow the kernel down: the
     // CTAs sharing a weight tile all prefetch it.)
     if (lane == 0) {
-      // issue (or only prefetch) the A and B boxes of k-block kb of tile ti
-      auto kblock = [&](const Tile& ti, int kb, bool prefetch_only, uint8_t* a_dst, uint8_t* b_dst,
-                        uint64_t* bar) {
+      // the A and B boxes of k-block kb of tile ti
+      auto kblock = [&](const Tile& ti, int kb, uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar) {
         const int k0 = kb * BK;
         if (MCAST) {  // this CTA's 64 rows of the A tile, into both CTAs
-          if (prefetch_only) tma_prefetch_2d(&tmA, k0, ti.m0 + 64 * (int)rank);
-          else tma_load_2d_mc(a_dst + 8192 * rank, &tmA, bar, k0, ti.m0 + 64 * (int)rank, 0x3);
+          tma_load_2d_mc(a_dst + 8192 * rank, &tmA, bar, k0, ti.m0 + 64 * (int)rank, 0x3);
         } else if (!A_MN) {
-          if (prefetch_only) tma_prefetch_2d(&tmA, k0, ti.m0);
-          else tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
+          tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
         } else {
-          for (int h = 0; h < 2; ++h) {
-            if (prefetch_only) tma_prefetch_2d(&tmA, ti.m0 + 64 * h, ti.k_begin + k0);
-            else tma_load_2d(a_dst + 8192 * h, &tmA, bar, ti.m0 + 64 * h, ti.k_begin + k0);
-          }
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(a_dst + 8192 * h, &tmA, bar, ti.m0 + 64 * h, ti.k_begin + k0);
         }
         if (!B_MN) {
           if (EPI == EPI_SWIGLU_FWD) {
             const int r0 = ti.grp * 2 * P.F;
-            for (int h = 0; h < 2; ++h) {
-              const int y = r0 + h * P.F + ti.n0;
-              if (prefetch_only) tma_prefetch_2d(&tmB, k0, y);
-              else tma_load_2d(b_dst + 16384 * h, &tmB, bar, k0, y);
-            }
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(b_dst + 16384 * h, &tmB, bar, k0, r0 + h * P.F + ti.n0);
           } else {
-            const int y = ti.grp * P.b_group_rows + ti.n0;
-            if (prefetch_only) tma_prefetch_2d(&tmB, k0, y);
-            else tma_load_2d(b_dst, &tmB, bar, k0, y);
+            tma_load_2d(b_dst, &tmB, bar, k0, ti.grp * P.b_group_rows + ti.n0);
           }
         } else {
           const int y = KGROUPED ? ti.k_begin + k0 : ti.grp * P.b_group_rows + k0;
-          for (int j = 0; j < 4; ++j) {
-            if (prefetch_only) tma_prefetch_2d(&tmB, ti.n0 + 64 * j, y);
-            else tma_load_2d(b_dst + j * 8192, &tmB, bar, ti.n0 + 64 * j, y);
-          }
+          for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + j * 8192, &tmB, bar, ti.n0 + 64 * j, y);
         }
       };
       int stage = 0;
@@ -598,7 +585,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
           uint64_t* bar = &sh.full[stage];
           mbar_expect_tx(bar, STAGE_BYTES);
-          kblock(ti, kb, false, a_dst, a_dst + A_STAGE_BYTES, bar);
+          kblock(ti, kb, a_dst, a_dst + A_STAGE_BYTES, bar);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
