@@ -70,6 +70,10 @@ __device__ __forceinline__ void tma_load_2d_s(uint32_t dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// TMA stores from shared memory; each store is its own bulk group, so
+// `bulk_wait_read<N>` lets at most N of this thread's stores still be reading
+// their shared-memory source, and `bulk_wait_all` waits until every store of
+// this thread has been written to global memory.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
