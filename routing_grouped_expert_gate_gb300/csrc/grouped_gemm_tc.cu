@@ -84,6 +84,7 @@ struct Params {
   // row (rows after it read as zeros), for the group's last K block; NULL =
   // the MMA warp zeroes those rows in shared memory instead
   const CUtensorMap* tail_maps;
+  int m128_tails;     // CTA pairs, M-grouped: a last tile of <= 128 rows runs as M = 128
 };
 
 struct __align__(8) Shared {
@@ -192,7 +193,51 @@ struct Tile {
   int k_begin;  // K-grouped: first row of the segment
   int k_end;
   int nk;       // k-blocks
+  int m128;     // CTA pair: a segment's last tile of at most 128 rows, computed
+                // with M = 128 (64 rows per CTA)
 };
+
+// Which accumulator cells an epilogue thread drains. TMEM lane = accumulator
+// row, except in an M = 128 pair tile, whose 64 rows x 256 columns per CTA
+// sit folded in 128 lanes x 128 columns: lanes 0-63 hold columns 0-127 and
+// lanes 64-127 hold columns 128-255 of the same 64 rows (measured).
+struct EpiCols {
+  int row;      // accumulator row of this thread, relative to the tile's m0
+  int cb, ncol; // TMEM columns [cb, cb + ncol) of this warp (plain outputs)
+  int dbase;    // output column of TMEM column 0 for this thread's lanes
+  int gcol;     // SwiGLU forward: TMEM column of the first gate value,
+  int up_off;   //   the matching up value up_off columns further,
+  int feat_off; //   its feature index relative to the tile's n0,
+  int nchunk;   //   and how many 32-feature chunks this warp takes
+};
+__device__ __forceinline__ EpiCols epi_cols(int q, int lane, int half, bool pair_glu, bool m128) {
+  EpiCols e;
+  if (!m128) {
+    e.row = q * 32 + lane;
+    e.cb = half * (BN / 2);
+    e.ncol = BN / 2;
+    e.dbase = 0;
+    if (pair_glu) {  // CTA pair: B = [64 gate | 64 up] rows per CTA
+      e.gcol = half * (BN / 2);
+      e.up_off = BN / 4;
+    } else {         // single CTA: B = [128 gate | 128 up] rows
+      e.gcol = half * (BN / 4);
+      e.up_off = BN / 2;
+    }
+    e.feat_off = half * (BN / 4);
+    e.nchunk = 2;
+  } else {
+    e.row = (q & 1) * 32 + lane;
+    e.cb = half * (BN / 4);
+    e.ncol = BN / 4;
+    e.dbase = q >= 2 ? BN / 2 : 0;
+    e.gcol = half * 32;
+    e.up_off = BN / 4;
+    e.feat_off = (q >= 2 ? BN / 4 : 0) + half * 32;
+    e.nchunk = 1;
+  }
+  return e;
+}
 
 // MCAST: the two CTAs of a cluster take neighbouring N tiles (2j, 2j + 1) of
 // the same expert and M tile; t counts such tile pairs.
@@ -219,6 +264,7 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
     ti.k_begin = 0;
     ti.k_end = P.K;
     ti.nk = (P.K + BK - 1) / BK;
+    ti.m128 = 0;
   } else {
     const int per = P.MT * P.NT;
     const int gi = t / per;
@@ -232,6 +278,7 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
     ti.k_begin = sh.off[g];
     ti.k_end = sh.off[g + 1];
     ti.nk = (ti.k_end - ti.k_begin + BK - 1) / BK;
+    ti.m128 = 0;
   }
   return ti;
 }
@@ -241,26 +288,26 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
 // with tcgen05.ld (all lanes of the warp together) and write the outputs.
 template <int EPI>
 __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint32_t t_row,
-                                           int row_in_tile, int half, const CUtensorMap* tmC,
+                                           const EpiCols& ec, const CUtensorMap* tmC,
                                            const CUtensorMap* tmD, uint32_t ebuf,
                                            uint64_t* load_bar, uint32_t& load_phase,
                                            int& abort_flag) {
   // the two warps of a lane quadrant split the accumulator's columns in halves
+  const int lane = ec.row & 31;
   if (EPI == EPI_SWIGLU_FWD) {
-    const int r = ti.m0 + row_in_tile;
+    const int r = ti.m0 + ec.row;
     const bool rv = r < ti.m_end;
     // whole 32 x 32 boxes through the TMA unit (h: tmC, gate|up: tmD) when the
     // warp's 32 rows are in the segment and the 32 columns inside F (a gate
     // box past F would land on the up columns of the same rows)
-    const int lane = row_in_tile & 31;
     const int y0 = r - lane;
     const bool rows_boxed = P.tma_out && y0 + 32 <= ti.m_end;
 #pragma unroll 1
-    for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
+    for (int k = 0; k < ec.nchunk; ++k) {
       float g[32], u[32];
-      tmem_ld32(t_row + c, g);
-      tmem_ld32(t_row + BN / 2 + c, u);
-      const int f0 = ti.n0 + c;
+      tmem_ld32(t_row + ec.gcol + 32 * k, g);
+      tmem_ld32(t_row + ec.gcol + ec.up_off + 32 * k, u);
+      const int f0 = ti.n0 + ec.feat_off + 32 * k;
       const bool boxed = rows_boxed && f0 + 32 <= P.F;
       if (boxed && P.out1) {
         store_box<false>(tmD, ebuf, lane, g, f0, y0, 0);
@@ -292,16 +339,16 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
       }
     }
   } else if (EPI == EPI_STORE) {
-    const int r = ti.m0 + row_in_tile;
+    const int r = ti.m0 + ec.row;
     const bool rv = r < ti.m_end;
     // the warp's 32 rows all in the segment: whole boxes through the TMA unit
-    const int lane = row_in_tile & 31;
     const int y0 = r - lane;
     const bool boxed = P.tma_out && y0 + 32 <= ti.m_end;
 #pragma unroll 1
-    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+    for (int ct = ec.cb; ct < ec.cb + ec.ncol; ct += 32) {
       float v[32];
-      tmem_ld32(t_row + c, v);
+      tmem_ld32(t_row + ct, v);
+      const int c = ec.dbase + ct;  // accumulator column
       if (boxed) {
         if (ti.n0 + c < P.N_out) store_box<false>(tmC, ebuf, lane, v, ti.n0 + c, y0, 0);
       } else if (rv) {
@@ -317,9 +364,8 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
     // time, as 32 x 16 boxes in the 32-byte swizzle (tmD: gate|up, tmC:
     // d_pre); each thread reads its row's chunks and writes dg/du in place.
     // Elsewhere each thread loads and stores its row directly.
-    const int r = ti.m0 + row_in_tile;
+    const int r = ti.m0 + ec.row;
     const bool rv = r < ti.m_end;
-    const int lane = row_in_tile & 31;
     const int y0 = r - lane;
     const bool rows_boxed = P.tma_out && y0 + 32 <= ti.m_end;
     const bf16* pr = P.aux_in + (int64_t)(rv ? r : ti.m0) * 2 * P.F;
@@ -337,12 +383,11 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
         for (int i = 0; i < 8; ++i) glu_bwd(gv[i], uv[i], d[i], P.act, dg[i], du[i]);
       }
     };
-    const int c_lo = half * (BN / 2), c_hi = c_lo + BN / 2;
 #pragma unroll 1
-    for (int c = c_lo; c < c_hi; c += 32) {
+    for (int ct = ec.cb; ct < ec.cb + ec.ncol; ct += 32) {
       float dh[32];
-      tmem_ld32(t_row + c, dh);
-      const int fc = ti.n0 + c;
+      tmem_ld32(t_row + ct, dh);
+      const int fc = ti.n0 + ec.dbase + ct;
       if (rows_boxed && fc + 32 <= P.F) {
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
@@ -402,12 +447,11 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
       }
     }
   } else {  // EPI_WGRAD
-    const int m = ti.m0 + row_in_tile;
+    const int m = ti.m0 + ec.row;
     const bool rv = m < P.M_out;
-    const int lane = row_in_tile & 31;
     bf16* dst_row = P.out0 + (int64_t)ti.grp * P.M_out * P.N_out + (int64_t)m * P.N_out;
 #pragma unroll 1
-    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+    for (int c = ec.cb; c < ec.cb + ec.ncol; c += 32) {
       float v[32];
       tmem_ld32(t_row + c, v);
       if (P.tma_out) {
@@ -676,7 +720,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
-      if (!drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf,
+      if (!drain_tile<EPI>(P, ti, t_row, epi_cols(q, lane, half, false, false), &tmC, &tmD, ebuf,
                            &sh.epi_load[warp - 2], epi_phase, sh.abort))
         break;
       tc_fence_before();
@@ -791,13 +835,16 @@ __device__ __forceinline__ Tile decode_pair_tile(const Shared2& sh, const Params
     const int mp = (rows + 2 * BM - 1) / (2 * BM);
     const int local = t - sh.prefix[g];
     const int ni = local / mp, mi = local - ni * mp;
+    // a last tile of at most 128 rows runs as M = 128: 64 rows per CTA
+    const bool m128 = P.m128_tails && mi == mp - 1 && rows - mi * 2 * BM <= BM;
     ti.grp = g;
-    ti.m0 = sh.off[g] + mi * 2 * BM + (int)rank * BM;
+    ti.m0 = sh.off[g] + mi * 2 * BM + (int)rank * (m128 ? BM / 2 : BM);
     ti.m_end = sh.off[g + 1];
     ti.n0 = ni * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
     ti.k_begin = 0;
     ti.k_end = P.K;
     ti.nk = (P.K + BK - 1) / BK;
+    ti.m128 = m128 ? 1 : 0;
   } else {
     // P.MT counts 256-row pair tiles along M
     const int per = P.MT * P.NT;
@@ -812,6 +859,7 @@ __device__ __forceinline__ Tile decode_pair_tile(const Shared2& sh, const Params
     ti.k_begin = sh.off[g];
     ti.k_end = sh.off[g + 1];
     ti.nk = (ti.k_end - ti.k_begin + BK - 1) / BK;
+    ti.m128 = 0;
   }
   return ti;
 }
@@ -941,10 +989,15 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
             tma_load_2d_pair(a_dst + 8192, amap, bar, ti.m0 + 64, ti.k_begin + k0);
           }
           if (!B_MN) {
-            int y;
-            if (EPI == EPI_SWIGLU_FWD) y = ti.grp * 2 * P.F + (int)rank * P.F + ti.n0;
-            else y = ti.grp * P.b_group_rows + ti.n0 + (int)rank * (BN / 2);
-            tma_load_2d_pair(b_dst, &tmB, bar, k0, y);
+            if (EPI == EPI_SWIGLU_FWD) {
+              // this CTA's 64 features: their gate rows, then their up rows
+              const int yg = ti.grp * 2 * P.F + ti.n0 + (int)rank * (BN / 4);
+              tma_load_2d_pair(b_dst, &tmB, bar, k0, yg);
+              tma_load_2d_pair(b_dst + 8192, &tmB, bar, k0, yg + P.F);
+            } else {
+              tma_load_2d_pair(b_dst, &tmB, bar, k0,
+                               ti.grp * P.b_group_rows + ti.n0 + (int)rank * (BN / 2));
+            }
           } else {
             const int y = KGROUPED ? ti.k_begin + k0 : ti.grp * P.b_group_rows + k0;
             const int x0 = ti.n0 + (int)rank * (BN / 2);
@@ -958,7 +1011,8 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ================= MMA issuer (the even CTA) =================
     if (leader) {
-      constexpr uint32_t IDESC = make_idesc_pair(A_MN, B_MN);
+      constexpr uint32_t IDESC = make_idesc_pair(A_MN, B_MN);  // M = 256
+      constexpr uint32_t IDESC128 = (IDESC & ~(0x1Fu << 24)) | ((uint32_t)(BM >> 4) << 24);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -969,6 +1023,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
         if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 12)) { aborted = true; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t idesc = ti.m128 ? IDESC128 : IDESC;
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 13)) { aborted = true; break; }
           tc_fence_after();
@@ -1006,7 +1061,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                                        : sw128_desc(a_addr + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? sw128_desc(b_addr + kk * 2048, 8192, 1024)
                                        : sw128_desc(b_addr + kk * 32, 16, 1024);
-              mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             };
             // a full stage as straight-line MMAs (measured: a bounds check in
             // the unrolled loop slowed the weight gradients by about 7%)
@@ -1047,7 +1102,9 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       if (!mbar_wait(&sh.tmem_full[acc], acc_phase, sh.abort, P, 14)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (!drain_tile<EPI>(P, ti, t_row, row_in_tile, half, &tmC, &tmD, ebuf,
+      if (!drain_tile<EPI>(P, ti, t_row,
+                           epi_cols(q, lane, half, EPI == EPI_SWIGLU_FWD, ti.m128 != 0), &tmC,
+                           &tmD, ebuf,
                            &sh.epi_load[warp - 2], epi_phase, sh.abort)) {
         aborted = true;
         break;
@@ -1364,6 +1421,11 @@ static cudaError_t launch_mgrouped(const Ctx& c, bool pair, const CUtensorMap& m
   return launch_one<false, B_MN, EPI, false>(c, ma, mb, mc, md, P, kind);
 }
 
+// M = 128 last tiles on CTA pairs: measured faster where the contraction's K
+// is long (Mixtral-sized: each kind 1-2% faster) and 1-6% slower with
+// K <= 2816 (fine-grained and Zipf-skewed layers), so only from K = 4096 on.
+static int m128_tails_for(int K) { return K >= 4096 ? 1 : 0; }
+
 static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* offsets) {
   Params P{};
   P.G = G;
@@ -1435,19 +1497,22 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   *err = MOE_OK;
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap mA, mB;
-  // fc1: A = x_rows [n_rows, d] (K-major), B = W1 [G*2F, d] (K-major, 128-row boxes)
-  if (!make_map(&mA, x_rows, n_rows, d, 128) || !make_map(&mB, w1, (int64_t)G * 2 * F, d, 128)) {
+  const bool pair = use_pair(G, n_rows);
+  // fc1: A = x_rows [n_rows, d] (K-major), B = W1 [G*2F, d] (K-major; single
+  // CTAs load 128 gate and 128 up rows, a CTA of a pair 64 of each)
+  if (!make_map(&mA, x_rows, n_rows, d, 128) ||
+      !make_map(&mB, w1, (int64_t)G * 2 * F, d, pair ? 64 : 128)) {
     *err = MOE_ERR_CUDA;
     return cudaSuccess;
   }
   Params P = base_params(c, G, n_rows, offsets);
   P.K = d;
+  P.m128_tails = m128_tails_for(P.K);
   P.F = F;
   P.NT = (F + BN / 2 - 1) / (BN / 2);
   P.out0 = static_cast<bf16*>(h);
   P.ld0 = F;
   P.out1 = static_cast<bf16*>(pre_gu);
-  const bool pair = use_pair(G, n_rows);
   // h and gate|up stored through the TMA unit (both maps, or neither)
   CUtensorMap mH, mGU;
   P.tma_out = make_store_map(&mH, h, n_rows, F, F) &&
@@ -1464,6 +1529,7 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   }
   Params Q = base_params(c, G, n_rows, offsets);
   Q.K = F;
+  Q.m128_tails = m128_tails_for(Q.K);
   Q.N_out = d;
   Q.NT = (d + BN - 1) / BN;
   Q.b_group_rows = d;
@@ -1508,6 +1574,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     }
     Params P = base_params(c, G, n_rows, offsets);
     P.K = d;
+    P.m128_tails = m128_tails_for(P.K);
     P.F = F;
     P.N_out = F;
     P.NT = (F + BN - 1) / BN;
@@ -1542,6 +1609,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     }
     Params Q = base_params(c, G, n_rows, offsets);
     Q.K = 2 * F;
+    Q.m128_tails = m128_tails_for(Q.K);
     Q.N_out = d;
     Q.NT = (d + BN - 1) / BN;
     Q.b_group_rows = 2 * F;

@@ -53,6 +53,10 @@ SMALL = {
     # epilogue (at smaller d a separate pass does)
     "mixtral_d4096_small": mi.shrink(W["mixtral_style"], name="mixtral_d4096_small", T=320,
                                      d=4096, F=192),
+    # F = 4096: fc2 forward and fc1 dgrad with K >= 4096, where CTA pairs run a
+    # segment's last tile of <= 128 rows as an M = 128 tile
+    "mixtral_f4096_small": mi.shrink(W["mixtral_style"], name="mixtral_f4096_small", T=160,
+                                     d=256, F=4096),
 }
 # bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
