@@ -869,7 +869,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC,
-                     const __grid_constant__ CUtensorMap tmD, const Params P) {
+                     const __grid_constant__ CUtensorMap tmD,
+                     const __grid_constant__ CUtensorMap tmA64, const Params P) {
   constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -972,7 +973,9 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
           uint8_t* a_dst = stage_base + stage * STAGE2_BYTES;
           uint8_t* b_dst = a_dst + A2_BYTES;
           const uint32_t bar = mapa_shared(su32(&sh.full[stage]), 0);  // the even CTA's
-          if (leader) mbar_expect_tx(&sh.full[stage], 2 * STAGE2_BYTES);
+          // an M = 128 tile loads only its 64 A rows per CTA (tmA64: 64-row boxes)
+          if (leader) mbar_expect_tx(&sh.full[stage], 2 * (ti.m128 ? STAGE2_BYTES - A2_BYTES / 2
+                                                                   : STAGE2_BYTES));
           const int k0 = kb * BK;
           const CUtensorMap* amap = &tmA;
           if (KGROUPED && P.tail_maps != nullptr && kb == ti.nk - 1 &&
@@ -983,7 +986,8 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
             tensormap_acquire(amap);
           }
           if (!A_MN) {
-            tma_load_2d_pair(a_dst, amap, bar, k0, ti.m0);
+            if (ti.m128) tma_load_2d_pair(a_dst, &tmA64, bar, k0, ti.m0);
+            else tma_load_2d_pair(a_dst, amap, bar, k0, ti.m0);
           } else {
             tma_load_2d_pair(a_dst, amap, bar, ti.m0, ti.k_begin + k0);
             tma_load_2d_pair(a_dst + 8192, amap, bar, ti.m0 + 64, ti.k_begin + k0);
@@ -1365,8 +1369,8 @@ static bool use_pair(int G, int64_t n_rows) {
 
 template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
-                               const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
-                               int kind) {
+                               const CUtensorMap& mc, const CUtensorMap& md,
+                               const CUtensorMap& ma64, const Params& P, int kind) {
   auto kern = tc_grouped_gemm_pair<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
   static int max_clusters[64];
@@ -1400,7 +1404,7 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
   }
   cfg.gridDim = dim3(2 * max_clusters[dev & 63]);
   timing_mark(kind, c.stream, true);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, ma64, P);
   note_launches(1);
   timing_mark(kind, c.stream, false);
   return e;
@@ -1414,17 +1418,20 @@ static cudaError_t launch_mgrouped(const Ctx& c, bool pair, const CUtensorMap& m
                                    int64_t a_rows, int64_t a_cols, const CUtensorMap& mb,
                                    const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
                                    int kind) {
-  if (pair) return launch_pair<false, B_MN, EPI>(c, ma, mb, mc, md, P, kind);
   CUtensorMap ma64;
+  if (pair) {  // its M = 128 last tiles load 64 A rows per CTA
+    if (!make_map(&ma64, a, a_rows, a_cols, 64)) return cudaErrorInvalidValue;
+    return launch_pair<false, B_MN, EPI>(c, ma, mb, mc, md, ma64, P, kind);
+  }
   if (g_tc_mode.load() != 3 && P.NT % 2 == 0 && make_map(&ma64, a, a_rows, a_cols, 64))
     return launch_one<false, B_MN, EPI, true>(c, ma64, mb, mc, md, P, kind);
   return launch_one<false, B_MN, EPI, false>(c, ma, mb, mc, md, P, kind);
 }
 
-// M = 128 last tiles on CTA pairs: measured faster where the contraction's K
-// is long (Mixtral-sized: each kind 1-2% faster) and 1-6% slower with
-// K <= 2816 (fine-grained and Zipf-skewed layers), so only from K = 4096 on.
-static int m128_tails_for(int K) { return K >= 4096 ? 1 : 0; }
+// M = 128 last tiles on CTA pairs (with 64-row A loads): measured 2% faster
+// on the Mixtral-sized step and about 1% on the fine-grained and Zipf-skewed
+// ones against 256-row tiles throughout.
+static int m128_tails_for(int) { return 1; }
 
 static Params base_params(const Ctx& c, int G, int64_t n_rows, const int32_t* offsets) {
   Params P{};
@@ -1649,7 +1656,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   R.out0 = static_cast<bf16*>(dw2);
   R.tma_out = make_wgrad_map(&mC, dw2, G, d, F);
   if (!R.tma_out) mC = mA;
-  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, R, kFc2Wgrad)
+  e = wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, mA, R, kFc2Wgrad)
             : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, R, kFc2Wgrad);
   if (e != cudaSuccess) return e;
   // fc1 wgrad: dW1_g [2F, d] = d_preᵀ x : A = d_pre [n_rows, 2F] MN-major, B = x_rows MN-major
@@ -1667,7 +1674,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   S.out0 = static_cast<bf16*>(dw1);
   S.tma_out = make_wgrad_map(&mC, dw1, G, 2 * F, d);
   if (!S.tma_out) mC = mA;
-  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, S, kFc1Wgrad)
+  return wpair ? launch_pair<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, mA, S, kFc1Wgrad)
                : launch_one<true, true, EPI_WGRAD>(c, mA, mB, mC, mC, S, kFc1Wgrad);
 }
 
