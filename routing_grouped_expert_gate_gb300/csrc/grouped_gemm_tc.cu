@@ -524,7 +524,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.tmem_full[a], 1);
-      mbar_init(&sh.tmem_empty[a], NUM_EPI_WARPS * 32);
+      mbar_init(&sh.tmem_empty[a], NUM_EPI_WARPS);  // one arrival per epilogue warp
     }
     for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(&sh.epi_load[w], 1);
     fence_barrier_init();
@@ -724,7 +724,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                            &sh.epi_load[warp - 2], epi_phase, sh.abort))
         break;
       tc_fence_before();
-      mbar_arrive(&sh.tmem_empty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.tmem_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -121,7 +121,7 @@ plane_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.acc_full[a], 1);
-      mbar_init(&sh.acc_empty[a], PB_EPI_WARPS * 32);
+      mbar_init(&sh.acc_empty[a], PB_EPI_WARPS);  // one arrival per epilogue warp
     }
     fence_barrier_init();
   }
@@ -256,7 +256,8 @@ plane_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         }
       }
       tc_fence_before();
-      mbar_arrive(&sh.acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -98,7 +98,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.acc_full[a], 1);
-      mbar_init(&sh.acc_empty[a], R_EPI_WARPS * 32);
+      mbar_init(&sh.acc_empty[a], R_EPI_WARPS);  // one arrival per fold warp
     }
     mbar_init(&sh.lo_full, 1);
     fence_barrier_init();
@@ -219,7 +219,8 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         }
       }
       tc_fence_before();
-      mbar_arrive(&sh.acc_empty[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
     }
     if (ok && mbar_wait(&sh.lo_full, 0, sh.abort, P, 25)) {
       tc_fence_after();
