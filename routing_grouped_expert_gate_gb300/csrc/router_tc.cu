@@ -140,48 +140,53 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       }
     }
   } else if (warp == 1) {
-    // ================= MMA issuer (whole warp walks; lane 0 issues) =================
-    constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
-    const uint32_t lo_acc = tmem + 2 * BN;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    int step = 0;
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 22)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t a_addr = su32(smem + stage * RT::kStage);
-      const uint32_t b_addr = a_addr + RT::kA;
-#pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk, ++step) {
-        const int win = step / fold;
-        const int pos = step - win * fold;
-        const int buf = win & 1;
-        if (pos == 0) {
-          // this buffer last held window win - 2: wait until it was folded
-          if (!mbar_wait(&sh.acc_empty[buf], ((win >> 1) & 1) ^ 1, sh.abort, P, 23)) {
-            ok = false;
-            break;
+    // ================= MMA issuer (lane 0) =================
+    // One thread walks the K loop: the four K16 steps of a stage unrolled,
+    // the operand descriptors formed once per stage (a K16 step advances the
+    // start address by 32 bytes, 2 in the descriptor's 16-byte units) and
+    // the window position kept as counters.
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
+      const uint32_t lo_acc = tmem + 2 * BN;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int step = 0, pos = 0, win = 0;  // K16 step, its place in the window, the window
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 22)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_addr = su32(smem + stage * RT::kStage);
+        const uint64_t da = sw128_desc(a_addr, 16, 1024);
+        const uint64_t db0 = sw128_desc(a_addr + RT::kA, 16, 1024);
+        const uint64_t db1 = sw128_desc(a_addr + RT::kA + RT::kB, 16, 1024);
+        const uint64_t db2 = sw128_desc(a_addr + RT::kA + 2 * RT::kB, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk, ++step) {
+          const int buf = win & 1;
+          if (pos == 0) {
+            // this buffer last held window win - 2: wait until it was folded
+            if (!mbar_wait(&sh.acc_empty[buf], ((win >> 1) & 1) ^ 1, sh.abort, P, 23)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
+          const uint64_t dk = (uint64_t)(2 * kk);
+          mma_bf16(tmem + buf * BN, da + dk, db0 + dk, IDESC, pos > 0 ? 1u : 0u);
+          mma_bf16(lo_acc, da + dk, db1 + dk, IDESC, step > 0 ? 1u : 0u);
+          mma_bf16(lo_acc, da + dk, db2 + dk, IDESC, 1u);
+          if (++pos == fold || step == steps - 1) {
+            mma_commit(&sh.acc_full[buf]);
+            pos = 0;
+            ++win;
+          }
         }
-        if (lane == 0) {
-          const uint64_t ad = sw128_desc(a_addr + kk * 32, 16, 1024);
-          mma_bf16(tmem + buf * BN, ad, sw128_desc(b_addr + kk * 32, 16, 1024), IDESC,
-                   pos > 0 ? 1u : 0u);
-          mma_bf16(lo_acc, ad, sw128_desc(b_addr + RT::kB + kk * 32, 16, 1024), IDESC,
-                   step > 0 ? 1u : 0u);
-          mma_bf16(lo_acc, ad, sw128_desc(b_addr + 2 * RT::kB + kk * 32, 16, 1024), IDESC, 1u);
-          if (pos == fold - 1 || step == steps - 1) mma_commit(&sh.acc_full[buf]);
-        }
-        __syncwarp();
+        if (!ok) break;
+        mma_commit(&sh.empty[stage]);
+        if (++stage == S) { stage = 0; phase ^= 1; }
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&sh.empty[stage]);
-      __syncwarp();
-      if (++stage == S) { stage = 0; phase ^= 1; }
+      if (ok) mma_commit(&sh.lo_full);
     }
-    if (ok && lane == 0) mma_commit(&sh.lo_full);
     __syncwarp();
   } else {
     // ================= fold + store: warps 2..9 =================
