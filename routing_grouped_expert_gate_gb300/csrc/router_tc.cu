@@ -14,13 +14,16 @@
 // (fold_k elements) and the epilogue warps then fold the window's sum into a
 // compensated (hi, lo) pair per logit (TwoSum), so the rounding that grows
 // with d stays inside one window. The x·W1 and x·W2 products are 2^-8 and
-// 2^-16 times smaller and accumulate in a third TMEM accumulator over all of
-// K; their rounding is far below fp32 resolution of the logit.
+// 2^-16 times smaller and accumulate over all of K in a 128-column TMEM
+// accumulator (x·W1 beside x·W2: the two plane tiles sit back to back in
+// shared memory, so one N = 128 MMA covers both); their rounding is far below
+// fp32 resolution of the logit.
 //
 // One CTA computes 128 tokens x 64 experts: warp 0 issues the TMA loads (x
 // tile + three W tiles per 64-wide K block), warp 1 owns 256 TMEM columns
-// (two 64-column window accumulators, one 64-column low-part accumulator) and
-// issues tcgen05.mma (M=128, N=64, K=16), warps 2..9 (two per TMEM lane
+// (two 64-column window accumulators, one 128-column low-part accumulator)
+// and issues two tcgen05.mma per K16 step (M=128, K=16; N=64 for x·W0, N=128
+// for x·W1 | x·W2), warps 2..9 (two per TMEM lane
 // quadrant, 32 columns each) fold the windows and write the logits; each fold
 // thread keeps its token's 32 (hi, lo) pairs in registers. Every mbarrier
 // wait is bounded (MOE_ERR_TIMEOUT + abort flag).
@@ -147,7 +150,8 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     // the window position kept as counters.
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
-      const uint32_t lo_acc = tmem + 2 * BN;
+      constexpr uint32_t IDESC_LO = idesc_bf16(false, false, 128, 2 * BN);
+      const uint32_t lo_acc = tmem + 2 * BN;  // x·W1 in its first BN columns, x·W2 after
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -159,7 +163,6 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         const uint64_t da = sw128_desc(a_addr, 16, 1024);
         const uint64_t db0 = sw128_desc(a_addr + RT::kA, 16, 1024);
         const uint64_t db1 = sw128_desc(a_addr + RT::kA + RT::kB, 16, 1024);
-        const uint64_t db2 = sw128_desc(a_addr + RT::kA + 2 * RT::kB, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk, ++step) {
           const int buf = win & 1;
@@ -173,8 +176,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           }
           const uint64_t dk = (uint64_t)(2 * kk);
           mma_bf16(tmem + buf * BN, da + dk, db0 + dk, IDESC, pos > 0 ? 1u : 0u);
-          mma_bf16(lo_acc, da + dk, db1 + dk, IDESC, step > 0 ? 1u : 0u);
-          mma_bf16(lo_acc, da + dk, db2 + dk, IDESC, 1u);
+          mma_bf16(lo_acc, da + dk, db1 + dk, IDESC_LO, step > 0 ? 1u : 0u);
           if (++pos == fold || step == steps - 1) {
             mma_commit(&sh.acc_full[buf]);
             pos = 0;
@@ -231,10 +233,13 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < NC; c += 32) {
-        float v[32];
-        tmem_ld32(base + 2 * BN + c, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) lo[c + i] += v[i];
+        for (int p = 0; p < 2; ++p) {  // x·W1, then x·W2
+          float v[32];
+          tmem_ld32(base + (2 + p) * BN + c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) lo[c + i] += v[i];
+        }
       }
       const int64_t t = (int64_t)m0 + row;
       const int e0 = n0 + half * NC;
