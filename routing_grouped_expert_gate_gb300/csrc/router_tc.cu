@@ -39,10 +39,33 @@ namespace rtc {
 
 using namespace tc;
 
-constexpr int R_THREADS = 320;
-constexpr int R_EPI_WARPS = 8;
-constexpr int R_TMEM_COLS = 256;
+constexpr int R_EPI_WARPS = 8;  // fold warps: R_EPI_WARPS / 4 per TMEM lane quadrant
+constexpr int R_THREADS = 64 + 32 * R_EPI_WARPS;
+constexpr int R_NWIN = 2;  // window accumulators in flight
+constexpr int R_TMEM_COLS = 256;  // R_NWIN windows of BN + the 2 BN low-part accumulator, rounded up
 constexpr int R_MAX_STAGES = 8;
+
+// 32 lanes x 16 or 32 consecutive fp32 TMEM columns; the wait takes the
+// registers as operands, so no use of them can move above it.
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 template <int BN>
 struct RTile {
@@ -65,8 +88,8 @@ struct RParams {
 struct __align__(8) RShared {
   uint64_t full[R_MAX_STAGES];
   uint64_t empty[R_MAX_STAGES];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full[R_NWIN];
+  uint64_t acc_empty[R_NWIN];
   uint64_t lo_full;
   uint32_t tmem_base;
   int abort;
@@ -78,7 +101,9 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  const RParams P) {
   using RT = RTile<BN>;
   constexpr int S = RT::kStages;
-  constexpr int NC = BN / 2;  // columns per fold warp
+  constexpr int NC = BN / (R_EPI_WARPS / 4);  // columns per fold warp
+  constexpr int CH = NC < 32 ? NC : 32;       // columns per TMEM read
+  static_assert(NC % CH == 0 && (CH == 16 || CH == 32), "fold warp columns");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -99,7 +124,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < R_NWIN; ++a) {
       mbar_init(&sh.acc_full[a], 1);
       mbar_init(&sh.acc_empty[a], R_EPI_WARPS);  // one arrival per fold warp
     }
@@ -151,11 +176,14 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
       constexpr uint32_t IDESC_LO = idesc_bf16(false, false, 128, 2 * BN);
-      const uint32_t lo_acc = tmem + 2 * BN;  // x·W1 in its first BN columns, x·W2 after
+      static_assert((R_NWIN + 2) * BN <= R_TMEM_COLS, "TMEM columns");
+      const uint32_t lo_acc = tmem + R_NWIN * BN;  // x·W1 in its first BN columns, x·W2 after
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int step = 0, pos = 0, win = 0;  // K16 step, its place in the window, the window
+      int step = 0, pos = 0;  // K16 step, its place in the window
+      int buf = 0;            // the window's accumulator
+      uint32_t wphase = 0;    // flips each time buf wraps
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 22)) { ok = false; break; }
         tc_fence_after();
@@ -165,10 +193,9 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         const uint64_t db1 = sw128_desc(a_addr + RT::kA + RT::kB, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk, ++step) {
-          const int buf = win & 1;
           if (pos == 0) {
-            // this buffer last held window win - 2: wait until it was folded
-            if (!mbar_wait(&sh.acc_empty[buf], ((win >> 1) & 1) ^ 1, sh.abort, P, 23)) {
+            // this buffer last held the window R_NWIN back: wait until it was folded
+            if (!mbar_wait(&sh.acc_empty[buf], wphase ^ 1, sh.abort, P, 23)) {
               ok = false;
               break;
             }
@@ -180,7 +207,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           if (++pos == fold || step == steps - 1) {
             mma_commit(&sh.acc_full[buf]);
             pos = 0;
-            ++win;
+            if (++buf == R_NWIN) { buf = 0; wphase ^= 1; }
           }
         }
         if (!ok) break;
@@ -193,9 +220,9 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   } else {
     // ================= fold + store: warps 2..9 =================
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 (the warp's quadrant)
-    const int half = (warp - 2) >> 2;
+    const int slice = (warp - 2) >> 2;  // the warp's NC of the tile's BN columns
     const int row = q * 32 + lane;
-    const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + half * NC;
+    const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + slice * NC;
     // Two levels: the window sums of a group of GROUP windows are added in
     // plain fp32 (round to nearest; the group's sum is a fraction of the
     // logit, so these roundings are far below the logit's ulp), and each
@@ -205,44 +232,46 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 #pragma unroll
     for (int j = 0; j < NC; ++j) hi[j] = lo[j] = grp[j] = 0.f;
     bool ok = true;
+    int buf = 0;
+    uint32_t wphase = 0;
     for (int win = 0; win < n_win; ++win) {
-      const int buf = win & 1;
-      if (!mbar_wait(&sh.acc_full[buf], (win >> 1) & 1, sh.abort, P, 24)) { ok = false; break; }
+      if (!mbar_wait(&sh.acc_full[buf], wphase, sh.abort, P, 24)) { ok = false; break; }
       tc_fence_after();
       const bool fold_now = (win % GROUP == GROUP - 1) || win == n_win - 1;
 #pragma unroll
-      for (int c = 0; c < NC; c += 32) {
-        float v[32];
-        tmem_ld32(base + buf * BN + c, v);
+      for (int c = 0; c < NC; c += CH) {
+        float v[CH];
+        tmem_ld_cols(base + buf * BN + c, v);
         if (fold_now) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < CH; ++i) {
             comp_add(hi[c + i], lo[c + i], __fadd_rn(grp[c + i], v[i]));
             grp[c + i] = 0.f;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) grp[c + i] = __fadd_rn(grp[c + i], v[i]);
+          for (int i = 0; i < CH; ++i) grp[c + i] = __fadd_rn(grp[c + i], v[i]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
+      if (++buf == R_NWIN) { buf = 0; wphase ^= 1; }
     }
     if (ok && mbar_wait(&sh.lo_full, 0, sh.abort, P, 25)) {
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < NC; c += 32) {
+      for (int c = 0; c < NC; c += CH) {
 #pragma unroll
         for (int p = 0; p < 2; ++p) {  // x·W1, then x·W2
-          float v[32];
-          tmem_ld32(base + (2 + p) * BN + c, v);
+          float v[CH];
+          tmem_ld_cols(base + (R_NWIN + p) * BN + c, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) lo[c + i] += v[i];
+          for (int i = 0; i < CH; ++i) lo[c + i] += v[i];
         }
       }
       const int64_t t = (int64_t)m0 + row;
-      const int e0 = n0 + half * NC;
+      const int e0 = n0 + slice * NC;
       if (t < P.T) {
         float* dst = P.logits + t * P.E + e0;
 #pragma unroll
