@@ -57,6 +57,11 @@ SMALL = {
     # segment's last tile of <= 128 rows as an M = 128 tile
     "mixtral_f4096_small": mi.shrink(W["mixtral_style"], name="mixtral_f4096_small", T=160,
                                      d=256, F=4096),
+    # d = 200: no multiple of the 64-wide K block or of the 32-column store box
+    # (router, fc1 and the weight gradients read a zero-filled last K block; fc2
+    # and the data gradients store a ragged last column box)
+    "ragged_d_small": mi.shrink(W["deepseek_v3_shaped"], name="ragged_d_small", T=200, d=200,
+                                E=64, k=6, F=96, F_shared=64, backward=True),
 }
 # bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
@@ -287,6 +292,38 @@ def test_small_router_hidden_sizes(built, E, d):
     assert err < 1e-6, err
     decided = r["gap"] >= 1e-6
     assert np.array_equal(to_np(idx)[decided], r["idx"][decided])
+
+
+@pytest.mark.parametrize("E,d,T", [(64, 200, 333), (128, 456, 129), (256, 1032, 257)])
+def test_router_gate_gemm_ragged_shapes(built, E, d, T):
+    """The tensor-core gate GEMM where d is no multiple of the 64-wide K block
+    (the last block's columns past d arrive as zeros) and T no multiple of
+    the 128-token tile: logits within 1e-6 of the float64 oracle, the
+    oracle's experts selected."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = mi.shrink(W["deepseek_v3_shaped"], name=f"router_tc_e{E}_d{d}_t{T}", T=T, d=d, E=E,
+                   F=64, F_shared=0)
+    inp = mi.make_inputs(wl, seed=11, device="cuda", with_dy=False)
+    cfg = moe.cfg_from_workload(wl)
+    assert L.router_uses_tensor_cores(cfg)
+    ref = {k: O.as_f64(v) for k, v in inp.items() if v is not None}
+    r = O.route(ref["x"], ref["w_router"], wl.k, wl.score, wl.scaling, ref.get("logit_bias"),
+                ref.get("sel_bias"))
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_ROUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+    logits = torch.full((wl.T, wl.E), float("nan"), device="cuda")
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.T, wl.k, device="cuda")
+    L.route_topk(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), inp.get("sel_bias"),
+                 logits, idx, w, ws)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    err = float(np.max(np.abs(to_np(logits) - r["logits"])))
+    assert err < 1e-6, err
+    decided = r["gap"] >= 1e-6
+    assert np.array_equal(to_np(idx)[decided], r["idx"][decided])
+    assert_close("w", to_np(w)[decided], r["w"][decided], TOL_F32)
 
 
 def test_zero_load_experts_exist_in_skewed_case(built):
