@@ -38,7 +38,8 @@ notes of the repository):
   * top-k ties: descending key, equal keys go to the lower expert index; the
     decision is taken on the key rounded once to fp32, the router's dtype
   * aux-loss probabilities: the softmax over all E logits (no bias); for the
-    sigmoid router, s / sum_e s (parity unpinned there except by invariants)
+    sigmoid router, s / sum_e s (parity unpinned there except by invariants
+    and a case of the reading worked by hand)
   * counts come from the final selection (bias included) and carry no gradient
   * the combine and every reduction are exact sums in float64
 

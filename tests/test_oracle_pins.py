@@ -255,6 +255,26 @@ def test_aux_loss_uniform_routing_equals_coeff():
     assert O.aux_loss(logits, counts, k, coeff, "sigmoid") == pytest.approx(coeff, rel=1e-14)
 
 
+def test_sigmoid_aux_reading_hand_worked():
+    """The sigmoid router's aux probabilities, read as s / sum_e s (the pages
+    give no form), on two tokens and two experts worked by hand: logits
+    (0, ln 3) and (-ln 3, ln 3) give scores (1/2, 3/4) and (1/4, 3/4), so
+    P = (2/5, 3/5) and (1/4, 3/4); top-1 sends both tokens to expert 1
+    (counts 0, 2) and aux = coeff * 2 / (1 * 2^2) * 2 * (3/5 + 3/4)
+    = 1.35 coeff. A softmax over all experts would give 1.65 coeff and the
+    unnormalised scores 1.5 coeff."""
+    l3 = np.log(3.0)
+    logits = np.array([[0.0, l3], [-l3, l3]])
+    idx = O.topk_sorted(O.sigmoid(logits), 1)
+    assert idx[:, 0].tolist() == [1, 1]
+    counts = O.dispatch(idx, 2)["counts"]
+    assert counts.tolist() == [0, 2]
+    np.testing.assert_allclose(O.aux_probs(logits, "sigmoid"), [[0.4, 0.6], [0.25, 0.75]],
+                               rtol=1e-15)
+    assert O.aux_loss(logits, counts, 1, 0.1, "sigmoid") == pytest.approx(0.135, rel=1e-14)
+    assert O.aux_loss(logits, counts, 1, 0.1, "softmax") == pytest.approx(0.165, rel=1e-14)
+
+
 def test_aux_loss_single_expert_is_one():
     g = _load("handbook_counts.json")["single_expert_aux"]
     rng = np.random.default_rng(5)
