@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip timing the router's optional companions (z-loss, sequence "
                          "aux loss, bias update, MaxVio) after the step")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip replaying the step from a CUDA graph after the timed region")
     ap.add_argument("--stage", default=None, choices=["route"],
                     help="time one stage alone at the workload's full size, drawing only its "
                          "inputs (a profiling aid; prints a stage line, not the step line)")
@@ -198,6 +200,44 @@ def recorded_traffic(workload, kernel_key):
 
 
 # ------------------------------------------------------------------ our arm
+def time_graph(L, step, K, dist, dev, ws, T):
+    """The step captured once into a CUDA graph and replayed K times (after
+    three untimed replays): the same kernels in the same order, with no host
+    work per launch. Timed with events on the replaying stream, max over ranks."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    n0 = L.launch_count()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    per_step = L.launch_count() - n0
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / K
+    rc, detail = L.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after graph replays: {rc} ({L.status_string(rc)}) {detail}")
+    return {"ms_per_step": round(ms, 4), "value": job_throughput(ws, T, ms), "replays": K,
+            "gpu_launches": per_step * K,
+            "note": "the step captured once into a CUDA graph and replayed; value in the same unit"}
+
+
 def time_extras(L, cfg, b, T, K):
     """The router's optional companions, timed one by one on the step's own
     logits, indices and counts after the timed step (not part of the step):
@@ -384,11 +424,8 @@ def run_ours(args, ws, rank, local):
     if rc != 0:
         raise RuntimeError(f"device status after warm-up: {rc} ({L.status_string(rc)}) {detail}")
 
-    # ---- timed region: K steps, events around every call
+    # ---- timed region: K steps and nothing else on the stream
     K = args.steps
-    names = [n for n, _ in step_calls]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step_calls) + 1)]
-          for _ in range(K)]
     clocks = ClockSampler(local)
     if dist:
         dist.barrier()
@@ -396,27 +433,39 @@ def run_ours(args, ws, rank, local):
     clocks.start()
     time.sleep(0.3)
     launches0 = L.launch_count()
-    L.kernel_timing(True)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     host_t0 = time.monotonic()
     t_start.record(stream)
     for i in range(K):
-        ev[i][0].record(stream)
-        for j, (_, fn) in enumerate(step_calls):
-            fn()
-            ev[i][j + 1].record(stream)
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     host_t1 = time.monotonic()
     launches = L.launch_count() - launches0
-    L.kernel_timing(False)
-    ktimes = L.kernel_times()
     clk = clocks.stop(window=(host_t0, host_t1))
     if dist:
         dist.barrier()
     total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
     ms_per_step = total_ms / K
+
+    # ---- the breakdown: K more steps with events around every call and the
+    # library's events around each GEMM launch (they cost a little time of
+    # their own, so the step time above is taken without them)
+    names = [n for n, _ in step_calls]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step_calls) + 1)]
+          for _ in range(K)]
+    L.kernel_timing(True)
+    torch.cuda.synchronize()
+    for i in range(K):
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(step_calls):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    L.kernel_timing(False)
+    ktimes = L.kernel_times()
+    breakdown_ms = ev[0][0].elapsed_time(ev[K - 1][len(step_calls)]) / K
     stage_ms = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
                 for j, n in enumerate(names)}
     rc, detail = L.last_device_status()
@@ -502,11 +551,14 @@ def run_ours(args, ws, rank, local):
         "roofline": roofline,
         "kernels": kernels,
         "stages": stages,
+        "breakdown_ms_per_step": round(breakdown_ms, 4),
         "gpu_launches": int(launches),
         "clocks": clk,
         "peaks": dict(peaks, fp32_alu_tflops=round(fp32_peak, 2)),
     }
     out["value"] = job_throughput(ws, T, ms_per_step)
+    if not args.no_graph:
+        out["graph"] = time_graph(L, step, K, dist, dev, ws, T)
     if not args.no_extras:
         out["extras"] = time_extras(L, cfg, b, T, K)
 
