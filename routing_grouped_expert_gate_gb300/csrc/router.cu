@@ -352,10 +352,7 @@ static cudaError_t launch_router_tiled(const Ctx& c, const Tx* x, const float* w
 // One warp per token. Lane l holds experts l, l+32, ... The k winners are found
 // by k rounds of a warp arg-max over (key descending, index ascending); a
 // non-finite key counts as -inf so a valid expert always wins.
-__device__ __forceinline__ bool outranks(float ka, int ea, float kb, int eb) {
-  return ka > kb || (ka == kb && ea < eb);
-}
-
+//
 // Quantile routing (beta != NULL): the key is the score minus beta, k + 1
 // experts are ranked, the first k are chosen and the (k+1)-th key is written
 // to alpha[t] (the token's threshold).
@@ -370,7 +367,6 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
     float key[EPL], lg[EPL];
-    bool taken[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
@@ -380,11 +376,9 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
         key[i] = (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE)
                      ? l : bias_score(l, score_fn);
         lg[i] = l;
-        taken[i] = false;
       } else {
         key[i] = -INFINITY;
         lg[i] = 0.f;
-        taken[i] = true;
       }
     }
     // pre-softmax: the key is the probability under the softmax over all E
@@ -417,82 +411,71 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
         key[i] = (kv == kv) ? kv : -INFINITY;
       }
     }
-    int sel_e[kMaxK + 1];
-    float sel_l[kMaxK + 1], sel_key[kMaxK + 1];
+    // Each candidate as one 64-bit integer that orders like (key descending,
+    // expert ascending): the key's bits made order-preserving as unsigned
+    // (-0 counted as +0) above the complemented expert index; slots past E hold
+    // 0, below every expert. Round j takes the warp's largest remaining value
+    // (a local max, then a butterfly max), its owner clears it, and lane j
+    // keeps the winner's expert and key.
+    uint64_t pk[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        uint32_t b = __float_as_uint(key[i] + 0.f);
+        b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        pk[i] = ((uint64_t)b << 32) | (uint64_t)(~(uint32_t)e);
+      } else {
+        pk[i] = 0ull;
+      }
+    }
+    int my_e = 0;
+    float my_key = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK + 1; ++j) {
-      sel_e[j] = 0;
-      sel_l[j] = 0.f;
-      sel_key[j] = 0.f;
       if (j < ksel) {
-        float bk = -INFINITY;
-        int be = 0x7fffffff;
+        uint64_t best = pk[0];
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-          if (!taken[i] && outranks(key[i], lane + 32 * i, bk, be)) {
-            bk = key[i];
-            be = lane + 32 * i;
-          }
+        for (int i = 1; i < EPL; ++i) best = pk[i] > best ? pk[i] : best;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-          const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-          if (outranks(ok, oe, bk, be)) {
-            bk = ok;
-            be = oe;
-          }
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+          best = o > best ? o : best;
         }
-        const int owner = be & 31, slot = be >> 5;
-        float l_own = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-          if (i == slot) {
-            if (lane == owner) taken[i] = true;
-            l_own = lg[i];
-          }
-        sel_e[j] = be;
-        sel_key[j] = bk;
-        sel_l[j] = __shfl_sync(0xffffffffu, l_own, owner);
+          if (pk[i] == best) pk[i] = 0ull;
+        if (lane == j) {
+          my_e = (int)(~(uint32_t)best);
+          uint32_t b = (uint32_t)(best >> 32);
+          b = (b & 0x80000000u) ? (b & 0x7fffffffu) : ~b;
+          my_key = best == 0ull ? -INFINITY : __uint_as_float(b);
+        }
       }
     }
-    if (alpha != nullptr && lane == 0) alpha[t] = sel_key[k];
-    // mixing weights of the chosen experts
-    float wv[kMaxK];
+    if (alpha != nullptr) {
+      const float ak = __shfl_sync(0xffffffffu, my_key, k);
+      if (lane == 0) alpha[t] = ak;
+    }
+    // mixing weights: lane j < k weighs the j-th chosen expert
+    const bool mine = lane < k;
+    const float l_j = mine ? logits[t * E + my_e] : 0.f;
+    float wj;
     if (score_fn == MOE_SCORE_SOFTMAX) {
-      float m = sel_l[0];
-#pragma unroll
-      for (int j = 1; j < kMaxK; ++j)
-        if (j < k) m = fmaxf(m, sel_l[j]);
-      float s = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        wv[j] = (j < k) ? expf(sel_l[j] - m) : 0.f;
-        s += wv[j];
-      }
-      const float inv = scaling / s;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) wv[j] *= inv;
+      const float m = warp_max(mine ? l_j : -INFINITY);
+      const float ex = mine ? expf(l_j - m) : 0.f;
+      wj = ex * (scaling / warp_sum(ex));
     } else if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        wv[j] = (j < k) ? expf(sel_l[j] - pre_max) * pre_inv * scaling : 0.f;
+      wj = mine ? expf(l_j - pre_max) * pre_inv * scaling : 0.f;
     } else {
-      float s = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        wv[j] = (j < k) ? bias_score(sel_l[j], score_fn) : 0.f;
-        s += wv[j];
-      }
-      const float inv = (k > 1) ? scaling / (s + 1e-20f) : scaling;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) wv[j] *= inv;
+      const float sj = mine ? bias_score(l_j, score_fn) : 0.f;
+      const float sum = warp_sum(sj);
+      wj = sj * ((k > 1) ? scaling / (sum + 1e-20f) : scaling);
     }
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j < k && lane == j) {
-        idx[t * k + j] = sel_e[j];
-        w[t * k + j] = wv[j];
-      }
+    if (mine) {
+      idx[t * k + lane] = my_e;
+      w[t * k + lane] = wj;
+    }
   }
 }
 
