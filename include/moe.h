@@ -24,7 +24,13 @@
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and never synchronises the host. Work whose size depends
  *    on the routing (the per-expert segments) is scheduled on the device from
- *    the offsets array, with no copy back to the host.
+ *    the offsets array, with no copy back to the host. So every call can be
+ *    captured into a CUDA graph: after one call of each kind on the device
+ *    (which sets function attributes once), a captured sequence replays to
+ *    the same bytes as the same calls issued on a stream. Tensor maps are
+ *    encoded at the call, so a captured call stays bound to the buffers it
+ *    was captured with. (moe_last_device_status synchronises and is not
+ *    capturable.)
  *  - Layouts are row-major and dense. act dtype (cfg->act_dtype) is bf16 or
  *    fp32 for x, expert weights and every activation; the router (W_r,
  *    logits, weights w, their gradients) is always fp32; indices are int32.
