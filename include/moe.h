@@ -456,12 +456,10 @@ int moe_selftest_wait_timeout(moe_stream_t stream);
 /* Which kernels run the grouped expert GEMMs (moe_grouped_swiglu and its
  * backward). MOE_GEMM_AUTO (default): bf16 on the tcgen05 tensor cores, with
  * the forward and data-gradient contractions on CTA pairs (cta_group::2) when
- * the segments average at least 512 rows and on single CTAs otherwise (2-CTA
- * clusters that multicast the shared A tile when the N tiles pair up), and
+ * the segments average at least 512 rows and on single CTAs otherwise, and
  * the weight gradients on CTA pairs; fp32 on CUDA cores.
  * MOE_GEMM_TC_SINGLE_CTA / MOE_GEMM_TC_PAIRS: bf16 on single-CTA / CTA-pair
  * tcgen05 kernels whatever the segment sizes (the weight gradients too).
- * MOE_GEMM_TC_SINGLE_CTA_NO_MULTICAST: single CTAs without the A multicast.
  * MOE_GEMM_CUDA_CORES: every dtype on the CUDA-core kernels (fp32
  * accumulation). All but the first are for cross-checking. Process-wide;
  * returns the previous setting, or MOE_ERR_INVALID_ARG. */
@@ -469,7 +467,6 @@ int moe_selftest_wait_timeout(moe_stream_t stream);
 #define MOE_GEMM_CUDA_CORES    1
 #define MOE_GEMM_TC_SINGLE_CTA 2
 #define MOE_GEMM_TC_PAIRS      3
-#define MOE_GEMM_TC_SINGLE_CTA_NO_MULTICAST 4
 int moe_set_grouped_gemm_impl(int impl);
 
 /* Which kernels compute the router's gate GEMM (moe_route_topk).

@@ -43,7 +43,6 @@ MOE_GEMM_AUTO = 0
 MOE_GEMM_CUDA_CORES = 1
 MOE_GEMM_TC_SINGLE_CTA = 2
 MOE_GEMM_TC_PAIRS = 3
-MOE_GEMM_TC_SINGLE_CTA_NO_MULTICAST = 4
 
 MOE_WS_PERMUTE = 0
 MOE_WS_GROUPED = 1

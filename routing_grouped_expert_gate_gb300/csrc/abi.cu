@@ -216,13 +216,10 @@ int moe_kernel_times(float* ms_total, int32_t* launches) {
 
 int moe_set_grouped_gemm_impl(int impl) {
   if (impl != MOE_GEMM_AUTO && impl != MOE_GEMM_CUDA_CORES && impl != MOE_GEMM_TC_SINGLE_CTA &&
-      impl != MOE_GEMM_TC_PAIRS && impl != MOE_GEMM_TC_SINGLE_CTA_NO_MULTICAST)
+      impl != MOE_GEMM_TC_PAIRS)
     return MOE_ERR_INVALID_ARG;
   static std::atomic<int> g_public{MOE_GEMM_AUTO};
-  tc_set_mode(impl == MOE_GEMM_TC_SINGLE_CTA                ? 1
-              : impl == MOE_GEMM_TC_PAIRS                   ? 2
-              : impl == MOE_GEMM_TC_SINGLE_CTA_NO_MULTICAST ? 3
-                                                            : 0);
+  tc_set_mode(impl == MOE_GEMM_TC_SINGLE_CTA ? 1 : impl == MOE_GEMM_TC_PAIRS ? 2 : 0);
   g_gemm_impl.store(impl == MOE_GEMM_CUDA_CORES ? MOE_GEMM_CUDA_CORES : MOE_GEMM_AUTO);
   return g_public.exchange(impl);
 }

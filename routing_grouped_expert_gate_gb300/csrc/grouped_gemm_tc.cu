@@ -239,11 +239,8 @@ __device__ __forceinline__ EpiCols epi_cols(int q, int lane, int half, bool pair
   return e;
 }
 
-// MCAST: the two CTAs of a cluster take neighbouring N tiles (2j, 2j + 1) of
-// the same expert and M tile; t counts such tile pairs.
-template <bool KGROUPED, int EPI, bool MCAST = false>
-__device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, int t,
-                                            uint32_t rank = 0) {
+template <bool KGROUPED, int EPI>
+__device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, int t) {
   Tile ti;
   if (!KGROUPED) {
     int lo = 0, hi = P.G;
@@ -255,8 +252,7 @@ __device__ __forceinline__ Tile decode_tile(const Shared& sh, const Params& P, i
     const int rows = sh.off[g + 1] - sh.off[g];
     const int mt = (rows + BM - 1) / BM;
     const int local = t - sh.prefix[g];
-    const int nj = local / mt, mi = local - nj * mt;
-    const int ni = MCAST ? 2 * nj + (int)rank : nj;
+    const int ni = local / mt, mi = local - ni * mt;
     ti.grp = g;
     ti.m0 = sh.off[g] + mi * BM;
     ti.m_end = sh.off[g + 1];
@@ -488,12 +484,7 @@ __device__ __forceinline__ void zero_wgrad_tile(const Params& P, const Tile& ti,
 }
 
 // ---------------------------------------------------------------- the kernel
-// MCAST (M-grouped, K-major A, an even number of N tiles): a 2-CTA cluster
-// computes the two neighbouring N tiles of one M tile; each CTA loads half of
-// the shared A tile (64 rows) and multicasts it into both CTAs, so a CTA reads
-// 40 KB per K block from L2 instead of 48 KB. A stage is free again once both
-// CTAs' MMAs have read it (each commit arrives on both CTAs' `empty`).
-template <bool A_MN, bool B_MN, int EPI, bool MCAST>
+template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -507,20 +498,18 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint8_t* epi_buf = smem + STAGES * STAGE_BYTES;  // 1024-byte aligned
   Shared& sh = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES + EPI_BUF_BYTES);
 
-  static_assert(!MCAST || (!A_MN && EPI != EPI_WGRAD), "multicast: M-grouped, K-major A");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const uint32_t rank = MCAST ? cluster_ctarank() : 0u;
-  const int tile0 = MCAST ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int tstep = MCAST ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int tile0 = (int)blockIdx.x;
+  const int tstep = (int)gridDim.x;
 
   // ---- set-up: segment offsets, tile prefix, barriers, TMEM
   if (tid == 0) {
     sh.abort = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], MCAST ? 2 : 1);
+      mbar_init(&sh.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.tmem_full[a], 1);
@@ -552,7 +541,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int acc = 0;
       for (int g = 0; g < P.G; ++g) {
         sh.prefix[g] = acc;
-        acc += ((sh.off[g + 1] - sh.off[g] + BM - 1) / BM) * (MCAST ? P.NT / 2 : P.NT);
+        acc += ((sh.off[g + 1] - sh.off[g] + BM - 1) / BM) * P.NT;
       }
       sh.prefix[P.G] = acc;
       sh.total_tiles = acc;
@@ -583,7 +572,6 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
-  if (MCAST) cluster_barrier();  // the peer's barriers exist before any multicast
   tc_fence_after();
 
   const int total = sh.total_tiles;
@@ -598,9 +586,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       // the A and B boxes of k-block kb of tile ti
       auto kblock = [&](const Tile& ti, int kb, uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar) {
         const int k0 = kb * BK;
-        if (MCAST) {  // this CTA's 64 rows of the A tile, into both CTAs
-          tma_load_2d_mc(a_dst + 8192 * rank, &tmA, bar, k0, ti.m0 + 64 * (int)rank, 0x3);
-        } else if (!A_MN) {
+        if (!A_MN) {
           tma_load_2d(a_dst, &tmA, bar, k0, ti.m0);
         } else {
           for (int h = 0; h < 2; ++h)
@@ -623,7 +609,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t phase = 0;
       bool ok = true;
       for (int t = tile0; t < total && ok; t += tstep) {
-        const Tile ti = decode_tile<KGROUPED, EPI, MCAST>(sh, P, t, rank);
+        const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
         for (int kb = 0; kb < ti.nk; ++kb) {
           if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh.abort, P, 1)) { ok = false; break; }
           uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
@@ -648,7 +634,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = tile0; t < total && ok; t += tstep) {
-      const Tile ti = decode_tile<KGROUPED, EPI, MCAST>(sh, P, t, rank);
+      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
       if (ti.nk == 0) continue;  // empty segment: the epilogue writes zeros itself
       if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 2)) { ok = false; break; }
       tc_fence_after();
@@ -689,8 +675,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             else bd = sw128_desc(b_addr + kk * 2048, 8192, 1024);
             mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (MCAST) mma_commit_mc(&sh.empty[stage], 0x3);
-          else mma_commit(&sh.empty[stage]);
+          mma_commit(&sh.empty[stage]);
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -711,7 +696,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = tile0; t < total; t += tstep) {
-      const Tile ti = decode_tile<KGROUPED, EPI, MCAST>(sh, P, t, rank);
+      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
       if (EPI == EPI_WGRAD && ti.nk == 0) {
         zero_wgrad_tile(P, ti, row_in_tile, half, &tmC, ebuf);
         continue;
@@ -734,7 +719,6 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
-  if (MCAST) cluster_barrier();  // neither CTA leaves while the other may still address it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -1310,44 +1294,26 @@ static void timing_mark(int kind, cudaStream_t s, bool start) {
   v.push_back(e);
 }
 
-template <bool A_MN, bool B_MN, int EPI, bool MCAST = false>
+template <bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
                               const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
                               int kind) {
-  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI, MCAST>;
+  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
   static std::atomic<uint64_t> attr_set_mask{0};
-  static int max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = c.stream;
-  cfg.attrs = MCAST ? attr : nullptr;
-  cfg.numAttrs = MCAST ? 1 : 0;
   if (!(attr_set_mask.load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    int n = c.sm_count / 2;
-    if (MCAST) {
-      cfg.gridDim = dim3(c.sm_count & ~1);
-      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-      if (e != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        n = c.sm_count / 2;
-      }
-    }
-    max_clusters[dev & 63] = n;
     attr_set_mask.fetch_or(bit);
   }
-  cfg.gridDim = dim3(MCAST ? 2 * max_clusters[dev & 63] : c.sm_count);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.sm_count);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = c.stream;
   timing_mark(kind, c.stream, true);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, P);
   note_launches(1);
@@ -1411,9 +1377,7 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
   return e;
 }
 
-// M-grouped contractions (K-major A): CTA pairs; else single CTAs whose
-// clusters multicast the A tile along N when the N tiles pair up (not in mode
-// 3, single CTAs without multicast); else plain single CTAs.
+// M-grouped contractions (K-major A): CTA pairs or single CTAs.
 template <bool B_MN, int EPI>
 static cudaError_t launch_mgrouped(const Ctx& c, bool pair, const CUtensorMap& ma, const void* a,
                                    int64_t a_rows, int64_t a_cols, const CUtensorMap& mb,
@@ -1424,9 +1388,7 @@ static cudaError_t launch_mgrouped(const Ctx& c, bool pair, const CUtensorMap& m
     if (!make_map(&ma64, a, a_rows, a_cols, 64)) return cudaErrorInvalidValue;
     return launch_pair<false, B_MN, EPI>(c, ma, mb, mc, md, ma64, P, kind);
   }
-  if (g_tc_mode.load() != 3 && P.NT % 2 == 0 && make_map(&ma64, a, a_rows, a_cols, 64))
-    return launch_one<false, B_MN, EPI, true>(c, ma64, mb, mc, md, P, kind);
-  return launch_one<false, B_MN, EPI, false>(c, ma, mb, mc, md, P, kind);
+  return launch_one<false, B_MN, EPI>(c, ma, mb, mc, md, P, kind);
 }
 
 // M = 128 last tiles on CTA pairs (with 64-row A loads): measured 2% faster
@@ -1561,7 +1523,7 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
   cudaError_t e;
   // the weight gradients' per-expert tail maps sit at the end of the workspace
   const int mode = g_tc_mode.load();
-  const bool wpair = mode != 1 && mode != 3;  // weight gradients: CTA pairs unless single-CTA
+  const bool wpair = mode != 1;  // weight gradients: CTA pairs unless single-CTA
   CUtensorMap* tail_maps = nullptr;
   if (n_rows > 0 && wpair && ws != nullptr && ws_bytes >= tc_tail_maps_bytes(G)) {
     const uintptr_t end = reinterpret_cast<uintptr_t>(ws) + ws_bytes;

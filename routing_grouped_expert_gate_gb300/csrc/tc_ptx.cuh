@@ -190,7 +190,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn, int m, i
 // missing or the encoder refuses the arguments.
 bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 
-// ---- 2-CTA clusters: rank, DSMEM addresses, barriers, multicast copies and commits
+// ---- 2-CTA clusters: rank, DSMEM addresses, barriers
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -216,25 +216,6 @@ __device__ __forceinline__ void fence_async_shared_cluster() {
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
-}
-// TMA load of one box into the same shared-memory offset of every CTA in
-// `mask`, each copy completing on the barrier at `bar`'s offset in its CTA
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar)), "h"(mask)
-      : "memory");
-}
-// commit of this CTA's MMAs, arriving on the barrier at `bar`'s offset in
-// every CTA of `mask`
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(su32(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 }  // namespace tc

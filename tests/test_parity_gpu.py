@@ -68,8 +68,6 @@ SMALL = {
 CASES = ([(n, "native", "tcgen05") for n in SMALL if n != "tiny_fp32"]
          + [(n, "native", "tcgen05_1cta") for n in SMALL if n != "tiny_fp32"]
          + [(n, "native", "tcgen05_pairs") for n in SMALL if n != "tiny_fp32"]
-         + [(n, "native", "tcgen05_1cta_nomc") for n in ("mixtral_small", "deepseek_small",
-                                                         "zipf_small")]
          + [(n, "native", "cudacores") for n in SMALL]
          + [(n, "f32", "cudacores") for n in SMALL if n != "tiny_fp32"])
 
@@ -92,7 +90,6 @@ def run_gpu(wl, seed=0, backward=True, impl="tcgen05"):
     old = L.set_grouped_gemm_impl({"tcgen05": L.MOE_GEMM_AUTO,
                                    "tcgen05_1cta": L.MOE_GEMM_TC_SINGLE_CTA,
                                    "tcgen05_pairs": L.MOE_GEMM_TC_PAIRS,
-                                   "tcgen05_1cta_nomc": L.MOE_GEMM_TC_SINGLE_CTA_NO_MULTICAST,
                                    "cudacores": L.MOE_GEMM_CUDA_CORES}[impl])
     # the CUDA-core run also takes the router's gate GEMM off the tensor cores
     old_r = L.set_router_impl(L.MOE_ROUTER_CUDA_CORES if impl == "cudacores"
