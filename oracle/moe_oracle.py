@@ -220,11 +220,24 @@ def mixing_weights(logits: np.ndarray, idx: np.ndarray, score: str,
 
 
 def route(x, w_router, k: int, score: str, scaling: float = 1.0,
-          logit_bias=None, sel_bias=None) -> Dict[str, np.ndarray]:
-    """S1 + S2 for every token: logits, sorted indices, weights, near-tie gaps."""
+          logit_bias=None, sel_bias=None, idx=None) -> Dict[str, np.ndarray]:
+    """S1 + S2 for every token: logits, sorted indices, weights, near-tie gaps.
+
+    `idx` [T, k], when given, is taken as the selection instead of the top-k of
+    the keys (a token whose k-th and (k+1)-th keys tie to within rounding may
+    be decided either way; everything after the choice follows the same
+    definitions). Each row must hold k distinct experts.
+    """
     logits = gate_logits(x, w_router, logit_bias)
     keys = selection_keys(logits, score, sel_bias)
-    idx = topk_sorted(keys, k)
+    if idx is None:
+        idx = topk_sorted(keys, k)
+    else:
+        idx = np.asarray(idx, dtype=np.int64)
+        E = logits.shape[1]
+        if idx.shape != (logits.shape[0], k) or np.any((idx < 0) | (idx >= E)) or any(
+                len(set(r)) != k for r in idx.tolist()):
+            raise ValueError("a given selection needs k distinct experts per token")
     w = mixing_weights(logits, idx, score, scaling)
     return {"logits": logits, "keys": keys, "idx": idx, "w": w, "gap": kth_gap(keys, k)}
 
@@ -620,10 +633,12 @@ def quantile_beta_update(beta: np.ndarray, accum: np.ndarray, count: int,
 # whole layer, forward
 # ----------------------------------------------------------------------------
 
-def layer_forward(wl, inp: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
-    """S1..S7 for a workload `wl` (moe_inputs.Workload) on float64 inputs."""
+def layer_forward(wl, inp: Dict[str, np.ndarray], idx=None) -> Dict[str, np.ndarray]:
+    """S1..S7 for a workload `wl` (moe_inputs.Workload) on float64 inputs.
+
+    `idx`: an optional given selection (see route)."""
     r = route(inp["x"], inp["w_router"], wl.k, wl.score, wl.scaling,
-              inp.get("logit_bias"), inp.get("sel_bias"))
+              inp.get("logit_bias"), inp.get("sel_bias"), idx=idx)
     act = act_of(wl)
     dsp = dispatch(r["idx"], wl.E)
     x_perm = permute_rows(inp["x"], dsp["src_tok"])

@@ -325,6 +325,37 @@ def test_grouped_matches_per_token_evaluation():
     np.testing.assert_allclose(tf["y"], f["y"], rtol=1e-12, atol=1e-12)
 
 
+def test_given_selection_on_exact_ties():
+    """Where the k-th and (k+1)-th keys tie exactly, either expert is a valid
+    choice (by default the lower index wins). The oracle takes a given
+    selection and continues with the same definitions: the output of each tied
+    token equals its per-token evaluation under that selection (a separate
+    code path: one FFN per chosen expert, weighted sum), the weights are the
+    softmax over the chosen logits, the counts move by one per tie, and a
+    selection that repeats an expert is refused."""
+    wl, inp = _tiny(E=4, k=2, T=24, seed=2)
+    inp["w_router"][2] = inp["w_router"][1]  # experts 1 and 2 tie on every token
+    f = O.layer_forward(wl, inp)
+    ties = np.nonzero(f["gap"] == 0.0)[0]
+    assert ties.size >= 2
+    given = f["idx"].copy()
+    for t in ties:
+        assert 1 in given[t] and 2 not in given[t]  # the lower index won
+        given[t][given[t] == 1] = 2
+    g = O.layer_forward(wl, inp, idx=given)
+    np.testing.assert_array_equal(g["idx"], given)
+    np.testing.assert_allclose(g["w"], f["w"], rtol=0, atol=1e-15)
+    tf = O.tokens_forward(wl, inp, list(ties), routing={"idx": given, "w": g["w"]})
+    np.testing.assert_allclose(g["y"][ties], tf["y"], rtol=1e-12, atol=1e-12)
+    assert np.max(np.abs(g["y"][ties] - f["y"][ties])) > 1e-3  # the choice matters
+    assert g["counts"][2] == f["counts"][2] + ties.size
+    assert g["counts"][1] == f["counts"][1] - ties.size
+    bad = given.copy()
+    bad[0] = [0, 0]
+    with pytest.raises(ValueError):
+        O.layer_forward(wl, inp, idx=bad)
+
+
 # ---------------------------------------------------------------- gradients
 
 def _fd_check(wl, inp, keys, eps=1e-6, rtol=2e-6, atol=1e-9):
