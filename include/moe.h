@@ -325,6 +325,17 @@ int moe_gate_logits(const moe_cfg* cfg, const void* x, const float* w_router,
                     const float* logit_bias, float* logits, void* ws, size_t ws_bytes,
                     moe_stream_t stream);
 
+/* Near ties of S2 (a diagnostic, not a step of the layer): *count = the
+ * number of tokens whose k-th and (k+1)-th selection keys differ by less than
+ * `band` (>= 0). The keys are the fp32 values moe_route_topk ranks (the
+ * logits for softmax, the probabilities for pre-softmax, sigmoid or
+ * sqrt(softplus) scores + sel_bias otherwise); for such a token the choice
+ * between the two experts rests on rounding (Handbook §3.1 "Precision": the
+ * router runs in fp32 so that these decisions are stable). count is one
+ * device int32, overwritten; 0 when k = E. Asynchronous on `stream`.       */
+int moe_route_near_ties(const moe_cfg* cfg, const float* logits, const float* sel_bias,
+                        float band, int32_t* count, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Quantile balancing (Handbook §3.3 "Load balancing", part "Quantile").
  * moe_quantile_route: per token, rank the experts by key = score - beta[e]

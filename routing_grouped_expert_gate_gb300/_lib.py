@@ -119,6 +119,7 @@ _SIGS = {
     "moe_set_grouped_gemm_impl": (c_int, [c_int]),
     "moe_set_router_impl": (c_int, [c_int]),
     "moe_gate_logits": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
+    "moe_route_near_ties": (c_int, [POINTER(MoeCfg), _VP, _VP, c_float, _VP, _VP]),
     "moe_quantile_route": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_quantile_accumulate": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP]),
     "moe_quantile_beta_update": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, c_float, _VP]),
@@ -359,6 +360,13 @@ def gate_logits(cfg, x, w_router, logit_bias, logits, ws=None, stream=None):
     _check(lib.moe_gate_logits(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias),
                                _p(logits), _p(ws), _nbytes(ws), _stream(stream)),
            "moe_gate_logits")
+
+
+def route_near_ties(cfg, logits, sel_bias, band, count, stream=None):
+    """count[0] (device int32) = tokens whose k-th and (k+1)-th keys differ by < band."""
+    _check(lib.moe_route_near_ties(ctypes.byref(cfg), _p(logits), _p(sel_bias), float(band),
+                                   _p(count), _stream(stream)),
+           "moe_route_near_ties")
 
 
 def quantile_route(cfg, logits, beta, idx, w, alpha, beta_local=None, stream=None):

@@ -296,6 +296,19 @@ int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
   return MOE_OK;
 }
 
+int moe_route_near_ties(const moe_cfg* cfg, const float* logits, const float* sel_bias,
+                        float band, int32_t* count, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  if (sel_bias != nullptr && !score_takes_bias(cfg->score_fn)) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE(std::isfinite(band) && band >= 0.f, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE(count != nullptr && (reinterpret_cast<uintptr_t>(count) & 3u) == 0, MOE_ERR_ALIGN);
+  if (cfg->T > 0) { MOE_PTR(logits); }
+  MOE_REQUIRE(sel_bias == nullptr || (reinterpret_cast<uintptr_t>(sel_bias) & 3u) == 0, MOE_ERR_ALIGN);
+  MOE_CTX(stream, c);
+  MOE_LAUNCH(launch_router_near_ties(c, *cfg, logits, sel_bias, band, count));
+  return MOE_OK;
+}
+
 int moe_permute(const moe_cfg* cfg, const void* x, const int32_t* idx, int32_t* counts,
                 int32_t* offsets, int32_t* row_of, int32_t* src_tok, void* x_perm, void* ws,
                 size_t ws_bytes, moe_stream_t stream) {

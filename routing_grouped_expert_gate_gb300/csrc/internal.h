@@ -76,6 +76,8 @@ cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void*
 // dx_router = d_logits · W_r for E <= 16 (fp32, experts summed in order)
 cudaError_t launch_router_dx_small(const Ctx& c, const moe_cfg& cfg, const float* d_logits,
                                    const float* w_router, float* dx_router);
+cudaError_t launch_router_near_ties(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                    const float* sel_bias, float band, int32_t* count);
 cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const float* logits,
                                      const int32_t* idx, const float* dw, float* d_logits,
                                      int accumulate);

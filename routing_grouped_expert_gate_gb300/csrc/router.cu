@@ -348,6 +348,64 @@ static cudaError_t launch_router_tiled(const Ctx& c, const Tx* x, const float* w
   return cudaSuccess;
 }
 
+// ------------------------------------------------------------------ S2 keys
+// The values a token's top-k ranks, lane l holding experts l, l+32, ...:
+// the logit (softmax), the probability under the softmax over all E
+// (pre-softmax), or the score (sigmoid, sqrt(softplus)); then + the selection
+// bias, or - the quantile bias; a NaN key ranks last (-inf); slots past E
+// hold -inf. pre_max / pre_inv: the pre-softmax's maximum and 1 / sum.
+template <int EPL>
+__device__ __forceinline__ void selection_keys(const float* __restrict__ lrow,
+                                               const float* __restrict__ sel_bias,
+                                               const float* __restrict__ beta, int E,
+                                               int score_fn, int lane, float (&key)[EPL],
+                                               float& pre_max, float& pre_inv) {
+  float lg[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float l = lrow[e];
+      // pre-softmax: replaced by the probability below
+      key[i] = (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE)
+                   ? l : bias_score(l, score_fn);
+      lg[i] = l;
+    } else {
+      key[i] = -INFINITY;
+      lg[i] = 0.f;
+    }
+  }
+  pre_inv = 0.f;
+  pre_max = 0.f;
+  if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) m = fmaxf(m, lg[i]);
+    m = warp_max(m);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) sum += expf(lg[i] - m);
+    sum = warp_sum(sum);
+    pre_max = m;
+    pre_inv = 1.f / sum;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) key[i] = expf(lg[i] - m) * pre_inv;
+  }
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      float kv = key[i];
+      if (sel_bias != nullptr) kv = __fadd_rn(kv, sel_bias[e]);
+      if (beta != nullptr) kv = __fsub_rn(kv, beta[e]);
+      key[i] = (kv == kv) ? kv : -INFINITY;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ S2
 // One warp per token. Lane l holds experts l, l+32, ... The k winners are found
 // by k rounds of a warp arg-max over (key descending, index ascending); a
@@ -366,51 +424,8 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
-    float key[EPL], lg[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        const float l = logits[t * E + e];
-        // pre-softmax: replaced by the probability below
-        key[i] = (score_fn == MOE_SCORE_SOFTMAX || score_fn == MOE_SCORE_SOFTMAX_PRE)
-                     ? l : bias_score(l, score_fn);
-        lg[i] = l;
-      } else {
-        key[i] = -INFINITY;
-        lg[i] = 0.f;
-      }
-    }
-    // pre-softmax: the key is the probability under the softmax over all E
-    float pre_inv = 0.f, pre_max = 0.f;
-    if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
-      float m = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < E) m = fmaxf(m, lg[i]);
-      m = warp_max(m);
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < E) sum += expf(lg[i] - m);
-      sum = warp_sum(sum);
-      pre_max = m;
-      pre_inv = 1.f / sum;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < E) key[i] = expf(lg[i] - m) * pre_inv;
-    }
-    // selection bias (added) or quantile bias (subtracted); NaN ranks last
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        float kv = key[i];
-        if (sel_bias != nullptr) kv = __fadd_rn(kv, sel_bias[e]);
-        if (beta != nullptr) kv = __fsub_rn(kv, beta[e]);
-        key[i] = (kv == kv) ? kv : -INFINITY;
-      }
-    }
+    float key[EPL], pre_max, pre_inv;
+    selection_keys<EPL>(logits + t * E, sel_bias, beta, E, score_fn, lane, key, pre_max, pre_inv);
     // Each candidate as one 64-bit integer that orders like (key descending,
     // expert ascending): the key's bits made order-preserving as unsigned
     // (-0 counted as +0) above the complemented expert index; slots past E hold
@@ -477,6 +492,67 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       w[t * k + lane] = wj;
     }
   }
+}
+
+// ------------------------------------------------------------------ S2 diagnostics
+// Near ties: tokens whose k-th and (k+1)-th selection keys, the fp32 keys the
+// top-k ranks (selection_keys), differ by less than `band`; for them the choice
+// rests on rounding. One warp per token ranks k + 1 experts as router_topk
+// does; each CTA adds its count to *count with one integer atomic, so the total
+// does not depend on the order. Needs k < E.
+template <int EPL>
+__global__ void __launch_bounds__(256)
+router_near_ties(const float* __restrict__ logits, const float* __restrict__ sel_bias, int64_t T,
+                 int E, int k, int score_fn, float band, int* __restrict__ count) {
+  __shared__ int s_cnt;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  int mine = 0;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    float key[EPL], pre_max, pre_inv;
+    selection_keys<EPL>(logits + t * E, sel_bias, nullptr, E, score_fn, lane, key, pre_max,
+                        pre_inv);
+    uint64_t pk[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        uint32_t b = __float_as_uint(key[i] + 0.f);
+        b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        pk[i] = ((uint64_t)b << 32) | (uint64_t)(~(uint32_t)e);
+      } else {
+        pk[i] = 0ull;
+      }
+    }
+    float kth = 0.f, next = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK + 1; ++j) {
+      if (j <= k) {
+        uint64_t best = pk[0];
+#pragma unroll
+        for (int i = 1; i < EPL; ++i) best = pk[i] > best ? pk[i] : best;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+          best = o > best ? o : best;
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (pk[i] == best) pk[i] = 0ull;
+        uint32_t b = (uint32_t)(best >> 32);
+        b = (b & 0x80000000u) ? (b & 0x7fffffffu) : ~b;
+        const float kv = best == 0ull ? -INFINITY : __uint_as_float(b);
+        if (j == k - 1) kth = kv;
+        if (j == k) next = kv;
+      }
+    }
+    if (lane == 0 && __fsub_rn(kth, next) < band) ++mine;
+  }
+  if (lane == 0 && mine) atomicAdd(&s_cnt, mine);
+  __syncthreads();
+  if (threadIdx.x == 0 && s_cnt) atomicAdd(count, s_cnt);
 }
 
 // ------------------------------------------------------------------ B2
@@ -789,6 +865,26 @@ cudaError_t launch_router_topk_q(const Ctx& c, const moe_cfg& cfg, const float* 
     default: MOE_TOPK(8); break;
   }
 #undef MOE_TOPK
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_near_ties(const Ctx& c, const moe_cfg& cfg, const float* logits,
+                                    const float* sel_bias, float band, int32_t* count) {
+  cudaError_t e = cudaMemsetAsync(count, 0, sizeof(int32_t), c.stream);
+  if (e != cudaSuccess || cfg.T == 0 || cfg.k >= cfg.E) return e;
+  const unsigned grid = warp_grid(c, cfg.T);
+  const int epl = (cfg.E + 31) / 32;
+#define MOE_TIES(N)                                                                   \
+  router_near_ties<N><<<grid, 256, 0, c.stream>>>(logits, sel_bias, cfg.T, cfg.E, cfg.k, \
+                                                  cfg.score_fn, band, count)
+  switch (epl) {
+    case 1: MOE_TIES(1); break;
+    case 2: MOE_TIES(2); break;
+    case 3: case 4: MOE_TIES(4); break;
+    default: MOE_TIES(8); break;
+  }
+#undef MOE_TIES
   note_launches(1);
   return cudaGetLastError();
 }

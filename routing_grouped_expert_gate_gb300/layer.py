@@ -29,13 +29,19 @@ def _act(cfg) -> torch.dtype:
     return torch.bfloat16 if cfg.act_dtype == L.MOE_BF16 else torch.float32
 
 
-def alloc_buffers(cfg, device, backward: bool = True) -> Dict[str, torch.Tensor]:
-    """Every intermediate and output of one forward (+ backward), allocated once."""
+def alloc_buffers(cfg, device, backward: bool = True, alloc=None) -> Dict[str, torch.Tensor]:
+    """Every intermediate and output of one forward (+ backward), allocated once.
+
+    `alloc(shape, dtype)`, when given, makes each buffer instead of
+    torch.empty on `device` (a test places guard regions after every buffer
+    this way)."""
     T, d, E, k, F, Fs = cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.F_shared
     A = T * k
     act = _act(cfg)
     dev = torch.device(device)
-    e = lambda *s, dt=act: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+    if alloc is None:
+        alloc = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+    e = lambda *s, dt=act: alloc(s, dt)  # noqa: E731
     b = {
         "logits": e(T, E, dt=torch.float32),
         "idx": e(T, k, dt=torch.int32),
@@ -77,7 +83,7 @@ def alloc_buffers(cfg, device, backward: bool = True) -> Dict[str, torch.Tensor]
         ws = max(ws, L.workspace_bytes(cfg, L.MOE_WS_GROUPED_BWD),
                  L.workspace_bytes(cfg, L.MOE_WS_ROUTE_BWD),
                  L.workspace_bytes(cfg, L.MOE_WS_SHARED_GATE_BWD))
-    b["ws"] = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+    b["ws"] = alloc((max(ws, 256),), torch.uint8)
     return b
 
 

@@ -80,6 +80,40 @@ def routing_checks(wl, b, f, report):
     return ok
 
 
+def gpu_choice_on_near_ties(wl, b, f):
+    """The selection to re-run the oracle on: the oracle's own on decided
+    tokens, the GPU's on near-tie tokens, after checking that the GPU's choice
+    there is one of the valid ones: k distinct experts, each with a key within
+    the near-tie band of the oracle's k-th key, and no expert left out whose
+    key beats a chosen one by more than the band."""
+    keys = f["keys"]
+    excl = f["gap"] < NEAR_TIE
+    g_idx = b["idx"].cpu().numpy().astype(np.int64)
+    idx = f["idx"].copy()
+    k = wl.k
+    for t in np.nonzero(excl)[0]:
+        chosen = g_idx[t]
+        assert len(set(chosen.tolist())) == k, f"token {t}: repeated expert"
+        kth = np.sort(keys[t])[::-1][k - 1]
+        ck = keys[t, chosen]
+        assert np.all(ck >= kth - NEAR_TIE), f"token {t}: a chosen key lies below the band"
+        left = np.setdiff1d(np.arange(wl.E), chosen)
+        if left.size:
+            assert keys[t, left].max() <= ck.min() + NEAR_TIE, f"token {t}: a better expert left out"
+        # the chosen are sorted by descending key, up to the band
+        assert np.all(np.diff(ck) <= NEAR_TIE), f"token {t}: selection not sorted"
+        idx[t] = chosen
+    return idx
+
+
+def record(case, **kw):
+    """One line of the run's parity summary (printed at the end of the session)."""
+    REPORTS.append((case, kw))
+
+
+REPORTS = []
+
+
 def matched_rows(b, f, ok):
     """(gpu rows, oracle rows) of the assignments of the decided tokens."""
     g_row = b["row_of"].cpu().numpy().astype(np.int64)

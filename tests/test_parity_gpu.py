@@ -14,8 +14,8 @@ import torch
 
 import moe_inputs as mi
 from oracle import moe_oracle as O
-from tests.parity import (TOL_AUX, TOL_BF16, TOL_F32, act_tol, assert_close, matched_rows,
-                          rel_err, routing_checks, to_np)
+from tests.parity import (TOL_AUX, TOL_F32, act_tol, assert_close, gpu_choice_on_near_ties,
+                          record, routing_checks, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,73 +114,101 @@ def built():
     import routing_grouped_expert_gate_gb300  # noqa: F401
 
 
+def oracle_on_gpu_selection(wl, ref, b, report):
+    """The oracle's forward and backward for the comparisons.
+
+    Routing is checked first against the oracle's own selection (bit-exact
+    outside near ties). Where near-tie tokens exist, the GPU's choice on them
+    is checked to be a valid one and the oracle is re-run on it, so that
+    every remaining output and gradient is compared in full; the number of
+    near-tie tokens goes into the run's parity summary."""
+    f0 = O.layer_forward(wl, ref)
+    routing_checks(wl, b, f0, report)
+    if report["near_tie_tokens"] == 0:
+        f = f0
+        report["oracle_selection"] = "own"
+    else:
+        f = O.layer_forward(wl, ref, idx=gpu_choice_on_near_ties(wl, b, f0))
+        report["oracle_selection"] = "GPU choice on near ties"
+    # with the same selection, the dispatch is identical everywhere
+    for key in ("counts", "offsets", "row_of", "src_tok"):
+        got = b[key].cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, f[key]), f"{key} differs from the oracle's"
+    return f
+
+
 @pytest.mark.parametrize("name,dt,impl", CASES)
-def test_layer_parity(built, name, dt, impl):
+def test_layer_parity(built, request, name, dt, impl):
     wl = _wl(name, dt)
     inp, b = run_gpu(wl, backward=True, impl=impl)
     ref = {k: O.as_f64(v) for k, v in inp.items()}
-    f = O.layer_forward(wl, ref)
-    g = O.layer_backward(wl, ref, f, ref["dy"])
     report = {}
+    f = oracle_on_gpu_selection(wl, ref, b, report)
+    g = O.layer_backward(wl, ref, f, ref["dy"])
     tol = act_tol(wl)
+    compared = []
+
+    def check(name, gpu, want, t):
+        assert_close(name, gpu, want, t)
+        compared.append(name)
 
     # S1/S2: logits and weights are fp32 results of exact inputs
-    assert_close("logits", b["logits"], f["logits"], TOL_F32)
+    check("logits", b["logits"], f["logits"], TOL_F32)
     assert float(np.max(np.abs(to_np(b["logits"]) - f["logits"]))) < 1e-6, \
         "logit error must stay far below the near-tie band"
-    ok = routing_checks(wl, b, f, report)
-    assert_close("w", to_np(b["w"])[ok], f["w"][ok], TOL_F32)
+    check("w", b["w"], f["w"], TOL_F32)
 
     # S3: the row copy is exact
-    gr, orow = matched_rows(b, f, ok)
     xp = to_np(b["x_perm"])
-    assert np.array_equal(xp[gr], f["x_perm"][orow])
-    src = b["src_tok"].cpu().numpy().astype(np.int64)
-    assert np.array_equal(xp, to_np(inp["x"])[src])
+    assert np.array_equal(xp, f["x_perm"])
+    compared.append("x_perm (exact)")
 
     # S4/S5
     F = wl.F
     pre = to_np(b["pre_gu"])
-    assert_close("gate", pre[gr, :F], f["g"][orow], tol)
-    assert_close("up", pre[gr, F:], f["u"][orow], tol)
-    assert_close("h", to_np(b["h"])[gr], f["h"][orow], tol)
-    assert_close("out_perm", to_np(b["out_perm"])[gr], f["out_perm"][orow], tol)
+    check("gate", pre[:, :F], f["g"], tol)
+    check("up", pre[:, F:], f["u"], tol)
+    check("h", b["h"], f["h"], tol)
+    check("out_perm", b["out_perm"], f["out_perm"], tol)
     if wl.F_shared:
-        assert_close("y_shared", b["y_s"], f["y_s"], tol)
+        check("y_shared", b["y_s"], f["y_s"], tol)
     if inp.get("w_gate_s") is not None:
-        assert_close("shared gate", b["gate_s"], f["gate_s"], TOL_F32)
+        check("shared gate", b["gate_s"], f["gate_s"], TOL_F32)
     # S6, S7
-    assert_close("y", to_np(b["y"])[ok], f["y"][ok], tol)
+    check("y", b["y"], f["y"], tol)
     aux = float(b["aux"].item())
     assert abs(aux - f["aux"]) <= TOL_AUX * abs(f["aux"]), (aux, f["aux"])
+    compared.append("aux")
 
     # backward (bf16 workloads: everything here is downstream of bf16 activations)
-    assert_close("d_out_perm", to_np(b["d_out_perm"])[gr], g["d_out_perm"][orow], tol)
-    assert_close("dw", to_np(b["dw"])[ok], g["dw"][ok], tol)
-    assert_close("d_pre", to_np(b["d_pre"])[gr], g["d_pre"][orow], tol)
-    assert_close("dx_perm", to_np(b["dx_perm"])[gr], g["dx_perm"][orow], tol)
-    if report["near_tie_tokens"] == 0:
-        assert_close("dW1", b["dw1"], g["dW1"], tol)
-        assert_close("dW2", b["dw2"], g["dW2"], tol)
-        assert_close("d_logits", b["d_logits"], g["d_logits"], tol)
-        assert_close("dW_r", b["dw_router"], g["dW_r"], tol)
-        assert_close("dx", b["dx"], g["dx"], tol)
-        if wl.F_shared:
-            assert_close("dW1_s", b["dw1_s"][0], g["dW1_s"], tol)
-            assert_close("dW2_s", b["dw2_s"][0], g["dW2_s"], tol)
+    check("d_out_perm", b["d_out_perm"], g["d_out_perm"], tol)
+    check("dw", b["dw"], g["dw"], tol)
+    check("d_pre", b["d_pre"], g["d_pre"], tol)
+    check("dx_perm", b["dx_perm"], g["dx_perm"], tol)
+    check("dW1", b["dw1"], g["dW1"], tol)
+    check("dW2", b["dw2"], g["dW2"], tol)
+    check("d_logits", b["d_logits"], g["d_logits"], tol)
+    check("dW_r", b["dw_router"], g["dW_r"], tol)
+    check("dx", b["dx"], g["dx"], tol)
+    if wl.F_shared:
+        check("dW1_s", b["dw1_s"][0], g["dW1_s"], tol)
+        check("dW2_s", b["dw2_s"][0], g["dW2_s"], tol)
     if inp.get("w_gate_s") is not None:
-        assert_close("d shared-gate logit", b["d_gate_logit_s"], g["d_gate_logit_s"], tol)
-        assert_close("dW_gate_s", b["dw_gate_s"], g["dW_gate_s"], tol)
-        assert_close("dy_s", b["dy_s"], g["dy_s"], tol)
+        check("d shared-gate logit", b["d_gate_logit_s"], g["d_gate_logit_s"], tol)
+        check("dW_gate_s", b["dw_gate_s"], g["dW_gate_s"], tol)
+        check("dy_s", b["dy_s"], g["dy_s"], tol)
     # experts that received no rows get an exactly zero weight gradient
     empty = np.nonzero(f["counts"] == 0)[0]
     for e in empty:
         assert float(b["dw1"][e].abs().max()) == 0.0 and float(b["dw2"][e].abs().max()) == 0.0
+    record(request.node.name, near_tie_tokens=report["near_tie_tokens"],
+           oracle_selection=report["oracle_selection"], compared=len(compared),
+           backward_compared=all(n in compared for n in ("dW1", "dW2", "d_logits", "dW_r", "dx")))
 
 
 @pytest.mark.parametrize("name", ["mixtral_small", "zipf_small"])
 @pytest.mark.parametrize("impl", ["tcgen05", "tcgen05_pairs"])
-def test_grouped_bwd_minimal_workspace(built, name, impl):
+def test_grouped_bwd_minimal_workspace(built, request, name, impl):
     """The grouped backward with a minimal workspace: the SwiGLU derivative in fc2's
     data-gradient epilogue, and the weight gradients' expert tails zeroed in
     shared memory instead of read through per-expert tensor maps. Same
@@ -204,17 +232,16 @@ def test_grouped_bwd_minimal_workspace(built, name, impl):
         L.set_grouped_gemm_impl(old)
     assert L.last_device_status()[0] == 0
     ref = {kk: O.as_f64(v) for kk, v in inp.items()}
-    f = O.layer_forward(wl, ref)
-    g = O.layer_backward(wl, ref, f, ref["dy"])
     report = {}
-    ok = routing_checks(wl, b, f, report)
-    gr, orow = matched_rows(b, f, ok)
+    f = oracle_on_gpu_selection(wl, ref, b, report)
+    g = O.layer_backward(wl, ref, f, ref["dy"])
     tol = act_tol(wl)
-    assert_close("d_pre", to_np(out["d_pre"])[gr], g["d_pre"][orow], tol)
-    assert_close("dx_perm", to_np(out["dx_perm"])[gr], g["dx_perm"][orow], tol)
-    if report["near_tie_tokens"] == 0:
-        assert_close("dW1", out["dw1"], g["dW1"], tol)
-        assert_close("dW2", out["dw2"], g["dW2"], tol)
+    assert_close("d_pre", out["d_pre"], g["d_pre"], tol)
+    assert_close("dx_perm", out["dx_perm"], g["dx_perm"], tol)
+    assert_close("dW1", out["dw1"], g["dW1"], tol)
+    assert_close("dW2", out["dw2"], g["dW2"], tol)
+    record(request.node.name, near_tie_tokens=report["near_tie_tokens"],
+           oracle_selection=report["oracle_selection"], compared=4, backward_compared=True)
     # dW2 (same inputs as in the layer run) does not depend on which way the
     # expert tails were cleared; dW1 follows d_pre, whose derivative here ran
     # on the fp32 accumulators instead of a bf16 dh
@@ -476,3 +503,38 @@ def test_bounded_wait_reports_timeout(built):
         assert float(torch.ones(4, device="cuda").sum()) == 4.0
     finally:
         L.set_wait_timeout_ns(old)
+
+
+@pytest.mark.parametrize("name", ["mixtral_small", "deepseek_small", "zipf_small",
+                                  "sqrtsoftplus_small", "presoftmax_small"])
+def test_near_tie_count(built, name):
+    """moe_route_near_ties counts the tokens whose k-th and (k+1)-th fp32
+    selection keys differ by less than the band: it agrees with the float64
+    keys computed from the same logits, up to tokens within a few fp32 ulps of
+    the band's edge."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = SMALL[name]
+    inp = mi.make_inputs(wl, seed=0, device="cuda", with_dy=False)
+    cfg = moe.cfg_from_workload(wl)
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_ROUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+    logits = torch.empty(wl.T, wl.E, device="cuda")
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.T, wl.k, device="cuda")
+    L.route_topk(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), inp.get("sel_bias"),
+                 logits, idx, w, ws)
+    sb = inp.get("sel_bias")
+    keys = O.selection_keys(to_np(logits), wl.score, None if sb is None else to_np(sb))
+    srt = -np.sort(-keys, axis=1)
+    gap = srt[:, wl.k - 1] - srt[:, wl.k]
+    cnt = torch.full((1,), -5, dtype=torch.int32, device="cuda")
+    margin = 2e-6
+    for band in (0.0, 1e-6, 1e-3, 3e-2, 1e9):
+        L.route_near_ties(cfg, logits, sb, band, cnt)
+        n = int(cnt.item())
+        lo = int((gap < band - margin).sum())
+        hi = int((gap < band + margin).sum()) if band > 0 else 0
+        assert lo <= n <= hi, (band, lo, n, hi)
+    assert n == wl.T  # every token is a near tie for an unbounded band
+    assert L.last_device_status()[0] == 0
