@@ -329,8 +329,10 @@ def time_extras(L, cfg, b, T, K):
     return out
 
 
-def stage_work(wl, cfg_backward):
-    """Algorithmic FLOPs / bytes of each ABI call of one step."""
+def stage_work(wl, cfg_backward, router_dx_fused=False):
+    """Algorithmic FLOPs / bytes of each ABI call of one step. router_dx_fused:
+    the permute backward forms d_logits · W_r itself (no fp32 dx_router is
+    written by the router backward or read back)."""
     es = 2 if wl.act_dtype == "bf16" else 4
     T, d, E, k, F, Fs = wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_shared
     A = T * k
@@ -338,8 +340,10 @@ def stage_work(wl, cfg_backward):
         "route": {"flops": 2.0 * T * d * E,
                   "bytes": T * d * es + E * d * 4 + T * E * 4 * 2 + T * k * 8},
         "permute": {"bytes": T * d * es + A * d * es + T * k * 12},
+        # x_perm in, h out and in, out_perm out (+ gate|up out, kept for a backward)
         "grouped_fwd": {"flops": 6.0 * A * d * F,
-                        "bytes": (A * d * 2 + A * F * 3 + A * 2 * F) * es + E * 3 * d * F * es},
+                        "bytes": (A * d * 2 + A * F * 2 + (A * 2 * F if cfg_backward else 0)) * es
+                                 + E * 3 * d * F * es},
         "combine": {"bytes": A * d * es + T * d * es * (2 if Fs else 1) + T * k * 8},
         "aux": {"bytes": T * E * 4},
     }
@@ -351,9 +355,16 @@ def stage_work(wl, cfg_backward):
         if Fs:
             w["shared_bwd"] = {"flops": 12.0 * T * d * Fs}
         w["aux_bwd"] = {"bytes": T * E * 8}
-        w["route_bwd"] = {"flops": 4.0 * T * d * E,
-                          "bytes": T * d * (es + 4) + T * E * 4 * 3 + E * d * 8}
-        w["permute_bwd"] = {"bytes": A * d * es + T * d * 4 + T * d * es * (2 if Fs else 1)}
+        if router_dx_fused:
+            w["route_bwd"] = {"flops": 2.0 * T * d * E,
+                              "bytes": T * d * es + T * E * 4 * 3 + E * d * 4}
+            w["permute_bwd"] = {"bytes": A * d * es + T * E * 4 + E * d * 4
+                                         + T * d * es * (2 if Fs else 1)}
+        else:
+            w["route_bwd"] = {"flops": 4.0 * T * d * E,
+                              "bytes": T * d * (es + 4) + T * E * 4 * 3 + E * d * 8}
+            w["permute_bwd"] = {"bytes": A * d * es + T * d * 4
+                                         + T * d * es * (2 if Fs else 1)}
     return w
 
 
@@ -371,7 +382,7 @@ class Layer:
     """One workload's inputs, buffers and step, as a list of (stage, call):
     every call goes through libmoe's C ABI on the current stream."""
 
-    def __init__(self, wl, backward, dev):
+    def __init__(self, wl, backward, dev, gather=False):
         import moe_inputs as mi
         import routing_grouped_expert_gate_gb300 as moe
         from routing_grouped_expert_gate_gb300 import layer
@@ -380,6 +391,9 @@ class Layer:
         self.inp = mi.make_inputs(wl, seed=0, device=dev, with_dy=backward)
         self.p = layer.params_from_inputs(self.inp)
         self.b = layer.alloc_buffers(self.cfg, dev, backward=backward)
+        # gather (forward only): the dispatch writes no x_perm and fc1 reads the
+        # token rows through src_tok inside its operand load
+        self.gather = gather and not backward
         self.step_calls = self.calls(self.inp["x"], self.inp["dy"])
 
     # the step; x and dy are bound per list (the end-to-end run uses its own buffers)
@@ -387,14 +401,20 @@ class Layer:
         from routing_grouped_expert_gate_gb300 import _lib as L
         cfg, p, b = self.cfg, self.p, self.b
         T, k, E, F, Fs = cfg.T, cfg.k, cfg.E, cfg.F, cfg.F_shared
+        # few experts: the permute backward forms d_logits · W_r itself
+        fused = L.router_dx_in_permute_bwd(cfg)
         c = [("route", lambda: L.route_topk(cfg, x, p["w_router"], p.get("logit_bias"),
                                              p.get("sel_bias"), b["logits"], b["idx"], b["w"],
                                              b["ws"])),
-             ("permute", lambda: L.permute(cfg, x, b["idx"], b["counts"], b["offsets"], b["row_of"],
-                                           b["src_tok"], b["x_perm"], b["ws"])),
-             ("grouped_fwd", lambda: L.grouped_swiglu(cfg, E, T * k, F, b["offsets"], b["x_perm"],
-                                                      p["w1"], p["w2"], b["pre_gu"], b["h"],
-                                                      b["out_perm"], b["ws"]))]
+             ("permute", lambda: L.permute(cfg, None if self.gather else x, b["idx"], b["counts"],
+                                           b["offsets"], b["row_of"], b["src_tok"],
+                                           None if self.gather else b["x_perm"], b["ws"])),
+             ("grouped_fwd", (lambda: L.grouped_swiglu_gather(
+                 cfg, E, T * k, F, b["offsets"], x, b["src_tok"], p["w1"], p["w2"], None, b["h"],
+                 b["out_perm"])) if self.gather else
+              (lambda: L.grouped_swiglu(cfg, E, T * k, F, b["offsets"], b["x_perm"], p["w1"],
+                                        p["w2"], b["pre_gu"] if self.backward else None, b["h"],
+                                        b["out_perm"], b["ws"])))]
         if Fs:
             c.append(("shared_fwd", lambda: L.grouped_swiglu(cfg, 1, T, Fs, None, x, p["w1_s"],
                                                              p["w2_s"], b["pre_gu_s"], b["h_s"],
@@ -417,10 +437,13 @@ class Layer:
                                                      b["d_logits"], 0)),
                   ("route_bwd", lambda: L.route_topk_bwd(cfg, x, p["w_router"], b["logits"],
                                                          b["idx"], b["dw"], b["d_logits"], 1,
-                                                         b["dx_router"], b["dw_router"], b["ws"])),
-                  ("permute_bwd", lambda: L.permute_bwd(cfg, b["dx_perm"], b["row_of"],
-                                                        b["dx_router"], b["dx_s"] if Fs else None,
-                                                        b["dx"]))]
+                                                         None if fused else b["dx_router"],
+                                                         b["dw_router"], b["ws"])),
+                  ("permute_bwd", lambda: L.permute_bwd(
+                      cfg, b["dx_perm"], b["row_of"], None if fused else b["dx_router"],
+                      b["dx_s"] if Fs else None, b["dx"],
+                      d_logits=b["d_logits"] if fused else None,
+                      w_router=p["w_router"] if fused else None))]
         return c
 
     def step(self):
@@ -493,7 +516,7 @@ def breakdown(lay, K, stream):
 
 def stage_table(lay, stage_ms, peaks, fp32_peak):
     from routing_grouped_expert_gate_gb300 import _lib as L
-    work = stage_work(lay.wl, lay.backward)
+    work = stage_work(lay.wl, lay.backward, L.router_dx_in_permute_bwd(lay.cfg))
     stages = {}
     for n, ms in stage_ms.items():
         e = {"ms": round(ms, 4)}
@@ -613,6 +636,25 @@ def summary_workload(name, args, dev, peaks, fp32_peak, dist, ws):
         for n, v in out["hbm_frac"].items():
             out["targets"][f"{n}_hbm_frac"] = {"value": v, "bar": 0.70,
                                                 "met": v is not None and v >= 0.70}
+    if not wl.backward:
+        # the dispatch's row copy fused into fc1's operand load (cp.async
+        # gather from x through src_tok), against the explicit x_perm above
+        lay.gather = True
+        lay.step_calls = lay.calls(lay.inp["x"], lay.inp["dy"])
+        for _ in range(3):
+            lay.step()
+        torch.cuda.synchronize()
+        check_status(L, f"after warm-up of {name} with the gathered fc1")
+        gms, _, gclk, _ = timed_steps(lay, K, stream, dist, dev)
+        _, gstage, _ = breakdown(lay, K, stream)
+        out["fused_gather"] = {
+            "ms_per_step": round(gms, 4), "tokens_per_s": job_throughput(ws, wl.T, gms),
+            "permute_index_ms": round(gstage["permute"], 4),
+            "grouped_fwd_ms": round(gstage["grouped_fwd"], 4),
+            "explicit_permute_ms": round(stage_ms["permute"], 4),
+            "explicit_grouped_fwd_ms": round(stage_ms["grouped_fwd"], 4),
+            "note": "fc1 gathers its rows from x (no x_perm); the step's other calls unchanged"}
+        lay.gather = False
     if wl.zipf_s:
         r = out["routing"]
         ok = r["busiest_over_mean"] > 10 and r["zero_load_experts"] >= 1

@@ -173,7 +173,9 @@ int moe_route_topk(const moe_cfg* cfg, const void* x, const float* w_router,
  *            skipped and recorded as MOE_ERR_DEVICE_INDEX)
  *   counts   [E] int32 out;  offsets [E+1] int32 out
  *   row_of   [T, k] int32 out;  src_tok [T·k] int32 out
- *   x_perm   [T·k, d] act dtype out
+ *   x_perm   [T·k, d] act dtype out, or NULL: counts, offsets, row_of and
+ *            src_tok only (for moe_grouped_swiglu_gather, which reads the rows
+ *            of x through src_tok itself; x may then be NULL too)
  *   ws       >= moe_workspace_bytes(cfg, MOE_WS_PERMUTE) bytes of scratch  */
 int moe_permute(const moe_cfg* cfg, const void* x, const int32_t* idx, int32_t* counts,
                 int32_t* offsets, int32_t* row_of, int32_t* src_tok, void* x_perm,
@@ -203,6 +205,23 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
                        const int32_t* offsets, const void* x_rows, const void* w1,
                        const void* w2, void* pre_gu, void* h, void* out, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
+
+/* S3's row copy fused into S4's operand load (the pages' "also worth trying":
+ * LeCompute, "Read the timeline before blaming the network" groups rows by
+ * expert before the expert GEMMs). The same as moe_grouped_swiglu on
+ * x_rows = x[src_rows[r]] without x_perm being written or read: fc1's A tile
+ * is gathered row by row from x with 16-byte asynchronous copies into the
+ * layout the tensor cores read. For a forward without a backward (the
+ * backward's weight gradient needs x_perm itself).
+ *   x         [x_rows, d] act dtype (the layer's tokens)
+ *   src_rows  [n_rows] int32: the token of each permuted row (moe_permute's
+ *             src_tok); a row outside [0, x_rows) reads as zeros
+ *   the rest as moe_grouped_swiglu. bf16 on the tensor cores only
+ *   (MOE_ERR_UNSUPPORTED otherwise). fc1 runs on single CTAs.            */
+int moe_grouped_swiglu_gather(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int32_t F,
+                              const int32_t* offsets, const void* x, int64_t x_rows,
+                              const int32_t* src_rows, const void* w1, const void* w2,
+                              void* pre_gu, void* h, void* out, moe_stream_t stream);
 
 /* S6. Weighted unpermute-combine: y[t] = Σ_{j<k} w[t,j]·out_perm[row_of[t,j]]
  * (+ g_t · shared_out[t]), accumulated in fp32 in j order, then rounded once.
@@ -297,7 +316,9 @@ int moe_aux_loss_bwd(const moe_cfg* cfg, const float* logits, const int32_t* cou
  * routed scaling factor, S = Σ chosen s + 1e-20). Then, with the full
  * d_logits (this part plus whatever d_logits already holds when
  * accumulate = 1, e.g. the aux-loss part):
- *   dx_router = d_logits · W_r   ([T, d] fp32 out)
+ *   dx_router = d_logits · W_r   ([T, d] fp32 out), or NULL when
+ *               moe_router_dx_in_permute_bwd(cfg) is 1: moe_permute_bwd then
+ *               forms this product itself (MOE_ERR_INVALID_ARG otherwise)
  *   dw_router = d_logitsᵀ · x    ([E, d] fp32 out)
  *   ws >= moe_workspace_bytes(cfg, MOE_WS_ROUTE_BWD)                       */
 int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
@@ -306,15 +327,29 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
                        float* dw_router, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* B1. Backward of the permutation, fused with the other input gradients:
- * dx[t] = Σ_j dx_perm[row_of[t,j]] (+ dx_router[t]) (+ dx_shared[t])
- *         (+ d_gate_logit[t] · w_gate), summed in fp32 and rounded once to the
- * act dtype.
+ * dx[t] = r[t] + Σ_j dx_perm[row_of[t,j]] (+ dx_shared[t])
+ *         (+ d_gate_logit[t] · w_gate), summed in fp32 in that order and
+ * rounded once to the act dtype, where the router's share r[t] is dx_router[t]
+ * when given, d_logits[t] · W_r formed here (fp32, experts in order: the value
+ * moe_route_topk_bwd would have written) when d_logits and w_router are
+ * given, else 0.
  *   dx_perm [T·k, d] act dtype; dx_router [T, d] fp32 or NULL;
  *   dx_shared [T, d] act dtype or NULL; d_gate_logit [T] and w_gate [d]
- *   fp32, both or neither (the shared-expert gate's path); dx [T, d] out   */
+ *   fp32, both or neither (the shared-expert gate's path); d_logits [T, E]
+ *   and w_router [E, d] fp32, both or neither, not with dx_router, and only
+ *   where moe_router_dx_in_permute_bwd(cfg) is 1 (else MOE_ERR_UNSUPPORTED);
+ *   dx [T, d] out                                                          */
 int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_of,
                     const float* dx_router, const void* dx_shared, const float* d_gate_logit,
-                    const float* w_gate, void* dx, moe_stream_t stream);
+                    const float* w_gate, const float* d_logits, const float* w_router, void* dx,
+                    moe_stream_t stream);
+
+/* 1 when moe_permute_bwd forms the router's input gradient d_logits · W_r
+ * itself for cfg (few experts: E <= 16, where the product has only E terms
+ * per element and writing it out as dx_router costs an fp32 [T, d] round
+ * trip through HBM), 0 when moe_route_topk_bwd should write dx_router (many
+ * experts: a real GEMM, on the tensor cores for bf16); < 0 on a bad cfg.    */
+int moe_router_dx_in_permute_bwd(const moe_cfg* cfg);
 
 /* ---------------------------- utilities --------------------------------- */
 

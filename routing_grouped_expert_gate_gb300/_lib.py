@@ -95,6 +95,8 @@ _SIGS = {
     "moe_permute": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
     "moe_grouped_swiglu": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP, _VP,
                                    _VP, _VP, _VP, _VP, _VP, c_size_t, _VP]),
+    "moe_grouped_swiglu_gather": (c_int, [POINTER(MoeCfg), c_int32, c_int64, c_int32, _VP, _VP,
+                                          c_int64, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_unpermute_combine": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_shared_gate": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP]),
     "moe_shared_gate_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -107,7 +109,9 @@ _SIGS = {
     "moe_aux_loss_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, c_float, _VP, c_int32, _VP]),
     "moe_route_topk_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, c_int32, _VP,
                                    _VP, _VP, c_size_t, _VP]),
-    "moe_permute_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_permute_bwd": (c_int, [POINTER(MoeCfg), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                _VP]),
+    "moe_router_dx_in_permute_bwd": (c_int, [POINTER(MoeCfg)]),
     "moe_workspace_bytes": (c_size_t, [POINTER(MoeCfg), c_int]),
     "moe_status_string": (c_char_p, [c_int]),
     "moe_last_cuda_error": (c_char_p, []),
@@ -297,6 +301,16 @@ def permute_noalloc(cfg, x, idx, counts, offsets, row_of, src_tok, x_perm, strea
            "moe_permute_noalloc")
 
 
+def grouped_swiglu_gather(cfg, n_groups, n_rows, F, offsets, x, src_rows, w1, w2, pre_gu, h, out,
+                          stream=None):
+    """grouped_swiglu on the rows x[src_rows[r]], gathered inside fc1's operand load."""
+    _check(lib.moe_grouped_swiglu_gather(ctypes.byref(cfg), int(n_groups), int(n_rows), int(F),
+                                         _p(offsets), _p(x), int(x.shape[0]), _p(src_rows),
+                                         _p(w1), _p(w2), _p(pre_gu), _p(h), _p(out),
+                                         _stream(stream)),
+           "moe_grouped_swiglu_gather")
+
+
 def grouped_swiglu(cfg, n_groups, n_rows, F, offsets, x_rows, w1, w2, pre_gu, h, out, ws,
                    stream=None):
     _check(lib.moe_grouped_swiglu(ctypes.byref(cfg), n_groups, n_rows, F, _p(offsets),
@@ -440,8 +454,16 @@ def route_topk_bwd(cfg, x, w_router, logits, idx, dw, d_logits, accumulate, dx_r
 
 
 def permute_bwd(cfg, dx_perm, row_of, dx_router, dx_shared, dx, stream=None,
-                d_gate_logit=None, w_gate=None):
+                d_gate_logit=None, w_gate=None, d_logits=None, w_router=None):
     _check(lib.moe_permute_bwd(ctypes.byref(cfg), _p(dx_perm), _p(row_of), _p(dx_router),
-                               _p(dx_shared), _p(d_gate_logit), _p(w_gate), _p(dx),
-                               _stream(stream)),
+                               _p(dx_shared), _p(d_gate_logit), _p(w_gate), _p(d_logits),
+                               _p(w_router), _p(dx), _stream(stream)),
            "moe_permute_bwd")
+
+
+def router_dx_in_permute_bwd(cfg) -> bool:
+    """Whether permute_bwd forms d_logits · W_r itself for cfg (then route_topk_bwd
+    takes dx_router=None)."""
+    rc = int(lib.moe_router_dx_in_permute_bwd(ctypes.byref(cfg)))
+    _check(min(rc, 0), "moe_router_dx_in_permute_bwd")
+    return rc == 1

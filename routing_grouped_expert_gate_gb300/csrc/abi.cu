@@ -315,7 +315,9 @@ int moe_permute(const moe_cfg* cfg, const void* x, const int32_t* idx, int32_t* 
   MOE_CHECK_CFG(cfg);
   MOE_PTR(counts); MOE_PTR(offsets);
   if (cfg->T > 0) {
-    MOE_PTR(x); MOE_PTR(idx); MOE_PTR(row_of); MOE_PTR(src_tok); MOE_PTR(x_perm); MOE_PTR(ws);
+    MOE_PTR(idx); MOE_PTR(row_of); MOE_PTR(src_tok); MOE_PTR(ws);
+    MOE_OPT_PTR(x_perm);  // NULL: the index outputs only, no row copy
+    if (x_perm != nullptr) { MOE_PTR(x); }
   }
   MOE_REQUIRE(ws_bytes >= permute_ws_bytes(*cfg), MOE_ERR_WORKSPACE);
   MOE_CTX(stream, c);
@@ -371,6 +373,30 @@ int moe_grouped_swiglu(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int
   g2.offsets = offsets; g2.n_groups = n_groups; g2.alpha = 1.f;
   MOE_LAUNCH(launch_simt_gemm(c, g2));
   return MOE_OK;
+}
+
+int moe_grouped_swiglu_gather(const moe_cfg* cfg, int32_t n_groups, int64_t n_rows, int32_t F,
+                              const int32_t* offsets, const void* x, int64_t x_rows,
+                              const int32_t* src_rows, const void* w1, const void* w2,
+                              void* pre_gu, void* h, void* out, moe_stream_t stream) {
+  MOE_CHECK_CFG(cfg);
+  MOE_REQUIRE(n_groups >= 1 && n_groups <= kMaxE && n_rows >= 0 && F > 0 && x_rows >= 0,
+              MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE((F & 7) == 0, MOE_ERR_ALIGN);
+  MOE_REQUIRE(offsets != nullptr || n_groups == 1, MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE(n_rows < (int64_t)0x7fffffff && x_rows < (int64_t)0x7fffffff, MOE_ERR_UNSUPPORTED);
+  // bf16 on the tensor cores only: the gather is the tcgen05 kernel's A load
+  if (!use_tc(cfg->act_dtype == MOE_BF16 ? kBF16 : kF32)) return MOE_ERR_UNSUPPORTED;
+  MOE_PTR(w1); MOE_PTR(w2); MOE_OPT_PTR(pre_gu); MOE_OPT_PTR(offsets);
+  if (n_rows > 0) { MOE_PTR(x); MOE_PTR(src_rows); MOE_PTR(h); MOE_PTR(out); }
+  MOE_CTX(stream, c);
+  c.act = glu_act_of(*cfg);
+  if (n_rows == 0) return MOE_OK;
+  int err = MOE_OK;
+  MOE_LAUNCH(launch_tc_grouped_swiglu_fwd_gather(c, n_groups, n_rows, F, cfg->d, offsets, x,
+                                                 x_rows, src_rows, w1, w2, pre_gu, h, out,
+                                                 &err));
+  return err;
 }
 
 int moe_unpermute_combine(const moe_cfg* cfg, const void* out_perm, const int32_t* row_of,
@@ -668,8 +694,11 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
   MOE_PTR(w_router); MOE_PTR(dw_router); MOE_PTR(ws);
   MOE_REQUIRE(ws_bytes >= route_bwd_ws(*cfg), MOE_ERR_WORKSPACE);
   if (cfg->T > 0) {
-    MOE_PTR(x); MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(dw); MOE_PTR(d_logits); MOE_PTR(dx_router);
+    MOE_PTR(x); MOE_PTR(logits); MOE_PTR(idx); MOE_PTR(dw); MOE_PTR(d_logits);
+    MOE_OPT_PTR(dx_router);
   }
+  // dx_router NULL: the caller has moe_permute_bwd form d_logits · W_r
+  if (dx_router == nullptr && !permute_bwd_forms_router_dx(*cfg)) return MOE_ERR_INVALID_ARG;
   MOE_CTX(stream, c);
   const int dtx = cfg->act_dtype == MOE_BF16 ? kBF16 : kF32;
   const int T = (int)cfg->T, E = cfg->E, d = cfg->d;
@@ -678,7 +707,9 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
     MOE_LAUNCH(launch_router_bwd_tc(c, *cfg, x, w_router, d_logits, dx_router, dw_router, ws));
     return MOE_OK;
   }
-  if (T > 0 && E <= 16) {
+  if (T > 0 && dx_router == nullptr) {
+    // formed later by moe_permute_bwd
+  } else if (T > 0 && E <= 16) {
     MOE_LAUNCH(launch_router_dx_small(c, *cfg, d_logits, w_router, dx_router));
   } else if (T > 0) {
     SimtGemm a{};  // dx_router = d_logits · W_r   [T, d], K = E
@@ -716,16 +747,25 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
 
 int moe_permute_bwd(const moe_cfg* cfg, const void* dx_perm, const int32_t* row_of,
                     const float* dx_router, const void* dx_shared, const float* d_gate_logit,
-                    const float* w_gate, void* dx, moe_stream_t stream) {
+                    const float* w_gate, const float* d_logits, const float* w_router, void* dx,
+                    moe_stream_t stream) {
   MOE_CHECK_CFG(cfg);
-  if (cfg->T == 0) return MOE_OK;
-  MOE_PTR(dx_perm); MOE_PTR(row_of); MOE_PTR(dx); MOE_OPT_PTR(dx_router); MOE_OPT_PTR(dx_shared);
+  if (cfg->T == 0) return MOE_OK;  // (empty buffers may come as NULL)
   MOE_REQUIRE((d_gate_logit == nullptr) == (w_gate == nullptr), MOE_ERR_INVALID_ARG);
-  MOE_OPT_PTR(d_gate_logit); MOE_OPT_PTR(w_gate);
+  MOE_REQUIRE((d_logits == nullptr) == (w_router == nullptr), MOE_ERR_INVALID_ARG);
+  MOE_REQUIRE(d_logits == nullptr || dx_router == nullptr, MOE_ERR_INVALID_ARG);
+  if (d_logits != nullptr && !permute_bwd_forms_router_dx(*cfg)) return MOE_ERR_UNSUPPORTED;
+  MOE_PTR(dx_perm); MOE_PTR(row_of); MOE_PTR(dx); MOE_OPT_PTR(dx_router); MOE_OPT_PTR(dx_shared);
+  MOE_OPT_PTR(d_gate_logit); MOE_OPT_PTR(w_gate); MOE_OPT_PTR(d_logits); MOE_OPT_PTR(w_router);
   MOE_CTX(stream, c);
   MOE_LAUNCH(launch_permute_bwd(c, *cfg, dx_perm, row_of, dx_router, dx_shared, d_gate_logit,
-                                w_gate, dx));
+                                w_gate, d_logits, w_router, dx));
   return MOE_OK;
+}
+
+int moe_router_dx_in_permute_bwd(const moe_cfg* cfg) {
+  MOE_CHECK_CFG(cfg);
+  return permute_bwd_forms_router_dx(*cfg) ? 1 : 0;
 }
 
 // ---- dispatch with a fixed device scratch array (no allocation by anyone)

@@ -74,6 +74,7 @@ template <int EPL>
 __global__ void __launch_bounds__(256)
 aux_partials(const float* __restrict__ logits, int64_t T, int E, int score_fn,
              float* __restrict__ part) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   __shared__ float wsum[8][kMaxE];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float col[EPL];
@@ -111,6 +112,7 @@ aux_partials(const float* __restrict__ logits, int64_t T, int E, int score_fn,
 __global__ void __launch_bounds__(1024)
 aux_finalize(const float* __restrict__ part, int64_t nblk, const int32_t* __restrict__ counts,
              int64_t T, int E, int k, float coeff, float* __restrict__ aux) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   __shared__ float colh[1024];
   __shared__ float coll[1024];
   __shared__ double term[kMaxE];
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(256)
 aux_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ counts, int64_t T,
                int E, int k, int score_fn, float g_scale, float* __restrict__ d_logits,
                int accumulate) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float dP[EPL];
@@ -554,8 +557,9 @@ cudaError_t launch_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logit
   float* part = static_cast<float*>(ws);
   const int epl = (cfg.E + 31) / 32;
   if (nblk > 0) {
-#define MOE_AUXP(N) \
-  aux_partials<N><<<(unsigned)nblk, 256, 0, c.stream>>>(logits, cfg.T, cfg.E, cfg.score_fn, part)
+#define MOE_AUXP(N)                                                                  \
+  launch_dependent(aux_partials<N>, dim3((unsigned)nblk), dim3(256), 0, c.stream, logits, \
+                   cfg.T, cfg.E, cfg.score_fn, part)
     switch (epl) {
       case 1: MOE_AUXP(1); break;
       case 2: MOE_AUXP(2); break;
@@ -564,8 +568,8 @@ cudaError_t launch_aux_loss(const Ctx& c, const moe_cfg& cfg, const float* logit
     }
 #undef MOE_AUXP
   }
-  aux_finalize<<<1, 1024, 0, c.stream>>>(part, nblk, counts, cfg.T, cfg.E, cfg.k, cfg.aux_coeff,
-                                         aux);
+  launch_dependent(aux_finalize, dim3(1), dim3(1024), 0, c.stream, part, nblk, counts, cfg.T,
+                   cfg.E, cfg.k, cfg.aux_coeff, aux);
   note_launches(nblk > 0 ? 2 : 1);
   return cudaGetLastError();
 }
@@ -581,9 +585,9 @@ cudaError_t launch_aux_loss_bwd(const Ctx& c, const moe_cfg& cfg, const float* l
   const int64_t cap = (int64_t)c.sm_count * 8;
   const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
   const int epl = (cfg.E + 31) / 32;
-#define MOE_AUXB(N)                                                                        \
-  aux_bwd_kernel<N><<<grid, 256, 0, c.stream>>>(logits, counts, cfg.T, cfg.E, cfg.k,      \
-                                                cfg.score_fn, g_scale, d_logits, accumulate)
+#define MOE_AUXB(N)                                                                       \
+  launch_dependent(aux_bwd_kernel<N>, dim3(grid), dim3(256), 0, c.stream, logits, counts,    \
+                   cfg.T, cfg.E, cfg.k, cfg.score_fn, g_scale, d_logits, accumulate)
   switch (epl) {
     case 1: MOE_AUXB(1); break;
     case 2: MOE_AUXB(2); break;

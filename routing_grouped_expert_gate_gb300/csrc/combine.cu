@@ -51,6 +51,7 @@ combine_kernel(const T* __restrict__ out_perm, const int32_t* __restrict__ row_o
                const float* __restrict__ w, const T* __restrict__ shared_out,
                const float* __restrict__ shared_gate, T* __restrict__ y, int64_t Tn, int k,
                int d, int64_t A, int* status) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   constexpr int U = KK >= 8 ? 1 : 8 / KK;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -107,6 +108,7 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ out_perm,
                    const int32_t* __restrict__ row_of, const float* __restrict__ w,
                    T* __restrict__ d_out_perm, float* __restrict__ dw, int64_t Tn, int k,
                    int d, int64_t A, int* status) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   constexpr int U = KK >= 8 ? 1 : 8 / KK;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -182,11 +184,11 @@ cudaError_t launch_combine(const Ctx& c, const moe_cfg& cfg, const void* out_per
   const unsigned grid = token_grid(c, cfg.T);
 #define MOE_COMBINE(KK)                                                                       \
   if (cfg.act_dtype == MOE_BF16)                                                             \
-    combine_kernel<bf16, KK><<<grid, 256, 0, c.stream>>>(                                     \
+    launch_dependent(combine_kernel<bf16, KK>, dim3(grid), dim3(256), 0, c.stream,          \
         static_cast<const bf16*>(out_perm), row_of, w, static_cast<const bf16*>(shared_out), \
         shared_gate, static_cast<bf16*>(y), cfg.T, cfg.k, cfg.d, A, c.status);               \
   else                                                                                       \
-    combine_kernel<float, KK><<<grid, 256, 0, c.stream>>>(                                    \
+    launch_dependent(combine_kernel<float, KK>, dim3(grid), dim3(256), 0, c.stream,         \
         static_cast<const float*>(out_perm), row_of, w,                                      \
         static_cast<const float*>(shared_out), shared_gate, static_cast<float*>(y), cfg.T,   \
         cfg.k, cfg.d, A, c.status)
@@ -204,11 +206,11 @@ cudaError_t launch_combine_bwd(const Ctx& c, const moe_cfg& cfg, const void* dy,
   const unsigned grid = token_grid(c, cfg.T);
 #define MOE_COMBINE_BWD(KK)                                                                 \
   if (cfg.act_dtype == MOE_BF16)                                                           \
-    combine_bwd_kernel<bf16, KK><<<grid, 256, 0, c.stream>>>(                               \
+    launch_dependent(combine_bwd_kernel<bf16, KK>, dim3(grid), dim3(256), 0, c.stream,    \
         static_cast<const bf16*>(dy), static_cast<const bf16*>(out_perm), row_of, w,       \
         static_cast<bf16*>(d_out_perm), dw, cfg.T, cfg.k, cfg.d, A, c.status);             \
   else                                                                                     \
-    combine_bwd_kernel<float, KK><<<grid, 256, 0, c.stream>>>(                              \
+    launch_dependent(combine_bwd_kernel<float, KK>, dim3(grid), dim3(256), 0, c.stream,   \
         static_cast<const float*>(dy), static_cast<const float*>(out_perm), row_of, w,     \
         static_cast<float*>(d_out_perm), dw, cfg.T, cfg.k, cfg.d, A, c.status)
   MOE_BY_K(cfg.k, MOE_COMBINE_BWD);

@@ -148,4 +148,62 @@ __device__ __forceinline__ float bias_score_deriv(float z, float s, int score_fn
   return score_fn == MOE_SCORE_SQRT_SOFTPLUS ? sigmoidf_acc(z) / (2.f * s) : s * (1.f - s);
 }
 
+// ---------------------------------------------------------------- W_r staging
+// W [E][d] fp32 (global) -> sW [E][2][d/8] float4 (shared): the two halves of
+// each 8-element group in separate planes, so that lanes taking consecutive
+// groups read consecutive 16-byte words. Each thread keeps eight loads in
+// flight before storing them (one load at a time would leave the copy bound by
+// memory latency). Ends with __syncthreads().
+__device__ __forceinline__ void stage_w_planes(float4* sW, const float* __restrict__ W, int E,
+                                               int d) {
+  const float4* W4 = reinterpret_cast<const float4*>(W);
+  const int q = d >> 2, ng = d >> 3;
+  const int n4 = E * q;
+  for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * blockDim.x) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n4) v[u] = __ldg(W4 + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n4) {
+        const int e = i / q, r = i - e * q;
+        sW[(e * 2 + (r & 1)) * ng + (r >> 1)] = v[u];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with launch_dependent may start while the previous kernel
+// on the stream is still running; before it reads anything that kernel (or an
+// earlier one) wrote, it must pass pdl_wait(), which returns once the previous
+// grid has finished and its writes are visible. pdl_launch_dependents() lets
+// the next dependent grid be scheduled early. Both are no-ops in a kernel
+// launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                           size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace moe

@@ -5,16 +5,24 @@
 // expert; "Read the timeline before blaming the network" groups the token rows
 // by expert before the expert GEMMs and restores the order afterwards.
 //
-// Four launches, all on the caller's stream, no host sync:
-//   count : per block of 128 tokens, a bitmask per expert of which tokens in the
-//           block chose it (shared memory), popcounts -> per-block counts
-//   scan  : one CTA; per expert, exclusive scan over blocks; exclusive scan over
-//           experts -> counts, offsets, absolute base row of each (block, expert)
-//   rank  : rebuilds the block's bitmasks; the rank of token t among the tokens
-//           of its block that chose e is a popcount of the bits below t, so
-//           row(t, e) = base(block, e) + rank: expert-contiguous, stable
-//   copy  : one warp per token reads its row once and writes it to its k rows
-//           with 16-byte accesses (the HBM-bound part)
+// Three launches on the caller's stream, no host sync, each a programmatic
+// dependent launch of the one before (scheduled while it runs, waiting on
+// griddepcontrol.wait for its results, which hides the launch gaps):
+//   count     : per block of 128 tokens, a bitmask per expert of which tokens in
+//               the block chose it (shared memory), popcounts -> per-block counts
+//   scan      : one CTA of 1024 threads; per expert, exclusive scan over blocks
+//               in chunks; exclusive scan over experts -> counts, offsets and
+//               the absolute base row of each (block, expert)
+//   rank+copy : several CTAs per 128-token block rebuild the block's bitmasks;
+//               the rank of token t among the block's tokens that chose e is a
+//               popcount of the bits below t, so row(t, e) = base(block, e) +
+//               rank: expert-contiguous and stable. Each CTA then copies its
+//               share of the block's tokens, one warp per token reading the row
+//               once and writing its k copies with 16-byte accesses (the
+//               HBM-bound part).
+// Where the wide scan would need more than 64 blocks per thread (more than
+// 64 * 1024 / E blocks of 128 tokens, or 4096 blocks) the older four-launch
+// form runs: count, a one-thread-per-expert scan, rank, copy.
 #include "common.cuh"
 #include "internal.h"
 
@@ -56,6 +64,7 @@ __global__ void __launch_bounds__(256)
 permute_count(const int32_t* __restrict__ idx, int64_t T, int k, int E,
               int32_t* __restrict__ block_counts, int* status) {
   __shared__ uint32_t masks[kMaxE][PB_WORDS];
+  pdl_wait();  // idx comes from the kernel before (when launched as a dependent)
   build_masks(masks, idx, T, k, E, status, true);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
@@ -138,6 +147,170 @@ permute_rank(const int32_t* __restrict__ idx, int64_t T, int k, int E,
   }
 }
 
+// ------------------------------------------------------------------ scan, wide
+constexpr int PS_THREADS = 1024;
+
+// One CTA of 1024 threads: the per-(block, expert) counts written by
+// permute_count become absolute base rows, with counts[] and offsets[]. Per
+// expert e the blocks are cut into C chunks of about sqrt(nblk) blocks;
+// thread (c, e) sums its chunk with all its loads in flight, the chunk sums are
+// scanned per expert, the expert totals scanned by one warp, and each thread
+// rewrites its chunk. (permute_scan does the same with one thread per expert
+// walking every block; this form has about sqrt(nblk) dependent steps.) The
+// launcher keeps chunks at <= 64 blocks.
+__global__ void __launch_bounds__(PS_THREADS)
+permute_scan_wide(int32_t* __restrict__ block_counts, int nblk, int E,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int32_t part[PS_THREADS];
+  __shared__ int32_t base[kMaxE];
+  pdl_wait();
+  int C = PS_THREADS / E;
+  int cs = 1;
+  while (cs * cs < nblk) ++cs;
+  if ((nblk + cs - 1) / cs < C) C = (nblk + cs - 1) / cs;
+  cs = (nblk + C - 1) / C;
+  const int e = threadIdx.x % E, c = threadIdx.x / E;
+  const bool act = c < C;
+  const int b0 = c * cs, b1 = min(nblk, b0 + cs);
+  int sum = 0;
+  if (act) {  // sixteen loads in flight at a time
+    for (int i0 = b0; i0 < b1; i0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = (i0 + i < b1) ? block_counts[(int64_t)(i0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sum += v[i];
+    }
+    part[c * E + e] = sum;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {  // chunk prefixes of expert e; its total
+    int run = 0;
+    for (int cc = 0; cc < C; ++cc) {
+      const int w = part[cc * E + threadIdx.x];
+      part[cc * E + threadIdx.x] = run;
+      run += w;
+    }
+    counts[threadIdx.x] = run;
+    base[threadIdx.x] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // exclusive scan of the expert totals, one warp
+    const int per = (E + 31) / 32;
+    const int lo = threadIdx.x * per;
+    int loc = 0;
+    for (int i = lo; i < lo + per && i < E; ++i) loc += base[i];
+    int incl = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int w = __shfl_up_sync(0xffffffffu, incl, off);
+      if ((int)threadIdx.x >= off) incl += w;
+    }
+    int run = incl - loc;
+    for (int i = lo; i < lo + per && i < E; ++i) {
+      const int w = base[i];
+      base[i] = run;
+      offsets[i] = run;
+      run += w;
+    }
+    if (threadIdx.x == 31) offsets[E] = incl;
+  }
+  __syncthreads();
+  if (act) {  // the chunk again (from L2), rewritten as base rows
+    int run = part[c * E + e] + base[e];
+    for (int i0 = b0; i0 < b1; i0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = (i0 + i < b1) ? block_counts[(int64_t)(i0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i0 + i < b1) {
+          block_counts[(int64_t)(i0 + i) * E + e] = run;
+          run += v[i];
+        }
+      }
+    }
+  }
+}
+
+// CTA (block b, part p) of `parts`: the bitmasks of block b, then for the
+// tokens of part p the rows row(t, j) = block_base[b][e] + rank (written to
+// row_of and src_tok) and the copy x_perm[row(t, j)] = x[t], one warp per token.
+template <typename T>
+__global__ void __launch_bounds__(256)
+permute_rank_copy(const T* __restrict__ x, const int32_t* __restrict__ idx, int64_t Tn, int k,
+                  int E, int d, int parts, const int32_t* __restrict__ block_base,
+                  int32_t* __restrict__ row_of, int32_t* __restrict__ src_tok,
+                  T* __restrict__ x_perm) {
+  __shared__ uint32_t masks[kMaxE][PB_WORDS];
+  __shared__ int32_t s_rows[PB_TOK][kMaxK];
+  pdl_wait();
+  const int blk = blockIdx.x / parts;
+  const int part = blockIdx.x - blk * parts;
+  for (int i = threadIdx.x; i < E * PB_WORDS; i += blockDim.x) masks[i / PB_WORDS][i % PB_WORDS] = 0u;
+  __syncthreads();
+  const int64_t t_base = (int64_t)blk * PB_TOK;
+  for (int i = threadIdx.x; i < PB_TOK * k; i += blockDim.x) {
+    const int tl = i / k;
+    const int64_t t = t_base + tl;
+    if (t >= Tn) continue;
+    const int e = idx[t * k + (i - tl * k)];
+    if (e >= 0 && e < E) atomicOr(&masks[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  const int per = PB_TOK / parts;
+  const int tl0 = part * per;
+  for (int i = threadIdx.x; i < per * k; i += blockDim.x) {
+    const int tl = tl0 + i / k;
+    const int j = i % k;
+    const int64_t t = t_base + tl;
+    if (t >= Tn) continue;
+    const int e = idx[t * k + j];
+    int row = -1;
+    if (e >= 0 && e < E) {
+      int rank = __popc(masks[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+      for (int w = 0; w < (tl >> 5); ++w) rank += __popc(masks[e][w]);
+      row = block_base[(int64_t)blk * E + e] + rank;
+      src_tok[row] = (int32_t)t;
+    }
+    row_of[t * k + j] = row;
+    s_rows[tl][j] = row;
+  }
+  if (x_perm == nullptr) return;  // the index outputs only
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = d * (int)sizeof(T) / 16;
+  for (int tl = tl0 + warp; tl < tl0 + per; tl += (int)(blockDim.x >> 5)) {
+    const int64_t t = t_base + tl;
+    if (t >= Tn) break;
+    int64_t rows[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) rows[j] = (j < k) ? s_rows[tl][j] : -1;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+    for (int v0 = 0; v0 < nvec; v0 += 128) {
+      uint4 buf[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < nvec) buf[u] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && rows[j] >= 0) {
+          uint4* dst = reinterpret_cast<uint4*>(x_perm + rows[j] * d);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < nvec) dst[v] = buf[u];
+          }
+        }
+      }
+    }
+  }
+}
+
 // One warp per token; 4 x 16 B loads in flight per lane before the k stores.
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -187,6 +360,35 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
                            int32_t* src_tok, void* x_perm, void* ws) {
   const int64_t nblk = permute_blocks(cfg.T);
   int32_t* block_counts = static_cast<int32_t*>(ws);
+  const int64_t A = cfg.T * cfg.k;
+  // the wide scan holds at most 64 blocks per thread
+  if (nblk > 0 && nblk <= 4096 && nblk <= (int64_t)64 * (PS_THREADS / cfg.E)) {
+    // count (one CTA per 128-token block), wide scan, rank + copy: each a
+    // dependent launch of the one before
+    cudaError_t e = launch_dependent(permute_count, dim3((unsigned)nblk), dim3(256), 0, c.stream,
+                                     idx, cfg.T, cfg.k, cfg.E, block_counts, c.status);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(permute_scan_wide, dim3(1), dim3(PS_THREADS), 0, c.stream,
+                         block_counts, (int)nblk, cfg.E, counts, offsets);
+    if (e != cudaSuccess) return e;
+    // CTAs per 128-token block: about four waves of the SMs in all
+    int64_t parts = ((int64_t)4 * c.sm_count + nblk - 1) / nblk;
+    parts = parts < 1 ? 1 : (parts > 16 ? 16 : parts);
+    while (PB_TOK % parts) --parts;
+    const unsigned grid = (unsigned)(nblk * parts);
+    if (cfg.act_dtype == MOE_BF16)
+      e = launch_dependent(permute_rank_copy<bf16>, dim3(grid), dim3(256), 0, c.stream,
+                           static_cast<const bf16*>(x), idx, cfg.T, cfg.k, cfg.E, cfg.d,
+                           (int)parts, static_cast<const int32_t*>(block_counts), row_of, src_tok,
+                           static_cast<bf16*>(x_perm));
+    else
+      e = launch_dependent(permute_rank_copy<float>, dim3(grid), dim3(256), 0, c.stream,
+                           static_cast<const float*>(x), idx, cfg.T, cfg.k, cfg.E, cfg.d,
+                           (int)parts, static_cast<const int32_t*>(block_counts), row_of, src_tok,
+                           static_cast<float*>(x_perm));
+    note_launches(3);
+    return e;
+  }
   if (nblk > 0) {
     permute_count<<<(unsigned)nblk, 256, 0, c.stream>>>(idx, cfg.T, cfg.k, cfg.E, block_counts,
                                                          c.status);
@@ -195,7 +397,10 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
   if (nblk > 0) {
     permute_rank<<<(unsigned)nblk, 256, 0, c.stream>>>(idx, cfg.T, cfg.k, cfg.E, block_counts,
                                                         row_of, src_tok, c.status);
-    const int64_t A = cfg.T * cfg.k;
+    if (x_perm == nullptr) {
+      note_launches(3);
+      return cudaGetLastError();
+    }
     if (cfg.act_dtype == MOE_BF16)
       permute_copy<bf16><<<copy_grid(c, cfg.T), 256, 0, c.stream>>>(
           static_cast<const bf16*>(x), row_of, static_cast<bf16*>(x_perm), cfg.T, cfg.k, cfg.d, A);
@@ -211,16 +416,31 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
 // ------------------------------------------------------------------ B1
 // dx[t] = dx_router[t] + sum_j dx_perm[row_of[t, j]] + dx_shared[t], in fp32 in
 // that order, rounded once. One warp per token, 8 elements per lane per step.
-template <typename T, int KK>
-__global__ void __launch_bounds__(256)
+//
+// ROUTER: the router's share d_logits[t] · W_r is formed here instead of read
+// as dx_router: per element, fp32 FMAs over the experts in order starting from
+// 0, the value the router backward would have written, so dx is the same bit
+// for bit while the fp32 [T, d] round trip through HBM is gone. W_r is staged
+// in shared memory (E·d·4 bytes, as [E][2][d/8] float4 planes so that the
+// lanes' consecutive groups read consecutive words) when w_smem is set, else
+// read from global memory.
+template <typename T, int KK, bool ROUTER = false, int EMAX = 16>
+__global__ void __launch_bounds__(ROUTER ? 512 : 256)
 permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ row_of,
                    const float* __restrict__ dx_router, const T* __restrict__ dx_shared,
                    const float* __restrict__ d_gate_logit, const float* __restrict__ w_gate,
-                   T* __restrict__ dx, int64_t Tn, int k, int d, int64_t A, int* status) {
-  constexpr int U = KK >= 8 ? 1 : 8 / KK;  // 8-element groups per lane per step
+                   T* __restrict__ dx, int64_t Tn, int k, int d, int64_t A, int* status,
+                   const float* __restrict__ d_logits = nullptr,
+                   const float* __restrict__ w_router = nullptr, int E = 0, int w_smem = 0) {
+  // 8-element groups per lane per step (half as many for fp32 rows when the
+  // router's share is formed here, which needs registers of its own)
+  constexpr int U = (ROUTER && sizeof(T) == 4) ? (KK >= 4 ? 1 : 4 / KK) : (KK >= 8 ? 1 : 8 / KK);
+  extern __shared__ float4 sW[];           // ROUTER and w_smem: [E][2][d/8]
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int ng = d >> 3;
+  if (ROUTER && w_smem) stage_w_planes(sW, w_router, E, d);
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
     int64_t rows[KK];
 #pragma unroll
@@ -233,13 +453,18 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
       rows[j] = r;
     }
     const float dgl = d_gate_logit != nullptr ? d_gate_logit[t] : 0.f;
+    float dl[ROUTER ? EMAX : 1];
+    if (ROUTER) {
+#pragma unroll
+      for (int e = 0; e < (ROUTER ? EMAX : 1); ++e) dl[e] = e < E ? __ldg(d_logits + t * E + e) : 0.f;
+    }
     for (int g0 = 0; g0 < ng; g0 += 32 * U) {
       Raw8<T> raw[U][KK], sraw[U];
       Raw8<float> rraw[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int g = g0 + 32 * u + lane;
-        if (g < ng && dx_router != nullptr) rraw[u].load(dx_router + t * d + 8 * g);
+        if (!ROUTER && g < ng && dx_router != nullptr) rraw[u].load(dx_router + t * d + 8 * g);
         else rraw[u].zero();
 #pragma unroll
         for (int j = 0; j < KK; ++j) {
@@ -254,7 +479,33 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
         const int g = g0 + 32 * u + lane;
         if (g >= ng) continue;
         float acc[8];
-        rraw[u].to_float(acc);
+        if (ROUTER) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+          for (int e = 0; e < (ROUTER ? EMAX : 1); ++e) {
+            if (e < E) {
+              float4 w0, w1;
+              if (w_smem) {
+                w0 = sW[(e * 2) * ng + g];
+                w1 = sW[(e * 2 + 1) * ng + g];
+              } else {
+                w0 = __ldg(reinterpret_cast<const float4*>(w_router + (int64_t)e * d + 8 * g));
+                w1 = __ldg(reinterpret_cast<const float4*>(w_router + (int64_t)e * d + 8 * g + 4));
+              }
+              acc[0] = fmaf(dl[e], w0.x, acc[0]);
+              acc[1] = fmaf(dl[e], w0.y, acc[1]);
+              acc[2] = fmaf(dl[e], w0.z, acc[2]);
+              acc[3] = fmaf(dl[e], w0.w, acc[3]);
+              acc[4] = fmaf(dl[e], w1.x, acc[4]);
+              acc[5] = fmaf(dl[e], w1.y, acc[5]);
+              acc[6] = fmaf(dl[e], w1.z, acc[6]);
+              acc[7] = fmaf(dl[e], w1.w, acc[7]);
+            }
+          }
+        } else {
+          rraw[u].to_float(acc);
+        }
 #pragma unroll
         for (int j = 0; j < KK; ++j) {
           if (j < k) {
@@ -281,24 +532,82 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
   }
 }
 
+// Shared memory the router-fused form may take for W_r.
+constexpr size_t kPermBwdWSmem = 160 * 1024;
+
+template <typename T, int KK, int EMAX>
+static cudaError_t launch_permute_bwd_router(const Ctx& c, const moe_cfg& cfg, const T* dx_perm,
+                                             const int32_t* row_of, const T* dx_shared,
+                                             const float* d_gate_logit, const float* w_gate,
+                                             const float* d_logits, const float* w_router,
+                                             T* dx) {
+  auto kern = permute_bwd_kernel<T, KK, true, EMAX>;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPermBwdWSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev & 63] = true;
+  }
+  const size_t wbytes = (size_t)cfg.E * cfg.d * sizeof(float);
+  const bool in_smem = wbytes <= kPermBwdWSmem;
+  // W_r staged once per CTA: one CTA per SM, each walking the tokens
+  const int64_t blocks = (cfg.T + 15) / 16;
+  const int64_t cap = in_smem ? (int64_t)c.sm_count : (int64_t)c.sm_count * 4;
+  const unsigned grid = (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+  return launch_dependent(kern, dim3(grid), dim3(512), in_smem ? wbytes : 0, c.stream, dx_perm,
+                          row_of, nullptr, dx_shared, d_gate_logit, w_gate, dx, cfg.T, cfg.k,
+                          cfg.d, cfg.T * cfg.k, c.status, d_logits, w_router, cfg.E,
+                          in_smem ? 1 : 0);
+}
+
+bool permute_bwd_forms_router_dx(const moe_cfg& cfg) { return cfg.E <= 16; }
+
 cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_perm,
                                const int32_t* row_of, const float* dx_router,
                                const void* dx_shared, const float* d_gate_logit,
-                               const float* w_gate, void* dx) {
+                               const float* w_gate, const float* d_logits,
+                               const float* w_router, void* dx) {
   if (cfg.T == 0) return cudaSuccess;
   const int64_t A = cfg.T * cfg.k;
+  if (d_logits != nullptr) {
+    if (cfg.E > 16) return cudaErrorInvalidValue;  // refused by the entry point first
+    cudaError_t e;
+#define MOE_PBWDR(TT, KK)                                                                     \
+  e = launch_permute_bwd_router<TT, KK, 16>(                                                   \
+      c, cfg, static_cast<const TT*>(dx_perm), row_of, static_cast<const TT*>(dx_shared),     \
+      d_gate_logit, w_gate, d_logits, w_router, static_cast<TT*>(dx))
+#define MOE_PBWDR_K(TT)                                              \
+  if (cfg.k <= 1) { MOE_PBWDR(TT, 1); }                              \
+  else if (cfg.k <= 2) { MOE_PBWDR(TT, 2); }                         \
+  else if (cfg.k <= 4) { MOE_PBWDR(TT, 4); }                         \
+  else { MOE_PBWDR(TT, 8); }
+    if (cfg.act_dtype == MOE_BF16) {
+      MOE_PBWDR_K(bf16)
+    } else {
+      MOE_PBWDR_K(float)
+    }
+#undef MOE_PBWDR_K
+#undef MOE_PBWDR
+    note_launches(1);
+    return e;
+  }
   const unsigned grid = copy_grid(c, cfg.T);
 #define MOE_PBWD(KK)                                                                          \
   if (cfg.act_dtype == MOE_BF16)                                                             \
-    permute_bwd_kernel<bf16, KK><<<grid, 256, 0, c.stream>>>(                                 \
-        static_cast<const bf16*>(dx_perm), row_of, dx_router,                                \
-        static_cast<const bf16*>(dx_shared), d_gate_logit, w_gate, static_cast<bf16*>(dx),   \
-        cfg.T, cfg.k, cfg.d, A, c.status);                                                   \
+    launch_dependent(permute_bwd_kernel<bf16, KK>, dim3(grid), dim3(256), 0, c.stream,       \
+                     static_cast<const bf16*>(dx_perm), row_of, dx_router,                   \
+                     static_cast<const bf16*>(dx_shared), d_gate_logit, w_gate,              \
+                     static_cast<bf16*>(dx), cfg.T, cfg.k, cfg.d, A, c.status, nullptr,      \
+                     nullptr, 0, 0);                                                         \
   else                                                                                       \
-    permute_bwd_kernel<float, KK><<<grid, 256, 0, c.stream>>>(                                \
-        static_cast<const float*>(dx_perm), row_of, dx_router,                               \
-        static_cast<const float*>(dx_shared), d_gate_logit, w_gate, static_cast<float*>(dx), \
-        cfg.T, cfg.k, cfg.d, A, c.status)
+    launch_dependent(permute_bwd_kernel<float, KK>, dim3(grid), dim3(256), 0, c.stream,      \
+                     static_cast<const float*>(dx_perm), row_of, dx_router,                  \
+                     static_cast<const float*>(dx_shared), d_gate_logit, w_gate,             \
+                     static_cast<float*>(dx), cfg.T, cfg.k, cfg.d, A, c.status, nullptr,     \
+                     nullptr, 0, 0)
   if (cfg.k <= 1) {
     MOE_PBWD(1);
   } else if (cfg.k <= 2) {

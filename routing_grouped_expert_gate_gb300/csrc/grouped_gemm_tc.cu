@@ -85,6 +85,11 @@ struct Params {
   // the MMA warp zeroes those rows in shared memory instead
   const CUtensorMap* tail_maps;
   int m128_tails;     // CTA pairs, M-grouped: a last tile of <= 128 rows runs as M = 128
+  // gathered A (fc1 forward): row r of the A operand is row a_src[r] of a_rows
+  // [a_src_rows, K]; rows r >= n_rows read as zeros
+  const bf16* a_rows;
+  const int32_t* a_src;
+  int a_src_rows;
 };
 
 struct __align__(8) Shared {
@@ -484,11 +489,22 @@ __device__ __forceinline__ void zero_wgrad_tile(const Params& P, const Tile& ti,
 }
 
 // ---------------------------------------------------------------- the kernel
-template <bool A_MN, bool B_MN, int EPI>
+// GATHER (M-grouped, K-major A): the A tile is not loaded by TMA from a
+// permuted copy but gathered row by row from a_rows through a_src (the
+// dispatch's src_tok), by the producer warp's 32 lanes with 16-byte cp.async
+// copies written in the 128-byte swizzle the MMA descriptors expect. A lane
+// keeps GATHER_LAG stages of its copies in flight; once a stage's copies have
+// landed it fences them towards the async proxy (which the MMA reads through)
+// and arrives on the stage's `full` barrier, which also waits for the B tile's
+// TMA bytes.
+constexpr int GATHER_LAG = STAGES - 1;
+
+template <bool A_MN, bool B_MN, int EPI, bool GATHER = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                 const Params P) {
+  static_assert(!GATHER || (!A_MN && EPI != EPI_WGRAD), "gather: M-grouped, K-major A");
   constexpr bool KGROUPED = (EPI == EPI_WGRAD);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled stages
@@ -504,11 +520,12 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const int tile0 = (int)blockIdx.x;
   const int tstep = (int)gridDim.x;
 
-  // ---- set-up: segment offsets, tile prefix, barriers, TMEM
+  // ---- set-up: barriers, TMEM, then (once the kernel before has finished:
+  // this kernel is a dependent launch) segment offsets and the tile prefix
   if (tid == 0) {
     sh.abort = 0;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.full[s], GATHER ? 33 : 1);  // gather: + one arrival per producer lane
       mbar_init(&sh.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -518,6 +535,15 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(&sh.epi_load[w], 1);
     fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  pdl_wait();
   for (int g = tid; g <= P.G; g += NUM_THREADS) {
     int v = P.offsets ? P.offsets[g] : (g == 0 ? 0 : P.n_rows);
     sh.off[g] = v;
@@ -562,14 +588,6 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       sh.order[rank] = g;
     }
   }
-  if (warp == 1) {
-    tmem_alloc(&sh.tmem_base, TMEM_COLS);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -577,7 +595,77 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const int total = sh.total_tiles;
   const uint32_t tmem_base = sh.tmem_base;
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ================= producer: gathered A rows (cp.async) + B by TMA =================
+    const int nchunk = P.K >> 3;  // 16-byte chunks per A row
+    int stage = 0;
+    uint32_t phase = 0;
+    int pend_stage[GATHER_LAG + 1];
+    int npend = 0;
+    bool ok = true;
+    auto release_oldest = [&]() {  // the oldest pending stage's copies have landed
+      fence_async_shared();
+      mbar_arrive(&sh.full[pend_stage[0]]);
+#pragma unroll
+      for (int i = 0; i < GATHER_LAG; ++i) pend_stage[i] = pend_stage[i + 1];
+      --npend;
+    };
+    for (int t = tile0; t < total && ok; t += tstep) {
+      const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
+      // this lane's four rows of the tile: r = lane + 32 i
+      const bf16* src[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = ti.m0 + lane + 32 * i;
+        int s_row = -1;
+        if (r < P.n_rows) s_row = P.a_src[r];
+        src[i] = (s_row >= 0 && s_row < P.a_src_rows) ? P.a_rows + (int64_t)s_row * P.K : nullptr;
+      }
+      for (int kb = 0; kb < ti.nk; ++kb) {
+        if (!mbar_wait(&sh.empty[stage], phase ^ 1, sh.abort, P, 5)) { ok = false; break; }
+        uint8_t* a_dst = stage_base + stage * STAGE_BYTES;
+        uint8_t* b_dst = a_dst + A_STAGE_BYTES;
+        if (lane == 0) {
+          uint64_t* bar = &sh.full[stage];
+          mbar_expect_tx(bar, B_STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (EPI == EPI_SWIGLU_FWD) {
+            const int r0 = ti.grp * 2 * P.F;
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(b_dst + 16384 * h, &tmB, bar, k0, r0 + h * P.F + ti.n0);
+          } else {
+            tma_load_2d(b_dst, &tmB, bar, k0, ti.grp * P.b_group_rows + ti.n0);
+          }
+        }
+        const uint32_t a_s = su32(a_dst);
+        const int c0 = kb * (BK / 8);  // first 16-byte chunk of this K block
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane + 32 * i;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const bool in = src[i] != nullptr && c0 + c < nchunk;
+            const void* g = in ? static_cast<const void*>(src[i] + 8 * (c0 + c))
+                               : static_cast<const void*>(P.a_rows);
+            cp_async16_zfill(a_s + r * 128 + ((c ^ (r & 7)) << 4), g, in ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        pend_stage[npend++] = stage;
+        if (npend > GATHER_LAG) {
+          cp_async_wait_group<GATHER_LAG>();
+          release_oldest();
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    cp_async_wait_all();
+    while (npend > 0) release_oldest();
+    if (!ok) {
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 2000000ull) { }
+    }
+  } else if (warp == 0) {
     // ================= TMA producer =================
     // Loads run up to STAGES k-blocks ahead of the MMAs. (An L2 prefetch of
     // later k-blocks by every CTA was measured to slow the kernel down: the
@@ -717,6 +805,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed
   }
 
+  pdl_launch_dependents();  // this CTA's work is done
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -885,6 +974,15 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(&sh.epi_load[w], 1);
     fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc_pair(&sh.tmem_base, PAIR_ACC * BN);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  pdl_wait();  // a dependent launch: the offsets come from the kernel before
   for (int g = tid; g <= P.G; g += NUM_THREADS)
     sh.off[g] = P.offsets ? P.offsets[g] : (g == 0 ? 0 : P.n_rows);
   __syncthreads();
@@ -924,14 +1022,6 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       }
       sh.order[r] = g;
     }
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(&sh.tmem_base, PAIR_ACC * BN);
-    tmem_relinquish_pair();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
   }
   tc_fence_before();
   __syncthreads();
@@ -1111,6 +1201,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
     const uint64_t t0 = global_timer_ns();
     while (global_timer_ns() - t0 < 2000000ull) { }
   }
+  pdl_launch_dependents();  // this CTA's work is done
   tc_fence_before();
   __syncthreads();
   cluster_barrier();  // neither CTA leaves while the other may still address it
@@ -1126,6 +1217,7 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
 __global__ void __launch_bounds__(256)
 glu_bwd_rows(const bf16* __restrict__ dh, const bf16* __restrict__ gu, bf16* __restrict__ d_pre,
              int64_t rows, int F, GluAct act) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int per_row = F >> 3;
   const int64_t n = rows * per_row;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -1157,8 +1249,8 @@ static cudaError_t launch_glu_bwd_rows(const Ctx& c, const bf16* dh, const bf16*
   const int64_t n = rows * (F / 8);
   const int64_t blocks = (n + 255) / 256;
   const int64_t cap = (int64_t)c.sm_count * 16;
-  glu_bwd_rows<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, c.stream>>>(dh, gu, d_pre, rows,
-                                                                              F, c.act);
+  launch_dependent(glu_bwd_rows, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0,
+                   c.stream, dh, gu, d_pre, rows, F, c.act);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -1172,6 +1264,7 @@ static cudaError_t launch_glu_bwd_rows(const Ctx& c, const bf16* dh, const bf16*
 __global__ void __launch_bounds__(256)
 build_tail_maps(const __grid_constant__ CUtensorMap t0, const __grid_constant__ CUtensorMap t1,
                 const int32_t* __restrict__ offsets, int G, int n_rows, CUtensorMap* out) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     int end = offsets ? offsets[g + 1] : n_rows;
     end = end < 1 ? 1 : (end > n_rows ? n_rows : end);
@@ -1274,6 +1367,8 @@ struct KernelTiming {
 };
 static KernelTiming g_timing;
 
+static bool timing_on() { return g_timing.on; }
+
 static void timing_mark(int kind, cudaStream_t s, bool start) {
   if (!g_timing.on) return;
   std::lock_guard<std::mutex> lk(g_timing.mu);
@@ -1294,11 +1389,11 @@ static void timing_mark(int kind, cudaStream_t s, bool start) {
   v.push_back(e);
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool GATHER = false>
 static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtensorMap& mb,
                               const CUtensorMap& mc, const CUtensorMap& md, const Params& P,
                               int kind) {
-  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI>;
+  auto kern = tc_grouped_gemm<A_MN, B_MN, EPI, GATHER>;
   static std::atomic<uint64_t> attr_set_mask{0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1310,10 +1405,15 @@ static cudaError_t launch_one(const Ctx& c, const CUtensorMap& ma, const CUtenso
     attr_set_mask.fetch_or(bit);
   }
   cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(c.sm_count);
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = timing_on() ? 0 : 1;  // per-kernel events between launches: plain launches
   timing_mark(kind, c.stream, true);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, P);
   note_launches(1);
@@ -1345,11 +1445,13 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = kSmemBytes2;
   cfg.stream = c.stream;
@@ -1370,6 +1472,7 @@ static cudaError_t launch_pair(const Ctx& c, const CUtensorMap& ma, const CUtens
     attr_set_mask.fetch_or(bit);
   }
   cfg.gridDim = dim3(2 * max_clusters[dev & 63]);
+  cfg.numAttrs = timing_on() ? 1 : 2;  // per-kernel events between launches: plain launches
   timing_mark(kind, c.stream, true);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, ma64, P);
   note_launches(1);
@@ -1511,6 +1614,58 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int G, int64_t n_rows, in
   return launch_mgrouped<false, EPI_STORE>(c, pair, mA, h, n_rows, F, mB, mC, mC, Q, kFc2Fwd);
 }
 
+cudaError_t launch_tc_grouped_swiglu_fwd_gather(const Ctx& c, int G, int64_t n_rows, int F, int d,
+                                                const int32_t* offsets, const void* x,
+                                                int64_t x_rows, const int32_t* src_rows,
+                                                const void* w1, const void* w2, void* pre_gu,
+                                                void* h, void* out, int* err) {
+  using namespace tc;
+  *err = MOE_OK;
+  if (n_rows == 0) return cudaSuccess;
+  // fc1 on single CTAs with the A rows gathered from x; B = W1 [G*2F, d]
+  CUtensorMap mB;
+  if (!make_map(&mB, w1, (int64_t)G * 2 * F, d, 128)) {
+    *err = MOE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  Params P = base_params(c, G, n_rows, offsets);
+  P.K = d;
+  P.F = F;
+  P.NT = (F + BN / 2 - 1) / (BN / 2);
+  P.out0 = static_cast<bf16*>(h);
+  P.ld0 = F;
+  P.out1 = static_cast<bf16*>(pre_gu);
+  P.a_rows = static_cast<const bf16*>(x);
+  P.a_src = src_rows;
+  P.a_src_rows = (int)x_rows;
+  CUtensorMap mH, mGU;
+  P.tma_out = make_store_map(&mH, h, n_rows, F, F) &&
+              (pre_gu == nullptr || make_store_map(&mGU, pre_gu, n_rows, 2 * F, 2 * F));
+  if (!P.tma_out) mH = mB;
+  if (!P.tma_out || pre_gu == nullptr) mGU = mH;
+  cudaError_t e = launch_one<false, false, EPI_SWIGLU_FWD, true>(c, mB, mB, mH, mGU, P, kFc1Fwd);
+  if (e != cudaSuccess) return e;
+  // fc2 as in the plain forward: A = h [n_rows, F]
+  CUtensorMap mA;
+  const bool pair = use_pair(G, n_rows);
+  if (!make_map(&mA, h, n_rows, F, 128) || !make_map(&mB, w2, (int64_t)G * d, F, pair ? 128 : 256)) {
+    *err = MOE_ERR_CUDA;
+    return cudaSuccess;
+  }
+  Params Q = base_params(c, G, n_rows, offsets);
+  Q.K = F;
+  Q.m128_tails = m128_tails_for(Q.K);
+  Q.N_out = d;
+  Q.NT = (d + BN - 1) / BN;
+  Q.b_group_rows = d;
+  Q.out0 = static_cast<bf16*>(out);
+  Q.ld0 = d;
+  CUtensorMap mC;
+  Q.tma_out = make_store_map(&mC, out, n_rows, d, d);
+  if (!Q.tma_out) mC = mA;
+  return launch_mgrouped<false, EPI_STORE>(c, pair, mA, h, n_rows, F, mB, mC, mC, Q, kFc2Fwd);
+}
+
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, int F, int d,
                                          const int32_t* offsets, const void* x_rows,
                                          const void* w1, const void* w2, const void* pre_gu,
@@ -1605,7 +1760,8 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
       *err = MOE_ERR_CUDA;
       return cudaSuccess;
     }
-    build_tail_maps<<<1, 256, 0, c.stream>>>(mA, mA1, offsets, G, (int)n_rows, tail_maps);
+    launch_dependent(build_tail_maps, dim3(1), dim3(256), 0, c.stream, mA, mA1, offsets, G,
+                     (int)n_rows, tail_maps);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -114,7 +114,11 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
 cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_perm,
                                const int32_t* row_of, const float* dx_router,
                                const void* dx_shared, const float* d_gate_logit,
-                               const float* w_gate, void* dx);
+                               const float* w_gate, const float* d_logits,
+                               const float* w_router, void* dx);
+// whether moe_permute_bwd forms the router's input gradient d_logits · W_r
+// itself (few experts) rather than reading it as dx_router
+bool permute_bwd_forms_router_dx(const moe_cfg& cfg);
 
 // ---- combine (combine.cu)
 cudaError_t launch_combine(const Ctx& c, const moe_cfg& cfg, const void* out_perm,
@@ -175,6 +179,13 @@ cudaError_t launch_tc_grouped_swiglu_fwd(const Ctx& c, int n_groups, int64_t n_r
                                          int d, const int32_t* offsets, const void* x_rows,
                                          const void* w1, const void* w2, void* pre_gu,
                                          void* h, void* out, void* ws, int* err);
+// fc1 with its A rows gathered from x through src_rows (x_rows rows in x),
+// then fc2; single CTAs for fc1
+cudaError_t launch_tc_grouped_swiglu_fwd_gather(const Ctx& c, int G, int64_t n_rows, int F, int d,
+                                                const int32_t* offsets, const void* x,
+                                                int64_t x_rows, const int32_t* src_rows,
+                                                const void* w1, const void* w2, void* pre_gu,
+                                                void* h, void* out, int* err);
 cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int n_groups, int64_t n_rows, int F,
                                          int d, const int32_t* offsets, const void* x_rows,
                                          const void* w1, const void* w2, const void* pre_gu,

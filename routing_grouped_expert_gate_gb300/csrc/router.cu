@@ -14,6 +14,8 @@
 // (hi, lo) pair with an error-free TwoSum, so the only rounding that grows with
 // d is confined to 32-term partial sums. The logits end within a few fp32 ulps
 // of the exact value, far inside the 1e-6 band that marks a near tie.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -150,6 +152,152 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
     if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
     logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
   }
+}
+
+// ------------------------------------------------------------------ S1, E <= 16, W resident
+// The same arithmetic as router_logits_small (FOLD = false: at most IT <= 4
+// groups of 8 elements per lane), with W kept in shared memory for the
+// kernel's life: one CTA per SM walks token groups of TB, so W is read from
+// HBM/L2 once per CTA instead of once per group, and each lane's x loads of
+// the next group are issued before the current group's products. W sits in
+// shared memory as [E][2][d/8] float4s (the two halves of each 8-element
+// group in separate planes), so the lanes of a warp, which take consecutive
+// groups, read consecutive 16-byte words. The logits equal
+// router_logits_small's bit for bit (same products, same order, same sums).
+template <typename Tx, int EMAX, int TB, int IT>
+__global__ void __launch_bounds__(256, 1)
+router_logits_resident(const Tx* __restrict__ x, const float* __restrict__ W,
+                       const float* __restrict__ logit_bias, float* __restrict__ logits,
+                       int64_t T, int d, int E) {
+  extern __shared__ float4 sW[];  // [E][2][ngroups]
+  __shared__ float s_hi[8][TB * EMAX];
+  __shared__ float s_lo[8][TB * EMAX];
+  static_assert(TB * EMAX == 32, "one pair per lane after the reduce-scatter");
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int ngroups = d >> 3;
+  const int g_lo = (int)((int64_t)ngroups * warp / 8);
+  const int g_hi = (int)((int64_t)ngroups * (warp + 1) / 8);
+  const int64_t n_tg = (T + TB - 1) / TB;
+  pdl_wait();  // x may come from the kernel before; logits may still be read by it
+
+  auto load_group = [&](int64_t tg, Raw8<Tx> (&buf)[IT][TB]) {
+    const int64_t t0 = tg * TB;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int g = g_lo + lane + 32 * it;
+#pragma unroll
+      for (int a = 0; a < TB; ++a) {
+        if (g < g_hi && t0 + a < T) buf[it][a].load(x + (t0 + a) * (int64_t)d + 8 * g);
+        else buf[it][a].zero();
+      }
+    }
+  };
+  Raw8<Tx> cur[IT][TB], nxt[IT][TB];
+  if ((int64_t)blockIdx.x < n_tg) load_group(blockIdx.x, cur);
+  stage_w_planes(sW, W, E, d);
+
+  for (int64_t tg = blockIdx.x; tg < n_tg; tg += gridDim.x) {
+    if (tg + gridDim.x < n_tg) load_group(tg + gridDim.x, nxt);
+    const int64_t t0 = tg * TB;
+    float acc[TB][EMAX];
+#pragma unroll
+    for (int a = 0; a < TB; ++a)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) acc[a][e] = 0.f;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int g = g_lo + lane + 32 * it;
+      if (g < g_hi) {
+        float xv[TB][8];
+#pragma unroll
+        for (int a = 0; a < TB; ++a) cur[it][a].to_float(xv[a]);
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          if (e < E) {
+            const float4 w0 = sW[(e * 2) * ngroups + g];
+            const float4 w1 = sW[(e * 2 + 1) * ngroups + g];
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int a = 0; a < TB; ++a)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[a][e] = fmaf(xv[a][i], wv[i], acc[a][e]);
+          }
+        }
+      }
+    }
+    float vh[32], vl[32];
+#pragma unroll
+    for (int a = 0; a < TB; ++a)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        vh[a * EMAX + e] = acc[a][e];
+        vl[a * EMAX + e] = 0.f;
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int q = 0; q < off; ++q) {
+        const float sh_ = upper ? vh[q] : vh[q + off];
+        const float sl_ = upper ? vl[q] : vl[q + off];
+        const float kh = upper ? vh[q + off] : vh[q];
+        const float kl = upper ? vl[q + off] : vl[q];
+        const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
+        const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
+        float s2, er;
+        two_sum(kh, rh, s2, er);
+        vh[q] = s2;
+        vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
+      }
+    }
+    s_hi[warp][lane] = vh[0];
+    s_lo[warp][lane] = vl[0];
+    __syncthreads();
+    for (int q = threadIdx.x; q < TB * EMAX; q += blockDim.x) {
+      const int a = q / EMAX, e = q - a * EMAX;
+      if (e >= E || t0 + a >= T) continue;
+      float h = s_hi[0][q], l = s_lo[0][q];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) {
+        float s2, er;
+        two_sum(h, s_hi[w][q], s2, er);
+        h = s2;
+        l = __fadd_rn(__fadd_rn(l, s_lo[w][q]), er);
+      }
+      if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
+      logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
+    }
+    __syncthreads();  // s_hi / s_lo are rewritten by the next group
+#pragma unroll
+    for (int it = 0; it < IT; ++it)
+#pragma unroll
+      for (int a = 0; a < TB; ++a) cur[it][a] = nxt[it][a];
+  }
+}
+
+// Shared memory the resident form may take for W (E x d fp32).
+constexpr size_t kRouterResidentSmem = 160 * 1024;
+
+template <typename Tx, int EMAX, int TB, int IT>
+static cudaError_t launch_router_resident(const Ctx& c, const Tx* x, const float* w_router,
+                                          const float* logit_bias, float* logits, int64_t T,
+                                          int d, int E) {
+  auto kern = router_logits_resident<Tx, EMAX, TB, IT>;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kRouterResidentSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev & 63] = true;
+  }
+  const int64_t n_tg = (T + TB - 1) / TB;
+  const int64_t grid = n_tg < c.sm_count ? n_tg : c.sm_count;
+  const size_t smem = (size_t)E * d * sizeof(float);
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(256), smem, c.stream, x, w_router,
+                          logit_bias, logits, T, d, E);
 }
 
 // ------------------------------------------------------------------ S1, E > 16
@@ -420,6 +568,7 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
             const float* __restrict__ beta, float* __restrict__ alpha,
             int32_t* __restrict__ idx, float* __restrict__ w, int64_t T, int E, int k,
             int score_fn, float scaling) {
+  pdl_wait();  // the logits come from the kernel before
   const int ksel = (alpha != nullptr) ? k + 1 : k;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -562,6 +711,7 @@ __global__ void __launch_bounds__(256)
 router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ idx,
                   const float* __restrict__ dw, float* __restrict__ d_logits, int64_t T,
                   int E, int k, int score_fn, float scaling, int accumulate, int* status) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
@@ -666,6 +816,7 @@ template <typename Tx, int EMAX>
 __global__ void __launch_bounds__(128)
 router_dw_small(const Tx* __restrict__ x, const float* __restrict__ d_logits,
                 float* __restrict__ part, int64_t T, int d, int E, int64_t tok_per_slice) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   constexpr int U = EMAX <= 8 ? 4 : 2;
   const int c0 = (blockIdx.x * 128 + threadIdx.x) * 8;
   const int64_t t_beg = (int64_t)blockIdx.y * tok_per_slice;
@@ -715,9 +866,9 @@ cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void*
   if (cfg.T == 0) return cudaSuccess;
   const int64_t per = (cfg.T + splits - 1) / splits;
   dim3 grid((unsigned)((cfg.d / 8 + 127) / 128), (unsigned)splits);
-#define MOE_DWS(TX, EM)                                                                   \
-  router_dw_small<TX, EM><<<grid, 128, 0, c.stream>>>(static_cast<const TX*>(x), d_logits, \
-                                                      part, cfg.T, cfg.d, cfg.E, per)
+#define MOE_DWS(TX, EM)                                                                 \
+  launch_dependent(router_dw_small<TX, EM>, dim3(grid), dim3(128), 0, c.stream,           \
+                   static_cast<const TX*>(x), d_logits, part, cfg.T, cfg.d, cfg.E, per)
   if (cfg.act_dtype == MOE_BF16) {
     if (cfg.E <= 8) MOE_DWS(bf16, 8); else MOE_DWS(bf16, 16);
   } else {
@@ -788,6 +939,28 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
   if (cfg.E <= 16) {
     // groups of 8 per lane: d / 8 split over 8 warps of 32 lanes
     const bool fold = (cfg.d / 8 + 255) / 256 > 4;
+    const int it = (cfg.d / 8 + 255) / 256;  // groups per lane
+    // fp32 x: at most two groups per lane (four would spill the prefetch buffers)
+    const int it_max = sizeof(Tx) == 2 ? 4 : 2;
+    if (!fold && it <= it_max && (size_t)cfg.E * cfg.d * sizeof(float) <= kRouterResidentSmem) {
+      cudaError_t e;
+      auto res = [&](auto em, auto tb) {
+        constexpr int EM = decltype(em)::value, TB_ = decltype(tb)::value;
+        if (it <= 1)
+          return launch_router_resident<Tx, EM, TB_, 1>(c, x, w_router, logit_bias, logits, T,
+                                                        cfg.d, cfg.E);
+        if (it <= 2 || sizeof(Tx) != 2)
+          return launch_router_resident<Tx, EM, TB_, 2>(c, x, w_router, logit_bias, logits, T,
+                                                        cfg.d, cfg.E);
+        return launch_router_resident<Tx, EM, TB_, (sizeof(Tx) == 2 ? 4 : 2)>(
+            c, x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
+      };
+      e = cfg.E <= 8 ? res(std::integral_constant<int, 8>{}, std::integral_constant<int, 4>{})
+                     : res(std::integral_constant<int, 16>{}, std::integral_constant<int, 2>{});
+      if (e != cudaSuccess) return e;
+      note_launches(1);
+      return cudaGetLastError();
+    }
     const unsigned grid8 = (unsigned)((T + 3) / 4), grid16 = (unsigned)((T + 1) / 2);
     if (cfg.E <= 8 && !fold)
       router_logits_small<Tx, 8, 4, false><<<grid8, 256, 0, c.stream>>>(x, w_router, logit_bias,
@@ -855,9 +1028,10 @@ cudaError_t launch_router_topk_q(const Ctx& c, const moe_cfg& cfg, const float* 
   if (cfg.T == 0) return cudaSuccess;
   const unsigned grid = warp_grid(c, cfg.T);
   const int epl = (cfg.E + 31) / 32;
-#define MOE_TOPK(N)                                                                        \
-  router_topk<N><<<grid, 256, 0, c.stream>>>(logits, sel_bias, beta, alpha, idx, w, cfg.T, \
-                                             cfg.E, cfg.k, cfg.score_fn, cfg.scaling)
+  cudaError_t e;
+#define MOE_TOPK(N)                                                                          \
+  e = launch_dependent(router_topk<N>, dim3(grid), dim3(256), 0, c.stream, logits, sel_bias, \
+                       beta, alpha, idx, w, cfg.T, cfg.E, cfg.k, cfg.score_fn, cfg.scaling)
   switch (epl) {
     case 1: MOE_TOPK(1); break;
     case 2: MOE_TOPK(2); break;
@@ -866,7 +1040,7 @@ cudaError_t launch_router_topk_q(const Ctx& c, const moe_cfg& cfg, const float* 
   }
 #undef MOE_TOPK
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_router_near_ties(const Ctx& c, const moe_cfg& cfg, const float* logits,
@@ -893,7 +1067,7 @@ cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const flo
                                      const int32_t* idx, const float* dw, float* d_logits,
                                      int accumulate) {
   if (cfg.T == 0) return cudaSuccess;
-  router_scores_bwd<<<warp_grid(c, cfg.T), 256, 0, c.stream>>>(
+  launch_dependent(router_scores_bwd, dim3(warp_grid(c, cfg.T)), dim3(256), 0, c.stream,
       logits, idx, dw, d_logits, cfg.T, cfg.E, cfg.k, cfg.score_fn, cfg.scaling, accumulate,
       c.status);
   note_launches(1);

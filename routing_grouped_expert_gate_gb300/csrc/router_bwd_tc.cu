@@ -273,6 +273,7 @@ plane_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
 // fp32 [n] -> three bf16 planes [3][n] (the same split as the forward's)
 __global__ void split3(const float* __restrict__ v, bf16* __restrict__ planes, int64_t n4) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int64_t n = 4 * n4;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -319,7 +320,7 @@ static void split_planes(const Ctx& c, const float* v, bf16* planes, int64_t n) 
   const int64_t n4 = n / 4;
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n4 + 255) / 256,
                                                                  (int64_t)c.sm_count * 8));
-  split3<<<blocks, 256, 0, c.stream>>>(v, planes, n4);
+  launch_dependent(split3, dim3(blocks), dim3(256), 0, c.stream, v, planes, n4);
   note_launches(1);
 }
 

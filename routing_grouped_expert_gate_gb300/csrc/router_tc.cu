@@ -300,6 +300,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 // w [n] fp32 -> planes [3][n] bf16 with w = p0 + p1 + p2 (to 2^-24 |w|)
 __global__ void router_split_planes(const float* __restrict__ w, bf16* __restrict__ planes,
                                     int64_t n4) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int64_t n = 4 * n4;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -375,7 +376,7 @@ cudaError_t launch_router_logits_tc(const Ctx& c, const moe_cfg& cfg, const void
   bf16* planes = static_cast<bf16*>(ws);
   const int64_t n4 = n / 4;
   const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)c.sm_count * 8);
-  router_split_planes<<<blocks, 256, 0, c.stream>>>(w_router, planes, n4);
+  launch_dependent(router_split_planes, dim3(blocks), dim3(256), 0, c.stream, w_router, planes, n4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   note_launches(1);

@@ -24,6 +24,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 shared_gate_fwd(const T* __restrict__ x, const float* __restrict__ w_gate,
                 float* __restrict__ gate, int64_t Tn, int d) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int ng = d >> 3;
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(256)
 shared_gate_bwd_tok(const T* __restrict__ dy, const T* __restrict__ y_s,
                     const float* __restrict__ gate, T* __restrict__ dy_s,
                     float* __restrict__ d_gate_logit, int64_t Tn, int d) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int ng = d >> 3;
@@ -72,10 +74,10 @@ cudaError_t launch_shared_gate(const Ctx& c, const moe_cfg& cfg, const void* x,
                                const float* w_gate, float* gate) {
   if (cfg.T == 0) return cudaSuccess;
   if (cfg.act_dtype == MOE_BF16)
-    shared_gate_fwd<bf16><<<gate_grid(c, cfg.T), 256, 0, c.stream>>>(
+    launch_dependent(shared_gate_fwd<bf16>, dim3(gate_grid(c, cfg.T)), dim3(256), 0, c.stream,
         static_cast<const bf16*>(x), w_gate, gate, cfg.T, cfg.d);
   else
-    shared_gate_fwd<float><<<gate_grid(c, cfg.T), 256, 0, c.stream>>>(
+    launch_dependent(shared_gate_fwd<float>, dim3(gate_grid(c, cfg.T)), dim3(256), 0, c.stream,
         static_cast<const float*>(x), w_gate, gate, cfg.T, cfg.d);
   note_launches(1);
   return cudaGetLastError();
@@ -86,11 +88,11 @@ cudaError_t launch_shared_gate_bwd_tokens(const Ctx& c, const moe_cfg& cfg, cons
                                           void* dy_shared, float* d_gate_logit) {
   if (cfg.T == 0) return cudaSuccess;
   if (cfg.act_dtype == MOE_BF16)
-    shared_gate_bwd_tok<bf16><<<gate_grid(c, cfg.T), 256, 0, c.stream>>>(
+    launch_dependent(shared_gate_bwd_tok<bf16>, dim3(gate_grid(c, cfg.T)), dim3(256), 0, c.stream,
         static_cast<const bf16*>(dy), static_cast<const bf16*>(shared_out), gate,
         static_cast<bf16*>(dy_shared), d_gate_logit, cfg.T, cfg.d);
   else
-    shared_gate_bwd_tok<float><<<gate_grid(c, cfg.T), 256, 0, c.stream>>>(
+    launch_dependent(shared_gate_bwd_tok<float>, dim3(gate_grid(c, cfg.T)), dim3(256), 0, c.stream,
         static_cast<const float*>(dy), static_cast<const float*>(shared_out), gate,
         static_cast<float*>(dy_shared), d_gate_logit, cfg.T, cfg.d);
   note_launches(1);

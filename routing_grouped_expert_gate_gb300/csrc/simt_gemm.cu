@@ -191,6 +191,7 @@ template <typename TO>
 __global__ void __launch_bounds__(256)
 reduce_partials_kernel(const float* __restrict__ part, int64_t stride, int nz, int64_t n,
                        TO* __restrict__ out, int accumulate) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     float v = 0.f;
@@ -206,11 +207,11 @@ cudaError_t launch_reduce_partials(const Ctx& c, const float* part, int64_t stri
   const int64_t blocks = (n + 255) / 256;
   const unsigned grid = (unsigned)(blocks < (int64_t)c.sm_count * 8 ? blocks : c.sm_count * 8);
   if (dt_out == kF32)
-    reduce_partials_kernel<float><<<grid, 256, 0, c.stream>>>(part, stride, nz, n,
-                                                              static_cast<float*>(out), accumulate);
+    launch_dependent(reduce_partials_kernel<float>, dim3(grid), dim3(256), 0, c.stream, part,
+                     stride, nz, n, static_cast<float*>(out), accumulate);
   else
-    reduce_partials_kernel<bf16><<<grid, 256, 0, c.stream>>>(part, stride, nz, n,
-                                                             static_cast<bf16*>(out), accumulate);
+    launch_dependent(reduce_partials_kernel<bf16>, dim3(grid), dim3(256), 0, c.stream, part,
+                     stride, nz, n, static_cast<bf16*>(out), accumulate);
   note_launches(1);
   return cudaGetLastError();
 }

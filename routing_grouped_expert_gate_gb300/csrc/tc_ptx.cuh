@@ -190,6 +190,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn, int m, i
 // missing or the encoder refuses the arguments.
 bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 
+// ---- 16-byte asynchronous copies (cp.async) for gathered rows
+// global -> shared, 16 bytes, the last (16 - src_bytes) bytes filled with zeros
+// (src_bytes = 0: nothing is read, the destination becomes zeros).
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- 2-CTA clusters: rank, DSMEM addresses, barriers
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

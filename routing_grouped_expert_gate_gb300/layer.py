@@ -136,11 +136,17 @@ def backward(cfg, p: Dict[str, Optional[torch.Tensor]], x: torch.Tensor, dy: tor
                              stream)
         dx_s = b["dx_s"]
     L.aux_loss_bwd(cfg, b["logits"], b["counts"], g_aux, b["d_logits"], 0, stream)
+    # few experts: the permute backward forms the router's input gradient
+    # d_logits · W_r itself, so the router backward writes no dx_router
+    fused = L.router_dx_in_permute_bwd(cfg)
     L.route_topk_bwd(cfg, x, p["w_router"], b["logits"], b["idx"], b["dw"], b["d_logits"], 1,
-                     b["dx_router"], b["dw_router"], ws, stream)
-    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], b["dx_router"], dx_s, b["dx"], stream,
+                     None if fused else b["dx_router"], b["dw_router"], ws, stream)
+    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], None if fused else b["dx_router"], dx_s,
+                  b["dx"], stream,
                   d_gate_logit=b["d_gate_logit_s"] if gated else None,
-                  w_gate=p["w_gate_s"] if gated else None)
+                  w_gate=p["w_gate_s"] if gated else None,
+                  d_logits=b["d_logits"] if fused else None,
+                  w_router=p["w_router"] if fused else None)
     return b
 
 

@@ -140,3 +140,26 @@ def test_activation_settings_validated(L):
         assert L.check_cfg(_cfg(L, **kw)) == L.MOE_OK, kw
     for kw in bad:
         assert L.check_cfg(_cfg(L, **kw)) == L.MOE_ERR_INVALID_ARG, kw
+
+
+def test_router_dx_placement_rules(L):
+    """Few experts: the permute backward forms d_logits · W_r (the router
+    backward may then skip dx_router); many experts: the router backward must
+    write it and the permute backward refuses to form it. Refusals come
+    before any device work."""
+    few, many = _cfg(L, E=8, k=2), _cfg(L, E=64, k=8)
+    assert L.router_dx_in_permute_bwd(few) and not L.router_dx_in_permute_bwd(many)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced
+    rc = L.lib.moe_permute_bwd(ctypes.byref(many), fake, fake, None, None, None, None, fake, fake,
+                               fake, None)
+    assert rc == L.MOE_ERR_UNSUPPORTED
+    rc = L.lib.moe_permute_bwd(ctypes.byref(few), fake, fake, fake, None, None, None, fake, fake,
+                               fake, None)
+    assert rc == L.MOE_ERR_INVALID_ARG  # dx_router together with d_logits
+    rc = L.lib.moe_permute_bwd(ctypes.byref(few), fake, fake, None, None, None, None, fake, None,
+                               fake, None)
+    assert rc == L.MOE_ERR_INVALID_ARG  # d_logits without w_router
+    ws_need = L.workspace_bytes(many, L.MOE_WS_ROUTE_BWD)
+    rc = L.lib.moe_route_topk_bwd(ctypes.byref(many), fake, fake, fake, fake, fake, fake, 1, None,
+                                  fake, fake, ws_need, None)
+    assert rc == L.MOE_ERR_INVALID_ARG

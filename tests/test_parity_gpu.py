@@ -538,3 +538,96 @@ def test_near_tie_count(built, name):
         assert lo <= n <= hi, (band, lo, n, hi)
     assert n == wl.T  # every token is a near tie for an unbounded band
     assert L.last_device_status()[0] == 0
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (127, 8, 2), (4096, 8, 2), (2051, 64, 8),
+                                   (20608, 256, 4), (16384, 128, 8), (33024, 256, 4)])
+def test_permute_index_paths(built, T, E, k):
+    """The dispatch on both of its index paths: a wide one-CTA scan of the
+    per-(128-token block, expert) counts followed by a fused rank + copy
+    while each scan thread holds at most 64 blocks, and beyond that (T =
+    33024, E = 256: 258 blocks) separate count, scan, rank and copy launches.
+    counts, offsets, row_of and src_tok bit-exact against the oracle's
+    dispatch; every copied row equal to its token's row."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    d = 64
+    cfg = moe.make_cfg(T=T, d=d, E=E, k=k, F=64)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(T * 31 + E)
+    # k distinct experts per token, skewed towards the low indices
+    keys = torch.rand(T, E, generator=g, device="cuda") * torch.linspace(1.0, 0.2, E,
+                                                                         device="cuda")
+    idx = torch.topk(keys, k, dim=1).indices.to(torch.int32).contiguous()
+    x = torch.randn(T, d, generator=g, device="cuda").to(torch.bfloat16)
+    counts = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    offsets = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+    row_of = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    src = torch.full((T * k,), -1, dtype=torch.int32, device="cuda")
+    xp = torch.zeros(T * k, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_PERMUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+    L.permute(cfg, x, idx, counts, offsets, row_of, src, xp, ws)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    ref = O.dispatch(idx.cpu().numpy().astype(np.int64), E)
+    for key, got in (("counts", counts), ("offsets", offsets), ("row_of", row_of),
+                     ("src_tok", src)):
+        assert np.array_equal(got.cpu().numpy().astype(np.int64), ref[key]), key
+    assert torch.equal(xp, x[src.long()])
+
+
+@pytest.mark.parametrize("name", ["mixtral_small", "presoftmax_top1_small", "tiny_fp32",
+                                  "mixtral_d4096_small"])
+def test_router_dx_formed_in_permute_bwd_is_bitwise_the_same(built, name):
+    """Few experts: the permute backward forms d_logits · W_r itself. Its dx
+    equals, bit for bit, the dx of the other order of work (the router
+    backward writing dx_router in fp32, the permute backward adding it)."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = SMALL[name]
+    cfg = moe.cfg_from_workload(wl)
+    assert L.router_dx_in_permute_bwd(cfg)
+    inp, b = run_gpu(wl, backward=True)
+    dx_fused = b["dx"].clone()
+    # d_logits rebuilt as the layer builds it (aux part, then the scores part)
+    # with the router backward now writing dx_router
+    L.aux_loss_bwd(cfg, b["logits"], b["counts"], 1.0, b["d_logits"], 0)
+    L.route_topk_bwd(cfg, inp["x"], inp["w_router"], b["logits"], b["idx"], b["dw"],
+                     b["d_logits"], 1, b["dx_router"], b["dw_router"], b["ws"])
+    dx2 = torch.empty_like(b["dx"])
+    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], b["dx_router"], None, dx2)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    assert torch.equal(dx2, dx_fused)
+
+
+@pytest.mark.parametrize("name", ["deepseek_small", "fine_grained_small", "ragged_d_small",
+                                  "mixtral_small", "zipf_small"])
+def test_gathered_fc1_equals_explicit_permute(built, name):
+    """fc1 reading its rows straight from x through src_tok (the dispatch copy
+    fused into the operand load) computes what the explicit x_perm path
+    computes, bit for bit: gate|up, h and fc2's output. The dispatch run
+    without x_perm produces the same index outputs."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = SMALL[name]
+    inp, b = run_gpu(wl, backward=False)
+    cfg = moe.cfg_from_workload(wl)
+    T, k, E, F = wl.T, wl.k, wl.E, wl.F
+    # index outputs only
+    idx_only = {n: torch.full_like(b[n], -3) for n in ("counts", "offsets", "row_of", "src_tok")}
+    L.permute(cfg, None, b["idx"], idx_only["counts"], idx_only["offsets"], idx_only["row_of"],
+              idx_only["src_tok"], None, b["ws"])
+    pre = torch.full_like(b["pre_gu"], float("nan"))
+    h = torch.full_like(b["h"], float("nan"))
+    out = torch.full_like(b["out_perm"], float("nan"))
+    L.grouped_swiglu_gather(cfg, E, T * k, F, b["offsets"], inp["x"], b["src_tok"], inp["w1"],
+                            inp["w2"], pre, h, out)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    for n, v in idx_only.items():
+        assert torch.equal(v, b[n]), n
+    assert torch.equal(pre, b["pre_gu"])
+    assert torch.equal(h, b["h"])
+    assert torch.equal(out, b["out_perm"])
