@@ -5,24 +5,24 @@
 // expert; "Read the timeline before blaming the network" groups the token rows
 // by expert before the expert GEMMs and restores the order afterwards.
 //
-// Three launches on the caller's stream, no host sync, each a programmatic
-// dependent launch of the one before (scheduled while it runs, waiting on
-// griddepcontrol.wait for its results, which hides the launch gaps):
+// Two launches on the caller's stream, no host sync, the second a programmatic
+// dependent launch of the first (scheduled while it runs, waiting on
+// griddepcontrol.wait for its results, which hides the launch gap):
 //   count     : per block of 128 tokens, a bitmask per expert of which tokens in
 //               the block chose it (shared memory), popcounts -> per-block counts
-//   scan      : one CTA of 1024 threads; per expert, exclusive scan over blocks
-//               in chunks; exclusive scan over experts -> counts, offsets and
-//               the absolute base row of each (block, expert)
-//   rank+copy : several CTAs per 128-token block rebuild the block's bitmasks;
-//               the rank of token t among the block's tokens that chose e is a
-//               popcount of the bits below t, so row(t, e) = base(block, e) +
-//               rank: expert-contiguous and stable. Each CTA then copies its
-//               share of the block's tokens, one warp per token reading the row
-//               once and writing its k copies with 16-byte accesses (the
-//               HBM-bound part).
-// Where the wide scan would need more than 64 blocks per thread (more than
-// 64 * 1024 / E blocks of 128 tokens, or 4096 blocks) the older four-launch
-// form runs: count, a one-thread-per-expert scan, rank, copy.
+//   rank+copy : several CTAs per 128-token block. Each sums the count matrix
+//               (expert totals, and per expert the blocks before its own), scans
+//               the totals over experts -> the base row of each expert in its
+//               block (CTA 0 writes counts and offsets); rebuilds the block's
+//               bitmasks: the rank of token t among the block's tokens that
+//               chose e is a popcount of the bits below t, so row(t, e) =
+//               base(block, e) + rank: expert-contiguous and stable. Each CTA
+//               then copies its share of the block's tokens, one warp per token
+//               reading the row once and writing its k copies with 16-byte
+//               accesses (the HBM-bound part).
+// Beyond 16384 (block, expert) cells the per-CTA sums would grow too large and
+// the older four-launch form runs: count, a one-thread-per-expert scan, rank,
+// copy.
 #include "common.cuh"
 #include "internal.h"
 
@@ -147,110 +147,87 @@ permute_rank(const int32_t* __restrict__ idx, int64_t T, int k, int E,
   }
 }
 
-// ------------------------------------------------------------------ scan, wide
-constexpr int PS_THREADS = 1024;
-
-// One CTA of 1024 threads: the per-(block, expert) counts written by
-// permute_count become absolute base rows, with counts[] and offsets[]. Per
-// expert e the blocks are cut into C chunks of about sqrt(nblk) blocks;
-// thread (c, e) sums its chunk with all its loads in flight, the chunk sums are
-// scanned per expert, the expert totals scanned by one warp, and each thread
-// rewrites its chunk. (permute_scan does the same with one thread per expert
-// walking every block; this form has about sqrt(nblk) dependent steps.) The
-// launcher keeps chunks at <= 64 blocks.
-__global__ void __launch_bounds__(PS_THREADS)
-permute_scan_wide(int32_t* __restrict__ block_counts, int nblk, int E,
-                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int32_t part[PS_THREADS];
-  __shared__ int32_t base[kMaxE];
-  pdl_wait();
-  int C = PS_THREADS / E;
-  int cs = 1;
-  while (cs * cs < nblk) ++cs;
-  if ((nblk + cs - 1) / cs < C) C = (nblk + cs - 1) / cs;
-  cs = (nblk + C - 1) / C;
-  const int e = threadIdx.x % E, c = threadIdx.x / E;
-  const bool act = c < C;
-  const int b0 = c * cs, b1 = min(nblk, b0 + cs);
-  int sum = 0;
-  if (act) {  // sixteen loads in flight at a time
-    for (int i0 = b0; i0 < b1; i0 += 16) {
-      int v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        v[i] = (i0 + i < b1) ? block_counts[(int64_t)(i0 + i) * E + e] : 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sum += v[i];
-    }
-    part[c * E + e] = sum;
-  }
-  __syncthreads();
-  if (threadIdx.x < E) {  // chunk prefixes of expert e; its total
-    int run = 0;
-    for (int cc = 0; cc < C; ++cc) {
-      const int w = part[cc * E + threadIdx.x];
-      part[cc * E + threadIdx.x] = run;
-      run += w;
-    }
-    counts[threadIdx.x] = run;
-    base[threadIdx.x] = run;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {  // exclusive scan of the expert totals, one warp
-    const int per = (E + 31) / 32;
-    const int lo = threadIdx.x * per;
-    int loc = 0;
-    for (int i = lo; i < lo + per && i < E; ++i) loc += base[i];
-    int incl = loc;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int w = __shfl_up_sync(0xffffffffu, incl, off);
-      if ((int)threadIdx.x >= off) incl += w;
-    }
-    int run = incl - loc;
-    for (int i = lo; i < lo + per && i < E; ++i) {
-      const int w = base[i];
-      base[i] = run;
-      offsets[i] = run;
-      run += w;
-    }
-    if (threadIdx.x == 31) offsets[E] = incl;
-  }
-  __syncthreads();
-  if (act) {  // the chunk again (from L2), rewritten as base rows
-    int run = part[c * E + e] + base[e];
-    for (int i0 = b0; i0 < b1; i0 += 16) {
-      int v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        v[i] = (i0 + i < b1) ? block_counts[(int64_t)(i0 + i) * E + e] : 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (i0 + i < b1) {
-          block_counts[(int64_t)(i0 + i) * E + e] = run;
-          run += v[i];
-        }
-      }
-    }
-  }
-}
-
-// CTA (block b, part p) of `parts`: the bitmasks of block b, then for the
-// tokens of part p the rows row(t, j) = block_base[b][e] + rank (written to
+// CTA (block b, part p) of `parts`, from the per-(block, expert) counts of
+// permute_count: the base rows it needs, then the bitmasks of block b, then for
+// the tokens of part p the rows row(t, j) = base(b, e) + rank (written to
 // row_of and src_tok) and the copy x_perm[row(t, j)] = x[t], one warp per token.
+// base(b, e) = offsets[e] + sum_{b' < b} cnt[b'][e], offsets the exclusive scan
+// of the expert totals: every CTA sums the count matrix itself (threads split
+// it by expert and by chunks of blocks), which takes the place of a separate
+// scan launch; CTA 0 also writes counts and offsets.
 template <typename T>
 __global__ void __launch_bounds__(256)
 permute_rank_copy(const T* __restrict__ x, const int32_t* __restrict__ idx, int64_t Tn, int k,
-                  int E, int d, int parts, const int32_t* __restrict__ block_base,
+                  int E, int d, int parts, int nblk, const int32_t* __restrict__ block_counts,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ row_of, int32_t* __restrict__ src_tok,
                   T* __restrict__ x_perm) {
   __shared__ uint32_t masks[kMaxE][PB_WORDS];
   __shared__ int32_t s_rows[PB_TOK][kMaxK];
+  __shared__ int32_t s_tot[256], s_pre[256];  // [chunk][expert] partial sums
+  __shared__ int32_t s_base[kMaxE];
   pdl_wait();
   const int blk = blockIdx.x / parts;
   const int part = blockIdx.x - blk * parts;
-  for (int i = threadIdx.x; i < E * PB_WORDS; i += blockDim.x) masks[i / PB_WORDS][i % PB_WORDS] = 0u;
-  __syncthreads();
+  // ---- the count matrix: expert totals and this block's prefix, per chunk
+  {
+    int C = (int)blockDim.x / E;
+    if (C > nblk) C = nblk;
+    const int e = threadIdx.x % E, c = threadIdx.x / E;
+    if (c < C) {
+      const int b0 = (int)((int64_t)nblk * c / C), b1 = (int)((int64_t)nblk * (c + 1) / C);
+      int tot = 0, pre = 0;
+      for (int i0 = b0; i0 < b1; i0 += 16) {
+        int v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          v[i] = (i0 + i < b1) ? block_counts[(int64_t)(i0 + i) * E + e] : 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          tot += v[i];
+          pre += (i0 + i < blk) ? v[i] : 0;
+        }
+      }
+      s_tot[c * E + e] = tot;
+      s_pre[c * E + e] = pre;
+    }
+    for (int i = threadIdx.x; i < E * PB_WORDS; i += blockDim.x) masks[i / PB_WORDS][i % PB_WORDS] = 0u;
+    __syncthreads();
+    if (threadIdx.x < E) {
+      int tot = 0, pre = 0;
+      for (int cc = 0; cc < C; ++cc) {
+        tot += s_tot[cc * E + threadIdx.x];
+        pre += s_pre[cc * E + threadIdx.x];
+      }
+      s_base[threadIdx.x] = tot;  // the total, scanned below
+      s_pre[threadIdx.x] = pre;   // (row 0 of s_pre: this thread's own cell)
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // exclusive scan of the totals over experts, one warp
+      const int per = (E + 31) / 32;
+      const int lo = threadIdx.x * per;
+      int loc = 0;
+      for (int i = lo; i < lo + per && i < E; ++i) loc += s_base[i];
+      int incl = loc;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int w = __shfl_up_sync(0xffffffffu, incl, off);
+        if ((int)threadIdx.x >= off) incl += w;
+      }
+      int run = incl - loc;
+      for (int i = lo; i < lo + per && i < E; ++i) {
+        const int w = s_base[i];
+        if (blockIdx.x == 0) {
+          counts[i] = w;
+          offsets[i] = run;
+        }
+        s_base[i] = run + s_pre[i];  // base row of (this block, expert i)
+        run += w;
+      }
+      if (blockIdx.x == 0 && threadIdx.x == 31) offsets[E] = incl;
+    }
+  }
+  // ---- bitmasks of the block (the block's indices kept for the ranks)
   const int64_t t_base = (int64_t)blk * PB_TOK;
   for (int i = threadIdx.x; i < PB_TOK * k; i += blockDim.x) {
     const int tl = i / k;
@@ -272,7 +249,7 @@ permute_rank_copy(const T* __restrict__ x, const int32_t* __restrict__ idx, int6
     if (e >= 0 && e < E) {
       int rank = __popc(masks[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
       for (int w = 0; w < (tl >> 5); ++w) rank += __popc(masks[e][w]);
-      row = block_base[(int64_t)blk * E + e] + rank;
+      row = s_base[e] + rank;
       src_tok[row] = (int32_t)t;
     }
     row_of[t * k + j] = row;
@@ -361,15 +338,11 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
   const int64_t nblk = permute_blocks(cfg.T);
   int32_t* block_counts = static_cast<int32_t*>(ws);
   const int64_t A = cfg.T * cfg.k;
-  // the wide scan holds at most 64 blocks per thread
-  if (nblk > 0 && nblk <= 4096 && nblk <= (int64_t)64 * (PS_THREADS / cfg.E)) {
-    // count (one CTA per 128-token block), wide scan, rank + copy: each a
-    // dependent launch of the one before
+  if (nblk > 0 && nblk * cfg.E <= 16384) {
+    // count (one CTA per 128-token block), then rank + copy, which also turns
+    // the counts into base rows: a dependent launch of the count
     cudaError_t e = launch_dependent(permute_count, dim3((unsigned)nblk), dim3(256), 0, c.stream,
                                      idx, cfg.T, cfg.k, cfg.E, block_counts, c.status);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(permute_scan_wide, dim3(1), dim3(PS_THREADS), 0, c.stream,
-                         block_counts, (int)nblk, cfg.E, counts, offsets);
     if (e != cudaSuccess) return e;
     // CTAs per 128-token block: about four waves of the SMs in all
     int64_t parts = ((int64_t)4 * c.sm_count + nblk - 1) / nblk;
@@ -379,14 +352,14 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
     if (cfg.act_dtype == MOE_BF16)
       e = launch_dependent(permute_rank_copy<bf16>, dim3(grid), dim3(256), 0, c.stream,
                            static_cast<const bf16*>(x), idx, cfg.T, cfg.k, cfg.E, cfg.d,
-                           (int)parts, static_cast<const int32_t*>(block_counts), row_of, src_tok,
-                           static_cast<bf16*>(x_perm));
+                           (int)parts, (int)nblk, static_cast<const int32_t*>(block_counts),
+                           counts, offsets, row_of, src_tok, static_cast<bf16*>(x_perm));
     else
       e = launch_dependent(permute_rank_copy<float>, dim3(grid), dim3(256), 0, c.stream,
                            static_cast<const float*>(x), idx, cfg.T, cfg.k, cfg.E, cfg.d,
-                           (int)parts, static_cast<const int32_t*>(block_counts), row_of, src_tok,
-                           static_cast<float*>(x_perm));
-    note_launches(3);
+                           (int)parts, (int)nblk, static_cast<const int32_t*>(block_counts),
+                           counts, offsets, row_of, src_tok, static_cast<float*>(x_perm));
+    note_launches(2);
     return e;
   }
   if (nblk > 0) {

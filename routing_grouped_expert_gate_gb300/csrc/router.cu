@@ -14,8 +14,6 @@
 // (hi, lo) pair with an error-free TwoSum, so the only rounding that grows with
 // d is confined to 32-term partial sums. The logits end within a few fp32 ulps
 // of the exact value, far inside the 1e-6 band that marks a near tie.
-#include <type_traits>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -155,63 +153,62 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 }
 
 // ------------------------------------------------------------------ S1, E <= 16, W resident
-// The same arithmetic as router_logits_small (FOLD = false: at most IT <= 4
-// groups of 8 elements per lane), with W kept in shared memory for the
-// kernel's life: one CTA per SM walks token groups of TB, so W is read from
-// HBM/L2 once per CTA instead of once per group, and each lane's x loads of
-// the next group are issued before the current group's products. W sits in
-// shared memory as [E][2][d/8] float4s (the two halves of each 8-element
-// group in separate planes), so the lanes of a warp, which take consecutive
-// groups, read consecutive 16-byte words. The logits equal
-// router_logits_small's bit for bit (same products, same order, same sums).
-template <typename Tx, int EMAX, int TB, int IT>
+// W stays in shared memory for the kernel's life ([E][2][d/8] float4 planes,
+// staged once per CTA) and every warp works alone on groups of TB tokens, one
+// CTA per SM walking the token groups: no block-wide barrier per group, so the
+// eight warps' loads and arithmetic overlap. A lane takes the 8-element groups
+// lane, lane + 32, ... of the hidden dimension in chunks of CH groups: the
+// chunk's x loads are issued together, its products with W (read from shared
+// memory, consecutive words across the lanes) are summed in plain fp32 FMAs
+// (at most 32 elements) and folded into a compensated (hi, lo) pair per
+// (token, expert). The lanes' pairs are then combined by a reduce-scatter with
+// TwoSums (lane q ends with pair q = token q / EMAX, expert q % EMAX), so each
+// logit carries only the rounding of its 32-element chunk sums.
+template <typename Tx, int EMAX, int TB>
 __global__ void __launch_bounds__(256, 1)
 router_logits_resident(const Tx* __restrict__ x, const float* __restrict__ W,
                        const float* __restrict__ logit_bias, float* __restrict__ logits,
                        int64_t T, int d, int E) {
   extern __shared__ float4 sW[];  // [E][2][ngroups]
-  __shared__ float s_hi[8][TB * EMAX];
-  __shared__ float s_lo[8][TB * EMAX];
   static_assert(TB * EMAX == 32, "one pair per lane after the reduce-scatter");
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int ngroups = d >> 3;
-  const int g_lo = (int)((int64_t)ngroups * warp / 8);
-  const int g_hi = (int)((int64_t)ngroups * (warp + 1) / 8);
-  const int64_t n_tg = (T + TB - 1) / TB;
+  constexpr int CH = sizeof(Tx) == 2 ? 4 : 2;  // groups of 8 per chunk
   pdl_wait();  // x may come from the kernel before; logits may still be read by it
-
-  auto load_group = [&](int64_t tg, Raw8<Tx> (&buf)[IT][TB]) {
-    const int64_t t0 = tg * TB;
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int g = g_lo + lane + 32 * it;
-#pragma unroll
-      for (int a = 0; a < TB; ++a) {
-        if (g < g_hi && t0 + a < T) buf[it][a].load(x + (t0 + a) * (int64_t)d + 8 * g);
-        else buf[it][a].zero();
-      }
-    }
-  };
-  Raw8<Tx> cur[IT][TB], nxt[IT][TB];
-  if ((int64_t)blockIdx.x < n_tg) load_group(blockIdx.x, cur);
   stage_w_planes(sW, W, E, d);
-
-  for (int64_t tg = blockIdx.x; tg < n_tg; tg += gridDim.x) {
-    if (tg + gridDim.x < n_tg) load_group(tg + gridDim.x, nxt);
+  const int lane = threadIdx.x & 31;
+  const int ngroups = d >> 3;
+  const int64_t n_tg = (T + TB - 1) / TB;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t tg = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tg < n_tg;
+       tg += warps) {
     const int64_t t0 = tg * TB;
-    float acc[TB][EMAX];
+    float hi[TB][EMAX], lo[TB][EMAX];
 #pragma unroll
     for (int a = 0; a < TB; ++a)
 #pragma unroll
-      for (int e = 0; e < EMAX; ++e) acc[a][e] = 0.f;
+      for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = 0.f;
+    for (int g0 = lane; g0 < ngroups; g0 += 32 * CH) {
+      Raw8<Tx> xr[CH][TB];
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int g = g_lo + lane + 32 * it;
-      if (g < g_hi) {
+      for (int c = 0; c < CH; ++c) {
+        const int g = g0 + 32 * c;
+#pragma unroll
+        for (int a = 0; a < TB; ++a) {
+          if (g < ngroups && t0 + a < T) xr[c][a].load(x + (t0 + a) * (int64_t)d + 8 * g);
+          else xr[c][a].zero();
+        }
+      }
+      float acc[TB][EMAX];
+#pragma unroll
+      for (int a = 0; a < TB; ++a)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[a][e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int g = g0 + 32 * c;
+        if (g >= ngroups) continue;
         float xv[TB][8];
 #pragma unroll
-        for (int a = 0; a < TB; ++a) cur[it][a].to_float(xv[a]);
+        for (int a = 0; a < TB; ++a) xr[c][a].to_float(xv[a]);
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
           if (e < E) {
@@ -225,14 +222,21 @@ router_logits_resident(const Tx* __restrict__ x, const float* __restrict__ W,
           }
         }
       }
+#pragma unroll
+      for (int a = 0; a < TB; ++a)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) comp_add(hi[a][e], lo[a][e], acc[a][e]);
     }
+    // reduce-scatter over the lanes: at each halving step a lane keeps one half
+    // of its pairs, gives the other half to its partner and adds what it
+    // receives with a TwoSum
     float vh[32], vl[32];
 #pragma unroll
     for (int a = 0; a < TB; ++a)
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) {
-        vh[a * EMAX + e] = acc[a][e];
-        vl[a * EMAX + e] = 0.f;
+        vh[a * EMAX + e] = hi[a][e];
+        vl[a * EMAX + e] = lo[a][e];
       }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -251,39 +255,23 @@ router_logits_resident(const Tx* __restrict__ x, const float* __restrict__ W,
         vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
       }
     }
-    s_hi[warp][lane] = vh[0];
-    s_lo[warp][lane] = vl[0];
-    __syncthreads();
-    for (int q = threadIdx.x; q < TB * EMAX; q += blockDim.x) {
-      const int a = q / EMAX, e = q - a * EMAX;
-      if (e >= E || t0 + a >= T) continue;
-      float h = s_hi[0][q], l = s_lo[0][q];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) {
-        float s2, er;
-        two_sum(h, s_hi[w][q], s2, er);
-        h = s2;
-        l = __fadd_rn(__fadd_rn(l, s_lo[w][q]), er);
-      }
+    const int a = lane / EMAX, e = lane - a * EMAX;
+    if (e < E && t0 + a < T) {
+      float h = vh[0], l = vl[0];
       if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
       logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
     }
-    __syncthreads();  // s_hi / s_lo are rewritten by the next group
-#pragma unroll
-    for (int it = 0; it < IT; ++it)
-#pragma unroll
-      for (int a = 0; a < TB; ++a) cur[it][a] = nxt[it][a];
   }
 }
 
 // Shared memory the resident form may take for W (E x d fp32).
 constexpr size_t kRouterResidentSmem = 160 * 1024;
 
-template <typename Tx, int EMAX, int TB, int IT>
+template <typename Tx, int EMAX, int TB>
 static cudaError_t launch_router_resident(const Ctx& c, const Tx* x, const float* w_router,
                                           const float* logit_bias, float* logits, int64_t T,
                                           int d, int E) {
-  auto kern = router_logits_resident<Tx, EMAX, TB, IT>;
+  auto kern = router_logits_resident<Tx, EMAX, TB>;
   static bool attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -294,7 +282,8 @@ static cudaError_t launch_router_resident(const Ctx& c, const Tx* x, const float
     attr_done[dev & 63] = true;
   }
   const int64_t n_tg = (T + TB - 1) / TB;
-  const int64_t grid = n_tg < c.sm_count ? n_tg : c.sm_count;
+  const int64_t need = (n_tg + 7) / 8;  // eight warps per CTA
+  const int64_t grid = need < c.sm_count ? need : c.sm_count;
   const size_t smem = (size_t)E * d * sizeof(float);
   return launch_dependent(kern, dim3((unsigned)grid), dim3(256), smem, c.stream, x, w_router,
                           logit_bias, logits, T, d, E);
@@ -939,24 +928,12 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
   if (cfg.E <= 16) {
     // groups of 8 per lane: d / 8 split over 8 warps of 32 lanes
     const bool fold = (cfg.d / 8 + 255) / 256 > 4;
-    const int it = (cfg.d / 8 + 255) / 256;  // groups per lane
-    // fp32 x: at most two groups per lane (four would spill the prefetch buffers)
-    const int it_max = sizeof(Tx) == 2 ? 4 : 2;
-    if (!fold && it <= it_max && (size_t)cfg.E * cfg.d * sizeof(float) <= kRouterResidentSmem) {
-      cudaError_t e;
-      auto res = [&](auto em, auto tb) {
-        constexpr int EM = decltype(em)::value, TB_ = decltype(tb)::value;
-        if (it <= 1)
-          return launch_router_resident<Tx, EM, TB_, 1>(c, x, w_router, logit_bias, logits, T,
-                                                        cfg.d, cfg.E);
-        if (it <= 2 || sizeof(Tx) != 2)
-          return launch_router_resident<Tx, EM, TB_, 2>(c, x, w_router, logit_bias, logits, T,
-                                                        cfg.d, cfg.E);
-        return launch_router_resident<Tx, EM, TB_, (sizeof(Tx) == 2 ? 4 : 2)>(
-            c, x, w_router, logit_bias, logits, T, cfg.d, cfg.E);
-      };
-      e = cfg.E <= 8 ? res(std::integral_constant<int, 8>{}, std::integral_constant<int, 4>{})
-                     : res(std::integral_constant<int, 16>{}, std::integral_constant<int, 2>{});
+    // W_r fits in shared memory: the resident form
+    if ((size_t)cfg.E * cfg.d * sizeof(float) <= kRouterResidentSmem) {
+      cudaError_t e = cfg.E <= 8
+          ? launch_router_resident<Tx, 8, 4>(c, x, w_router, logit_bias, logits, T, cfg.d, cfg.E)
+          : launch_router_resident<Tx, 16, 2>(c, x, w_router, logit_bias, logits, T, cfg.d,
+                                              cfg.E);
       if (e != cudaSuccess) return e;
       note_launches(1);
       return cudaGetLastError();

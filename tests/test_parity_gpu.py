@@ -543,10 +543,10 @@ def test_near_tie_count(built, name):
 @pytest.mark.parametrize("T,E,k", [(1, 8, 2), (127, 8, 2), (4096, 8, 2), (2051, 64, 8),
                                    (20608, 256, 4), (16384, 128, 8), (33024, 256, 4)])
 def test_permute_index_paths(built, T, E, k):
-    """The dispatch on both of its index paths: a wide one-CTA scan of the
-    per-(128-token block, expert) counts followed by a fused rank + copy
-    while each scan thread holds at most 64 blocks, and beyond that (T =
-    33024, E = 256: 258 blocks) separate count, scan, rank and copy launches.
+    """The dispatch on both of its index paths: per-block counts followed by a
+    rank + copy kernel that turns them into base rows itself, while there are
+    at most 16384 (128-token block, expert) cells, and beyond that (T = 20608
+    and 33024 at E = 256) separate count, scan, rank and copy launches.
     counts, offsets, row_of and src_tok bit-exact against the oracle's
     dispatch; every copied row equal to its token's row."""
     import routing_grouped_expert_gate_gb300 as moe
