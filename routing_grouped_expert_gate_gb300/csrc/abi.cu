@@ -138,8 +138,10 @@ static int cuda_failed(cudaError_t e) {
 
 // K (token) slices of the dW_r reduction; partials [S][E][d] fp32 in the workspace
 static int route_bwd_splits(const moe_cfg& cfg) {
+  // few experts: slices of >= 32 tokens, up to 128 of them (enough CTAs of the
+  // column-blocked kernel to keep every SM's loads in flight)
   int64_t s = (cfg.E <= 16) ? (cfg.T + 31) / 32 : (cfg.T + 511) / 512;
-  const int64_t cap = (cfg.E <= 16) ? 64 : 32;
+  const int64_t cap = (cfg.E <= 16) ? 128 : 32;
   if (s < 1) s = 1;
   if (s > cap) s = cap;
   return (int)s;

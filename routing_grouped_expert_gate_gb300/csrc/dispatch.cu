@@ -389,31 +389,17 @@ cudaError_t launch_permute(const Ctx& c, const moe_cfg& cfg, const void* x, cons
 // ------------------------------------------------------------------ B1
 // dx[t] = dx_router[t] + sum_j dx_perm[row_of[t, j]] + dx_shared[t], in fp32 in
 // that order, rounded once. One warp per token, 8 elements per lane per step.
-//
-// ROUTER: the router's share d_logits[t] · W_r is formed here instead of read
-// as dx_router: per element, fp32 FMAs over the experts in order starting from
-// 0, the value the router backward would have written, so dx is the same bit
-// for bit while the fp32 [T, d] round trip through HBM is gone. W_r is staged
-// in shared memory (E·d·4 bytes, as [E][2][d/8] float4 planes so that the
-// lanes' consecutive groups read consecutive words) when w_smem is set, else
-// read from global memory.
-template <typename T, int KK, bool ROUTER = false, int EMAX = 16>
-__global__ void __launch_bounds__(ROUTER ? 512 : 256)
+template <typename T, int KK>
+__global__ void __launch_bounds__(256)
 permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ row_of,
                    const float* __restrict__ dx_router, const T* __restrict__ dx_shared,
                    const float* __restrict__ d_gate_logit, const float* __restrict__ w_gate,
-                   T* __restrict__ dx, int64_t Tn, int k, int d, int64_t A, int* status,
-                   const float* __restrict__ d_logits = nullptr,
-                   const float* __restrict__ w_router = nullptr, int E = 0, int w_smem = 0) {
-  // 8-element groups per lane per step (half as many for fp32 rows when the
-  // router's share is formed here, which needs registers of its own)
-  constexpr int U = (ROUTER && sizeof(T) == 4) ? (KK >= 4 ? 1 : 4 / KK) : (KK >= 8 ? 1 : 8 / KK);
-  extern __shared__ float4 sW[];           // ROUTER and w_smem: [E][2][d/8]
+                   T* __restrict__ dx, int64_t Tn, int k, int d, int64_t A, int* status) {
+  constexpr int U = KK >= 8 ? 1 : 8 / KK;  // 8-element groups per lane per step
   pdl_wait();  // a dependent launch: inputs come from the kernels before
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int ng = d >> 3;
-  if (ROUTER && w_smem) stage_w_planes(sW, w_router, E, d);
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += nwarps) {
     int64_t rows[KK];
 #pragma unroll
@@ -426,18 +412,13 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
       rows[j] = r;
     }
     const float dgl = d_gate_logit != nullptr ? d_gate_logit[t] : 0.f;
-    float dl[ROUTER ? EMAX : 1];
-    if (ROUTER) {
-#pragma unroll
-      for (int e = 0; e < (ROUTER ? EMAX : 1); ++e) dl[e] = e < E ? __ldg(d_logits + t * E + e) : 0.f;
-    }
     for (int g0 = 0; g0 < ng; g0 += 32 * U) {
       Raw8<T> raw[U][KK], sraw[U];
       Raw8<float> rraw[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int g = g0 + 32 * u + lane;
-        if (!ROUTER && g < ng && dx_router != nullptr) rraw[u].load(dx_router + t * d + 8 * g);
+        if (g < ng && dx_router != nullptr) rraw[u].load(dx_router + t * d + 8 * g);
         else rraw[u].zero();
 #pragma unroll
         for (int j = 0; j < KK; ++j) {
@@ -452,33 +433,7 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
         const int g = g0 + 32 * u + lane;
         if (g >= ng) continue;
         float acc[8];
-        if (ROUTER) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-          for (int e = 0; e < (ROUTER ? EMAX : 1); ++e) {
-            if (e < E) {
-              float4 w0, w1;
-              if (w_smem) {
-                w0 = sW[(e * 2) * ng + g];
-                w1 = sW[(e * 2 + 1) * ng + g];
-              } else {
-                w0 = __ldg(reinterpret_cast<const float4*>(w_router + (int64_t)e * d + 8 * g));
-                w1 = __ldg(reinterpret_cast<const float4*>(w_router + (int64_t)e * d + 8 * g + 4));
-              }
-              acc[0] = fmaf(dl[e], w0.x, acc[0]);
-              acc[1] = fmaf(dl[e], w0.y, acc[1]);
-              acc[2] = fmaf(dl[e], w0.z, acc[2]);
-              acc[3] = fmaf(dl[e], w0.w, acc[3]);
-              acc[4] = fmaf(dl[e], w1.x, acc[4]);
-              acc[5] = fmaf(dl[e], w1.y, acc[5]);
-              acc[6] = fmaf(dl[e], w1.z, acc[6]);
-              acc[7] = fmaf(dl[e], w1.w, acc[7]);
-            }
-          }
-        } else {
-          rraw[u].to_float(acc);
-        }
+        rraw[u].to_float(acc);
 #pragma unroll
         for (int j = 0; j < KK; ++j) {
           if (j < k) {
@@ -505,6 +460,128 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
   }
 }
 
+// B1 with the router's share formed here (few experts): dx[t] = r[t] +
+// sum_j dx_perm[row_of[t, j]] + dx_shared[t] (+ d_gate_logit[t] w_gate),
+// where r[t] = d_logits[t] · W_r is computed per element with fp32 FMAs over
+// the experts in order from 0 (the value the router backward would have
+// written as dx_router), and the rest is added in the same order as in
+// permute_bwd_kernel, so dx is the same bit for bit while the fp32 [T, d]
+// round trip through HBM is gone. W_r sits in shared memory ([E][2][d/8]
+// float4 planes, lanes reading consecutive words) when w_smem is set, else it
+// is read from global memory. A warp takes TB tokens at a time so that each W
+// value read from shared memory serves TB tokens, and U groups of 8 elements
+// per lane per step so that enough row loads are in flight.
+template <typename T, int KK, int EMAX, int TB>
+__global__ void __launch_bounds__(256, 1)
+permute_bwd_router(const T* __restrict__ dx_perm, const int32_t* __restrict__ row_of,
+                   const T* __restrict__ dx_shared, const float* __restrict__ d_gate_logit,
+                   const float* __restrict__ w_gate, const float* __restrict__ d_logits,
+                   const float* __restrict__ w_router, T* __restrict__ dx, int64_t Tn, int k,
+                   int d, int64_t A, int E, int w_smem, int* status) {
+  constexpr int U = sizeof(T) == 2 ? 2 : 1;
+  extern __shared__ float4 sW[];
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
+  if (w_smem) stage_w_planes(sW, w_router, E, d);
+  const int lane = threadIdx.x & 31;
+  const int ng = d >> 3;
+  const int64_t n_tg = (Tn + TB - 1) / TB;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t tg = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tg < n_tg;
+       tg += warps) {
+    const int64_t t0 = tg * TB;
+    int64_t rows[TB][KK];
+    float dl[TB][EMAX], dgl[TB];
+#pragma unroll
+    for (int a = 0; a < TB; ++a) {
+      const int64_t t = t0 + a;
+      const bool tv = t < Tn;
+#pragma unroll
+      for (int j = 0; j < KK; ++j) {
+        int r = (tv && j < k) ? row_of[t * k + j] : -1;
+        if (tv && j < k && (r < 0 || r >= A)) {
+          if (lane == 0) record_error(status, MOE_ERR_DEVICE_INDEX, (int)t);
+          r = -1;
+        }
+        rows[a][j] = r;
+      }
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) dl[a][e] = (tv && e < E) ? __ldg(d_logits + t * E + e) : 0.f;
+      dgl[a] = (tv && d_gate_logit != nullptr) ? d_gate_logit[t] : 0.f;
+    }
+    for (int g0 = 0; g0 < ng; g0 += 32 * U) {
+      Raw8<T> raw[U][TB][KK];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u + lane;
+#pragma unroll
+        for (int a = 0; a < TB; ++a)
+#pragma unroll
+          for (int j = 0; j < KK; ++j) {
+            if (g < ng && j < k && rows[a][j] >= 0)
+              raw[u][a][j].load(dx_perm + rows[a][j] * d + 8 * g);
+            else
+              raw[u][a][j].zero();
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u + lane;
+        if (g >= ng) continue;
+        float acc[TB][8];
+#pragma unroll
+        for (int a = 0; a < TB; ++a)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[a][i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          if (e < E) {
+            float4 w0, w1;
+            if (w_smem) {
+              w0 = sW[(e * 2) * ng + g];
+              w1 = sW[(e * 2 + 1) * ng + g];
+            } else {
+              w0 = __ldg(reinterpret_cast<const float4*>(w_router + (int64_t)e * d + 8 * g));
+              w1 = __ldg(reinterpret_cast<const float4*>(w_router + (int64_t)e * d + 8 * g + 4));
+            }
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int a = 0; a < TB; ++a)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[a][i] = fmaf(dl[a][e], wv[i], acc[a][i]);
+          }
+        }
+        float wg[8];
+        if (d_gate_logit != nullptr) load8(w_gate + 8 * g, wg);
+#pragma unroll
+        for (int a = 0; a < TB; ++a) {
+          if (t0 + a >= Tn) continue;
+#pragma unroll
+          for (int j = 0; j < KK; ++j) {
+            if (j < k) {
+              float v[8];
+              raw[u][a][j].to_float(v);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[a][i] += v[i];
+            }
+          }
+          Raw8<T> sraw;
+          if (dx_shared != nullptr) sraw.load(dx_shared + (t0 + a) * d + 8 * g);
+          else sraw.zero();
+          float sv[8];
+          sraw.to_float(sv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[a][i] += sv[i];
+          if (d_gate_logit != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[a][i] = fmaf(dgl[a], wg[i], acc[a][i]);
+          }
+          store8(dx + (t0 + a) * d + 8 * g, acc[a]);
+        }
+      }
+    }
+  }
+}
+
 // Shared memory the router-fused form may take for W_r.
 constexpr size_t kPermBwdWSmem = 160 * 1024;
 
@@ -514,7 +591,10 @@ static cudaError_t launch_permute_bwd_router(const Ctx& c, const moe_cfg& cfg, c
                                              const float* d_gate_logit, const float* w_gate,
                                              const float* d_logits, const float* w_router,
                                              T* dx) {
-  auto kern = permute_bwd_kernel<T, KK, true, EMAX>;
+  // tokens per warp: each W value read serves TB tokens; fewer with many rows
+  constexpr int TB0 = KK >= 8 ? 1 : (KK >= 4 ? 2 : 4);
+  constexpr int TB = EMAX > 8 && TB0 > 2 ? 2 : TB0;
+  auto kern = permute_bwd_router<T, KK, EMAX, TB>;
   static bool attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -526,14 +606,13 @@ static cudaError_t launch_permute_bwd_router(const Ctx& c, const moe_cfg& cfg, c
   }
   const size_t wbytes = (size_t)cfg.E * cfg.d * sizeof(float);
   const bool in_smem = wbytes <= kPermBwdWSmem;
-  // W_r staged once per CTA: one CTA per SM, each walking the tokens
-  const int64_t blocks = (cfg.T + 15) / 16;
+  // W_r staged once per CTA: one CTA per SM, its eight warps walking the tokens
+  const int64_t need = ((cfg.T + TB - 1) / TB + 7) / 8;
   const int64_t cap = in_smem ? (int64_t)c.sm_count : (int64_t)c.sm_count * 4;
-  const unsigned grid = (unsigned)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-  return launch_dependent(kern, dim3(grid), dim3(512), in_smem ? wbytes : 0, c.stream, dx_perm,
-                          row_of, nullptr, dx_shared, d_gate_logit, w_gate, dx, cfg.T, cfg.k,
-                          cfg.d, cfg.T * cfg.k, c.status, d_logits, w_router, cfg.E,
-                          in_smem ? 1 : 0);
+  const unsigned grid = (unsigned)(need < cap ? (need > 0 ? need : 1) : cap);
+  return launch_dependent(kern, dim3(grid), dim3(256), in_smem ? wbytes : 0, c.stream, dx_perm,
+                          row_of, dx_shared, d_gate_logit, w_gate, d_logits, w_router, dx, cfg.T,
+                          cfg.k, cfg.d, cfg.T * cfg.k, cfg.E, in_smem ? 1 : 0, c.status);
 }
 
 bool permute_bwd_forms_router_dx(const moe_cfg& cfg) { return cfg.E <= 16; }
@@ -549,7 +628,10 @@ cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_
     if (cfg.E > 16) return cudaErrorInvalidValue;  // refused by the entry point first
     cudaError_t e;
 #define MOE_PBWDR(TT, KK)                                                                     \
-  e = launch_permute_bwd_router<TT, KK, 16>(                                                   \
+  e = cfg.E <= 8 ? launch_permute_bwd_router<TT, KK, 8>(                                      \
+      c, cfg, static_cast<const TT*>(dx_perm), row_of, static_cast<const TT*>(dx_shared),     \
+      d_gate_logit, w_gate, d_logits, w_router, static_cast<TT*>(dx))                        \
+                 : launch_permute_bwd_router<TT, KK, 16>(                                     \
       c, cfg, static_cast<const TT*>(dx_perm), row_of, static_cast<const TT*>(dx_shared),     \
       d_gate_logit, w_gate, d_logits, w_router, static_cast<TT*>(dx))
 #define MOE_PBWDR_K(TT)                                              \
@@ -573,14 +655,12 @@ cudaError_t launch_permute_bwd(const Ctx& c, const moe_cfg& cfg, const void* dx_
     launch_dependent(permute_bwd_kernel<bf16, KK>, dim3(grid), dim3(256), 0, c.stream,       \
                      static_cast<const bf16*>(dx_perm), row_of, dx_router,                   \
                      static_cast<const bf16*>(dx_shared), d_gate_logit, w_gate,              \
-                     static_cast<bf16*>(dx), cfg.T, cfg.k, cfg.d, A, c.status, nullptr,      \
-                     nullptr, 0, 0);                                                         \
+                     static_cast<bf16*>(dx), cfg.T, cfg.k, cfg.d, A, c.status);              \
   else                                                                                       \
     launch_dependent(permute_bwd_kernel<float, KK>, dim3(grid), dim3(256), 0, c.stream,      \
                      static_cast<const float*>(dx_perm), row_of, dx_router,                  \
                      static_cast<const float*>(dx_shared), d_gate_logit, w_gate,             \
-                     static_cast<float*>(dx), cfg.T, cfg.k, cfg.d, A, c.status, nullptr,     \
-                     nullptr, 0, 0)
+                     static_cast<float*>(dx), cfg.T, cfg.k, cfg.d, A, c.status)
   if (cfg.k <= 1) {
     MOE_PBWD(1);
   } else if (cfg.k <= 2) {

@@ -157,11 +157,11 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 // staged once per CTA) and every warp works alone on groups of TB tokens, one
 // CTA per SM walking the token groups: no block-wide barrier per group, so the
 // eight warps' loads and arithmetic overlap. A lane takes the 8-element groups
-// lane, lane + 32, ... of the hidden dimension in chunks of CH groups: the
-// chunk's x loads are issued together, its products with W (read from shared
-// memory, consecutive words across the lanes) are summed in plain fp32 FMAs
-// (at most 32 elements) and folded into a compensated (hi, lo) pair per
-// (token, expert). The lanes' pairs are then combined by a reduce-scatter with
+// lane, lane + 32, ... of the hidden dimension in chunks of CH = 2 groups: the
+// next chunk's x loads are issued before the current chunk's products with W
+// (read from shared memory, consecutive words across the lanes) are summed in
+// plain fp32 FMAs (16 elements) and folded into a compensated (hi, lo) pair
+// per (token, expert). The lanes' pairs are then combined by a reduce-scatter with
 // TwoSums (lane q ends with pair q = token q / EMAX, expert q % EMAX), so each
 // logit carries only the rounding of its 32-element chunk sums.
 template <typename Tx, int EMAX, int TB>
@@ -171,96 +171,122 @@ router_logits_resident(const Tx* __restrict__ x, const float* __restrict__ W,
                        int64_t T, int d, int E) {
   extern __shared__ float4 sW[];  // [E][2][ngroups]
   static_assert(TB * EMAX == 32, "one pair per lane after the reduce-scatter");
-  constexpr int CH = sizeof(Tx) == 2 ? 4 : 2;  // groups of 8 per chunk
+  constexpr int CH = 2;  // groups of 8 per chunk: 16 elements per plain-fp32 chunk sum
   pdl_wait();  // x may come from the kernel before; logits may still be read by it
-  stage_w_planes(sW, W, E, d);
   const int lane = threadIdx.x & 31;
   const int ngroups = d >> 3;
   const int64_t n_tg = (T + TB - 1) / TB;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t tg = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tg < n_tg;
-       tg += warps) {
+
+  // the warp walks (token group, chunk) positions; the next position's x is
+  // loaded while the current one is multiplied
+  // (gb is warp-uniform: the chunk's first group; lane takes gb + lane + 32 c)
+  auto load_chunk = [&](int64_t tg, int gb, Raw8<Tx> (&buf)[CH][TB]) {
     const int64_t t0 = tg * TB;
-    float hi[TB][EMAX], lo[TB][EMAX];
 #pragma unroll
-    for (int a = 0; a < TB; ++a)
+    for (int c = 0; c < CH; ++c) {
+      const int g = gb + lane + 32 * c;
 #pragma unroll
-      for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = 0.f;
-    for (int g0 = lane; g0 < ngroups; g0 += 32 * CH) {
-      Raw8<Tx> xr[CH][TB];
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int g = g0 + 32 * c;
-#pragma unroll
-        for (int a = 0; a < TB; ++a) {
-          if (g < ngroups && t0 + a < T) xr[c][a].load(x + (t0 + a) * (int64_t)d + 8 * g);
-          else xr[c][a].zero();
-        }
+      for (int a = 0; a < TB; ++a) {
+        if (g < ngroups && t0 + a < T) buf[c][a].load(x + (t0 + a) * (int64_t)d + 8 * g);
+        else buf[c][a].zero();
       }
-      float acc[TB][EMAX];
-#pragma unroll
-      for (int a = 0; a < TB; ++a)
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) acc[a][e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int g = g0 + 32 * c;
-        if (g >= ngroups) continue;
-        float xv[TB][8];
-#pragma unroll
-        for (int a = 0; a < TB; ++a) xr[c][a].to_float(xv[a]);
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-          if (e < E) {
-            const float4 w0 = sW[(e * 2) * ngroups + g];
-            const float4 w1 = sW[(e * 2 + 1) * ngroups + g];
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int a = 0; a < TB; ++a)
-#pragma unroll
-              for (int i = 0; i < 8; ++i) acc[a][e] = fmaf(xv[a][i], wv[i], acc[a][e]);
-          }
-        }
-      }
-#pragma unroll
-      for (int a = 0; a < TB; ++a)
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) comp_add(hi[a][e], lo[a][e], acc[a][e]);
     }
-    // reduce-scatter over the lanes: at each halving step a lane keeps one half
-    // of its pairs, gives the other half to its partner and adds what it
-    // receives with a TwoSum
-    float vh[32], vl[32];
+  };
+  int64_t tg = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int gb = 0;
+  Raw8<Tx> cur[CH][TB], nxt[CH][TB];
+  if (tg < n_tg) load_chunk(tg, gb, cur);  // in flight while W is staged
+  stage_w_planes(sW, W, E, d);
+
+  float hi[TB][EMAX], lo[TB][EMAX];
+  while (tg < n_tg) {
+    int64_t tg_n = tg;
+    int gb_n = gb + 32 * CH;
+    if (gb_n >= ngroups) {
+      tg_n = tg + warps;
+      gb_n = 0;
+    }
+    if (tg_n < n_tg) load_chunk(tg_n, gb_n, nxt);
+    if (gb == 0) {
+#pragma unroll
+      for (int a = 0; a < TB; ++a)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = 0.f;
+    }
+    float acc[TB][EMAX];
 #pragma unroll
     for (int a = 0; a < TB; ++a)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) acc[a][e] = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int g = gb + lane + 32 * c;
+      if (g >= ngroups) continue;
+      float xv[TB][8];
+#pragma unroll
+      for (int a = 0; a < TB; ++a) cur[c][a].to_float(xv[a]);
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) {
-        vh[a * EMAX + e] = hi[a][e];
-        vl[a * EMAX + e] = lo[a][e];
-      }
+        if (e < E) {
+          const float4 w0 = sW[(e * 2) * ngroups + g];
+          const float4 w1 = sW[(e * 2 + 1) * ngroups + g];
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const bool upper = (lane & off) != 0;
+          for (int a = 0; a < TB; ++a)
 #pragma unroll
-      for (int q = 0; q < off; ++q) {
-        const float sh_ = upper ? vh[q] : vh[q + off];
-        const float sl_ = upper ? vl[q] : vl[q + off];
-        const float kh = upper ? vh[q + off] : vh[q];
-        const float kl = upper ? vl[q + off] : vl[q];
-        const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
-        const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
-        float s2, er;
-        two_sum(kh, rh, s2, er);
-        vh[q] = s2;
-        vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
+            for (int i = 0; i < 8; ++i) acc[a][e] = fmaf(xv[a][i], wv[i], acc[a][e]);
+        }
       }
     }
-    const int a = lane / EMAX, e = lane - a * EMAX;
-    if (e < E && t0 + a < T) {
-      float h = vh[0], l = vl[0];
-      if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
-      logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
+#pragma unroll
+    for (int a = 0; a < TB; ++a)
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) comp_add(hi[a][e], lo[a][e], acc[a][e]);
+
+    if (tg_n != tg) {
+      // the group is complete: reduce-scatter over the lanes (at each halving
+      // step a lane keeps one half of its pairs, gives the other half to its
+      // partner and adds what it receives with a TwoSum), lane q -> pair q
+      float vh[32], vl[32];
+#pragma unroll
+      for (int a = 0; a < TB; ++a)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          vh[a * EMAX + e] = hi[a][e];
+          vl[a * EMAX + e] = lo[a][e];
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int q = 0; q < off; ++q) {
+          const float sh_ = upper ? vh[q] : vh[q + off];
+          const float sl_ = upper ? vl[q] : vl[q + off];
+          const float kh = upper ? vh[q + off] : vh[q];
+          const float kl = upper ? vl[q + off] : vl[q];
+          const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
+          const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
+          float s2, er;
+          two_sum(kh, rh, s2, er);
+          vh[q] = s2;
+          vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
+        }
+      }
+      const int64_t t0 = tg * TB;
+      const int a = lane / EMAX, e = lane - a * EMAX;
+      if (e < E && t0 + a < T) {
+        float h = vh[0], l = vl[0];
+        if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
+        logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
+      }
     }
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+      for (int a = 0; a < TB; ++a) cur[c][a] = nxt[c][a];
+    tg = tg_n;
+    gb = gb_n;
   }
 }
 

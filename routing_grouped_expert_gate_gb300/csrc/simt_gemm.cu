@@ -194,8 +194,16 @@ reduce_partials_kernel(const float* __restrict__ part, int64_t stride, int nz, i
   pdl_wait();  // a dependent launch: inputs come from the kernels before
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
+    // the partials added in slice order, sixteen loads in flight at a time
     float v = 0.f;
-    for (int z = 0; z < nz; ++z) v += part[(int64_t)z * stride + i];
+    for (int z0 = 0; z0 < nz; z0 += 16) {
+      float p[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) p[u] = z0 + u < nz ? part[(int64_t)(z0 + u) * stride + i] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (z0 + u < nz) v += p[u];
+    }
     if (accumulate) v += to_f32<TO>(out[i]);
     out[i] = from_f32<TO>(v);
   }

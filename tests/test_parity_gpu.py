@@ -288,14 +288,16 @@ def test_router_gate_gemm_paths(built, name, fold_k):
         L.set_router_fold(old_f)
 
 
-@pytest.mark.parametrize("E", [8, 16])
-@pytest.mark.parametrize("d", [4096, 8704])
+@pytest.mark.parametrize("E,d", [(8, 4096), (8, 8704), (16, 4096), (16, 8704), (16, 2048),
+                                 (8, 200), (12, 1032)])
 def test_small_router_hidden_sizes(built, E, d):
-    """The few-expert gate GEMM (E <= 16) on both of its accumulation forms:
-    one fp32 chunk per lane (d <= 8192) and 32-element chunks folded into
-    compensated pairs (d > 8192); a ragged token count that leaves the last
-    CTA partly empty. Logits within 1e-6 of the float64 oracle, the oracle's
-    experts selected."""
+    """The few-expert gate GEMM (E <= 16) on its forms: W_r resident in shared
+    memory with one warp per token group (E·d·4 <= 160 KB, including hidden
+    sizes that are no multiple of the lanes' 512-element stride), and, for
+    larger W_r, CTAs that split d over their warps with one fp32 chunk per
+    lane (d <= 8192) or 32-element chunks folded into compensated pairs; a
+    ragged token count. Logits within 1e-6 of the float64 oracle, the
+    oracle's experts selected."""
     import routing_grouped_expert_gate_gb300 as moe
     from routing_grouped_expert_gate_gb300 import _lib as L
     wl = mi.shrink(W["mixtral_style"], name=f"router_e{E}_d{d}", T=37, d=d, E=E, F=64)
