@@ -258,7 +258,9 @@ int moe_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* counts,
  *   before any device work.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture. The address is kept for the rest of the
+ *   process: a cudaDeviceReset between calls is not supported (the module
+ *   would be reloaded at another address).
  *   Every call shares the one array and leaves its contents behind; nothing in
  *   it needs to start at zero. Calls that overlap on the GPU (other streams,
  *   other host threads) race on the array: serialise them.               */
