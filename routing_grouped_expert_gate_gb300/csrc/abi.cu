@@ -448,9 +448,10 @@ int moe_shared_gate_bwd(const moe_cfg* cfg, const void* x, const float* gate, co
   one.E = 1;
   const int S = route_bwd_splits(one);
   float* part = static_cast<float*>(ws);
-  MOE_LAUNCH(launch_router_dw_small(c, one, x, d_gate_logit, part, S));
-  MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)cfg->d, S, (int64_t)cfg->d, dw_gate, kF32,
-                                    0));
+  int used = S;
+  MOE_LAUNCH(launch_router_dw_small(c, one, x, d_gate_logit, part, S, &used));
+  MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)cfg->d, used, (int64_t)cfg->d, dw_gate,
+                                    kF32, 0));
   return MOE_OK;
 }
 
@@ -735,12 +736,14 @@ int moe_route_topk_bwd(const moe_cfg* cfg, const void* x, const float* w_router,
   b.C = part; b.c_sm = 1; b.c_sn = d; b.c_sg = (int64_t)E * d;
   b.n_groups = 1; b.alpha = 1.f; b.split_k = S;
   if (T > 0) {
+    int used = S;
     if (E <= 16) {
-      MOE_LAUNCH(launch_router_dw_small(c, *cfg, x, d_logits, part, S));
+      MOE_LAUNCH(launch_router_dw_small(c, *cfg, x, d_logits, part, S, &used));
     } else {
       MOE_LAUNCH(launch_simt_gemm(c, b));
     }
-    MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)E * d, S, (int64_t)E * d, dw_router, kF32, 0));
+    MOE_LAUNCH(launch_reduce_partials(c, part, (int64_t)E * d, used, (int64_t)E * d, dw_router,
+                                      kF32, 0));
   } else {
     MOE_LAUNCH(cudaMemsetAsync(dw_router, 0, (size_t)E * d * sizeof(float), c.stream));
   }

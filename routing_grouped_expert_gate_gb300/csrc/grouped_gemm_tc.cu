@@ -1320,6 +1320,19 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+bool make_map_bf16_plain(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                         int box_rows, int box_cols) {
+  if (!get_encoder()) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim,
+                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
   return make_map_bf16(m, base, rows, cols, box_rows);
 }

@@ -70,9 +70,10 @@ cudaError_t launch_quantile_accumulate(const Ctx& c, const moe_cfg& cfg, const f
                                        float* accum, int32_t* count);
 cudaError_t launch_quantile_beta_update(const Ctx& c, const moe_cfg& cfg, float* beta,
                                         float* accum, int32_t* count, float ema);
-// dW_r partials [splits][E][d] for E <= 16 (sum them in slice order)
+// dW_r partials [used][E][d] for E <= 16, used <= splits token slices (sum
+// them in slice order)
 cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void* x,
-                                   const float* d_logits, float* part, int splits);
+                                   const float* d_logits, float* part, int splits, int* used);
 // dx_router = d_logits · W_r for E <= 16 (fp32, experts summed in order)
 cudaError_t launch_router_dx_small(const Ctx& c, const moe_cfg& cfg, const float* d_logits,
                                    const float* w_router, float* dx_router);

@@ -14,8 +14,11 @@
 // (hi, lo) pair with an error-free TwoSum, so the only rounding that grows with
 // d is confined to 32-term partial sums. The logits end within a few fp32 ulps
 // of the exact value, far inside the 1e-6 band that marks a near tie.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -152,6 +155,53 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
   }
 }
 
+// The lanes of a warp each hold TB x EMAX compensated (hi, lo) pairs of the
+// same TB tokens (TB * EMAX = 32), partial sums over different elements. A
+// reduce-scatter over the lanes (at each halving step a lane keeps one half of
+// its pairs, gives the other half to its partner and adds what it receives
+// with a TwoSum) leaves lane q with pair q = (token q / EMAX, expert q % EMAX),
+// which it rounds once (after the logit bias) and stores.
+template <int TB, int EMAX>
+__device__ __forceinline__ void store_pair_logits(const float (&hi)[TB][EMAX],
+                                                  const float (&lo)[TB][EMAX], int64_t t0,
+                                                  int64_t T, int E,
+                                                  const float* __restrict__ logit_bias,
+                                                  float* __restrict__ logits) {
+  static_assert(TB * EMAX == 32, "one pair per lane after the reduce-scatter");
+  const int lane = threadIdx.x & 31;
+  float vh[32], vl[32];
+#pragma unroll
+  for (int a = 0; a < TB; ++a)
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      vh[a * EMAX + e] = hi[a][e];
+      vl[a * EMAX + e] = lo[a][e];
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int q = 0; q < off; ++q) {
+      const float sh_ = upper ? vh[q] : vh[q + off];
+      const float sl_ = upper ? vl[q] : vl[q + off];
+      const float kh = upper ? vh[q + off] : vh[q];
+      const float kl = upper ? vl[q + off] : vl[q];
+      const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
+      const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
+      float s2, er;
+      two_sum(kh, rh, s2, er);
+      vh[q] = s2;
+      vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
+    }
+  }
+  const int a = lane / EMAX, e = lane - a * EMAX;
+  if (e < E && t0 + a < T) {
+    float h = vh[0], l = vl[0];
+    if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
+    logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
+  }
+}
+
 // ------------------------------------------------------------------ S1, E <= 16, W resident
 // W stays in shared memory for the kernel's life ([E][2][d/8] float4 planes,
 // staged once per CTA) and every warp works alone on groups of TB tokens, one
@@ -244,43 +294,7 @@ router_logits_resident(const Tx* __restrict__ x, const float* __restrict__ W,
 #pragma unroll
       for (int e = 0; e < EMAX; ++e) comp_add(hi[a][e], lo[a][e], acc[a][e]);
 
-    if (tg_n != tg) {
-      // the group is complete: reduce-scatter over the lanes (at each halving
-      // step a lane keeps one half of its pairs, gives the other half to its
-      // partner and adds what it receives with a TwoSum), lane q -> pair q
-      float vh[32], vl[32];
-#pragma unroll
-      for (int a = 0; a < TB; ++a)
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-          vh[a * EMAX + e] = hi[a][e];
-          vl[a * EMAX + e] = lo[a][e];
-        }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int q = 0; q < off; ++q) {
-          const float sh_ = upper ? vh[q] : vh[q + off];
-          const float sl_ = upper ? vl[q] : vl[q + off];
-          const float kh = upper ? vh[q + off] : vh[q];
-          const float kl = upper ? vl[q + off] : vl[q];
-          const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
-          const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
-          float s2, er;
-          two_sum(kh, rh, s2, er);
-          vh[q] = s2;
-          vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
-        }
-      }
-      const int64_t t0 = tg * TB;
-      const int a = lane / EMAX, e = lane - a * EMAX;
-      if (e < E && t0 + a < T) {
-        float h = vh[0], l = vl[0];
-        if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
-        logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
-      }
-    }
+    if (tg_n != tg) store_pair_logits<TB, EMAX>(hi, lo, tg * TB, T, E, logit_bias, logits);
 #pragma unroll
     for (int c = 0; c < CH; ++c)
 #pragma unroll
@@ -313,6 +327,201 @@ static cudaError_t launch_router_resident(const Ctx& c, const Tx* x, const float
   const size_t smem = (size_t)E * d * sizeof(float);
   return launch_dependent(kern, dim3((unsigned)grid), dim3(256), smem, c.stream, x, w_router,
                           logit_bias, logits, T, d, E);
+}
+
+// ------------------------------------------------------------------ S1, E <= 16, bf16 x streamed
+// W_r stays in shared memory ([E][d] fp32, one bulk copy) and the tokens'
+// rows stream through a ring of slots, each TBLK = 8 TB tokens x 256 columns,
+// one TMA tile load per slot from a producer thread (rows past T and columns
+// past d arrive as zeros): the bytes in flight per SM are bounded by the ring
+// (up to 128 KB), not by registers. Eight consumer warps take TB tokens each of every slot; lane l
+// takes columns 4l..4l+3 and 128+4l..128+4l+3 (W and x read from shared memory
+// at consecutive addresses across the lanes). Per slot a lane forms, for each
+// of its tokens and each expert, a chain of 8 fp32 FMAs; every two slots (16
+// elements) the chain folds into the (token, expert) compensated pair, and
+// store_pair_logits combines the lanes' pairs at the end of the block. Every
+// mbarrier wait is bounded (MOE_ERR_TIMEOUT + abort flag).
+struct StreamParams {
+  int64_t T;
+  int d, E, ns;  // ns: ring slots
+  const float* logit_bias;
+  float* logits;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+constexpr int kStreamThreads = 288;  // 8 consumer warps + 1 producer warp
+constexpr int kStreamCols = 256;     // columns per slot
+constexpr int kStreamMaxSlots = 8;
+
+template <int EMAX>
+struct StreamTile {
+  static constexpr int TB = 32 / EMAX;                   // tokens per consumer warp
+  static constexpr int TBLK = 8 * TB;                    // tokens per slot
+  static constexpr int kSlot = TBLK * kStreamCols * 2;   // bytes (bf16)
+};
+
+template <int EMAX>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+router_logits_stream(const __grid_constant__ CUtensorMap tmX, const float* __restrict__ W,
+                     const StreamParams P) {
+  using ST = StreamTile<EMAX>;
+  constexpr int TB = ST::TB;
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t full[kStreamMaxSlots], empty[kStreamMaxSlots], wbar;
+  __shared__ int abort_flag;
+  const size_t w_bytes = ((size_t)P.E * P.d * sizeof(float) + 127) & ~(size_t)127;
+  float* sW = reinterpret_cast<float*>(sm_raw);
+  uint8_t* ring = sm_raw + w_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = P.d, E = P.E, ns = P.ns;
+  const int nsl = (d + kStreamCols - 1) / kStreamCols;
+  const int64_t nblk = (P.T + ST::TBLK - 1) / ST::TBLK;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < ns; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 8);  // one arrival per consumer warp
+    }
+    tc::mbar_init(&wbar, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();  // x may come from the kernel before; logits may still be read by it
+
+  if (warp == 8) {
+    // ---------------- producer (one thread): W once, then the ring
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmX);
+      const uint32_t wb = (uint32_t)((size_t)E * d * sizeof(float));
+      tc::mbar_expect_tx(&wbar, wb);
+      tc::bulk_load_1d(sW, W, wb, &wbar);
+    }
+    int slot = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int64_t b = blockIdx.x; b < nblk && ok && lane == 0; b += gridDim.x) {
+      const int t0 = (int)(b * ST::TBLK);
+      for (int j = 0; j < nsl; ++j) {
+        if (!tc::mbar_wait(&empty[slot], ph ^ 1, abort_flag, P, 41)) { ok = false; break; }
+        tc::mbar_expect_tx(&full[slot], (uint32_t)ST::kSlot);
+        tc::tma_load_2d(ring + (size_t)slot * ST::kSlot, &tmX, &full[slot], j * kStreamCols, t0);
+        if (++slot == ns) { slot = 0; ph ^= 1; }
+      }
+    }
+    if (!ok && lane == 0) {
+      // let the copies already in flight land before the CTA exits
+      const uint64_t t_start = global_timer_ns();
+      while (global_timer_ns() - t_start < 2000000ull) { }
+    }
+  } else {
+    // ---------------- consumers
+    bool ok = tc::mbar_wait(&wbar, 0, abort_flag, P, 42);
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int64_t b = blockIdx.x; b < nblk && ok; b += gridDim.x) {
+      float hi[TB][EMAX], lo[TB][EMAX], acc[TB][EMAX];
+#pragma unroll
+      for (int a = 0; a < TB; ++a)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) hi[a][e] = lo[a][e] = acc[a][e] = 0.f;
+      for (int j = 0; j < nsl; ++j) {
+        if (!tc::mbar_wait(&full[slot], ph, abort_flag, P, 43)) { ok = false; break; }
+        const uint8_t* sl = ring + (size_t)slot * ST::kSlot + (size_t)warp * TB * (kStreamCols * 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cl = h * 128 + 4 * lane;  // column within the slot
+          const int c = j * kStreamCols + cl;
+          if (c < d) {
+            float xv[TB][4];
+#pragma unroll
+            for (int a = 0; a < TB; ++a) {
+              const uint2 r = *reinterpret_cast<const uint2*>(sl + a * (kStreamCols * 2) + cl * 2);
+              const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+              const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+              xv[a][0] = f0.x; xv[a][1] = f0.y; xv[a][2] = f1.x; xv[a][3] = f1.y;
+            }
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+              if (e < E) {
+                const float4 wv = *reinterpret_cast<const float4*>(sW + (size_t)e * d + c);
+#pragma unroll
+                for (int a = 0; a < TB; ++a) {
+                  acc[a][e] = fmaf(xv[a][0], wv.x, acc[a][e]);
+                  acc[a][e] = fmaf(xv[a][1], wv.y, acc[a][e]);
+                  acc[a][e] = fmaf(xv[a][2], wv.z, acc[a][e]);
+                  acc[a][e] = fmaf(xv[a][3], wv.w, acc[a][e]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[slot]);
+        if (++slot == ns) { slot = 0; ph ^= 1; }
+        if ((j & 1) || j == nsl - 1) {
+#pragma unroll
+          for (int a = 0; a < TB; ++a)
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+              comp_add(hi[a][e], lo[a][e], acc[a][e]);
+              acc[a][e] = 0.f;
+            }
+        }
+      }
+      if (!ok) break;
+      store_pair_logits<TB, EMAX>(hi, lo, b * ST::TBLK + warp * TB, P.T, E, P.logit_bias,
+                                  P.logits);
+    }
+  }
+}
+
+// Dynamic shared memory the streamed form may take (W and the ring; the
+// barriers sit in static shared memory, within the 227 KB a CTA may hold).
+constexpr size_t kStreamSmemMax = 226 * 1024;
+
+// Ring slots for the streamed form (0: it does not apply).
+template <int EMAX>
+static int stream_slots(const moe_cfg& cfg) {
+  const size_t w_bytes = ((size_t)cfg.E * cfg.d * sizeof(float) + 127) & ~(size_t)127;
+  if (w_bytes + 2 * (size_t)StreamTile<EMAX>::kSlot > kStreamSmemMax) return 0;
+  const size_t n = (kStreamSmemMax - w_bytes) / StreamTile<EMAX>::kSlot;
+  return (int)(n < (size_t)kStreamMaxSlots ? n : (size_t)kStreamMaxSlots);
+}
+
+template <int EMAX>
+static cudaError_t launch_router_stream(const Ctx& c, const moe_cfg& cfg, const bf16* x,
+                                        const float* w_router, const float* logit_bias,
+                                        float* logits, int ns) {
+  auto kern = router_logits_stream<EMAX>;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kStreamSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_done[dev & 63] = true;
+  }
+  StreamParams P{};
+  P.T = cfg.T;
+  P.d = cfg.d;
+  P.E = cfg.E;
+  P.ns = ns;
+  P.logit_bias = logit_bias;
+  P.logits = logits;
+  P.status = c.status;
+  P.timeout_ns = c.timeout_ns;
+  const size_t w_bytes = ((size_t)cfg.E * cfg.d * sizeof(float) + 127) & ~(size_t)127;
+  const size_t smem = w_bytes + (size_t)ns * StreamTile<EMAX>::kSlot;
+  const int64_t nblk = (cfg.T + StreamTile<EMAX>::TBLK - 1) / StreamTile<EMAX>::TBLK;
+  const int64_t grid = nblk < c.sm_count ? nblk : c.sm_count;
+  CUtensorMap mx;
+  if (!tc::make_map_bf16_plain(&mx, x, cfg.T, cfg.d, StreamTile<EMAX>::TBLK, kStreamCols))
+    return cudaErrorInvalidValue;
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(kStreamThreads), smem, c.stream, mx,
+                          w_router, P);
 }
 
 // ------------------------------------------------------------------ S1, E > 16
@@ -820,6 +1029,169 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ B3, E <= 16, bf16 x streamed
+// dW_r partials for few experts, bf16 x: part[s][e][c] = sum over the tokens
+// of slice s of d_logits[t][e] * x[t][c], from a TMA ring. A CTA takes 1024
+// columns of one token slice (consumer thread i: columns 4i..4i+3). The
+// slice's x rows stream through slots of 16 tokens x 1024 columns (four tile
+// loads of 256 columns each, issued by a producer thread; columns past d
+// arrive as zeros and are not used); the slice's d_logits rows sit in shared
+// memory, padded to EMAX per token with zeros. A thread adds the tokens in
+// order into EMAX x 4 fp32 sums; the slices are summed afterwards in slice
+// order. Every mbarrier wait is bounded (MOE_ERR_TIMEOUT + abort flag).
+constexpr int kDwCols = 1024, kDwTok = 16;
+constexpr int kDwSlot = kDwTok * kDwCols * 2;  // 32 KB
+
+struct DwParams {
+  int64_t T;
+  int d, E, ns;
+  int tok_per_slice;
+  float* part;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int EMAX>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+router_dw_stream(const __grid_constant__ CUtensorMap tmX, const float* __restrict__ g,
+                 const DwParams P) {
+  static_assert(EMAX % 4 == 0, "d_logits rows read as float4");
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t full[kStreamMaxSlots], empty[kStreamMaxSlots];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = P.d, E = P.E, ns = P.ns;
+  const int c0 = blockIdx.x * kDwCols;
+  const int64_t t_beg = (int64_t)blockIdx.y * P.tok_per_slice;
+  const int ntok = (int)(P.T - t_beg < P.tok_per_slice ? P.T - t_beg : P.tok_per_slice);
+  const int nsl = (ntok + kDwTok - 1) / kDwTok;
+  float* sg = reinterpret_cast<float*>(sm_raw);  // [tok_per_slice][EMAX]
+  const size_t g_bytes = ((size_t)P.tok_per_slice * EMAX * sizeof(float) + 127) & ~(size_t)127;
+  uint8_t* ring = sm_raw + g_bytes;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < ns; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 8);  // one arrival per consumer warp
+    }
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
+
+  if (warp == 8) {
+    // ---------------- producer (one thread)
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmX);
+      const int nbox = (d - c0 + 255) / 256 < 4 ? (d - c0 + 255) / 256 : 4;
+      int slot = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int j = 0; j < nsl; ++j) {
+        if (!tc::mbar_wait(&empty[slot], ph ^ 1, abort_flag, P, 44)) { ok = false; break; }
+        tc::mbar_expect_tx(&full[slot], (uint32_t)(nbox * kDwSlot / 4));
+        for (int k = 0; k < nbox; ++k)
+          tc::tma_load_2d(ring + (size_t)slot * kDwSlot + k * (kDwSlot / 4), &tmX, &full[slot],
+                          c0 + 256 * k, (int)(t_beg + j * kDwTok));
+        if (++slot == ns) { slot = 0; ph ^= 1; }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA exits
+        const uint64_t t_start = global_timer_ns();
+        while (global_timer_ns() - t_start < 2000000ull) { }
+      }
+    }
+  } else {
+    // ---------------- consumers (256 threads)
+    const int tid = threadIdx.x;
+    for (int i = tid; i < ntok * EMAX; i += 256) {
+      const int t = i / EMAX, e = i - t * EMAX;
+      sg[i] = e < E ? g[(t_beg + t) * E + e] : 0.f;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the consumers only
+    const int k = tid >> 6, cq = (tid & 63) * 4;
+    const int col = c0 + 256 * k + cq;
+    const bool active = col < d;
+    float acc[EMAX][4];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[e][q] = 0.f;
+    bool ok = true;
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < nsl; ++j) {
+      if (!tc::mbar_wait(&full[slot], ph, abort_flag, P, 45)) { ok = false; break; }
+      const int rows = ntok - j * kDwTok < kDwTok ? ntok - j * kDwTok : kDwTok;
+      if (active) {
+        const uint8_t* base = ring + (size_t)slot * kDwSlot + k * (kDwSlot / 4) + cq * 2;
+        const float* gs = sg + (size_t)j * kDwTok * EMAX;
+#pragma unroll 4
+        for (int r = 0; r < rows; ++r) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(base + r * 512);
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+          const float xv[4] = {f0.x, f0.y, f1.x, f1.y};
+#pragma unroll
+          for (int e4 = 0; e4 < EMAX; e4 += 4) {
+            const float4 gv = *reinterpret_cast<const float4*>(gs + r * EMAX + e4);
+            const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[e4 + u][q] = fmaf(gg[u], xv[q], acc[e4 + u][q]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
+      if (++slot == ns) { slot = 0; ph ^= 1; }
+    }
+    if (ok && active) {
+      float* out = P.part + (int64_t)blockIdx.y * E * d;
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e)
+        if (e < E)
+          *reinterpret_cast<float4*>(out + (int64_t)e * d + col) =
+              make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
+    }
+  }
+}
+
+template <int EMAX>
+static cudaError_t launch_router_dw_stream(const Ctx& c, const moe_cfg& cfg, const bf16* x,
+                                           const float* d_logits, float* part, int tps,
+                                           int n_ts) {
+  auto kern = router_dw_stream<EMAX>;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kStreamSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_done[dev & 63] = true;
+  }
+  const size_t g_bytes = ((size_t)tps * EMAX * sizeof(float) + 127) & ~(size_t)127;
+  size_t ns = (kStreamSmemMax - g_bytes) / kDwSlot;
+  if (ns > (size_t)kStreamMaxSlots) ns = kStreamMaxSlots;
+  DwParams P{};
+  P.T = cfg.T;
+  P.d = cfg.d;
+  P.E = cfg.E;
+  P.ns = (int)ns;
+  P.tok_per_slice = tps;
+  P.part = part;
+  P.status = c.status;
+  P.timeout_ns = c.timeout_ns;
+  CUtensorMap mx;
+  if (!tc::make_map_bf16_plain(&mx, x, cfg.T, cfg.d, kDwTok, 256)) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)((cfg.d + kDwCols - 1) / kDwCols), (unsigned)n_ts);
+  return launch_dependent(kern, grid, dim3(kStreamThreads), g_bytes + ns * kDwSlot, c.stream, mx,
+                          d_logits, P);
+}
+
 // ------------------------------------------------------------------ B3, E <= 16
 // dW_r partials for few experts: part[s][e][c] = sum over the tokens of slice s
 // of d_logits[t][e] * x[t][c]. A thread owns 8 consecutive columns and every
@@ -877,8 +1249,32 @@ router_dw_small(const Tx* __restrict__ x, const float* __restrict__ d_logits,
 }
 
 cudaError_t launch_router_dw_small(const Ctx& c, const moe_cfg& cfg, const void* x,
-                                   const float* d_logits, float* part, int splits) {
+                                   const float* d_logits, float* part, int splits, int* used) {
+  *used = splits;
   if (cfg.T == 0) return cudaSuccess;
+  if (cfg.act_dtype == MOE_BF16 && cfg.d % 8 == 0 && cfg.T <= (int64_t)INT32_MAX - 64 &&
+      (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+    // the streamed form: about one CTA per SM, token slices of a multiple of
+    // 16 tokens whose padded d_logits rows take at most 32 KB
+    const int emax = cfg.E <= 8 ? 8 : 16;
+    const int64_t n_cs = (cfg.d + kDwCols - 1) / kDwCols;
+    const int64_t want = c.sm_count / n_cs > 1 ? c.sm_count / n_cs : 1;
+    int64_t tps = ((cfg.T + want - 1) / want + kDwTok - 1) / kDwTok * kDwTok;
+    const int64_t cap = 8192 / emax;
+    if (tps > cap) tps = cap;
+    const int64_t n_ts = (cfg.T + tps - 1) / tps;
+    if (n_ts <= splits) {
+      cudaError_t e = emax == 8
+          ? launch_router_dw_stream<8>(c, cfg, static_cast<const bf16*>(x), d_logits, part,
+                                       (int)tps, (int)n_ts)
+          : launch_router_dw_stream<16>(c, cfg, static_cast<const bf16*>(x), d_logits, part,
+                                        (int)tps, (int)n_ts);
+      if (e != cudaSuccess) return e;
+      note_launches(1);
+      *used = (int)n_ts;
+      return cudaGetLastError();
+    }
+  }
   const int64_t per = (cfg.T + splits - 1) / splits;
   dim3 grid((unsigned)((cfg.d / 8 + 127) / 128), (unsigned)splits);
 #define MOE_DWS(TX, EM)                                                                 \
@@ -954,6 +1350,21 @@ static cudaError_t router_logits_dispatch(const Ctx& c, const moe_cfg& cfg, cons
   if (cfg.E <= 16) {
     // groups of 8 per lane: d / 8 split over 8 warps of 32 lanes
     const bool fold = (cfg.d / 8 + 255) / 256 > 4;
+    // bf16 x, W_r and a ring of at least two slots fit in shared memory, rows
+    // and W_r 16-byte aligned: the streamed form
+    if constexpr (std::is_same<Tx, bf16>::value) {
+      const int ns = cfg.E <= 8 ? stream_slots<8>(cfg) : stream_slots<16>(cfg);
+      if (ns >= 2 && cfg.d % 8 == 0 && cfg.T <= (int64_t)INT32_MAX - 64 &&
+          (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+          (reinterpret_cast<uintptr_t>(w_router) & 15) == 0) {
+        cudaError_t e = cfg.E <= 8
+            ? launch_router_stream<8>(c, cfg, x, w_router, logit_bias, logits, ns)
+            : launch_router_stream<16>(c, cfg, x, w_router, logit_bias, logits, ns);
+        if (e != cudaSuccess) return e;
+        note_launches(1);
+        return cudaGetLastError();
+      }
+    }
     // W_r fits in shared memory: the resident form
     if ((size_t)cfg.E * cfg.d * sizeof(float) <= kRouterResidentSmem) {
       cudaError_t e = cfg.E <= 8

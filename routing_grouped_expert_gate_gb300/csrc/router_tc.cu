@@ -41,9 +41,16 @@ using namespace tc;
 
 constexpr int R_EPI_WARPS = 8;  // fold warps: R_EPI_WARPS / 4 per TMEM lane quadrant
 constexpr int R_THREADS = 64 + 32 * R_EPI_WARPS;
-constexpr int R_NWIN = 2;  // window accumulators in flight
-constexpr int R_TMEM_COLS = 256;  // R_NWIN windows of BN + the 2 BN low-part accumulator, rounded up
+constexpr int R_MAX_NWIN = 6;  // window accumulators in flight, at most
 constexpr int R_MAX_STAGES = 8;
+
+// TMEM columns for NW window accumulators of BN columns and the 2 BN
+// low-part accumulator, rounded up to the power of two tcgen05.alloc takes.
+constexpr int r_tmem_cols(int BN, int NW) {
+  int c = 32;
+  while (c < (NW + 2) * BN) c *= 2;
+  return c;
+}
 
 // 32 lanes x 16 or 32 consecutive fp32 TMEM columns; the wait takes the
 // registers as operands, so no use of them can move above it.
@@ -88,14 +95,14 @@ struct RParams {
 struct __align__(8) RShared {
   uint64_t full[R_MAX_STAGES];
   uint64_t empty[R_MAX_STAGES];
-  uint64_t acc_full[R_NWIN];
-  uint64_t acc_empty[R_NWIN];
+  uint64_t acc_full[R_MAX_NWIN];
+  uint64_t acc_empty[R_MAX_NWIN];
   uint64_t lo_full;
   uint32_t tmem_base;
   int abort;
 };
 
-template <int BN>
+template <int BN, int NW>
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                  const RParams P) {
@@ -103,7 +110,9 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   constexpr int S = RT::kStages;
   constexpr int NC = BN / (R_EPI_WARPS / 4);  // columns per fold warp
   constexpr int CH = NC < 32 ? NC : 32;       // columns per TMEM read
+  constexpr int COLS = r_tmem_cols(BN, NW);
   static_assert(NC % CH == 0 && (CH == 16 || CH == 32), "fold warp columns");
+  static_assert(NW >= 2 && NW <= R_MAX_NWIN && COLS <= 512, "window accumulators");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -124,7 +133,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 1);
     }
-    for (int a = 0; a < R_NWIN; ++a) {
+    for (int a = 0; a < NW; ++a) {
       mbar_init(&sh.acc_full[a], 1);
       mbar_init(&sh.acc_empty[a], R_EPI_WARPS);  // one arrival per fold warp
     }
@@ -132,7 +141,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sh.tmem_base, R_TMEM_COLS);
+    tmem_alloc(&sh.tmem_base, COLS);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -169,50 +178,50 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     }
   } else if (warp == 1) {
     // ================= MMA issuer (lane 0) =================
-    // One thread walks the K loop: the four K16 steps of a stage unrolled,
-    // the operand descriptors formed once per stage (a K16 step advances the
-    // start address by 32 bytes, 2 in the descriptor's 16-byte units) and
-    // the window position kept as counters.
+    // One thread walks the K16 steps in a single flat loop: at a stage's
+    // first step it waits for the stage's tiles, at a window's first step
+    // for the window's accumulator; the operand descriptors are the first
+    // stage's plus fixed offsets (a stage is kStage bytes, a K16 step 32
+    // bytes: 2 in the descriptor's 16-byte units); at a stage's last step the
+    // stage is released to the producer.
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
       constexpr uint32_t IDESC_LO = idesc_bf16(false, false, 128, 2 * BN);
-      static_assert((R_NWIN + 2) * BN <= R_TMEM_COLS, "TMEM columns");
-      const uint32_t lo_acc = tmem + R_NWIN * BN;  // x·W1 in its first BN columns, x·W2 after
+      const uint32_t lo_acc = tmem + NW * BN;  // x·W1 in its first BN columns, x·W2 after
+      const uint64_t d0 = sw128_desc(su32(smem), 16, 1024);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int step = 0, pos = 0;  // K16 step, its place in the window
-      int buf = 0;            // the window's accumulator
-      uint32_t wphase = 0;    // flips each time buf wraps
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 22)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a_addr = su32(smem + stage * RT::kStage);
-        const uint64_t da = sw128_desc(a_addr, 16, 1024);
-        const uint64_t db0 = sw128_desc(a_addr + RT::kA, 16, 1024);
-        const uint64_t db1 = sw128_desc(a_addr + RT::kA + RT::kB, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk, ++step) {
-          if (pos == 0) {
-            // this buffer last held the window R_NWIN back: wait until it was folded
-            if (!mbar_wait(&sh.acc_empty[buf], wphase ^ 1, sh.abort, P, 23)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          const uint64_t dk = (uint64_t)(2 * kk);
-          mma_bf16(tmem + buf * BN, da + dk, db0 + dk, IDESC, pos > 0 ? 1u : 0u);
-          mma_bf16(lo_acc, da + dk, db1 + dk, IDESC_LO, step > 0 ? 1u : 0u);
-          if (++pos == fold || step == steps - 1) {
-            mma_commit(&sh.acc_full[buf]);
-            pos = 0;
-            if (++buf == R_NWIN) { buf = 0; wphase ^= 1; }
-          }
+      int pos = 0;          // the step's place in its window
+      int buf = 0;          // the window's accumulator
+      uint32_t wphase = 0;  // flips each time buf wraps
+      uint64_t da = d0;
+      for (int step = 0; step < steps; ++step) {
+        const int kk = step & 3;
+        if (kk == 0) {
+          if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 22)) { ok = false; break; }
+          tc_fence_after();
+          da = d0 + (uint64_t)(stage * (RT::kStage >> 4));
         }
-        if (!ok) break;
-        mma_commit(&sh.empty[stage]);
-        if (++stage == S) { stage = 0; phase ^= 1; }
+        if (pos == 0) {
+          // this buffer last held the window NW back: wait until it was folded
+          if (!mbar_wait(&sh.acc_empty[buf], wphase ^ 1, sh.abort, P, 23)) { ok = false; break; }
+          tc_fence_after();
+        }
+        const uint64_t a_d = da + (uint64_t)(2 * kk);
+        const uint64_t b0_d = a_d + (uint64_t)(RT::kA >> 4);
+        const uint64_t b1_d = b0_d + (uint64_t)(RT::kB >> 4);
+        mma_bf16(tmem + buf * BN, a_d, b0_d, IDESC, pos > 0 ? 1u : 0u);
+        mma_bf16(lo_acc, a_d, b1_d, IDESC_LO, step > 0 ? 1u : 0u);
+        if (++pos == fold || step == steps - 1) {
+          mma_commit(&sh.acc_full[buf]);
+          pos = 0;
+          if (++buf == NW) { buf = 0; wphase ^= 1; }
+        }
+        if (kk == 3) {
+          mma_commit(&sh.empty[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
       }
       if (ok) mma_commit(&sh.lo_full);
     }
@@ -256,7 +265,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.acc_empty[buf]);
-      if (++buf == R_NWIN) { buf = 0; wphase ^= 1; }
+      if (++buf == NW) { buf = 0; wphase ^= 1; }
     }
     if (ok && mbar_wait(&sh.lo_full, 0, sh.abort, P, 25)) {
       tc_fence_after();
@@ -265,7 +274,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 #pragma unroll
         for (int p = 0; p < 2; ++p) {  // x·W1, then x·W2
           float v[CH];
-          tmem_ld_cols(base + (R_NWIN + p) * BN + c, v);
+          tmem_ld_cols(base + (NW + p) * BN + c, v);
 #pragma unroll
           for (int i = 0; i < CH; ++i) lo[c + i] += v[i];
         }
@@ -293,7 +302,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, R_TMEM_COLS);
+    tmem_dealloc(tmem, COLS);
   }
 }
 
@@ -326,10 +335,10 @@ constexpr size_t r_smem_bytes() {
   return 1024 + (size_t)RTile<BN>::kStages * RTile<BN>::kStage + sizeof(RShared);
 }
 
-template <int BN>
+template <int BN, int NW>
 static cudaError_t launch_tc(const Ctx& c, const CUtensorMap& mx, const CUtensorMap& mw,
                              const RParams& P) {
-  auto kern = router_logits_tc<BN>;
+  auto kern = router_logits_tc<BN, NW>;
   constexpr size_t smem = r_smem_bytes<BN>();
   static std::atomic<uint64_t> attr_set_mask{0};
   int dev = 0;
@@ -395,7 +404,7 @@ cudaError_t launch_router_logits_tc(const Ctx& c, const moe_cfg& cfg, const void
   P.logits = logits;
   P.status = c.status;
   P.timeout_ns = c.timeout_ns;
-  e = launch_tc<BN>(c, mx, mw, P);
+  e = launch_tc<BN, 6>(c, mx, mw, P);
   note_launches(1);
   return e;
 }

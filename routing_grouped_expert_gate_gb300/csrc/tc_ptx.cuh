@@ -61,6 +61,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
       : "memory");
 }
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on `bar`'s transaction count.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          su32(dst)),
+      "l"(src), "r"(bytes), "r"(su32(bar))
+      : "memory");
+}
 // The same with the destination and barrier as shared-memory addresses.
 __device__ __forceinline__ void tma_load_2d_s(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                               int x, int y) {
@@ -189,6 +199,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn, int m, i
 // swizzle, zero fill outside the array. False when the driver entry point is
 // missing or the encoder refuses the arguments.
 bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+// The same without swizzle, with a box of box_cols (<= 256, box_cols * 2 a
+// multiple of 16) x box_rows; rows and columns past the array arrive as zeros.
+bool make_map_bf16_plain(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                         int box_rows, int box_cols);
 
 // ---- 16-byte asynchronous copies (cp.async) for gathered rows
 // global -> shared, 16 bytes, the last (16 - src_bytes) bytes filled with zeros

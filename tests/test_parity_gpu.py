@@ -320,6 +320,37 @@ def test_small_router_hidden_sizes(built, E, d):
     assert np.array_equal(to_np(idx)[decided], r["idx"][decided])
 
 
+@pytest.mark.parametrize("E,d,T", [(8, 264, 9741), (16, 520, 5003), (3, 1024, 4865),
+                                   (8, 4096, 1000)])
+def test_streamed_router_many_blocks(built, E, d, T):
+    """The few-expert gate GEMM with bf16 x streamed through the shared-memory
+    ring: more token blocks than CTAs (each CTA walks several blocks and the
+    ring wraps many times), a last 256-column slice that is partly past d, E
+    below the lane layout's expert count, and a ragged last block. Logits
+    within 1e-6 of the float64 oracle, the oracle's experts selected."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = mi.shrink(W["mixtral_style"], name=f"router_stream_e{E}_d{d}_t{T}", T=T, d=d, E=E,
+                   k=min(2, E), F=64)
+    inp = mi.make_inputs(wl, seed=17, device="cuda", with_dy=False)
+    cfg = moe.cfg_from_workload(wl)
+    ref = {k: O.as_f64(v) for k, v in inp.items() if v is not None}
+    r = O.route(ref["x"], ref["w_router"], wl.k, wl.score, wl.scaling, ref.get("logit_bias"),
+                ref.get("sel_bias"))
+    ws = torch.empty(max(L.workspace_bytes(cfg, L.MOE_WS_ROUTE), 256), dtype=torch.uint8,
+                     device="cuda")
+    logits = torch.full((wl.T, wl.E), float("nan"), device="cuda")
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.T, wl.k, device="cuda")
+    L.route_topk(cfg, inp["x"], inp["w_router"], None, None, logits, idx, w, ws)
+    torch.cuda.synchronize()
+    assert L.last_device_status()[0] == 0
+    err = float(np.max(np.abs(to_np(logits) - r["logits"])))
+    assert err < 1e-6, err
+    decided = r["gap"] >= 1e-6
+    assert np.array_equal(to_np(idx)[decided], r["idx"][decided])
+
+
 @pytest.mark.parametrize("E,d,T", [(64, 200, 333), (128, 456, 129), (256, 1032, 257)])
 def test_router_gate_gemm_ragged_shapes(built, E, d, T):
     """The tensor-core gate GEMM where d is no multiple of the 64-wide K block
