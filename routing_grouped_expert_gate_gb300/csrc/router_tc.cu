@@ -20,8 +20,8 @@
 // fp32 resolution of the logit.
 //
 // One CTA computes 128 tokens x 64 experts: warp 0 issues the TMA loads (x
-// tile + three W tiles per 64-wide K block); warp 1 owns 256 TMEM columns
-// (two 64-column window accumulators, one 128-column low-part accumulator)
+// tile + three W tiles per 64-wide K block); warp 1 owns 512 TMEM columns
+// (six 64-column window accumulators, one 128-column low-part accumulator)
 // and one of its lanes issues two tcgen05.mma per K16 step (M=128, K=16;
 // N=64 for x·W0, N=128 for x·W1 | x·W2); warps 2..9 (two per TMEM lane
 // quadrant, 32 columns each) fold the windows and write the logits, each fold
