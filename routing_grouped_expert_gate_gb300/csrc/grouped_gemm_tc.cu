@@ -20,8 +20,10 @@
 // Tiles are 128 x 256 (M x N) with K stepping 64 bf16 (one 128-byte swizzle row)
 // per pipeline stage. Warp 0 issues TMA loads into a 4-stage shared-memory ring;
 // warp 1 allocates 512 TMEM columns (two 256-column fp32 accumulators) and one
-// of its threads issues tcgen05.mma (M=128, N=256, K=16); warps 2..5 drain an
-// accumulator through tcgen05.ld while the next tile accumulates in the other.
+// of its threads issues tcgen05.mma (M=128, N=256, K=16); warps 2..9 drain an
+// accumulator through tcgen05.ld while the next tile accumulates in the other;
+// warp 10 waits on the mbarriers the MMA warp needs and meets it at a named
+// barrier per stage, so that the issuing thread never waits on an mbarrier.
 // The tile list is built on the device from the segment offsets: no host sync.
 // M-grouped tiles of one expert run m-fastest so that concurrently running CTAs
 // share the expert's weight tile through L2. K-grouped tiles take the experts
@@ -53,7 +55,9 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int NUM_EPI_WARPS = 8;                 // two per TMEM lane quadrant
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // producer, MMA, epilogue warps
+constexpr int RELAY_WARP = 2 + NUM_EPI_WARPS;     // waits for the MMA warp (after the epilogue warps)
+constexpr int NUM_THREADS = 32 * (RELAY_WARP + 1);  // producer, MMA, epilogue, relay warps
+constexpr int RELAY_BAR = 1;                      // named barrier of the MMA and relay warps
 constexpr int TMEM_COLS = 512;
 constexpr int MAXG = 256;
 // per epilogue warp: one 32 x 32 bf16 output box staged for a TMA store
@@ -105,6 +109,41 @@ struct __align__(8) Shared {
   int prefix[MAXG + 1];
   int order[MAXG];
 };
+
+// Named barrier of two whole warps (64 threads): the MMA warp and its relay.
+__device__ __forceinline__ void warp_pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// The relay warp: it walks the MMA warp's tiles and k-blocks, waits on the
+// barriers the MMA warp needs (at a tile's first k-block the accumulator's
+// tmem_empty, then the stage's full) and meets the MMA warp at RELAY_BAR once
+// per k-block. An mbarrier wait in the thread that issues the MMAs stalls the
+// tensor pipe at every stage (measured: 4 N=256 MMAs per stage take 512
+// cycles from one thread alone, 670 with a wait on an already completed
+// barrier and a commit per stage, 512 with the wait moved to this warp); the
+// named barrier costs nothing there. After a failed wait (timeout or abort,
+// recorded in the status word) the relay stops waiting and only meets the
+// MMA warp, which runs through its remaining k-blocks on whatever the stages
+// hold: the call reports the error, and no warp is left waiting.
+template <class SH, class PP, class Decode>
+__device__ __forceinline__ void relay_waits(SH& sh, const PP& P, int t0, int tstep, int total,
+                                            Decode decode, int stages, int accs, int site) {
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool ok = true;
+  for (int t = t0; t < total; t += tstep) {
+    const auto ti = decode(t);
+    if (ti.nk == 0) continue;
+    for (int kb = 0; kb < ti.nk; ++kb) {
+      if (ok && kb == 0) ok = mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, site);
+      if (ok) ok = mbar_wait(&sh.full[stage], phase, sh.abort, P, site + 1);
+      warp_pair_sync(RELAY_BAR);
+      if (++stage == stages) { stage = 0; phase ^= 1; }
+    }
+    if (++acc == accs) { acc = 0; acc_phase ^= 1; }
+  }
+}
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
 // A/B major-ness (0 = K-major, 1 = MN-major), N>>3 at [17,23), M>>4 at [24,29).
@@ -714,21 +753,18 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
     }
   } else if (warp == 1) {
-    // ================= MMA issuer (whole warp walks; lane 0 issues) =================
+    // ================= MMA issuer (whole warp walks; lane 0 issues; warp 10 waits) =================
     constexpr uint32_t IDESC = make_idesc(A_MN, B_MN);
     int stage = 0;
-    uint32_t phase = 0;
     int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = tile0; t < total && ok; t += tstep) {
+    for (int t = tile0; t < total; t += tstep) {
       const Tile ti = decode_tile<KGROUPED, EPI>(sh, P, t);
       if (ti.nk == 0) continue;  // empty segment: the epilogue writes zeros itself
-      if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 2)) { ok = false; break; }
-      tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < ti.nk; ++kb) {
-        if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 3)) { ok = false; break; }
+        // the relay warp has seen this stage's tiles land (and, at kb == 0,
+        // this accumulator drained by the epilogue)
+        warp_pair_sync(RELAY_BAR);
         tc_fence_after();
         uint8_t* a_s = stage_base + stage * STAGE_BYTES;
         uint8_t* b_s = a_s + A_STAGE_BYTES;
@@ -766,16 +802,17 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           mma_commit(&sh.empty[stage]);
         }
         __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (++stage == STAGES) stage = 0;
       }
-      if (!ok) break;
       if (lane == 0) mma_commit(&sh.tmem_full[acc]);
       __syncwarp();
       acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
     }
+  } else if (warp == RELAY_WARP) {
+    relay_waits(sh, P, tile0, tstep, total, [&](int t) { return decode_tile<KGROUPED, EPI>(sh, P, t); },
+                STAGES, 2, 2);
   } else {
-    // ================= epilogue: warps 2..5 =================
+    // ================= epilogue: warps 2..9 =================
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
     const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
@@ -1093,18 +1130,16 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
       constexpr uint32_t IDESC = make_idesc_pair(A_MN, B_MN);  // M = 256
       constexpr uint32_t IDESC128 = (IDESC & ~(0x1Fu << 24)) | ((uint32_t)(BM >> 4) << 24);
       int stage = 0;
-      uint32_t phase = 0;
       int acc = 0;
-      uint32_t acc_phase = 0;
-      for (int t = cluster_id; t < total && !aborted; t += n_clusters) {
+      for (int t = cluster_id; t < total; t += n_clusters) {
         const Tile ti = decode_pair_tile<KGROUPED, EPI>(sh, P, t, rank);
         if (ti.nk == 0) continue;  // empty segment: the epilogues write zeros themselves
-        if (!mbar_wait(&sh.tmem_empty[acc], acc_phase ^ 1, sh.abort, P, 12)) { aborted = true; break; }
-        tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         const uint32_t idesc = ti.m128 ? IDESC128 : IDESC;
         for (int kb = 0; kb < ti.nk; ++kb) {
-          if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 13)) { aborted = true; break; }
+          // the relay warp has seen both CTAs' tiles of this stage land (and,
+          // at kb == 0, this accumulator drained by both CTAs' epilogues)
+          warp_pair_sync(RELAY_BAR);
           tc_fence_after();
           uint8_t* a_s = stage_base + stage * STAGE2_BYTES;
           int nkk = BK / 16;  // K16 steps of this stage that hold rows of the segment
@@ -1154,16 +1189,20 @@ tc_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA,
             mma_commit_pair(&sh.empty[stage], 0x3);
           }
           __syncwarp();
-          if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+          if (++stage == STAGES2) stage = 0;
         }
-        if (aborted) break;
         if (lane == 0) mma_commit_pair(&sh.tmem_full[acc], 0x3);
         __syncwarp();
-        if (++acc == PAIR_ACC) { acc = 0; acc_phase ^= 1; }
+        if (++acc == PAIR_ACC) acc = 0;
       }
     }
+  } else if (warp == RELAY_WARP) {
+    if (leader)
+      relay_waits(sh, P, (int)cluster_id, (int)n_clusters, total,
+                  [&](int t) { return decode_pair_tile<KGROUPED, EPI>(sh, P, t, rank); }, STAGES2,
+                  PAIR_ACC, 12);
   } else {
-    // ================= epilogue: warps 2.. of both CTAs =================
+    // ================= epilogue: warps 2..9 of both CTAs =================
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;

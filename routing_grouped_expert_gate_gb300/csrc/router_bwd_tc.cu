@@ -16,7 +16,9 @@
 // over a K range, 128 x BNT tiles: warp 0 issues TMA loads of the planes per
 // 64-wide K block, warp 1 owns TMEM (two accumulators) and issues
 // tcgen05.mma (M=128, N=BNT, K=16) for every plane pair, warps 2..9 drain the
-// idle accumulator (two warps per lane quadrant) with 16-byte fp32 stores.
+// idle accumulator (two warps per lane quadrant) with 16-byte fp32 stores,
+// warp 10 waits on the mbarriers the MMA warp needs (a named barrier per
+// stage between the two: the issuing thread never waits on an mbarrier).
 // Split K writes slice partials [S][M][N], summed afterwards in slice order.
 // Every mbarrier wait is bounded (MOE_ERR_TIMEOUT + abort flag).
 #include <algorithm>
@@ -31,8 +33,10 @@ namespace rbw {
 
 using namespace tc;
 
-constexpr int PB_THREADS = 320;
 constexpr int PB_EPI_WARPS = 8;
+constexpr int PB_RELAY_WARP = 2 + PB_EPI_WARPS;  // waits for the MMA warp
+constexpr int PB_THREADS = 32 * (PB_RELAY_WARP + 1);
+constexpr int PB_RELAY_BAR = 1;  // named barrier of the MMA and relay warps (64 threads)
 constexpr int PB_MAX_STAGES = 4;
 
 struct PParams {
@@ -186,16 +190,15 @@ plane_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     // ================= MMA issuer =================
     constexpr uint32_t IDESC = idesc_bf16(A_MN, B_MN, 128, BNT);
     int stage = 0, acc = 0;
-    uint32_t phase = 0, acc_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const PTileId id = decode(P, t);
       if (id.nk == 0) continue;  // an empty K slice: the epilogue writes its zeros itself
-      if (!mbar_wait(&sh.acc_empty[acc], acc_phase ^ 1, sh.abort, P, 32)) { ok = false; break; }
-      tc_fence_after();
       const uint32_t d_tmem = tmem + acc * BNT;
       for (int kb = 0; kb < id.nk; ++kb) {
-        if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 33)) { ok = false; break; }
+        // the relay warp has seen this stage's tiles land (and, at kb == 0,
+        // this accumulator drained): an mbarrier wait in the issuing thread
+        // stalls the tensor pipe, a named barrier does not
+        asm volatile("bar.sync %0, 64;" ::"r"(PB_RELAY_BAR) : "memory");
         tc_fence_after();
         if (lane == 0) {
           const uint32_t base = su32(smem + stage * PT::kStage);
@@ -215,11 +218,29 @@ plane_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           mma_commit(&sh.empty[stage]);
         }
         __syncwarp();
-        if (++stage == S) { stage = 0; phase ^= 1; }
+        if (++stage == S) stage = 0;
       }
-      if (!ok) break;
       if (lane == 0) mma_commit(&sh.acc_full[acc]);
       __syncwarp();
+      acc ^= 1;
+    }
+  } else if (warp == PB_RELAY_WARP) {
+    // ================= relay: the MMA warp's waits =================
+    // After a failed wait (timeout or abort, recorded in the status word) it
+    // stops waiting and only meets the MMA warp, which runs through its
+    // remaining k-blocks: no warp is left waiting.
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const PTileId id = decode(P, t);
+      if (id.nk == 0) continue;
+      for (int kb = 0; kb < id.nk; ++kb) {
+        if (ok && kb == 0) ok = mbar_wait(&sh.acc_empty[acc], acc_phase ^ 1, sh.abort, P, 32);
+        if (ok) ok = mbar_wait(&sh.full[stage], phase, sh.abort, P, 33);
+        asm volatile("bar.sync %0, 64;" ::"r"(PB_RELAY_BAR) : "memory");
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -25,8 +25,9 @@
 // and one of its lanes issues two tcgen05.mma per K16 step (M=128, K=16;
 // N=64 for x·W0, N=128 for x·W1 | x·W2); warps 2..9 (two per TMEM lane
 // quadrant, 32 columns each) fold the windows and write the logits, each fold
-// thread keeping its token's 32 (hi, lo) pairs in registers. Every mbarrier
-// wait is bounded (MOE_ERR_TIMEOUT + abort flag).
+// thread keeping its token's 32 (hi, lo) pairs in registers; warp 10 waits on
+// the mbarriers the MMA warp needs (the issuing thread never waits on an
+// mbarrier). Every mbarrier wait is bounded (MOE_ERR_TIMEOUT + abort flag).
 #include <algorithm>
 #include <atomic>
 
@@ -40,7 +41,9 @@ namespace rtc {
 using namespace tc;
 
 constexpr int R_EPI_WARPS = 8;  // fold warps: R_EPI_WARPS / 4 per TMEM lane quadrant
-constexpr int R_THREADS = 64 + 32 * R_EPI_WARPS;
+constexpr int R_RELAY_WARP = 2 + R_EPI_WARPS;  // waits for the MMA warp
+constexpr int R_THREADS = 32 * (R_RELAY_WARP + 1);
+constexpr int R_RELAY_BAR = 1;  // named barrier of the MMA and relay warps (64 threads)
 constexpr int R_MAX_NWIN = 6;  // window accumulators in flight, at most
 constexpr int R_MAX_STAGES = 8;
 
@@ -177,55 +180,72 @@ router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       }
     }
   } else if (warp == 1) {
-    // ================= MMA issuer (lane 0) =================
-    // One thread walks the K16 steps in a single flat loop: at a stage's
-    // first step it waits for the stage's tiles, at a window's first step
-    // for the window's accumulator; the operand descriptors are the first
-    // stage's plus fixed offsets (a stage is kStage bytes, a K16 step 32
-    // bytes: 2 in the descriptor's 16-byte units); at a stage's last step the
-    // stage is released to the producer.
-    if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
-      constexpr uint32_t IDESC_LO = idesc_bf16(false, false, 128, 2 * BN);
-      const uint32_t lo_acc = tmem + NW * BN;  // x·W1 in its first BN columns, x·W2 after
-      const uint64_t d0 = sw128_desc(su32(smem), 16, 1024);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      int pos = 0;          // the step's place in its window
-      int buf = 0;          // the window's accumulator
-      uint32_t wphase = 0;  // flips each time buf wraps
-      uint64_t da = d0;
-      for (int step = 0; step < steps; ++step) {
-        const int kk = step & 3;
-        if (kk == 0) {
-          if (!mbar_wait(&sh.full[stage], phase, sh.abort, P, 22)) { ok = false; break; }
-          tc_fence_after();
-          da = d0 + (uint64_t)(stage * (RT::kStage >> 4));
-        }
-        if (pos == 0) {
-          // this buffer last held the window NW back: wait until it was folded
-          if (!mbar_wait(&sh.acc_empty[buf], wphase ^ 1, sh.abort, P, 23)) { ok = false; break; }
-          tc_fence_after();
-        }
+    // ================= MMA issuer =================
+    // The whole warp walks the K16 steps in one flat loop and one lane issues:
+    // at a step where the stage's tiles or the window's accumulator must be
+    // waited for, the relay warp has done the waiting and the two warps meet
+    // at R_RELAY_BAR (an mbarrier wait in the issuing thread stalls the tensor
+    // pipe). The operand descriptors are the first stage's plus fixed offsets
+    // (a stage is kStage bytes, a K16 step 32 bytes: 2 in the descriptor's
+    // 16-byte units); at a stage's last step the stage is released to the
+    // producer.
+    constexpr uint32_t IDESC = idesc_bf16(false, false, 128, BN);
+    constexpr uint32_t IDESC_LO = idesc_bf16(false, false, 128, 2 * BN);
+    const uint32_t lo_acc = tmem + NW * BN;  // x·W1 in its first BN columns, x·W2 after
+    const uint64_t d0 = sw128_desc(su32(smem), 16, 1024);
+    int stage = 0;
+    int pos = 0;  // the step's place in its window
+    int buf = 0;  // the window's accumulator
+    uint64_t da = d0;
+    for (int step = 0; step < steps; ++step) {
+      const int kk = step & 3;
+      if (kk == 0 || pos == 0) {
+        asm volatile("bar.sync %0, 64;" ::"r"(R_RELAY_BAR) : "memory");
+        tc_fence_after();
+      }
+      if (kk == 0) da = d0 + (uint64_t)(stage * (RT::kStage >> 4));
+      if (lane == 0) {
         const uint64_t a_d = da + (uint64_t)(2 * kk);
         const uint64_t b0_d = a_d + (uint64_t)(RT::kA >> 4);
         const uint64_t b1_d = b0_d + (uint64_t)(RT::kB >> 4);
         mma_bf16(tmem + buf * BN, a_d, b0_d, IDESC, pos > 0 ? 1u : 0u);
         mma_bf16(lo_acc, a_d, b1_d, IDESC_LO, step > 0 ? 1u : 0u);
-        if (++pos == fold || step == steps - 1) {
-          mma_commit(&sh.acc_full[buf]);
-          pos = 0;
-          if (++buf == NW) { buf = 0; wphase ^= 1; }
-        }
-        if (kk == 3) {
-          mma_commit(&sh.empty[stage]);
-          if (++stage == S) { stage = 0; phase ^= 1; }
-        }
       }
-      if (ok) mma_commit(&sh.lo_full);
+      if (++pos == fold || step == steps - 1) {
+        if (lane == 0) mma_commit(&sh.acc_full[buf]);
+        pos = 0;
+        if (++buf == NW) buf = 0;
+      }
+      if (kk == 3) {
+        if (lane == 0) mma_commit(&sh.empty[stage]);
+        if (++stage == S) stage = 0;
+      }
+      __syncwarp();
     }
+    if (lane == 0) mma_commit(&sh.lo_full);
     __syncwarp();
+  } else if (warp == R_RELAY_WARP) {
+    // ================= relay: the MMA warp's waits =================
+    // After a failed wait (timeout or abort, recorded in the status word) it
+    // stops waiting and only meets the MMA warp, which runs through its
+    // remaining steps: no warp is left waiting.
+    int stage = 0;
+    uint32_t phase = 0;
+    int pos = 0, buf = 0;
+    uint32_t wphase = 0;
+    bool ok = true;
+    for (int step = 0; step < steps; ++step) {
+      const int kk = step & 3;
+      if (kk == 0 && ok) ok = mbar_wait(&sh.full[stage], phase, sh.abort, P, 22);
+      // this buffer last held the window NW back: wait until it was folded
+      if (pos == 0 && ok) ok = mbar_wait(&sh.acc_empty[buf], wphase ^ 1, sh.abort, P, 23);
+      if (kk == 0 || pos == 0) asm volatile("bar.sync %0, 64;" ::"r"(R_RELAY_BAR) : "memory");
+      if (++pos == fold || step == steps - 1) {
+        pos = 0;
+        if (++buf == NW) { buf = 0; wphase ^= 1; }
+      }
+      if (kk == 3 && ++stage == S) { stage = 0; phase ^= 1; }
+    }
   } else {
     // ================= fold + store: warps 2..9 =================
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 (the warp's quadrant)
