@@ -778,6 +778,33 @@ __device__ __forceinline__ void selection_keys(const float* __restrict__ lrow,
   }
 }
 
+// Sorts n = 1, 2, 4 or 8 values descending in registers with a fixed
+// compare-exchange network (the 19-comparator network for 8 inputs; checked on
+// every 0/1 input).
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t (&v)[N]) {
+  static_assert(N == 1 || N == 2 || N == 4 || N == 8, "network sizes");
+  if constexpr (N == 2) {
+    cas_desc(v[0], v[1]);
+  } else if constexpr (N == 4) {
+    cas_desc(v[0], v[1]); cas_desc(v[2], v[3]);
+    cas_desc(v[0], v[2]); cas_desc(v[1], v[3]);
+    cas_desc(v[1], v[2]);
+  } else if constexpr (N == 8) {
+    cas_desc(v[0], v[2]); cas_desc(v[1], v[3]); cas_desc(v[4], v[6]); cas_desc(v[5], v[7]);
+    cas_desc(v[0], v[4]); cas_desc(v[1], v[5]); cas_desc(v[2], v[6]); cas_desc(v[3], v[7]);
+    cas_desc(v[0], v[1]); cas_desc(v[2], v[3]); cas_desc(v[4], v[5]); cas_desc(v[6], v[7]);
+    cas_desc(v[2], v[4]); cas_desc(v[3], v[5]);
+    cas_desc(v[1], v[4]); cas_desc(v[3], v[6]);
+    cas_desc(v[1], v[2]); cas_desc(v[3], v[4]); cas_desc(v[5], v[6]);
+  }
+}
+
 // ------------------------------------------------------------------ S2
 // One warp per token. Lane l holds experts l, l+32, ... The k winners are found
 // by k rounds of a warp arg-max over (key descending, index ascending); a
@@ -803,7 +830,7 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
     // expert ascending): the key's bits made order-preserving as unsigned
     // (-0 counted as +0) above the complemented expert index; slots past E hold
     // 0, below every expert. Round j takes the warp's largest remaining value
-    // (a local max, then a butterfly max), its owner clears it, and lane j
+    // (a butterfly max over the lanes' heads), its owner drops it, and lane j
     // keeps the winner's expert and key.
     uint64_t pk[EPL];
 #pragma unroll
@@ -817,6 +844,9 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
         pk[i] = 0ull;
       }
     }
+    // the lane's candidates sorted descending once, so that a round needs
+    // only each lane's head: the winner's lane moves its next one up
+    sort_desc<EPL>(pk);
     int my_e = 0;
     float my_key = 0.f;
 #pragma unroll
@@ -824,15 +854,15 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       if (j < ksel) {
         uint64_t best = pk[0];
 #pragma unroll
-        for (int i = 1; i < EPL; ++i) best = pk[i] > best ? pk[i] : best;
-#pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
           const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
           best = o > best ? o : best;
         }
+        if (pk[0] == best) {  // the one lane whose head won (values are distinct)
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-          if (pk[i] == best) pk[i] = 0ull;
+          for (int i = 0; i + 1 < EPL; ++i) pk[i] = pk[i + 1];
+          pk[EPL - 1] = 0ull;
+        }
         if (lane == j) {
           my_e = (int)(~(uint32_t)best);
           uint32_t b = (uint32_t)(best >> 32);
