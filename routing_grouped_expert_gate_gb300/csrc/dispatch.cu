@@ -23,8 +23,11 @@
 // Beyond 16384 (block, expert) cells the per-CTA sums would grow too large and
 // the older four-launch form runs: count, a one-thread-per-expert scan, rank,
 // copy.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -582,6 +585,273 @@ permute_bwd_router(const T* __restrict__ dx_perm, const int32_t* __restrict__ ro
   }
 }
 
+// N = 4 or 8 consecutive bf16 in shared memory <-> N floats (one 8- or
+// 16-byte access); stores round to nearest like store8.
+template <int N>
+__device__ __forceinline__ void load_smem_bf16(const uint8_t* p, float (&v)[N]) {
+  static_assert(N == 4 || N == 8, "4 or 8 elements");
+  if constexpr (N == 8) {
+    load8(reinterpret_cast<const bf16*>(p), v);
+  } else {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_bf16_n(bf16* p, const float (&v)[N]) {
+  static_assert(N == 4 || N == 8, "4 or 8 elements");
+  if constexpr (N == 8) {
+    store8(p, v);
+  } else {
+    uint2 r;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+    h[0] = __floats2bfloat162_rn(v[0], v[1]);
+    h[1] = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2*>(p) = r;
+  }
+}
+
+// The same sums for bf16 rows streamed through shared memory. A CTA takes a
+// 1024-column slice of d and a slice of the tokens. The slice's rows, d_logits
+// and gate logits are staged in shared memory once at the start; then a
+// producer warp copies, per ring slot of TS tokens, each token's k row slices
+// of dx_perm (and the one of dx_shared) with one bulk copy each, without
+// waiting on any load, while the consumer warps keep their lanes' columns of
+// W_r (EMAX x CPL values) and of w_gate in registers for the whole kernel (so
+// W_r is read once per CTA) and add the slot's rows. Per element the
+// arithmetic is that of permute_bwd_router, in the same order: dx is the same
+// bit for bit. Every mbarrier wait is bounded (MOE_ERR_TIMEOUT + abort flag).
+constexpr int kPbCols = 1024;       // columns per CTA
+constexpr int kPbRowsPerSlot = 16;  // row slices per slot (TS tokens x (k + shared))
+constexpr int kPbMaxSlots = 6;
+constexpr int kPbThreads = 288;     // 8 consumer warps + 1 producer warp
+constexpr size_t kPbRingSmem = 192 * 1024;
+constexpr size_t kPbTableSmem = 32 * 1024;
+
+struct PbParams {
+  int64_t T, A;
+  int d, k, E, ns, tok_per_cta;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int KK, int EMAX, bool SH>
+struct PbTile {
+  static constexpr int CPL = EMAX <= 8 ? 8 : 4;       // columns per lane
+  static constexpr int WCOLS = 32 * CPL;              // columns per warp
+  static constexpr int QUARTERS = kPbCols / WCOLS;    // warps across the slice: 4 or 8
+  static constexpr int TGROUPS = 8 / QUARTERS;        // token classes: 2 or 1
+  static constexpr int RPT = KK + (SH ? 1 : 0);       // row slices per token (+ shared)
+  static constexpr int TS = kPbRowsPerSlot / RPT > 0 ? kPbRowsPerSlot / RPT : 1;  // tokens per slot
+  static constexpr int kSlot = TS * RPT * kPbCols * 2;  // bytes
+};
+
+template <int KK, int EMAX, bool SH>
+__global__ void __launch_bounds__(kPbThreads, 1)
+permute_bwd_router_stream(const bf16* __restrict__ dx_perm, const int32_t* __restrict__ row_of,
+                          const bf16* __restrict__ dx_shared, const float* __restrict__ d_gate_logit,
+                          const float* __restrict__ w_gate, const float* __restrict__ d_logits,
+                          const float* __restrict__ w_router, bf16* __restrict__ dx,
+                          const PbParams P) {
+  using PT = PbTile<KK, EMAX, SH>;
+  constexpr int TS = PT::TS, RPT = PT::RPT, CPL = PT::CPL;
+  static_assert(TS * RPT <= 32, "one row slice per producer lane");
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t full[kPbMaxSlots], empty[kPbMaxSlots];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = P.d, k = P.k, E = P.E, ns = P.ns;
+  const int c0 = blockIdx.x * kPbCols;
+  const int cols = d - c0 < kPbCols ? d - c0 : kPbCols;
+  const int64_t t_beg = (int64_t)blockIdx.y * P.tok_per_cta;
+  const int64_t t_end = t_beg + P.tok_per_cta < P.T ? t_beg + P.tok_per_cta : P.T;
+  const int ntok = (int)(t_end - t_beg);
+  const int nslots = (ntok + TS - 1) / TS;
+  // the CTA's tokens' rows, d_logits and gate logits, after the ring
+  int* s_rows = reinterpret_cast<int*>(sm_raw + (size_t)ns * PT::kSlot);  // [tok][KK]
+  float* s_dl = reinterpret_cast<float*>(s_rows + (size_t)P.tok_per_cta * KK);  // [tok][EMAX]
+  float* s_dgl = s_dl + (size_t)P.tok_per_cta * EMAX;                            // [tok]
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < ns; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 8);  // one arrival per consumer warp
+    }
+    tc::fence_barrier_init();
+  }
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
+  for (int i = threadIdx.x; i < ntok * KK; i += blockDim.x) {
+    const int a = i / KK, j = i - a * KK;
+    const int64_t t = t_beg + a;
+    int r = j < k ? row_of[t * k + j] : -1;
+    if (j < k && (r < 0 || r >= P.A)) {
+      record_error(P.status, MOE_ERR_DEVICE_INDEX, (int)t);
+      r = -1;
+    }
+    s_rows[i] = r;
+  }
+  for (int i = threadIdx.x; i < ntok * EMAX; i += blockDim.x) {
+    const int a = i / EMAX, e = i - a * EMAX;
+    s_dl[i] = e < E ? d_logits[(t_beg + a) * E + e] : 0.f;
+  }
+  for (int i = threadIdx.x; i < ntok; i += blockDim.x)
+    s_dgl[i] = d_gate_logit != nullptr ? d_gate_logit[t_beg + i] : 0.f;
+  __syncthreads();
+
+  if (warp == 8) {
+    // ---------------- producer: one bulk copy per row slice, lane = (token, row)
+    int slot = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    const int a = lane / RPT, j = lane - (lane / RPT) * RPT;
+    for (int i = 0; i < nslots; ++i) {
+      int w_ok = 1;
+      if (lane == 0) w_ok = tc::mbar_wait(&empty[slot], ph ^ 1, abort_flag, P, 51) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
+      const int ta = i * TS + a;  // the lane's token within the CTA
+      int64_t src = -1;           // element offset of the slice's source row
+      if (a < TS && ta < ntok) {
+        if (j < KK) {
+          const int r = j < k ? s_rows[ta * KK + j] : -1;
+          if (r >= 0) src = (int64_t)r * d + c0;
+        } else if (SH) {
+          src = (t_beg + ta) * d + c0;
+        }
+      }
+      const uint32_t bytes = (uint32_t)cols * 2;
+      const unsigned issue = __ballot_sync(0xffffffffu, src >= 0);
+      if (lane == 0) tc::mbar_expect_tx(&full[slot], bytes * (uint32_t)__popc(issue));
+      __syncwarp();
+      if (src >= 0) {
+        const bf16* g = (j < KK) ? dx_perm + src : dx_shared + src;
+        tc::bulk_load_1d(sm_raw + (size_t)slot * PT::kSlot + (size_t)(a * RPT + j) * (kPbCols * 2),
+                         g, bytes, &full[slot]);
+      }
+      if (++slot == ns) { slot = 0; ph ^= 1; }
+    }
+    if (!ok && lane == 0) {
+      // let the copies already in flight land before the CTA exits
+      const uint64_t t_start = global_timer_ns();
+      while (global_timer_ns() - t_start < 2000000ull) { }
+    }
+  } else {
+    // ---------------- consumers
+    const int q = warp % PT::QUARTERS, tg = warp / PT::QUARTERS;
+    const int cl = q * PT::WCOLS + lane * CPL;  // column within the slice
+    const int col = c0 + cl;
+    const bool active = cl < cols;
+    float w[EMAX][CPL], wg[CPL];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i)
+        w[e][i] = (active && e < E) ? __ldg(w_router + (int64_t)e * d + col + i) : 0.f;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i)
+      wg[i] = (active && d_gate_logit != nullptr) ? __ldg(w_gate + col + i) : 0.f;
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < nslots; ++i) {
+      if (!tc::mbar_wait(&full[slot], ph, abort_flag, P, 52)) break;
+      const uint8_t* base = sm_raw + (size_t)slot * PT::kSlot + (size_t)cl * 2;
+      for (int a = tg; a < TS; a += PT::TGROUPS) {
+        const int ta = i * TS + a;
+        if (ta >= ntok || !active) continue;
+        float acc[CPL];
+#pragma unroll
+        for (int ii = 0; ii < CPL; ++ii) acc[ii] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+          if (e < E) {
+            const float dl = s_dl[ta * EMAX + e];
+#pragma unroll
+            for (int ii = 0; ii < CPL; ++ii) acc[ii] = fmaf(dl, w[e][ii], acc[ii]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < KK; ++j) {
+          if (j < k && s_rows[ta * KK + j] >= 0) {
+            float v[CPL];
+            load_smem_bf16<CPL>(base + (size_t)(a * RPT + j) * (kPbCols * 2), v);
+#pragma unroll
+            for (int ii = 0; ii < CPL; ++ii) acc[ii] += v[ii];
+          } else if (j < k) {
+#pragma unroll
+            for (int ii = 0; ii < CPL; ++ii) acc[ii] += 0.f;
+          }
+        }
+        float sv[CPL];
+        if (SH) {
+          load_smem_bf16<CPL>(base + (size_t)(a * RPT + (SH ? KK : 0)) * (kPbCols * 2), sv);
+        } else {
+#pragma unroll
+          for (int ii = 0; ii < CPL; ++ii) sv[ii] = 0.f;
+        }
+#pragma unroll
+        for (int ii = 0; ii < CPL; ++ii) acc[ii] += sv[ii];
+        if (d_gate_logit != nullptr) {
+          const float dgl = s_dgl[ta];
+#pragma unroll
+          for (int ii = 0; ii < CPL; ++ii) acc[ii] = fmaf(dgl, wg[ii], acc[ii]);
+        }
+        store_bf16_n<CPL>(dx + (t_beg + ta) * d + col, acc);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
+      if (++slot == ns) { slot = 0; ph ^= 1; }
+    }
+  }
+}
+
+template <int KK, int EMAX, bool SH>
+static cudaError_t launch_permute_bwd_stream(const Ctx& c, const moe_cfg& cfg, const bf16* dx_perm,
+                                             const int32_t* row_of, const bf16* dx_shared,
+                                             const float* d_gate_logit, const float* w_gate,
+                                             const float* d_logits, const float* w_router,
+                                             bf16* dx) {
+  using PT = PbTile<KK, EMAX, SH>;
+  auto kern = permute_bwd_router_stream<KK, EMAX, SH>;
+  static bool attr_done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_done[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kPbRingSmem + kPbTableSmem));
+    if (e != cudaSuccess) return e;
+    attr_done[dev & 63] = true;
+  }
+  size_t ns = kPbRingSmem / PT::kSlot;
+  if (ns > (size_t)kPbMaxSlots) ns = kPbMaxSlots;
+  // about one CTA per SM: 1024-column slices x token slices of a multiple of
+  // TS, with the slice's per-token tables (rows, d_logits, gate logit) within
+  // kPbTableSmem
+  const size_t per_tok = (size_t)KK * 4 + (size_t)EMAX * 4 + 4;
+  const int64_t cap = (int64_t)(kPbTableSmem / per_tok) / PT::TS * PT::TS;
+  const int64_t n_cs = (cfg.d + kPbCols - 1) / kPbCols;
+  const int64_t want = c.sm_count / n_cs > 1 ? c.sm_count / n_cs : 1;
+  int64_t tpc = ((cfg.T + want - 1) / want + PT::TS - 1) / PT::TS * PT::TS;
+  if (tpc > cap) tpc = cap;
+  if (tpc < PT::TS) tpc = PT::TS;
+  const int64_t n_ts = (cfg.T + tpc - 1) / tpc;
+  const size_t smem = ns * PT::kSlot + (size_t)tpc * per_tok;
+  PbParams P{};
+  P.T = cfg.T;
+  P.A = cfg.T * cfg.k;
+  P.d = cfg.d;
+  P.k = cfg.k;
+  P.E = cfg.E;
+  P.ns = (int)ns;
+  P.tok_per_cta = (int)tpc;
+  P.status = c.status;
+  P.timeout_ns = c.timeout_ns;
+  return launch_dependent(kern, dim3((unsigned)n_cs, (unsigned)n_ts), dim3(kPbThreads), smem,
+                          c.stream, dx_perm, row_of, dx_shared, d_gate_logit, w_gate, d_logits,
+                          w_router, dx, P);
+}
+
 // Shared memory the router-fused form may take for W_r.
 constexpr size_t kPermBwdWSmem = 160 * 1024;
 
@@ -603,6 +873,20 @@ static cudaError_t launch_permute_bwd_router(const Ctx& c, const moe_cfg& cfg, c
                                          (int)kPermBwdWSmem);
     if (e != cudaSuccess) return e;
     attr_done[dev & 63] = true;
+  }
+  if constexpr (std::is_same<T, bf16>::value) {
+    // bf16 rows, 16-byte aligned, d a multiple of 8: the streamed form
+    const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    if (cfg.d % 8 == 0 && cfg.T <= (int64_t)INT32_MAX && al(dx_perm) && al(dx) &&
+        (dx_shared == nullptr || al(dx_shared))) {
+      return dx_shared != nullptr
+                 ? launch_permute_bwd_stream<KK, EMAX, true>(c, cfg, dx_perm, row_of, dx_shared,
+                                                             d_gate_logit, w_gate, d_logits,
+                                                             w_router, dx)
+                 : launch_permute_bwd_stream<KK, EMAX, false>(c, cfg, dx_perm, row_of, dx_shared,
+                                                              d_gate_logit, w_gate, d_logits,
+                                                              w_router, dx);
+    }
   }
   const size_t wbytes = (size_t)cfg.E * cfg.d * sizeof(float);
   const bool in_smem = wbytes <= kPermBwdWSmem;

@@ -60,7 +60,8 @@ CASES = [("ragged_d_small", "native", "tcgen05"), ("ragged_d_small", "native", "
          ("mixtral_f4096_small", "native", "tcgen05"),
          ("mixtral_d4096_small", "native", "tcgen05"),
          ("presoftmax_top1_small", "native", "tcgen05"),
-         ("gated_shared_small", "native", "tcgen05"), ("tiny_fp32", "native", "cudacores")]
+         ("gated_shared_small", "native", "tcgen05"), ("few_shared_small", "native", "tcgen05"),
+         ("tiny_fp32", "native", "cudacores")]
 
 
 @pytest.mark.parametrize("name,dt,impl", CASES)

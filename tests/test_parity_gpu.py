@@ -62,6 +62,11 @@ SMALL = {
     # and the data gradients store a ragged last column box)
     "ragged_d_small": mi.shrink(W["deepseek_v3_shaped"], name="ragged_d_small", T=200, d=200,
                                 E=64, k=6, F=96, F_shared=64, backward=True),
+    # few experts with a gated shared expert, top-4, d = 1288 (a 1024-column
+    # slice and a ragged 264-column one): the permute backward that forms
+    # d_logits · W_r streams k + 1 row slices per token through its ring
+    "few_shared_small": mi.shrink(W["mixtral_style"], name="few_shared_small", T=2999, d=1288,
+                                  E=12, k=4, F=96, F_shared=64, shared_gate=True),
 }
 # bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
@@ -611,11 +616,13 @@ def test_permute_index_paths(built, T, E, k):
 
 
 @pytest.mark.parametrize("name", ["mixtral_small", "presoftmax_top1_small", "tiny_fp32",
-                                  "mixtral_d4096_small"])
+                                  "mixtral_d4096_small", "few_shared_small"])
 def test_router_dx_formed_in_permute_bwd_is_bitwise_the_same(built, name):
-    """Few experts: the permute backward forms d_logits · W_r itself. Its dx
-    equals, bit for bit, the dx of the other order of work (the router
-    backward writing dx_router in fp32, the permute backward adding it)."""
+    """Few experts: the permute backward forms d_logits · W_r itself (for
+    bf16 rows streaming them through its shared-memory ring, W_r's columns in
+    registers). Its dx equals, bit for bit, the dx of the other order of work
+    (the router backward writing dx_router in fp32, the permute backward
+    adding it), with and without a gated shared expert."""
     import routing_grouped_expert_gate_gb300 as moe
     from routing_grouped_expert_gate_gb300 import _lib as L
     wl = SMALL[name]
@@ -629,7 +636,11 @@ def test_router_dx_formed_in_permute_bwd_is_bitwise_the_same(built, name):
     L.route_topk_bwd(cfg, inp["x"], inp["w_router"], b["logits"], b["idx"], b["dw"],
                      b["d_logits"], 1, b["dx_router"], b["dw_router"], b["ws"])
     dx2 = torch.empty_like(b["dx"])
-    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], b["dx_router"], None, dx2)
+    gated = wl.F_shared > 0 and wl.shared_gate
+    L.permute_bwd(cfg, b["dx_perm"], b["row_of"], b["dx_router"],
+                  b["dx_s"] if wl.F_shared > 0 else None, dx2,
+                  d_gate_logit=b["d_gate_logit_s"] if gated else None,
+                  w_gate=inp["w_gate_s"] if gated else None)
     torch.cuda.synchronize()
     assert L.last_device_status()[0] == 0
     assert torch.equal(dx2, dx_fused)
