@@ -504,7 +504,7 @@ int moe_selftest_wait_timeout(moe_stream_t stream);
 /* Which kernels run the grouped expert GEMMs (moe_grouped_swiglu and its
  * backward). MOE_GEMM_AUTO (default): bf16 on the tcgen05 tensor cores, with
  * the forward and data-gradient contractions on CTA pairs (cta_group::2) when
- * the segments average at least 512 rows and on single CTAs otherwise, and
+ * the segments average at least 128 rows and on single CTAs otherwise, and
  * the weight gradients on CTA pairs; fp32 on CUDA cores.
  * MOE_GEMM_TC_SINGLE_CTA / MOE_GEMM_TC_PAIRS: bf16 on single-CTA / CTA-pair
  * tcgen05 kernels whatever the segment sizes (the weight gradients too).

@@ -1478,12 +1478,16 @@ constexpr size_t kSmemBytes2 = 1024 + (size_t)STAGES2 * STAGE2_BYTES + EPI_BUF_B
 // 0: CTA pairs for long segments (default); 1: single CTAs only; 2: CTA pairs always
 static std::atomic<int> g_tc_mode{0};
 
-// CTA pairs compute 256-row tiles; when the experts' segments are short the
-// second half of many pair tiles would be empty rows, so small segments stay
-// on single CTAs (measured: a 256-row average is faster single-CTA).
+// CTA pairs compute 256-row tiles (a segment's last tile of at most 128 rows
+// as an M = 128 tile); when the experts' segments are very short, most pair
+// tiles would run at half size, so segments averaging under 128 rows stay on
+// single CTAs. Measured on DeepSeek-V3-shaped layers (0 to 947 rows per expert
+// at T = 8192): with the relay warp the forward at a 256-row average takes
+// 5.64-5.67 ms on pairs against 5.73-5.75 ms on single CTAs; before it, a
+// 128-row average (T = 4096) already ran 3.11 ms on pairs against 3.17 ms.
 static bool use_pair(int G, int64_t n_rows) {
   const int mode = g_tc_mode.load();
-  return mode == 2 || (mode == 0 && n_rows >= (int64_t)512 * G);
+  return mode == 2 || (mode == 0 && n_rows >= (int64_t)128 * G);
 }
 
 template <bool A_MN, bool B_MN, int EPI>
