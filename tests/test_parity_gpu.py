@@ -529,6 +529,32 @@ def test_out_of_range_index_is_reported_not_faulted(built):
     assert L.last_device_status()[0] == 0  # reading clears it
 
 
+@pytest.mark.parametrize("E", [8, 32])
+def test_repeated_expert_is_reported(built, E):
+    """A token that names the same expert twice is recorded as a bad index
+    (its repeat counts once, the other rows stay consistent); no fault."""
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    T, d, k = 64, 64, 2
+    cfg = moe.make_cfg(T=T, d=d, E=E, k=k, F=64)
+    dev = "cuda"
+    x = torch.randn(T, d, device=dev).to(torch.bfloat16)
+    idx = torch.stack([torch.arange(T) % E, (torch.arange(T) + 1) % E], 1).to(torch.int32).to(dev)
+    idx[9, 1] = idx[9, 0]  # token 9 repeats its first expert
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T, k, dtype=torch.int32, device=dev)
+    src = torch.zeros(T * k, dtype=torch.int32, device=dev)
+    xp = torch.zeros(T * k, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.workspace_bytes(cfg, L.MOE_WS_PERMUTE), dtype=torch.uint8, device=dev)
+    L.last_device_status()
+    L.permute(cfg, x, idx, counts, offsets, row_of, src, xp, ws)
+    rc, detail = L.last_device_status()
+    assert rc == L.MOE_ERR_DEVICE_INDEX and detail == 9
+    assert int(offsets[-1]) == T * k - 1  # the repeat counted once
+    assert L.last_device_status()[0] == 0
+
+
 def test_bounded_wait_reports_timeout(built):
     from routing_grouped_expert_gate_gb300 import _lib as L
     old = L.set_wait_timeout_ns(2_000_000)  # 2 ms
@@ -578,19 +604,22 @@ def test_near_tie_count(built, name):
     assert L.last_device_status()[0] == 0
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (127, 8, 2), (4096, 8, 2), (2051, 64, 8),
-                                   (20608, 256, 4), (16384, 128, 8), (33024, 256, 4)])
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (127, 8, 2), (4096, 8, 2), (5000, 8, 1),
+                                   (999, 12, 1), (32767, 16, 2), (40000, 8, 2), (3001, 12, 4),
+                                   (2051, 64, 8), (20608, 256, 4), (16384, 128, 8),
+                                   (33024, 256, 4)])
 def test_permute_index_paths(built, T, E, k):
     """The dispatch on both of its index paths: per-block counts followed by a
     rank + copy kernel that turns them into base rows itself, while there are
-    at most 16384 (128-token block, expert) cells, and beyond that (T = 20608
-    and 33024 at E = 256) separate count, scan, rank and copy launches.
-    counts, offsets, row_of and src_tok bit-exact against the oracle's
-    dispatch; every copied row equal to its token's row."""
+    at most 16384 (128-token block, expert) cells (k = 1 to 8, E = 8 to 128),
+    and beyond that (T = 20608 and 33024 at E = 256) separate count, scan,
+    rank and copy launches. counts, offsets, row_of and src_tok bit-exact
+    against the oracle's dispatch; every copied row equal to its token's row."""
     import routing_grouped_expert_gate_gb300 as moe
     from routing_grouped_expert_gate_gb300 import _lib as L
     d = 64
-    cfg = moe.make_cfg(T=T, d=d, E=E, k=k, F=64)
+    # (top-1 softmax is refused, so k = 1 routes with sigmoid scores)
+    cfg = moe.make_cfg(T=T, d=d, E=E, k=k, F=64, score="softmax" if k > 1 else "sigmoid")
     g = torch.Generator(device="cuda")
     g.manual_seed(T * 31 + E)
     # k distinct experts per token, skewed towards the low indices
