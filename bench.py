@@ -58,7 +58,7 @@ def parse():
                          "DeepSeek-V3-shaped workloads), a comma list, or 'none'")
     ap.add_argument("--workload-steps", type=int, default=10,
                     help="timed steps per workload of the `workloads` object")
-    ap.add_argument("--stage", default=None, choices=["route"],
+    ap.add_argument("--stage", default=None, choices=["route", "permute_bwd"],
                     help="time one stage alone at the workload's full size, drawing only its "
                          "inputs (a profiling aid; prints a stage line, not the step line)")
     return ap.parse_args()
@@ -989,11 +989,64 @@ def run_stage_route(args):
             "gbs_algorithmic": round(nbytes / (us * 1e-6) / 1e9, 1)}
 
 
+def run_stage_permute_bwd(args):
+    """moe_permute_bwd alone on the full workload: dx[t] = sum_j dx_perm[row_of[t, j]]
+    (+ d_logits[t] · W_r where the permute backward forms the router's share)."""
+    import torch
+    import moe_inputs as mi
+    from routing_grouped_expert_gate_gb300 import build as B
+    B.build()
+    import routing_grouped_expert_gate_gb300 as moe
+    from routing_grouped_expert_gate_gb300 import _lib as L
+    wl = mi.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        wl = mi.shrink(wl, name=f"{wl.name}_T{args.tokens}", T=args.tokens)
+    cfg = moe.cfg_from_workload(wl)
+    T, E, k, d = wl.T, wl.E, wl.k, wl.d
+    dt = torch.bfloat16 if wl.act_dtype == "bf16" else torch.float32
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    dx_perm = torch.randn(T * k, d, generator=g, device="cuda").to(dt)
+    row_of = torch.randperm(T * k, generator=g, device="cuda").to(torch.int32).view(T, k)
+    fused = L.router_dx_in_permute_bwd(cfg)
+    d_logits = torch.randn(T, E, generator=g, device="cuda") * 1e-3
+    w_router = torch.randn(E, d, generator=g, device="cuda") * d ** -0.5
+    dx_router = None if fused else torch.randn(T, d, generator=g, device="cuda")
+    dx = torch.empty(T, d, dtype=dt, device="cuda")
+
+    def call():
+        L.permute_bwd(cfg, dx_perm, row_of, dx_router, None, dx,
+                      d_logits=d_logits if fused else None, w_router=w_router if fused else None)
+
+    for _ in range(max(args.warmup, 0)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    rc, detail = L.last_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} ({L.status_string(rc)}) {detail}")
+    us = e0.elapsed_time(e1) / max(args.steps, 1) * 1e3
+    es = dx.element_size()
+    nbytes = T * k * d * es + T * d * es + T * k * 4 + (T * E * 4 + E * d * 4 if fused
+                                                          else T * d * 4)
+    return {"stage": "permute_bwd", "workload": workload_desc(wl, True), "steps": args.steps,
+            "us_per_call": round(us, 2), "router_share_formed_here": fused,
+            "gbs_algorithmic": round(nbytes / (us * 1e-6) / 1e9, 1)}
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
     if args.stage == "route":
         print(json.dumps(run_stage_route(args)), flush=True)
+        return 0
+    if args.stage == "permute_bwd":
+        print(json.dumps(run_stage_permute_bwd(args)), flush=True)
         return 0
     if args.impl == "reference":
         out = run_reference(args, ws, rank)
