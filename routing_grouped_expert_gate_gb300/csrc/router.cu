@@ -156,20 +156,22 @@ router_logits_small(const Tx* __restrict__ x, const float* __restrict__ W,
 }
 
 // The lanes of a warp each hold TB x EMAX compensated (hi, lo) pairs of the
-// same TB tokens (TB * EMAX = 32), partial sums over different elements. A
-// reduce-scatter over the lanes (at each halving step a lane keeps one half of
-// its pairs, gives the other half to its partner and adds what it receives
-// with a TwoSum) leaves lane q with pair q = (token q / EMAX, expert q % EMAX),
-// which it rounds once (after the logit bias) and stores.
+// same TB tokens (TB * EMAX = 32 or 16), partial sums over different elements.
+// A reduce-scatter over the lanes (at each halving step a lane keeps one half
+// of its pairs, gives the other half to its partner and adds what it receives
+// with a TwoSum) leaves lane q with pair q = (token q / EMAX, expert q % EMAX)
+// (with 16 pairs, lanes 2q and 2q + 1 with pair q, which they then add the
+// same way), which it rounds once (after the logit bias) and stores.
 template <int TB, int EMAX>
 __device__ __forceinline__ void store_pair_logits(const float (&hi)[TB][EMAX],
                                                   const float (&lo)[TB][EMAX], int64_t t0,
                                                   int64_t T, int E,
                                                   const float* __restrict__ logit_bias,
                                                   float* __restrict__ logits) {
-  static_assert(TB * EMAX == 32, "one pair per lane after the reduce-scatter");
+  constexpr int N = TB * EMAX;
+  static_assert(N == 32 || N == 16, "one pair per lane or lane pair after the reduce-scatter");
   const int lane = threadIdx.x & 31;
-  float vh[32], vl[32];
+  float vh[N], vl[N];
 #pragma unroll
   for (int a = 0; a < TB; ++a)
 #pragma unroll
@@ -178,24 +180,34 @@ __device__ __forceinline__ void store_pair_logits(const float (&hi)[TB][EMAX],
       vl[a * EMAX + e] = lo[a][e];
     }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const bool upper = (lane & off) != 0;
+  for (int off = N / 2, bit = 16; off > 0; off >>= 1, bit >>= 1) {
+    const bool upper = (lane & bit) != 0;
 #pragma unroll
     for (int q = 0; q < off; ++q) {
       const float sh_ = upper ? vh[q] : vh[q + off];
       const float sl_ = upper ? vl[q] : vl[q + off];
       const float kh = upper ? vh[q + off] : vh[q];
       const float kl = upper ? vl[q + off] : vl[q];
-      const float rh = __shfl_xor_sync(0xffffffffu, sh_, off);
-      const float rl = __shfl_xor_sync(0xffffffffu, sl_, off);
+      const float rh = __shfl_xor_sync(0xffffffffu, sh_, bit);
+      const float rl = __shfl_xor_sync(0xffffffffu, sl_, bit);
       float s2, er;
       two_sum(kh, rh, s2, er);
       vh[q] = s2;
       vl[q] = __fadd_rn(__fadd_rn(kl, rl), er);
     }
   }
-  const int a = lane / EMAX, e = lane - a * EMAX;
-  if (e < E && t0 + a < T) {
+  int q = lane;
+  if constexpr (N == 16) {
+    const float rh = __shfl_xor_sync(0xffffffffu, vh[0], 1);
+    const float rl = __shfl_xor_sync(0xffffffffu, vl[0], 1);
+    float s2, er;
+    two_sum(vh[0], rh, s2, er);
+    vh[0] = s2;
+    vl[0] = __fadd_rn(__fadd_rn(vl[0], rl), er);
+    q = lane >> 1;
+  }
+  const int a = q / EMAX, e = q - a * EMAX;
+  if ((N == 32 || (lane & 1) == 0) && e < E && t0 + a < T) {
     float h = vh[0], l = vl[0];
     if (logit_bias != nullptr) comp_add(h, l, logit_bias[e]);
     logits[(t0 + a) * (int64_t)E + e] = __fadd_rn(h, l);
@@ -331,11 +343,13 @@ static cudaError_t launch_router_resident(const Ctx& c, const Tx* x, const float
 
 // ------------------------------------------------------------------ S1, E <= 16, bf16 x streamed
 // W_r stays in shared memory ([E][d] fp32, one bulk copy) and the tokens'
-// rows stream through a ring of slots, each TBLK = 8 TB tokens x 256 columns,
+// rows stream through a ring of slots, each TBLK = 16 TB tokens x 256 columns,
 // one TMA tile load per slot from a producer thread (rows past T and columns
 // past d arrive as zeros): the bytes in flight per SM are bounded by the ring
-// (up to 128 KB), not by registers. Eight consumer warps take TB tokens each of every slot; lane l
-// takes columns 4l..4l+3 and 128+4l..128+4l+3 (W and x read from shared memory
+// (up to 128 KB), not by registers. Sixteen consumer warps take TB = 16 / EMAX
+// tokens each of every slot (the kernel is bound by instruction issue: eight
+// warps of twice the tokens measured 23.8 us for the route call at T = 4096,
+// d = 4096, E = 8, sixteen 22.4 us); lane l takes columns 4l..4l+3 and 128+4l..128+4l+3 (W and x read from shared memory
 // at consecutive addresses across the lanes). Per slot a lane forms, for each
 // of its tokens and each expert, a chain of 8 fp32 FMAs; every two slots (16
 // elements) the chain folds into the (token, expert) compensated pair, and
@@ -350,19 +364,21 @@ struct StreamParams {
   uint64_t timeout_ns;
 };
 
-constexpr int kStreamThreads = 288;  // 8 consumer warps + 1 producer warp
+constexpr int kStreamThreads = 288;  // 8 consumer warps + 1 producer warp (dW_r stream)
+constexpr int kLsConsumers = 16;     // consumer warps of the logits stream
+constexpr int kLsThreads = 32 * (kLsConsumers + 1);  // + 1 producer warp
 constexpr int kStreamCols = 256;     // columns per slot
 constexpr int kStreamMaxSlots = 8;
 
 template <int EMAX>
 struct StreamTile {
-  static constexpr int TB = 32 / EMAX;                   // tokens per consumer warp
-  static constexpr int TBLK = 8 * TB;                    // tokens per slot
+  static constexpr int TB = 16 / EMAX;                   // tokens per consumer warp
+  static constexpr int TBLK = kLsConsumers * TB;         // tokens per slot
   static constexpr int kSlot = TBLK * kStreamCols * 2;   // bytes (bf16)
 };
 
 template <int EMAX>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+__global__ void __launch_bounds__(kLsThreads, 1)
 router_logits_stream(const __grid_constant__ CUtensorMap tmX, const float* __restrict__ W,
                      const StreamParams P) {
   using ST = StreamTile<EMAX>;
@@ -382,7 +398,7 @@ router_logits_stream(const __grid_constant__ CUtensorMap tmX, const float* __res
     abort_flag = 0;
     for (int s = 0; s < ns; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 8);  // one arrival per consumer warp
+      tc::mbar_init(&empty[s], kLsConsumers);  // one arrival per consumer warp
     }
     tc::mbar_init(&wbar, 1);
     tc::fence_barrier_init();
@@ -390,7 +406,7 @@ router_logits_stream(const __grid_constant__ CUtensorMap tmX, const float* __res
   __syncthreads();
   pdl_wait();  // x may come from the kernel before; logits may still be read by it
 
-  if (warp == 8) {
+  if (warp == kLsConsumers) {
     // ---------------- producer (one thread): W once, then the ring
     if (lane == 0) {
       tc::prefetch_tmap(&tmX);
@@ -520,7 +536,7 @@ static cudaError_t launch_router_stream(const Ctx& c, const moe_cfg& cfg, const 
   CUtensorMap mx;
   if (!tc::make_map_bf16_plain(&mx, x, cfg.T, cfg.d, StreamTile<EMAX>::TBLK, kStreamCols))
     return cudaErrorInvalidValue;
-  return launch_dependent(kern, dim3((unsigned)grid), dim3(kStreamThreads), smem, c.stream, mx,
+  return launch_dependent(kern, dim3((unsigned)grid), dim3(kLsThreads), smem, c.stream, mx,
                           w_router, P);
 }
 
