@@ -422,8 +422,11 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
     // The warp's 32 rows inside the segment and the columns inside F: gate/up
     // come in and d_pre goes out through the warp's buffer, 16 columns at a
     // time, as 32 x 16 boxes in the 32-byte swizzle (tmD: gate|up, tmC:
-    // d_pre); each thread reads its row's chunks and writes dg/du in place.
-    // Elsewhere each thread loads and stores its row directly.
+    // d_pre; each a 3-D map whose one copy moves the box of both halves, the
+    // gate or dg box then the up or du box, 1 KB apart: half the TMA copies
+    // of two 2-D boxes, measured 1% faster); each thread reads its row's
+    // chunks and writes dg/du in place. Elsewhere each thread loads and
+    // stores its row directly.
     const int r = ti.m0 + ec.row;
     const bool rv = r < ti.m_end;
     const int y0 = r - lane;
@@ -455,8 +458,7 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
           if (lane == 0) {
             bulk_wait_read<0>();  // the previous boxes have left the buffer
             mbar_expect_tx(load_bar, 2048);
-            tma_load_2d_s(ebuf, tmD, su32(load_bar), x, y0);
-            tma_load_2d_s(ebuf + 1024, tmD, su32(load_bar), P.F + x, y0);
+            tma_load_3d_s(ebuf, tmD, su32(load_bar), x, y0, 0);
           }
           if (!mbar_wait(load_bar, load_phase, abort_flag, P, 16)) return false;
           load_phase ^= 1;
@@ -486,10 +488,7 @@ __device__ __forceinline__ bool drain_tile(const Params& P, const Tile& ti, uint
           }
           fence_async_shared();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(tmC, ebuf, x, y0);
-            tma_store_2d(tmC, ebuf + 1024, P.F + x, y0);
-          }
+          if (lane == 0) tma_store_3d(tmC, ebuf, x, y0, 0);
         }
       } else if (rv) {
 #pragma unroll
@@ -1429,6 +1428,21 @@ static bool make_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t col
 static bool make_store_map16(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
   return make_out_map(m, base, rows, cols, ld, 16);
 }
+// [rows, 2F] gate|up (or dg|du) as [2][rows][F]: one 32 x 16 box from each
+// half per copy, the halves one after the other in shared memory (1 KB each)
+static bool make_halves_map16(CUtensorMap* m, void* base, int64_t rows, int64_t F) {
+  if (base == nullptr || rows <= 0 || F <= 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0 ||
+      (F * 2) % 16 != 0 || !get_encoder())
+    return false;
+  cuuint64_t gdim[3] = {(cuuint64_t)F, (cuuint64_t)rows, 2u};
+  cuuint64_t gstride[2] = {(cuuint64_t)F * 4, (cuuint64_t)F * 2};
+  cuuint32_t box[3] = {16u, 32u, 2u};
+  cuuint32_t estride[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 // Weight-gradient outputs [G][rows][cols] take the staged 16-byte stores when
 // their rows start on 16-byte boundaries.
 static bool wgrad_rows_aligned(const void* base, int64_t cols) {
@@ -1801,10 +1815,10 @@ cudaError_t launch_tc_grouped_swiglu_bwd(const Ctx& c, int G, int64_t n_rows, in
     } else {
       P.out0 = static_cast<bf16*>(d_pre);
       P.aux_in = static_cast<const bf16*>(pre_gu);
-      // d_pre out (tmC) and gate|up in (tmD) as 32 x 16 boxes
+      // d_pre out (tmC) and gate|up in (tmD) as 32 x 16 boxes of both halves
       CUtensorMap mGU;
-      P.tma_out = make_store_map16(&mC, d_pre, n_rows, 2 * F, 2 * F) &&
-                  make_store_map16(&mGU, const_cast<void*>(pre_gu), n_rows, 2 * F, 2 * F);
+      P.tma_out = make_halves_map16(&mC, d_pre, n_rows, F) &&
+                  make_halves_map16(&mGU, const_cast<void*>(pre_gu), n_rows, F);
       if (!P.tma_out) mC = mGU = mA;
       e = launch_mgrouped<true, EPI_SWIGLU_BWD>(c, pair, mA, d_out, n_rows, d, mB, mC, mGU, P,
                                                 kFc2Dgrad);
