@@ -1403,33 +1403,25 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 }
 
 // Output maps for the epilogues' TMA stores: bf16 [rows, cols] with a row
-// pitch of `ld` elements, 32-row boxes of 32 columns (64-byte swizzle, the
-// staging layout of stage_box_row) or 16 columns (32-byte swizzle,
-// stage_box16_chunk's layout). False (plain stores then) when the address or
-// the pitch is not a multiple of 16 bytes.
-static bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld,
-                         int box_cols) {
+// pitch of `ld` elements, 32 x 32 boxes in the 64-byte swizzle (the staging
+// layout of stage_box_row). False (plain stores then) when the address or the
+// pitch is not a multiple of 16 bytes.
+static bool make_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
   if (base == nullptr || rows <= 0 || cols <= 0 ||
       (reinterpret_cast<uintptr_t>(base) & 15) != 0 || (ld * 2) % 16 != 0 || !get_encoder())
     return false;
   cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t gstride[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, 32u};
+  cuuint32_t box[2] = {32u, 32u};
   cuuint32_t estride[2] = {1u, 1u};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-static bool make_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
-  return make_out_map(m, base, rows, cols, ld, 32);
-}
-static bool make_store_map16(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
-  return make_out_map(m, base, rows, cols, ld, 16);
-}
 // [rows, 2F] gate|up (or dg|du) as [2][rows][F]: one 32 x 16 box from each
-// half per copy, the halves one after the other in shared memory (1 KB each)
+// half per copy (32-byte swizzle, stage_box16_chunk's layout), the halves one
+// after the other in shared memory (1 KB each)
 static bool make_halves_map16(CUtensorMap* m, void* base, int64_t rows, int64_t F) {
   if (base == nullptr || rows <= 0 || F <= 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0 ||
       (F * 2) % 16 != 0 || !get_encoder())

@@ -71,15 +71,7 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
       "l"(src), "r"(bytes), "r"(su32(bar))
       : "memory");
 }
-// The same with the destination and barrier as shared-memory addresses.
-__device__ __forceinline__ void tma_load_2d_s(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                              int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
+// A 3-D tile load with the destination and barrier as shared-memory addresses.
 __device__ __forceinline__ void tma_load_3d_s(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                               int x, int y, int z) {
   asm volatile(
