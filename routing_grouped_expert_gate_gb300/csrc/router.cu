@@ -737,12 +737,28 @@ static cudaError_t launch_router_tiled(const Ctx& c, const Tx* x, const float* w
 }
 
 // ------------------------------------------------------------------ S2 keys
+// Reductions over a group of G lanes (G = 32: the whole warp).
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o, G));
+  return v;
+}
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o, G);
+  return v;
+}
+
 // The values a token's top-k ranks, lane l holding experts l, l+32, ...:
 // the logit (softmax), the probability under the softmax over all E
 // (pre-softmax), or the score (sigmoid, sqrt(softplus)); then + the selection
 // bias, or - the quantile bias; a NaN key ranks last (-inf); slots past E
-// hold -inf. pre_max / pre_inv: the pre-softmax's maximum and 1 / sum.
-template <int EPL>
+// hold -inf. pre_max / pre_inv: the pre-softmax's maximum and 1 / sum. With
+// G < 32 a token takes a group of G lanes (EPL = 1, E <= G), `lane` its lane
+// in the group.
+template <int EPL, int G = 32>
 __device__ __forceinline__ void selection_keys(const float* __restrict__ lrow,
                                                const float* __restrict__ sel_bias,
                                                const float* __restrict__ beta, int E,
@@ -770,12 +786,12 @@ __device__ __forceinline__ void selection_keys(const float* __restrict__ lrow,
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
       if (lane + 32 * i < E) m = fmaxf(m, lg[i]);
-    m = warp_max(m);
+    m = group_max<G>(m);
     float sum = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
       if (lane + 32 * i < E) sum += expf(lg[i] - m);
-    sum = warp_sum(sum);
+    sum = group_sum<G>(sum);
     pre_max = m;
     pre_inv = 1.f / sum;
 #pragma unroll
@@ -824,24 +840,33 @@ __device__ __forceinline__ void sort_desc(uint64_t (&v)[N]) {
 // ------------------------------------------------------------------ S2
 // One warp per token. Lane l holds experts l, l+32, ... The k winners are found
 // by k rounds of a warp arg-max over (key descending, index ascending); a
-// non-finite key counts as -inf so a valid expert always wins.
+// non-finite key counts as -inf so a valid expert always wins. With E <= G < 32
+// a warp takes 32 / G tokens at once, a group of G lanes each, one expert per
+// lane, and every reduction runs over the group (the same keys and order).
 //
 // Quantile routing (beta != NULL): the key is the score minus beta, k + 1
 // experts are ranked, the first k are chosen and the (k+1)-th key is written
 // to alpha[t] (the token's threshold).
-template <int EPL>
+template <int EPL, int G = 32>
 __global__ void __launch_bounds__(256)
 router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias,
             const float* __restrict__ beta, float* __restrict__ alpha,
             int32_t* __restrict__ idx, float* __restrict__ w, int64_t T, int E, int k,
             int score_fn, float scaling) {
   pdl_wait();  // the logits come from the kernel before
+  static_assert(G == 32 || EPL == 1, "groups of G < 32 lanes hold one expert each");
+  constexpr int SLOTS = 32 / G;  // tokens per warp at a time
   const int ksel = (alpha != nullptr) ? k + 1 : k;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & (G - 1);  // the lane within the token's group
+  const int slot = (threadIdx.x & 31) / G;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+  for (int64_t tb = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * SLOTS; tb < T;
+       tb += nwarps * SLOTS) {
+    const int64_t t = tb + slot;
+    const bool live = t < T;  // (a group past T still takes part in the shuffles)
     float key[EPL], pre_max, pre_inv;
-    selection_keys<EPL>(logits + t * E, sel_bias, beta, E, score_fn, lane, key, pre_max, pre_inv);
+    selection_keys<EPL, G>(logits + (live ? t : tb) * E, sel_bias, beta, E, score_fn, lane, key,
+                           pre_max, pre_inv);
     // Each candidate as one 64-bit integer that orders like (key descending,
     // expert ascending): the key's bits made order-preserving as unsigned
     // (-0 counted as +0) above the complemented expert index; slots past E hold
@@ -870,8 +895,8 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       if (j < ksel) {
         uint64_t best = pk[0];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+        for (int off = G / 2; off > 0; off >>= 1) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off, G);
           best = o > best ? o : best;
         }
         if (pk[0] == best) {  // the one lane whose head won (values are distinct)
@@ -888,22 +913,22 @@ router_topk(const float* __restrict__ logits, const float* __restrict__ sel_bias
       }
     }
     if (alpha != nullptr) {
-      const float ak = __shfl_sync(0xffffffffu, my_key, k);
-      if (lane == 0) alpha[t] = ak;
+      const float ak = __shfl_sync(0xffffffffu, my_key, k, G);
+      if (lane == 0 && live) alpha[t] = ak;
     }
     // mixing weights: lane j < k weighs the j-th chosen expert
-    const bool mine = lane < k;
+    const bool mine = lane < k && live;
     const float l_j = mine ? logits[t * E + my_e] : 0.f;
     float wj;
     if (score_fn == MOE_SCORE_SOFTMAX) {
-      const float m = warp_max(mine ? l_j : -INFINITY);
+      const float m = group_max<G>(mine ? l_j : -INFINITY);
       const float ex = mine ? expf(l_j - m) : 0.f;
-      wj = ex * (scaling / warp_sum(ex));
+      wj = ex * (scaling / group_sum<G>(ex));
     } else if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
       wj = mine ? expf(l_j - pre_max) * pre_inv * scaling : 0.f;
     } else {
       const float sj = mine ? bias_score(l_j, score_fn) : 0.f;
-      const float sum = warp_sum(sj);
+      const float sum = group_sum<G>(sj);
       wj = sj * ((k > 1) ? scaling / (sum + 1e-20f) : scaling);
     }
     if (mine) {
@@ -975,6 +1000,48 @@ router_near_ties(const float* __restrict__ logits, const float* __restrict__ sel
 }
 
 // ------------------------------------------------------------------ B2
+// d l_j for a token's k chosen logits lj[] from the upstream gradients gj[] of
+// its mixing weights: the softmax over the chosen logits, or the normalised
+// sigmoid-like scores (not the pre-softmax, where every logit moves).
+__device__ __forceinline__ void chosen_logit_grads(const float (&lj)[kMaxK],
+                                                   const float (&gj)[kMaxK], int k, int score_fn,
+                                                   float scaling, float (&dl)[kMaxK]) {
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    float m = lj[0];
+#pragma unroll
+    for (int j = 1; j < kMaxK; ++j)
+      if (j < k) m = fmaxf(m, lj[j]);
+    float p[kMaxK], s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      p[j] = (j < k) ? expf(lj[j] - m) : 0.f;
+      s += p[j];
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      p[j] /= s;
+      dot += p[j] * (scaling * gj[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) dl[j] = p[j] * (scaling * gj[j] - dot);
+  } else {
+    float sj[kMaxK], S = 0.f, dsd = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      sj[j] = (j < k) ? bias_score(lj[j], score_fn) : 0.f;
+      S += sj[j];
+      dsd += gj[j] * sj[j];
+    }
+    S += 1e-20f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      const float ds = (k > 1) ? scaling * (gj[j] - dsd / S) / S : scaling * gj[j];
+      dl[j] = ds * bias_score_deriv(lj[j], sj[j], score_fn);
+    }
+  }
+}
+
 // One warp per token: zero the row (unless accumulating), then each of the
 // first k lanes adds the gradient of its chosen logit.
 __global__ void __launch_bounds__(256)
@@ -1011,26 +1078,7 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
       continue;
     }
     float dl[kMaxK];
-    if (score_fn == MOE_SCORE_SOFTMAX) {
-      float m = lj[0];
-#pragma unroll
-      for (int j = 1; j < kMaxK; ++j)
-        if (j < k) m = fmaxf(m, lj[j]);
-      float p[kMaxK], s = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        p[j] = (j < k) ? expf(lj[j] - m) : 0.f;
-        s += p[j];
-      }
-      float dot = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        p[j] /= s;
-        dot += p[j] * (scaling * gj[j]);
-      }
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) dl[j] = p[j] * (scaling * gj[j] - dot);
-    } else if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
+    if (score_fn == MOE_SCORE_SOFTMAX_PRE) {
       // w_j = c P[idx_j] with P the softmax over all E: every logit moves,
       // d l_e = c P_e (g_e - sum_j P[idx_j] dw_j)
       float m = -INFINITY;
@@ -1053,25 +1101,56 @@ router_scores_bwd(const float* __restrict__ logits, const int32_t* __restrict__ 
         d_logits[t * E + e] += pe * (ge - dot);
       }
       continue;
-    } else {
-      float sj[kMaxK], S = 0.f, dsd = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        sj[j] = (j < k) ? bias_score(lj[j], score_fn) : 0.f;
-        S += sj[j];
-        dsd += gj[j] * sj[j];
-      }
-      S += 1e-20f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        const float ds = (k > 1) ? scaling * (gj[j] - dsd / S) / S : scaling * gj[j];
-        dl[j] = ds * bias_score_deriv(lj[j], sj[j], score_fn);
-      }
     }
+    chosen_logit_grads(lj, gj, k, score_fn, scaling, dl);
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j)
       if (j < k && lane == j) d_logits[t * E + ej[j]] += dl[j];
+  }
+}
+
+
+// The same for few experts and scores other than the pre-softmax: one thread
+// per token (its k indices, logits and weight gradients loaded together), so
+// that a warp takes 32 tokens instead of one.
+__global__ void __launch_bounds__(256)
+router_scores_bwd_rows(const float* __restrict__ logits, const int32_t* __restrict__ idx,
+                       const float* __restrict__ dw, float* __restrict__ d_logits, int64_t T,
+                       int E, int k, int score_fn, float scaling, int accumulate, int* status) {
+  pdl_wait();  // a dependent launch: inputs come from the kernels before
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    int ej[kMaxK];
+    float lj[kMaxK], gj[kMaxK], dl[kMaxK];
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      ej[j] = 0;
+      gj[j] = 0.f;
+      if (j < k) {
+        int e = idx[t * k + j];
+        if (e < 0 || e >= E) {
+          ok = false;
+          e = 0;
+        }
+        ej[j] = e;
+        gj[j] = dw[t * k + j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) lj[j] = (j < k) ? logits[t * E + ej[j]] : 0.f;
+    if (!ok) {
+      record_error(status, MOE_ERR_DEVICE_INDEX, (int)t);
+      continue;
+    }
+    chosen_logit_grads(lj, gj, k, score_fn, scaling, dl);
+    float* row = d_logits + t * E;
+    if (!accumulate)
+      for (int e = 0; e < E; ++e) row[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) row[ej[j]] += dl[j];
   }
 }
 
@@ -1489,6 +1568,19 @@ cudaError_t launch_router_topk_q(const Ctx& c, const moe_cfg& cfg, const float* 
   const unsigned grid = warp_grid(c, cfg.T);
   const int epl = (cfg.E + 31) / 32;
   cudaError_t e;
+  if (cfg.E <= 16) {
+    // a group of 8 or 16 lanes per token
+    if (cfg.E <= 8)
+      e = launch_dependent(router_topk<1, 8>, dim3(warp_grid(c, (cfg.T + 3) / 4)), dim3(256), 0,
+                           c.stream, logits, sel_bias, beta, alpha, idx, w, cfg.T, cfg.E, cfg.k,
+                           cfg.score_fn, cfg.scaling);
+    else
+      e = launch_dependent(router_topk<1, 16>, dim3(warp_grid(c, (cfg.T + 1) / 2)), dim3(256), 0,
+                           c.stream, logits, sel_bias, beta, alpha, idx, w, cfg.T, cfg.E, cfg.k,
+                           cfg.score_fn, cfg.scaling);
+    note_launches(1);
+    return e;
+  }
 #define MOE_TOPK(N)                                                                          \
   e = launch_dependent(router_topk<N>, dim3(grid), dim3(256), 0, c.stream, logits, sel_bias, \
                        beta, alpha, idx, w, cfg.T, cfg.E, cfg.k, cfg.score_fn, cfg.scaling)
@@ -1527,6 +1619,15 @@ cudaError_t launch_router_scores_bwd(const Ctx& c, const moe_cfg& cfg, const flo
                                      const int32_t* idx, const float* dw, float* d_logits,
                                      int accumulate) {
   if (cfg.T == 0) return cudaSuccess;
+  if (cfg.E <= 16 && cfg.score_fn != MOE_SCORE_SOFTMAX_PRE) {
+    const int64_t blocks = (cfg.T + 255) / 256;
+    const int64_t cap = (int64_t)c.sm_count * 8;
+    launch_dependent(router_scores_bwd_rows, dim3((unsigned)(blocks < cap ? blocks : cap)),
+                     dim3(256), 0, c.stream, logits, idx, dw, d_logits, cfg.T, cfg.E, cfg.k,
+                     cfg.score_fn, cfg.scaling, accumulate, c.status);
+    note_launches(1);
+    return cudaGetLastError();
+  }
   launch_dependent(router_scores_bwd, dim3(warp_grid(c, cfg.T)), dim3(256), 0, c.stream,
       logits, idx, dw, d_logits, cfg.T, cfg.E, cfg.k, cfg.score_fn, cfg.scaling, accumulate,
       c.status);
