@@ -17,6 +17,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "lane_groups.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -737,20 +738,6 @@ static cudaError_t launch_router_tiled(const Ctx& c, const Tx* x, const float* w
 }
 
 // ------------------------------------------------------------------ S2 keys
-// Reductions over a group of G lanes (G = 32: the whole warp).
-template <int G>
-__device__ __forceinline__ float group_max(float v) {
-#pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o, G));
-  return v;
-}
-template <int G>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o, G);
-  return v;
-}
-
 // The values a token's top-k ranks, lane l holding experts l, l+32, ...:
 // the logit (softmax), the probability under the softmax over all E
 // (pre-softmax), or the score (sigmoid, sqrt(softplus)); then + the selection
