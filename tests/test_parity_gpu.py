@@ -67,6 +67,14 @@ SMALL = {
     # d_logits · W_r streams k + 1 row slices per token through its ring
     "few_shared_small": mi.shrink(W["mixtral_style"], name="few_shared_small", T=2999, d=1288,
                                   E=12, k=4, F=96, F_shared=64, shared_gate=True),
+    # few experts with sigmoid scores and a selection bias, fwd + bwd: the
+    # top-k in 16-lane groups, the per-token scores backward and the grouped
+    # aux-loss partials on their sigmoid branches
+    "sigmoid_few_small": mi.shrink(W["deepseek_v3_shaped"], name="sigmoid_few_small", T=321,
+                                   d=256, E=12, k=3, F=96, F_shared=64, backward=True),
+    "sqrtsoftplus_few_small": mi.shrink(W["deepseek_v3_shaped"], name="sqrtsoftplus_few_small",
+                                        score="sqrtsoftplus", T=263, d=192, E=8, k=2, F=64,
+                                        F_shared=0, backward=True),
 }
 # bf16 workloads run on the tcgen05 kernels (the default) and, as a cross-check,
 # on the CUDA-core kernels; fp32 workloads run on the CUDA-core kernels.
